@@ -1,0 +1,212 @@
+"""CPU oracle for online-softmax attention: test infrastructure, not product.
+
+This package is the plain, slow, obviously-correct fp64 definition of what the
+GPU library computes.  It shares no code with the CUDA path and neither
+imports the other.  Only the test-suite, the smoke check and the bench's
+CPU-baseline leg may import it; the product path never does.
+
+The arithmetic lives in ``oracle.c`` (plain C11, fp64, one thread pool over
+independent rows).  This module only marshals numpy arrays to it and builds
+the shared object with gcc on first use.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against the
+pages' printed worked examples (``tests/golden/``), closed forms, invariants,
+brute force and fp64 library routines.  None is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F64, F32, BF16 = 0, 1, 2
+
+_c_dbl_p = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboa_oracle.so next to it (if stale) and return its path."""
+    with _lock:
+        stale = (not os.path.exists(_LIB_PATH)) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+        if force or stale:
+            tmp = _LIB_PATH + f".tmp{os.getpid()}"
+            cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-shared", "-fPIC",
+                   "-pthread", "-o", tmp, _SRC, "-lm"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    vp, i64, i32, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+    lib.oracle_softmax_rows.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, i32]
+    lib.oracle_softmax_rows.restype = i32
+    lib.oracle_attn.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, dbl, vp, vp, i64, vp, vp, i32]
+    lib.oracle_attn.restype = i32
+    lib.oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
+    lib.oracle_lse_merge.restype = i32
+    lib.oracle_online_stats.argtypes = [vp, i64, _c_dbl_p, _c_dbl_p]
+    lib.oracle_online_stats.restype = None
+    lib.oracle_online_stats_trace.argtypes = [vp, i64, vp, vp]
+    lib.oracle_online_stats_trace.restype = None
+    lib.oracle_merge_ml.argtypes = [dbl, dbl, dbl, dbl, _c_dbl_p, _c_dbl_p]
+    lib.oracle_merge_ml.restype = None
+    lib.oracle_attn_fa1.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, dbl, vp]
+    lib.oracle_attn_fa1.restype = i32
+    _lib = lib
+    return lib
+
+
+def _threads(n):
+    return int(n) if n else (os.cpu_count() or 1)
+
+
+def _as_input(a):
+    """Return (contiguous array, dtype code).  bf16 arrives as uint16 bit patterns."""
+    a = np.asarray(a)
+    if a.dtype == np.float64:
+        code = F64
+    elif a.dtype == np.float32:
+        code = F32
+    elif a.dtype == np.uint16:
+        code = BF16
+    else:
+        a = a.astype(np.float64)
+        code = F64
+    return np.ascontiguousarray(a), code
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def softmax_rows(x, nthreads=None):
+    """Three-pass safe softmax of each row of a 2-D array, plus its natural log-sum-exp.
+
+    x: [rows, cols] float64/float32, or uint16 holding bf16 bits.  Returns (y, lse) in fp64.
+    """
+    xa, code = _as_input(x)
+    if xa.ndim != 2:
+        raise ValueError("x must be 2-D")
+    rows, cols = xa.shape
+    y = np.empty((rows, cols), np.float64)
+    lse = np.empty(rows, np.float64)
+    rc = _load().oracle_softmax_rows(_ptr(xa), code, rows, cols, cols, _ptr(y), cols, _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_softmax_rows failed")
+    return y, lse
+
+
+def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthreads=None):
+    """Materialised softmax(Q K^T * scale) V and per-row LSE, in fp64.
+
+    q [B,H,Nq,d], k/v [B,H,Nk,d] (same dtype code).  kv_len: None or int array [B].
+    rows: None for every row, else flattened row indices (b*H + h)*Nq + i; then the
+    result has shape [len(rows), d] and [len(rows)].
+    """
+    qa, code = _as_input(q)
+    ka, kcode = _as_input(k)
+    va, vcode = _as_input(v)
+    if not (code == kcode == vcode):
+        raise ValueError("q, k, v must share a dtype")
+    if qa.ndim != 4 or ka.ndim != 4 or va.ndim != 4:
+        raise ValueError("q, k, v must be [B,H,N,d]")
+    B, H, Nq, d = qa.shape
+    Nk = ka.shape[2]
+    if ka.shape != (B, H, Nk, d) or va.shape != (B, H, Nk, d):
+        raise ValueError("k/v shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kvl = None
+    if kv_len is not None:
+        kvl = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32))
+        if kvl.shape != (B,):
+            raise ValueError("kv_len must be [B]")
+    if rows is None:
+        n = B * H * Nq
+        ra = None
+    else:
+        ra = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n = ra.shape[0]
+    o = np.zeros((n, d), np.float64)
+    lse = np.empty(n, np.float64)
+    rc = _load().oracle_attn(_ptr(qa), _ptr(ka), _ptr(va), code, B, H, Nq, Nk, d, int(bool(causal)),
+                             float(scale), _ptr(kvl), _ptr(ra), n, _ptr(o), _ptr(lse), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn failed")
+    if rows is None:
+        return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
+    return o, lse
+
+
+def lse_merge(part_o, part_lse):
+    """Merge split partials (normalised o_c [S,R,d], lse_c [S,R]) into (o [R,d], lse [R])."""
+    pl = np.ascontiguousarray(np.asarray(part_lse, np.float64))
+    S, R = pl.shape
+    if part_o is None:
+        d = 0
+        po = None
+    else:
+        po = np.ascontiguousarray(np.asarray(part_o, np.float64))
+        d = po.shape[2]
+        if po.shape[:2] != (S, R):
+            raise ValueError("part_o must be [S,R,d]")
+    o = np.zeros((R, d), np.float64)
+    lse = np.empty(R, np.float64)
+    rc = _load().oracle_lse_merge(_ptr(po), _ptr(pl), S, R, d, _ptr(o) if d > 0 else None, _ptr(lse))
+    if rc != 0:
+        raise RuntimeError("oracle_lse_merge failed")
+    return o, lse
+
+
+def online_stats(x):
+    """Single-pass running (m, l) over a 1-D array (the element-by-element scan)."""
+    xa = np.ascontiguousarray(np.asarray(x, np.float64).reshape(-1))
+    m, l = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_online_stats(_ptr(xa), xa.shape[0], ctypes.byref(m), ctypes.byref(l))
+    return m.value, l.value
+
+
+def online_stats_trace(x):
+    """(m_k, d_k) after each element of the scan, as two arrays."""
+    xa = np.ascontiguousarray(np.asarray(x, np.float64).reshape(-1))
+    ms = np.empty_like(xa)
+    ls = np.empty_like(xa)
+    _load().oracle_online_stats_trace(_ptr(xa), xa.shape[0], _ptr(ms), _ptr(ls))
+    return ms, ls
+
+
+def merge_ml(m1, l1, m2, l2):
+    """Merge two (m, l) segment statistics; 0 is the reference when both maxima are -inf."""
+    m, l = ctypes.c_double(), ctypes.c_double()
+    _load().oracle_merge_ml(float(m1), float(l1), float(m2), float(l2), ctypes.byref(m), ctypes.byref(l))
+    return m.value, l.value
+
+
+def attention_fa1(q, k, v, Br=4, Bc=3, scale=None):
+    """FlashAttention V1 block order for one head (non-causal), fp64: q [N,d], k/v [Nk,d]."""
+    qa = np.ascontiguousarray(np.asarray(q, np.float64))
+    ka = np.ascontiguousarray(np.asarray(k, np.float64))
+    va = np.ascontiguousarray(np.asarray(v, np.float64))
+    N, d = qa.shape
+    Nk = ka.shape[0]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.zeros((N, d), np.float64)
+    rc = _load().oracle_attn_fa1(_ptr(qa), _ptr(ka), _ptr(va), N, Nk, d, Br, Bc, float(scale), _ptr(o))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_fa1 failed")
+    return o

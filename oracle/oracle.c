@@ -1,0 +1,382 @@
+/*
+ * oracle.c -- the plain, slow, obviously-correct CPU definition of what the
+ * GPU path computes.  TEST INFRASTRUCTURE ONLY: nothing in the product
+ * library links, includes or calls this file.  Only tests/, the smoke check
+ * and the bench's CPU-baseline leg use it.
+ *
+ * Everything is computed in IEEE double (fp64).  Inputs may be given as
+ * fp64, fp32 or bf16 (raw uint16 bit patterns); they are widened exactly to
+ * double before any arithmetic.  No blocking, fusion or reordering beyond the
+ * plain definitions below: each function names the passage it follows.
+ *
+ * Sources (web pages on online softmax):
+ *   [OS-RM]  "Online Softmax -- the mathematical heart of FlashAttention"
+ *            (inference-engineering roadmap page), sections 1-7.
+ *   [OS-RH]  "Online Softmax" (research-hub concept page), "Key math".
+ *   [OS-PT]  "Online softmax in attention -- why and how".
+ *   [OS-IL]  "Online Softmax & FlashAttention -- AI infra interview lesson",
+ *            Step 1 (online stats and merge) and Step 2 (FlashAttention V1).
+ *
+ * Conventions fixed where the pages leave a point open (each is listed in
+ * the design notes of the repository):
+ *   - a score or input element equal to -inf contributes exactly zero;
+ *   - a row whose elements are all -inf (fully masked) has output +0.0 and
+ *     log-sum-exp -inf, never NaN ([OS-RM] s.7 "fully-masked rows";
+ *     [OS-IL] Step 1, both-sides -inf special case);
+ *   - causal visibility: key j is visible to query i iff j <= i
+ *     ([OS-PT] "Why this matters for attention specifically": t2 = 0..t1);
+ *   - the log-sum-exp is natural-log, over the scaled scores.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC -pthread.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_F64 0
+#define ORACLE_F32 1
+#define ORACLE_BF16 2
+
+/* Exact widening of one element of an input buffer to double. */
+static double widen(const void* p, int dtype, int64_t idx) {
+  if (dtype == ORACLE_F64) return ((const double*)p)[idx];
+  if (dtype == ORACLE_F32) return (double)((const float*)p)[idx];
+  /* bf16: the 16 stored bits are the top half of an fp32 bit pattern */
+  uint32_t bits = (uint32_t)((const uint16_t*)p)[idx] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* ------------------------------------------------------------------ */
+/* Simple static partition of [0, n) over worker threads.              */
+/* ------------------------------------------------------------------ */
+typedef void (*range_fn)(void* ctx, int64_t begin, int64_t end, double* scratch);
+
+typedef struct {
+  range_fn fn;
+  void* ctx;
+  int64_t begin, end;
+  int64_t scratch_len;
+  int failed;
+} worker_arg;
+
+static void* worker_main(void* p) {
+  worker_arg* a = (worker_arg*)p;
+  double* scratch = NULL;
+  if (a->scratch_len > 0) {
+    scratch = (double*)malloc((size_t)a->scratch_len * sizeof(double));
+    if (!scratch) {
+      a->failed = 1;
+      return NULL;
+    }
+  }
+  a->fn(a->ctx, a->begin, a->end, scratch);
+  free(scratch);
+  return NULL;
+}
+
+/* Runs fn over [0, n) split into nthreads contiguous pieces.  Returns 0 on
+ * success, -1 if a thread or its scratch could not be created. */
+static int parallel_for(int64_t n, int nthreads, int64_t scratch_len, range_fn fn, void* ctx) {
+  if (n <= 0) return 0;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > n) nthreads = (int)n;
+  pthread_t tid[256];
+  worker_arg args[256];
+  int started[256];
+  int rc = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    args[t].fn = fn;
+    args[t].ctx = ctx;
+    args[t].begin = n * t / nthreads;
+    args[t].end = n * (t + 1) / nthreads;
+    args[t].scratch_len = scratch_len;
+    args[t].failed = 0;
+    started[t] = (pthread_create(&tid[t], NULL, worker_main, &args[t]) == 0);
+    if (!started[t]) {
+      worker_main(&args[t]); /* run inline rather than fail */
+    }
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    if (started[t]) pthread_join(tid[t], NULL);
+    if (args[t].failed) rc = -1;
+  }
+  return rc;
+}
+
+/* ------------------------------------------------------------------ */
+/* Row softmax with log-sum-exp: the three-pass safe softmax.          */
+/* [OS-RM] s.1 "Standard (offline) softmax -- 3 passes";               */
+/* [OS-PT] "The textbook softmax: stable, but two passes".             */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  const void* x;
+  int dtype;
+  int64_t cols, ld_x, ld_y;
+  double* y;
+  double* lse;
+} softmax_ctx;
+
+static void softmax_range(void* p, int64_t r0, int64_t r1, double* scratch) {
+  (void)scratch;
+  const softmax_ctx* c = (const softmax_ctx*)p;
+  for (int64_t r = r0; r < r1; ++r) {
+    const int64_t base = r * c->ld_x;
+    /* pass 1: m = max_j x_j */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < c->cols; ++j) {
+      double xj = widen(c->x, c->dtype, base + j);
+      if (xj > m) m = xj;
+    }
+    if (m == -INFINITY) { /* fully -inf row: y = 0, lse = -inf */
+      if (c->y)
+        for (int64_t j = 0; j < c->cols; ++j) c->y[r * c->ld_y + j] = 0.0;
+      if (c->lse) c->lse[r] = -INFINITY;
+      continue;
+    }
+    /* pass 2: d = sum_j exp(x_j - m) */
+    double d = 0.0;
+    for (int64_t j = 0; j < c->cols; ++j) d += exp(widen(c->x, c->dtype, base + j) - m);
+    /* pass 3: y_j = exp(x_j - m) / d */
+    if (c->y)
+      for (int64_t j = 0; j < c->cols; ++j)
+        c->y[r * c->ld_y + j] = exp(widen(c->x, c->dtype, base + j) - m) / d;
+    if (c->lse) c->lse[r] = m + log(d);
+  }
+}
+
+/* x: rows x cols, row stride ld_x elements; y: rows x cols (row stride ld_y)
+ * or NULL; lse: rows or NULL.  Returns 0, or -1 on a bad argument. */
+int oracle_softmax_rows(const void* x, int dtype, int64_t rows, int64_t cols, int64_t ld_x,
+                        double* y, int64_t ld_y, double* lse, int nthreads) {
+  if (!x || rows < 0 || cols < 0 || ld_x < cols || (y && ld_y < cols)) return -1;
+  softmax_ctx c = {x, dtype, cols, ld_x, ld_y, y, lse};
+  return parallel_for(rows, nthreads, 0, softmax_range, &c);
+}
+
+/* ------------------------------------------------------------------ */
+/* Attention: materialise one full score row, safe softmax, weighted    */
+/* sum of value rows.                                                   */
+/* [OS-RM] s.5: A_i = sum_j softmax(Q K^T)_ij V_j;                      */
+/* [OS-PT]: s_t2 = (q_t1 . k_t2) / sqrt(hd), causal t2 <= t1;           */
+/* [OS-IL] Step 2: S = q K^T * scale.                                   */
+/* Layout: q [B,H,Nq,d], k and v [B,H,Nk,d], row-major contiguous.      */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  const void *q, *k, *v;
+  int dtype;
+  int64_t B, H, Nq, Nk, d;
+  int causal;
+  double scale;
+  const int32_t* kv_len;
+  const int64_t* rows; /* flattened (b*H + h)*Nq + i, or NULL for all */
+  double* o;
+  double* lse;
+} attn_ctx;
+
+static void attn_range(void* p, int64_t t0, int64_t t1, double* s) {
+  const attn_ctx* c = (const attn_ctx*)p;
+  const int64_t d = c->d;
+  for (int64_t t = t0; t < t1; ++t) {
+    const int64_t row = c->rows ? c->rows[t] : t;
+    const int64_t bh = row / c->Nq, i = row % c->Nq, b = bh / c->H;
+    int64_t kvl = c->Nk;
+    if (c->kv_len) {
+      kvl = c->kv_len[b];
+      if (kvl > c->Nk) kvl = c->Nk;
+      if (kvl < 0) kvl = 0;
+    }
+    const int64_t qbase = row * d, kvbase = bh * c->Nk * d;
+    /* full score row, -inf where masked */
+    for (int64_t j = 0; j < c->Nk; ++j) {
+      int visible = (j < kvl) && (!c->causal || j <= i);
+      if (!visible) {
+        s[j] = -INFINITY;
+        continue;
+      }
+      double dot = 0.0;
+      for (int64_t e = 0; e < d; ++e)
+        dot += widen(c->q, c->dtype, qbase + e) * widen(c->k, c->dtype, kvbase + j * d + e);
+      s[j] = c->scale * dot;
+    }
+    double* o = c->o ? c->o + t * d : NULL;
+    if (o)
+      for (int64_t e = 0; e < d; ++e) o[e] = 0.0;
+    /* three-pass safe softmax over the row */
+    double m = -INFINITY;
+    for (int64_t j = 0; j < c->Nk; ++j)
+      if (s[j] > m) m = s[j];
+    if (m == -INFINITY) {
+      if (c->lse) c->lse[t] = -INFINITY;
+      continue; /* o stays +0.0 */
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < c->Nk; ++j) l += exp(s[j] - m);
+    if (o)
+      for (int64_t j = 0; j < c->Nk; ++j) {
+        if (s[j] == -INFINITY) continue; /* weight exactly zero */
+        double y = exp(s[j] - m) / l;
+        for (int64_t e = 0; e < d; ++e) o[e] += y * widen(c->v, c->dtype, kvbase + j * d + e);
+      }
+    if (c->lse) c->lse[t] = m + log(l);
+  }
+}
+
+/* Computes output rows of softmax(Q K^T * scale) V and their log-sum-exp.
+ * rows == NULL: all B*H*Nq rows, o is [B*H*Nq, d]; else only the nrows
+ * listed flattened rows, o is [nrows, d], lse is [nrows].  kv_len (NULL or
+ * int32[B]) hides keys j >= kv_len[b].  Returns 0, or -1 on bad arguments. */
+int oracle_attn(const void* q, const void* k, const void* v, int dtype, int64_t B, int64_t H,
+                int64_t Nq, int64_t Nk, int64_t d, int causal, double scale, const int32_t* kv_len,
+                const int64_t* rows, int64_t nrows, double* o, double* lse, int nthreads) {
+  if (!q || !k || !v || B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return -1;
+  attn_ctx c = {q, k, v, dtype, B, H, Nq, Nk, d, causal, scale, kv_len, rows, o, lse};
+  int64_t n = rows ? nrows : B * H * Nq;
+  if (rows)
+    for (int64_t t = 0; t < nrows; ++t)
+      if (rows[t] < 0 || rows[t] >= B * H * Nq) return -1;
+  return parallel_for(n, nthreads, Nk > 0 ? Nk : 1, attn_range, &c);
+}
+
+/* ------------------------------------------------------------------ */
+/* Merge of split partials: each partial c of row r holds the output   */
+/* normalised over its own keys, o_c, and its log-sum-exp lse_c.  The   */
+/* merged row is the softmax over the union of the keys:                */
+/*   lse = log sum_c exp(lse_c),  o = sum_c exp(lse_c - lse) o_c.       */
+/* A partial with lse_c = -inf (no visible key) has weight zero; if all */
+/* are -inf, o = 0 and lse = -inf.                                      */
+/* [OS-IL] Step 1 (merge of (m, l), direct logsumexp) and Step 2        */
+/* (O_new = (l_old e^(m_old-m_new) O_old + ...)/l_new).                 */
+/* part_o [S, R, d] (may be NULL when d == 0), part_lse [S, R].         */
+/* ------------------------------------------------------------------ */
+int oracle_lse_merge(const double* part_o, const double* part_lse, int64_t S, int64_t R,
+                     int64_t d, double* o, double* lse) {
+  if (!part_lse || S < 0 || R < 0 || d < 0 || (d > 0 && (!part_o || !o))) return -1;
+  for (int64_t r = 0; r < R; ++r) {
+    double L = -INFINITY;
+    for (int64_t c = 0; c < S; ++c)
+      if (part_lse[c * R + r] > L) L = part_lse[c * R + r];
+    for (int64_t e = 0; e < d; ++e) o[r * d + e] = 0.0;
+    if (L == -INFINITY) {
+      if (lse) lse[r] = -INFINITY;
+      continue;
+    }
+    double W = 0.0;
+    for (int64_t c = 0; c < S; ++c) W += exp(part_lse[c * R + r] - L);
+    double total = L + log(W);
+    for (int64_t c = 0; c < S; ++c) {
+      double lc = part_lse[c * R + r];
+      if (lc == -INFINITY) continue;
+      double w = exp(lc - total);
+      for (int64_t e = 0; e < d; ++e) o[r * d + e] += w * part_o[(c * R + r) * d + e];
+    }
+    if (lse) lse[r] = total;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* The algorithmic forms, kept only so the tests can show that they     */
+/* reach the definitions above.  They follow the pages' steps in order.  */
+/* ------------------------------------------------------------------ */
+
+/* Single pass over x: running max m and running sum l, referred to m.
+ * [OS-RM] s.2 recurrence; [OS-IL] Step 1 "a single-pass scan merges in
+ * each element as (x_i, 1)", skipping elements while nothing finite has
+ * been seen (avoids -inf - -inf). */
+void oracle_online_stats(const double* x, int64_t n, double* m_out, double* l_out) {
+  double m = -INFINITY, l = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double m_new = x[i] > m ? x[i] : m;
+    if (m_new == -INFINITY) continue;
+    l = l * exp(m - m_new) + exp(x[i] - m_new);
+    m = m_new;
+  }
+  *m_out = m;
+  *l_out = l;
+}
+
+/* Online stats that also records (m_k, d_k) after every element, for the
+ * step-by-step worked example ([OS-RM] s.3).  m_steps and l_steps hold n. */
+void oracle_online_stats_trace(const double* x, int64_t n, double* m_steps, double* l_steps) {
+  double m = -INFINITY, l = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    double m_new = x[i] > m ? x[i] : m;
+    if (m_new != -INFINITY) {
+      l = l * exp(m - m_new) + exp(x[i] - m_new);
+      m = m_new;
+    }
+    m_steps[i] = m;
+    l_steps[i] = l;
+  }
+}
+
+/* Merge of two segment statistics ([OS-IL] Step 1):
+ *   m = max(m1, m2),  l = exp(m1 - m) l1 + exp(m2 - m) l2,
+ * with 0 used as the reference when both sides are -inf. */
+void oracle_merge_ml(double m1, double l1, double m2, double l2, double* m_out, double* l_out) {
+  double m = m1 > m2 ? m1 : m2;
+  double safe = (m == -INFINITY) ? 0.0 : m;
+  *m_out = m;
+  *l_out = l1 * exp(m1 - safe) + l2 * exp(m2 - safe);
+}
+
+/* FlashAttention V1 for one head, non-causal ([OS-IL] Step 2): KV blocks
+ * of Bc rows outside, Q blocks of Br rows inside; O, m, l kept normalised
+ * and merged per block.  q [N,d], k and v [Nk,d] fp64; o [N,d].  Needs
+ * scratch for O/m/l only.  Returns 0, or -1 on bad arguments. */
+int oracle_attn_fa1(const double* q, const double* k, const double* v, int64_t N, int64_t Nk,
+                    int64_t d, int64_t Br, int64_t Bc, double scale, double* o) {
+  if (!q || !k || !v || !o || N < 0 || Nk < 0 || d < 0 || Br < 1 || Bc < 1) return -1;
+  double* m = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+  double* l = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+  double* S = (double*)malloc((size_t)(Br * Bc) * sizeof(double));
+  double* PV = (double*)malloc((size_t)(d > 0 ? d : 1) * sizeof(double));
+  if (!m || !l || !S || !PV) {
+    free(m), free(l), free(S), free(PV);
+    return -1;
+  }
+  for (int64_t i = 0; i < N; ++i) {
+    m[i] = -INFINITY;
+    l[i] = 0.0;
+    for (int64_t e = 0; e < d; ++e) o[i * d + e] = 0.0;
+  }
+  for (int64_t j0 = 0; j0 < Nk; j0 += Bc) {
+    int64_t bc = (Nk - j0 < Bc) ? Nk - j0 : Bc;
+    for (int64_t i0 = 0; i0 < N; i0 += Br) {
+      int64_t br = (N - i0 < Br) ? N - i0 : Br;
+      for (int64_t a = 0; a < br; ++a) {
+        const int64_t i = i0 + a;
+        /* S = q K^T * scale for this block row, and its block-local max */
+        double m_ij = -INFINITY;
+        for (int64_t b = 0; b < bc; ++b) {
+          double dot = 0.0;
+          for (int64_t e = 0; e < d; ++e) dot += q[i * d + e] * k[(j0 + b) * d + e];
+          S[a * Bc + b] = dot * scale;
+          if (S[a * Bc + b] > m_ij) m_ij = S[a * Bc + b];
+        }
+        /* P = exp(S - m_ij), l_ij = sum P, PV = P V_j */
+        double l_ij = 0.0;
+        for (int64_t e = 0; e < d; ++e) PV[e] = 0.0;
+        for (int64_t b = 0; b < bc; ++b) {
+          double p = exp(S[a * Bc + b] - m_ij);
+          l_ij += p;
+          for (int64_t e = 0; e < d; ++e) PV[e] += p * v[(j0 + b) * d + e];
+        }
+        double m_new, l_new;
+        oracle_merge_ml(m[i], l[i], m_ij, l_ij, &m_new, &l_new);
+        double w_old = l[i] * exp(m[i] - m_new); /* 0 on the first block */
+        double w_new = exp(m_ij - m_new);
+        for (int64_t e = 0; e < d; ++e) o[i * d + e] = (w_old * o[i * d + e] + w_new * PV[e]) / l_new;
+        m[i] = m_new;
+        l[i] = l_new;
+      }
+    }
+  }
+  free(m), free(l), free(S), free(PV);
+  return 0;
+}

@@ -1,0 +1,418 @@
+"""Pins for the CPU oracle: it must agree with something other than itself.
+
+Each test ties one oracle function to values printed on the pages
+(tests/golden/), to a closed form, to an invariant the pages state, to brute
+force on a tiny input, or to an fp64 library routine.  Chosen so that a dropped
+term, a wrong sign or index, a missing scale or a transposed operand in the
+oracle fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+import synth_inputs as si
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+NEG_INF = float("-inf")
+
+
+def golden(name):
+    with open(os.path.join(GOLD, name)) as f:
+        return json.load(f)
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Worked examples printed on the pages
+# ---------------------------------------------------------------------------
+
+def test_roadmap_worked_example_offline():
+    """Roadmap page s.3: x=[1,3,2] -> exps, sum and y as printed (4 decimals)."""
+    g = golden("roadmap_s3_worked_example.json")
+    half_ulp = 0.5 * 10 ** -g["printed_decimals"]
+    y, lse = oracle.softmax_rows(np.array([g["x"]]))
+    assert np.all(np.abs(y[0] - np.array(g["y"])) <= half_ulp)
+    total = math.exp(lse[0] - g["max"])  # the sum of exp(x - max)
+    assert abs(total - g["sum"]) <= half_ulp
+    assert np.all(np.abs(y[0] * total - np.array(g["exponents"])) <= half_ulp)
+
+
+def test_roadmap_worked_example_online_steps():
+    """Roadmap page s.3: the running (m_k, d_k) after each element, as printed."""
+    g = golden("roadmap_s3_worked_example.json")
+    half_ulp = 0.5 * 10 ** -g["printed_decimals"]
+    ms, ls = oracle.online_stats_trace(g["x"])
+    for step, m, l in zip(g["online_steps"], ms, ls):
+        assert m == step["m"]
+        assert abs(l - step["d"]) <= half_ulp
+
+
+def test_lesson_step1_stats_and_softmax():
+    """Interview lesson Step 1: [1,3,2,5] -> m = 5, l = 1.2034379904932107 (1e-6); y == torch.softmax."""
+    g = golden("lesson_step1_stats.json")
+    m, l = oracle.online_stats(g["x"])
+    assert m == g["m"]
+    assert abs(l - g["l"]) < g["l_tolerance"]
+    y, lse = oracle.softmax_rows(np.array([g["x"]]))
+    ref = torch.softmax(torch.tensor(g["x"], dtype=torch.float64), 0).numpy()
+    np.testing.assert_allclose(y[0], ref, rtol=1e-13, atol=0)
+    # the scan's (m, l) and the three-pass lse describe the same normaliser
+    assert abs((m + math.log(l)) - lse[0]) < 1e-14
+
+
+def test_offline_equals_online_suggested_example():
+    """Page 'Online softmax in attention', closing suggestion: x = [1, 5, 3] -- the
+    incremental (m, s) must match the two/three-pass result to rounding noise."""
+    x = [1.0, 5.0, 3.0]
+    m, l = oracle.online_stats(x)
+    y, lse = oracle.softmax_rows(np.array([x]))
+    assert m == 5.0
+    assert abs(m + math.log(l) - lse[0]) < 1e-15
+    # closed form of the normaliser referred to the max: 1 + e^-2 + e^-4
+    assert abs(l - (1.0 + math.exp(-2.0) + math.exp(-4.0))) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# The lesson's chunking / merge-order asserts (Step 1)
+# ---------------------------------------------------------------------------
+
+def _lesson_chunks(X):
+    widths = golden("lesson_step1_stats.json")["chunk_widths"]
+    out, c0 = [], 0
+    for w in widths:
+        out.append(X[:, c0:c0 + w])
+        c0 += w
+    assert c0 == X.shape[1]
+    return out
+
+
+def test_lesson_merge_order_invariance():
+    """Any chunking and any merge order: left fold == tree == direct logsumexp;
+    the fully masked row keeps l == 0, m == -inf, and nothing is NaN."""
+    g = golden("lesson_step1_stats.json")
+    X = si.lesson_matrix(seed=0).double().numpy()
+    assert X.shape == tuple(g["matrix_shape"])
+    chunks = _lesson_chunks(X)
+    stats = [[oracle.online_stats(c[r]) for r in range(X.shape[0])] for c in chunks]
+    ref = torch.logsumexp(torch.from_numpy(X), -1).numpy()
+    _, lse_def = oracle.softmax_rows(X)
+    for r in range(X.shape[0]):
+        m_f, l_f = stats[0][r]
+        for c in range(1, len(chunks)):
+            m_f, l_f = oracle.merge_ml(m_f, l_f, *stats[c][r])
+        a = oracle.merge_ml(*stats[0][r], *stats[1][r])
+        b = oracle.merge_ml(*stats[2][r], *stats[3][r])
+        m_t, l_t = oracle.merge_ml(*oracle.merge_ml(*a, *b), *stats[4][r])
+        assert not math.isnan(l_f) and not math.isnan(l_t)
+        assert m_t == m_f
+        assert abs(l_t - l_f) <= 1e-12 * max(1.0, l_f)
+        lse_f = m_f + math.log(l_f) if l_f > 0 else NEG_INF
+        if r == g["fully_masked_row"]:
+            assert l_f == 0.0 and m_f == NEG_INF and lse_f == NEG_INF
+            assert ref[r] == NEG_INF and lse_def[r] == NEG_INF
+        else:
+            assert abs(lse_f - ref[r]) < 1e-12
+            assert abs(lse_def[r] - ref[r]) < 1e-12
+
+
+def test_lesson_merge_on_lse_partials():
+    """The same chunks merged as (lse_c) partials by the oracle's merge (d = 0)."""
+    X = si.lesson_matrix(seed=3).double().numpy()
+    parts = np.stack([oracle.softmax_rows(c)[1] for c in _lesson_chunks(X)])
+    _, lse = oracle.lse_merge(None, parts)
+    ref = torch.logsumexp(torch.from_numpy(X), -1).numpy()
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(lse[fin], ref[fin], rtol=0, atol=1e-12)
+    # merge order does not matter
+    _, lse_rev = oracle.lse_merge(None, parts[::-1].copy())
+    np.testing.assert_allclose(lse_rev[fin], lse[fin], rtol=0, atol=1e-13)
+
+
+def test_naive_merge_is_nan_and_oracle_merge_is_not():
+    """Interview lesson: the naive merge gives NaN when both sides are -inf."""
+    m_bad = NEG_INF
+    with np.errstate(invalid="ignore"):
+        naive_l = 0.0 * np.exp(np.float64(m_bad) - max(m_bad, m_bad))
+    assert math.isnan(naive_l)
+    m, l = oracle.merge_ml(NEG_INF, 0.0, NEG_INF, 0.0)
+    assert m == NEG_INF and l == 0.0
+    m, l = oracle.merge_ml(NEG_INF, 0.0, 2.0, 3.0)  # one empty side has no weight
+    assert m == 2.0 and l == 3.0
+
+
+# ---------------------------------------------------------------------------
+# Row softmax: library routines, closed forms, special cases
+# ---------------------------------------------------------------------------
+
+def test_softmax_rows_vs_torch_fp64():
+    x, full, pre, _ = si.softmax_input(64, 301, seed=5, frac_full=0.05, frac_prefix=0.2)
+    xd = x.double()
+    y, lse = oracle.softmax_rows(x.numpy())
+    ref_lse = torch.logsumexp(xd, -1).numpy()
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse))
+    fin = np.isfinite(ref_lse)
+    np.testing.assert_allclose(lse[fin], ref_lse[fin], rtol=0, atol=1e-12)
+    ref_y = torch.softmax(xd[torch.from_numpy(fin)], -1).numpy()
+    np.testing.assert_allclose(y[fin], ref_y, rtol=1e-12, atol=1e-300)
+    # fully -inf rows: +0.0 everywhere, no NaN
+    assert np.all(y[~fin] == 0.0) and not np.any(np.signbit(y[~fin]))
+    assert len(full) > 0 and np.all(~fin[full.numpy()])
+    # -inf elements get exactly +0.0
+    assert np.all(y[np.isneginf(x.numpy())] == 0.0)
+
+
+def test_softmax_closed_forms():
+    n = 37
+    c = 2.75
+    y, lse = oracle.softmax_rows(np.full((1, n), c))
+    np.testing.assert_allclose(y[0], 1.0 / n, rtol=1e-15)
+    assert abs(lse[0] - (c + math.log(n))) < 1e-14
+    # sum to one, and invariance to a constant shift
+    x = np.random.default_rng(1).normal(size=(4, 100)) * 5
+    y, lse = oracle.softmax_rows(x)
+    np.testing.assert_allclose(y.sum(1), 1.0, rtol=1e-14)
+    y2, lse2 = oracle.softmax_rows(x + 123.0)
+    np.testing.assert_allclose(y2, y, rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(lse2, lse + 123.0, rtol=1e-15)
+    # two-element closed form
+    y, lse = oracle.softmax_rows(np.array([[0.0, math.log(3.0)]]))
+    np.testing.assert_allclose(y[0], [0.25, 0.75], rtol=1e-15)
+
+
+def test_softmax_fp32_overflow_argument():
+    """Page 'Online softmax in attention': fp32 exp(89) overflows; the safe form does not."""
+    g = golden("fp32_exp_overflow.json")
+    a = g["overflowing_argument"]
+    with np.errstate(over="ignore"):
+        assert np.isinf(np.exp(np.float32(a)))
+    y, lse = oracle.softmax_rows(np.array([[a, 0.0]], dtype=np.float32))
+    assert np.all(np.isfinite(y)) and np.isfinite(lse[0])
+    e = math.exp(-a)
+    np.testing.assert_allclose(y[0], [1.0 / (1.0 + e), e / (1.0 + e)], rtol=1e-15)
+
+
+def test_softmax_dtype_widening_is_exact():
+    x = si.randn((3, 50), seed=9, dtype=torch.bfloat16, mul=3.0)
+    y16, l16 = oracle.softmax_rows(bf16_bits(x))
+    y64, l64 = oracle.softmax_rows(x.double().numpy())
+    np.testing.assert_array_equal(y16, y64)
+    np.testing.assert_array_equal(l16, l64)
+
+
+# ---------------------------------------------------------------------------
+# Attention: SDPA in fp64, closed forms, invariants, brute force (FA-1 order)
+# ---------------------------------------------------------------------------
+
+def _sdpa_ref(q, k, v, causal, scale, kv_len=None):
+    """fp64 library reference with an explicit boolean mask, plus logsumexp of the scores."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    vis = torch.ones(B, 1, Nq, Nk, dtype=torch.bool)
+    if causal:
+        vis &= torch.ones(Nq, Nk, dtype=torch.bool).tril()
+    if kv_len is not None:
+        vis &= (torch.arange(Nk)[None, :] < torch.as_tensor(kv_len)[:, None]).view(B, 1, 1, Nk)
+    o = F.scaled_dot_product_attention(q, k, v, attn_mask=vis, scale=scale)
+    s = torch.einsum("bhid,bhjd->bhij", q, k) * scale
+    s = s.masked_fill(~vis, NEG_INF)
+    return o, torch.logsumexp(s, -1), vis
+
+
+@pytest.mark.parametrize("N,Nk,d", golden("lesson_step2_shapes.json")["cases"])
+def test_attention_vs_sdpa_lesson_shapes(N, Nk, d):
+    q, k, v = si.attn_inputs(1, 1, N, Nk, d, torch.float64, seed=N * 100 + Nk)
+    o, lse = oracle.attention(q.numpy(), k.numpy(), v.numpy())
+    ro, rl, _ = _sdpa_ref(q, k, v, False, 1 / math.sqrt(d))
+    np.testing.assert_allclose(o, ro.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, rl.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_vs_sdpa_masked(causal):
+    B, H, N, d = 3, 2, 37, 16
+    q, k, v = si.attn_inputs(B, H, N, N, d, torch.float64, seed=11)
+    kv_len = [37, 1, 20]
+    o, lse = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=causal, kv_len=kv_len)
+    ro, rl, _ = _sdpa_ref(q, k, v, causal, 1 / math.sqrt(d), kv_len)
+    np.testing.assert_allclose(o, ro.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, rl.numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_scale_and_noncausal_rectangular():
+    B, H, Nq, Nk, d = 2, 3, 5, 29, 8
+    q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=12)
+    for scale in (0.1, 1.0, 2.5):
+        o, lse = oracle.attention(q.numpy(), k.numpy(), v.numpy(), scale=scale)
+        ro, rl, _ = _sdpa_ref(q, k, v, False, scale)
+        np.testing.assert_allclose(o, ro.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse, rl.numpy(), rtol=0, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    B, H, N, d = 2, 2, 19, 8
+    q, k, v = si.attn_inputs(B, H, N, N, d, torch.float64, seed=13)
+    qn, kn, vn = q.numpy(), k.numpy(), v.numpy()
+    scale = 1 / math.sqrt(d)
+    # causal row 0 sees only key 0: O_0 = V_0, LSE_0 = scale * q_0 . k_0
+    o, lse = oracle.attention(qn, kn, vn, causal=True)
+    np.testing.assert_array_equal(o[:, :, 0], vn[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], scale * np.einsum("bhd,bhd->bh", qn[:, :, 0], kn[:, :, 0]),
+                               rtol=0, atol=1e-14)
+    # kv_len = 1: every row sees only key 0
+    o, lse = oracle.attention(qn, kn, vn, kv_len=[1, 1])
+    np.testing.assert_array_equal(o, np.broadcast_to(vn[:, :, :1], o.shape))
+    # K == 0: uniform weights over the visible keys
+    kz = np.zeros_like(kn)
+    o, lse = oracle.attention(qn, kz, vn, kv_len=[N, 7])
+    np.testing.assert_allclose(o[0], np.broadcast_to(vn[0].mean(1, keepdims=True), o[0].shape), atol=1e-14)
+    np.testing.assert_allclose(o[1], np.broadcast_to(vn[1, :, :7].mean(1, keepdims=True), o[1].shape), atol=1e-14)
+    np.testing.assert_allclose(lse[0], math.log(N), atol=1e-14)
+    np.testing.assert_allclose(lse[1], math.log(7), atol=1e-14)
+    # causal + K == 0: row i averages V_0..V_i, LSE = ln(i + 1)
+    o, lse = oracle.attention(qn, kz, vn, causal=True)
+    csum = np.cumsum(vn, axis=2) / np.arange(1, N + 1)[None, None, :, None]
+    np.testing.assert_allclose(o, csum, atol=1e-14)
+    np.testing.assert_allclose(lse, np.broadcast_to(np.log(np.arange(1, N + 1)), lse.shape), atol=1e-14)
+    # no visible key: O = +0.0, LSE = -inf, no NaN
+    o, lse = oracle.attention(qn, kn, vn, kv_len=[0, N])
+    assert np.all(o[0] == 0.0) and not np.any(np.signbit(o[0])) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(o[1]))
+
+
+def test_attention_permutation_invariance():
+    B, H, Nq, Nk, d = 1, 2, 9, 23, 8
+    q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=14)
+    perm = torch.randperm(Nk, generator=torch.Generator().manual_seed(2))
+    o1, l1 = oracle.attention(q.numpy(), k.numpy(), v.numpy())
+    o2, l2 = oracle.attention(q.numpy(), k[:, :, perm].numpy(), v[:, :, perm].numpy())
+    np.testing.assert_allclose(o2, o1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l2, l1, rtol=0, atol=1e-13)
+
+
+def test_attention_rows_subset_and_bf16_widening():
+    B, H, N, d = 2, 3, 40, 16
+    q, k, v = si.attn_inputs(B, H, N, N, d, torch.bfloat16, seed=15)
+    of, lf = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True)
+    o64, l64 = oracle.attention(q.double().numpy(), k.double().numpy(), v.double().numpy(), causal=True)
+    np.testing.assert_array_equal(of, o64)
+    np.testing.assert_array_equal(lf, l64)
+    rows = np.array([0, 5, 39, 40, 119, 200, 239])
+    o_s, l_s = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True, rows=rows)
+    np.testing.assert_array_equal(o_s, of.reshape(-1, d)[rows])
+    np.testing.assert_array_equal(l_s, lf.reshape(-1)[rows])
+
+
+def test_fa1_block_order_reaches_definition():
+    """Brute force of the lesson's V1 loop (Br=4, Bc=3) against the materialised
+    definition: the online block merge is exact up to rounding."""
+    ws = golden("lesson_step2_shapes.json")["walk_shapes"]
+    q, k, v = si.attn_inputs(1, 1, ws["N"], ws["Nk"], ws["d"], torch.float32, seed=0)
+    qd, kd, vd = (t[0, 0].double().numpy() for t in (q, k, v))
+    o_fa1 = oracle.attention_fa1(qd, kd, vd, Br=ws["Br"], Bc=ws["Bc"])
+    o_def, _ = oracle.attention(qd[None, None], kd[None, None], vd[None, None])
+    np.testing.assert_allclose(o_fa1, o_def[0, 0], rtol=0, atol=1e-12)
+    for N, Nk, d in golden("lesson_step2_shapes.json")["cases"]:
+        q, k, v = si.attn_inputs(1, 1, N, Nk, d, torch.float64, seed=7 + N)
+        for Br, Bc in ((4, 3), (1, 1), (3, 5), (64, 64)):
+            o_fa1 = oracle.attention_fa1(q[0, 0].numpy(), k[0, 0].numpy(), v[0, 0].numpy(), Br=Br, Bc=Bc)
+            o_def, _ = oracle.attention(q.numpy(), k.numpy(), v.numpy())
+            np.testing.assert_allclose(o_fa1, o_def[0, 0], rtol=0, atol=1e-12)
+
+
+def test_lesson_fa1_page_tolerance_against_sdpa():
+    """The lesson's own check, atol 1e-5, on the same shapes (float32 inputs as on the page)."""
+    g = golden("lesson_step2_shapes.json")
+    for N, Nk, d in g["cases"]:
+        q, k, v = si.attn_inputs(1, 1, N, Nk, d, torch.float32, seed=N)
+        o = oracle.attention_fa1(q[0, 0].double().numpy(), k[0, 0].double().numpy(), v[0, 0].double().numpy())
+        ref = F.scaled_dot_product_attention(q[0], k[0], v[0])[0].double().numpy()
+        assert np.max(np.abs(o - ref)) < g["atol"]
+
+
+# ---------------------------------------------------------------------------
+# Split-KV partials and their merge
+# ---------------------------------------------------------------------------
+
+def _partials(q, k, v, chunk, kv_len=None):
+    """Per-chunk oracle attention over key slices; chunks beyond kv_len are empty."""
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    S = (Nk + chunk - 1) // chunk
+    po = np.zeros((S, B * H * Nq, d))
+    pl = np.zeros((S, B * H * Nq))
+    for c in range(S):
+        j0, j1 = c * chunk, min(Nk, (c + 1) * chunk)
+        kl = None
+        if kv_len is not None:
+            kl = np.clip(np.asarray(kv_len) - j0, 0, j1 - j0)
+        o, l = oracle.attention(q, k[:, :, j0:j1], v[:, :, j0:j1], kv_len=kl)
+        po[c] = o.reshape(-1, d)
+        pl[c] = l.reshape(-1)
+    return po, pl
+
+
+def test_lse_merge_reaches_unsplit_attention():
+    B, H, Nq, Nk, d = 3, 2, 2, 50, 8
+    q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=16)
+    qn, kn, vn = q.numpy(), k.numpy(), v.numpy()
+    kv_len = [50, 9, 0]
+    po, pl = _partials(qn, kn, vn, 7, kv_len)
+    o, lse = oracle.lse_merge(po, pl)
+    ro, rl = oracle.attention(qn, kn, vn, kv_len=kv_len)
+    np.testing.assert_allclose(o, ro.reshape(-1, d), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(rl.reshape(-1)))
+    fin = np.isfinite(rl.reshape(-1))
+    np.testing.assert_allclose(lse[fin], rl.reshape(-1)[fin], rtol=0, atol=1e-12)
+    # batch 2 has no key at all: O = +0.0, LSE = -inf
+    last = slice(2 * H * Nq, 3 * H * Nq)
+    assert np.all(o[last] == 0.0) and np.all(np.isneginf(lse[last]))
+    # the merge is order-free
+    perm = np.random.default_rng(0).permutation(po.shape[0])
+    o2, l2 = oracle.lse_merge(po[perm], pl[perm])
+    np.testing.assert_allclose(o2, o, rtol=0, atol=1e-13)
+
+
+def test_lse_merge_closed_forms():
+    # two equal partials: same o, lse + ln 2
+    po = np.array([[[1.0, -2.0]], [[1.0, -2.0]]])
+    pl = np.array([[0.5], [0.5]])
+    o, lse = oracle.lse_merge(po, pl)
+    np.testing.assert_allclose(o[0], [1.0, -2.0], rtol=1e-15)
+    assert abs(lse[0] - (0.5 + math.log(2.0))) < 1e-15
+    # weights e^a/(e^a+e^b)
+    po = np.array([[[2.0]], [[-4.0]]])
+    pl = np.array([[1.0], [3.0]])
+    o, lse = oracle.lse_merge(po, pl)
+    w = 1.0 / (1.0 + math.exp(2.0))
+    assert abs(o[0, 0] - (2.0 * w - 4.0 * (1 - w))) < 1e-14
+    # an empty partial (-inf, o = 0) has no weight; all empty gives 0 and -inf
+    po = np.array([[[5.0]], [[0.0]]])
+    pl = np.array([[0.25], [NEG_INF]])
+    o, lse = oracle.lse_merge(po, pl)
+    assert o[0, 0] == 5.0 and lse[0] == 0.25
+    o, lse = oracle.lse_merge(np.zeros((3, 1, 2)), np.full((3, 1), NEG_INF))
+    assert np.all(o == 0.0) and np.isneginf(lse[0])
+
+
+def test_synth_recipes():
+    x, full, pre, lens = si.softmax_input(4096, 64, seed=0)
+    assert len(full) == 41 and len(pre) == 410
+    assert set(full.tolist()).isdisjoint(pre.tolist())
+    xn = x.numpy()
+    assert np.all(np.isneginf(xn[full.numpy()]))
+    for r, n in zip(pre.tolist()[:20], lens.tolist()[:20]):
+        assert np.all(np.isneginf(xn[r, :n])) and np.all(np.isfinite(xn[r, n:]))
+    kv = si.decode_kv_len(32, 32768, seed=0)
+    assert kv.dtype == torch.int32 and int((kv < 32768).sum()) <= 2 and int(kv.min()) >= 1
+    r = si.sample_rows(1000, 40, seed=0)
+    assert r[0] == 0 and r[-1] == 999 and 127 in r.tolist() and 128 in r.tolist()
