@@ -1,0 +1,203 @@
+/*
+ * oa.h -- C ABI of the online-softmax tiled attention library for GB300
+ * (sm_103a).  Plain pointers and sizes only; no C++ or framework types.
+ *
+ * What it computes (sources are web pages on online softmax):
+ *   - "Online Softmax -- the mathematical heart of FlashAttention"
+ *     (inference-engineering roadmap page): s.1 three-pass safe softmax,
+ *     s.2 online recurrence, s.4 tile recurrence, s.5 attention promotion,
+ *     s.7 numerics (fp32 accumulation, fully masked rows).
+ *   - "Online Softmax" (research-hub concept page), "Key math": running
+ *     (m, l, o) with rescale alpha = exp(m_old - m_new), exact result.
+ *   - "Online softmax in attention -- why and how": scores
+ *     (q . k) / sqrt(hd), causal mask t2 <= t1.
+ *   - "Online Softmax & FlashAttention -- AI infra interview lesson":
+ *     Step 1 (m, l) merge with the both-sides -inf special case and
+ *     LSE = m + log l; Step 2 normalised-output merge; Steps 3-5
+ *     (Q-outer order returning LSE, causal tile classes, split-KV decode
+ *     merged by LSE).
+ *
+ * Conventions shared by every entry point
+ *   Ownership   The caller owns every buffer.  All data pointers are DEVICE
+ *               pointers (cudaMalloc / framework allocations) unless stated.
+ *               The library allocates no device memory.
+ *   Streams     Every compute call is asynchronous on `stream` (a
+ *               cudaStream_t; NULL means the legacy default stream).  A
+ *               successful return means the work was enqueued.
+ *   Errors      Arguments are validated on the host before anything is
+ *               launched; an invalid call launches nothing and returns
+ *               OA_ERR_INVALID or OA_ERR_UNSUPPORTED.  A failed launch
+ *               returns OA_ERR_CUDA.  Kernels never trap: every wait on the
+ *               device is bounded, and a wait that expires records a code in
+ *               a device status word, after which the kernel tears down and
+ *               returns.  oa_sync_status() reports (and clears) that word.
+ *               oa_last_error() gives a one-line description of the most
+ *               recent failure on the calling thread.
+ *   Masking     -inf scores/inputs contribute exactly zero.  A row with no
+ *               visible element (all -inf, kv_len 0, or an empty split) has
+ *               output +0.0 and LSE -inf; no path produces NaN.
+ *   LSE         Natural-log log-sum-exp of the (scaled) scores of the row.
+ */
+#ifndef OA_H_
+#define OA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* oa_stream_t;
+
+typedef enum {
+  OA_OK = 0,
+  OA_ERR_INVALID = 1,     /* bad pointer, size, stride or alignment */
+  OA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+  OA_ERR_CUDA = 3,        /* a CUDA runtime/driver call or launch failed */
+  OA_ERR_TIMEOUT = 4      /* a bounded device wait expired (see oa_sync_status) */
+} oa_status;
+
+typedef enum { OA_F32 = 0, OA_BF16 = 1 } oa_dtype;
+
+/* Static text for a status code. */
+const char* oa_status_string(int status);
+
+/* One-line description of the last failure on the calling thread ("" if none). */
+const char* oa_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int oa_version(void);
+
+/*
+ * Row softmax with per-row log-sum-exp.
+ *   y[r, j] = exp(x[r, j] - m_r) / l_r,  lse[r] = m_r + ln l_r,
+ *   m_r = max_j x[r, j],  l_r = sum_j exp(x[r, j] - m_r),
+ * computed in one read of x: per-thread running (m, l) (roadmap page s.2),
+ * merged across threads, warps and the CTAs of a cluster with the (m, l)
+ * merge (interview lesson Step 1).  Rows wider than the on-chip capacity
+ * (65536 fp32) are streamed twice instead of once.
+ *   x      fp32 [rows, cols], row stride ld_x elements (ld_x >= cols).
+ *   y      fp32 [rows, cols], row stride ld_y (ld_y >= cols), or NULL for
+ *          statistics only.  y may be x itself (same pointer and stride);
+ *          any other overlap is undefined.
+ *   lse    fp32 [rows], or NULL.  y and lse may not both be NULL.
+ * A fully -inf row gives y = +0.0 and lse = -inf.  Inputs must be finite
+ * or -inf (+inf and NaN are outside the contract).
+ * Errors: OA_ERR_INVALID for NULL x, rows or cols < 1, a stride < cols or
+ * both outputs NULL.
+ */
+oa_status oa_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y,
+                          int64_t ld_y, float* lse, oa_stream_t stream);
+
+/*
+ * Fused attention forward, O = softmax(Q K^T * scale) V, with per-row LSE,
+ * never writing the Nq x Nk score matrix to memory (roadmap page s.5;
+ * interview lesson Step 3: Q-outer loop, one normalisation at the end,
+ * LSE returned; Step 4: causal tiles skipped, fully visible or masked).
+ *   q      [B, H, Nq, d], k and v [B, H, Nk, d], o [B, H, Nq, d]: all of
+ *          dtype dt, contiguous row-major, 16-byte aligned.
+ *   lse    fp32 [B, H, Nq], or NULL.
+ *   causal 0 or 1.  Key j is visible to query i iff j <= i; needs Nq == Nk.
+ *   scale  multiplies q . k before the softmax (callers normally pass
+ *          1/sqrt(d)).  Must be finite and > 0.
+ *   kv_len NULL, or a device int32 [B]: keys j >= kv_len[b] are masked
+ *          (values are clamped to [0, Nk]).
+ * bf16: tcgen05 tensor-core kernel, fp32 accumulation, bf16 O; d must be
+ * 64 or 128 (else OA_ERR_UNSUPPORTED).  fp32: SIMT kernel in fp32,
+ * 1 <= d <= 256.
+ * Errors: OA_ERR_INVALID for NULL q/k/v/o, sizes < 1 (B, H, Nq, Nk, d),
+ * misalignment or a bad scale; OA_ERR_UNSUPPORTED for causal with
+ * Nq != Nk or an unsupported (dtype, d).
+ */
+oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,
+                      int B, int H, int Nq, int Nk, int d, int causal, float scale,
+                      const int32_t* kv_len, oa_stream_t stream);
+
+/*
+ * The fp32 SIMT attention forward with explicit tile sizes: Br query rows
+ * per CTA and Bc keys per step of the online recurrence (1 <= Br, Bc <= 64).
+ * Same contract as oa_attn_fwd with dt = OA_F32; the result does not
+ * depend on the tiles beyond rounding.  Follows the lesson's worked shapes
+ * (Br = 4, Bc = 3) when asked to.
+ */
+oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, float* o,
+                                float* lse, int B, int H, int Nq, int Nk, int d, int causal,
+                                float scale, const int32_t* kv_len, int Br, int Bc,
+                                oa_stream_t stream);
+
+/*
+ * Bytes of workspace oa_attn_splitkv needs: num_splits * B*H*Nq * (d + 1)
+ * fp32 values (normalised partial outputs, then their LSEs), rounded up to
+ * 256 bytes.  0 for invalid sizes.
+ */
+size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * Split-KV attention (decode style; interview lesson Step 5): the keys of
+ * each row are cut into num_splits chunks of ceil(Nk / num_splits); one
+ * CTA per (row, chunk) runs the online recurrence over its chunk and writes
+ * the chunk's normalised output O_c and lse_c (an empty chunk writes
+ * O_c = 0, lse_c = -inf); a second kernel merges the partials with the LSE
+ * merge of oa_lse_merge.  Non-causal.
+ *   q [B, H, Nq, d], k and v [B, H, Nk, d], o [B, H, Nq, d]: dtype dt,
+ *   contiguous, 16-byte aligned.  lse fp32 [B, H, Nq] or NULL.
+ *   kv_len NULL or device int32 [B] (clamped to [0, Nk]).
+ *   workspace: device, >= oa_splitkv_workspace_bytes(...) bytes, 16-byte
+ *   aligned; the caller owns it and must not touch it until the call's
+ *   work has completed on `stream`.
+ * Supported: bf16 with d in {8, 16, 32, 64, 128, 256}; fp32 with d in
+ * {4, 8, 16, 32, 64, 128}; 1 <= num_splits <= 1024.
+ * Errors: OA_ERR_INVALID (NULL, sizes, alignment, workspace too small),
+ * OA_ERR_UNSUPPORTED (dtype/d).
+ */
+oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                          oa_dtype dt, int B, int H, int Nq, int Nk, int d, float scale,
+                          const int32_t* kv_len, int num_splits, void* workspace,
+                          size_t workspace_bytes, oa_stream_t stream);
+
+/*
+ * Merge of S split partials per row (interview lesson Step 1 merge and
+ * Step 2 normalised-output rule; log-sum-exp form):
+ *   L = max_c lse_c,  w_c = exp(lse_c - L),  W = sum_c w_c,
+ *   lse = L + ln W,   o = sum_c (w_c / W) o_c,
+ * with o = +0.0 and lse = -inf when every lse_c is -inf.
+ *   part_o   fp32 [S, R, d] normalised partial outputs, or NULL iff d == 0.
+ *   part_lse fp32 [S, R].
+ *   o        [R, d] of dtype o_dt (fp32 or bf16), or NULL iff d == 0.
+ *   lse      fp32 [R], or NULL (then d must be > 0).
+ * Alignment: part_o and o 16-byte aligned when d % 4 == 0 (vector path);
+ * any 4-byte alignment otherwise.  1 <= S <= 65535, R >= 1, 0 <= d <= 1024.
+ */
+oa_status oa_lse_merge(const float* part_o, const float* part_lse, int S, int64_t R, int d,
+                       void* o, oa_dtype o_dt, float* lse, oa_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the device status word that
+ * kernels set when a bounded wait expires.  Returns OA_OK, OA_ERR_TIMEOUT
+ * (with the code of the expired wait in oa_last_error()) or OA_ERR_CUDA if
+ * the synchronisation itself failed.
+ */
+oa_status oa_sync_status(oa_stream_t stream);
+
+/*
+ * Upper bound, in nanoseconds, on any single device-side wait (default
+ * 2e9).  Applies to launches made after the call.  0 restores the default.
+ */
+void oa_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Self-test of the failure path: launches one warp that waits, with the
+ * library's bounded wait, on an mbarrier that nothing ever arrives on.  The
+ * wait gives up after `limit_ns` nanoseconds and records a timeout in the
+ * status word; oa_sync_status() then returns OA_ERR_TIMEOUT and the context
+ * stays usable.  limit_ns must be in [1e3, 1e10].
+ */
+oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OA_H_ */

@@ -1,0 +1,269 @@
+"""Python binding of the online-softmax tiled attention library for GB300.
+
+A thin ctypes layer over ``liboa.so`` (the C ABI in ``include/oa.h``): it
+allocates output tensors with PyTorch, passes device pointers, sizes and the
+current CUDA stream, and turns status codes into exceptions.  Every step of
+the computation runs in the library's CUDA kernels; there is no CPU or
+PyTorch fallback -- if the library is missing or cannot load, calls raise.
+
+Entry points (same names as the C ABI, without the ``oa_`` prefix):
+  softmax_rows, attn_fwd, attn_fwd_f32_tiles, attn_splitkv,
+  splitkv_workspace_bytes, lse_merge, sync_status, set_wait_limit_ns,
+  selftest_wait_timeout.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "liboa.so")
+
+OA_OK, OA_ERR_INVALID, OA_ERR_UNSUPPORTED, OA_ERR_CUDA, OA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+OA_F32, OA_BF16 = 0, 1
+
+EXPORTS = (
+    "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd",
+    "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv", "oa_lse_merge",
+    "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
+)
+
+
+class OAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _status_name(s):
+    return {0: "OA_OK", 1: "OA_ERR_INVALID", 2: "OA_ERR_UNSUPPORTED", 3: "OA_ERR_CUDA",
+            4: "OA_ERR_TIMEOUT"}.get(s, f"status {s}")
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load liboa.so (building it with nvcc first if it is absent).  Raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            if not build_if_missing:
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH}")
+            from ._build import build
+
+            build()
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i64, i32, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                      ctypes.c_uint64, ctypes.c_size_t)
+        sig = {
+            "oa_status_string": ([i32], ctypes.c_char_p),
+            "oa_last_error": ([], ctypes.c_char_p),
+            "oa_version": ([], i32),
+            "oa_softmax_rows": ([vp, i64, i64, i64, vp, i64, vp, vp], i32),
+            "oa_attn_fwd": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp], i32),
+            "oa_attn_fwd_f32_tiles": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, i32, vp],
+                                      i32),
+            "oa_splitkv_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
+            "oa_attn_splitkv": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp], i32),
+            "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
+            "oa_sync_status": ([vp], i32),
+            "oa_set_wait_limit_ns": ([u64], None),
+            "oa_selftest_wait_timeout": ([u64, vp], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != OA_OK:
+        msg = load().oa_last_error().decode(errors="replace")
+        raise OAError(status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return OA_F32
+    if dt == torch.bfloat16:
+        return OA_BF16
+    raise OAError(OA_ERR_UNSUPPORTED, f"dtype {dt} (need float32 or bfloat16)")
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise OAError(OA_ERR_INVALID, "tensors must live on a CUDA device")
+
+
+def version() -> int:
+    return load().oa_version()
+
+
+def softmax_rows(x: torch.Tensor, y: torch.Tensor | None = None, lse: torch.Tensor | None = None,
+                 want_y: bool = True, want_lse: bool = True):
+    """Row softmax of a 2-D fp32 tensor (unit column stride; any row stride) and per-row LSE.
+
+    Returns (y, lse); either is None when not requested.
+    """
+    _require_cuda(x, y, lse)
+    if x.dim() != 2 or x.dtype != torch.float32 or x.stride(1) != 1:
+        raise OAError(OA_ERR_INVALID, "x must be a 2-D float32 tensor with unit column stride")
+    rows, cols = x.shape
+    if want_y and y is None:
+        y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
+    if want_lse and lse is None:
+        lse = torch.empty(rows, dtype=torch.float32, device=x.device)
+    if y is not None and (y.shape != x.shape or y.stride(1) != 1 or y.dtype != torch.float32):
+        raise OAError(OA_ERR_INVALID, "y must match x's shape with unit column stride")
+    with torch.cuda.device(x.device):
+        _check(load().oa_softmax_rows(_ptr(x), rows, cols, x.stride(0), _ptr(y), y.stride(0) if y is not None else 0,
+                                      _ptr(lse), _stream(x.device)))
+    return y, lse
+
+
+def _attn_shapes(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise OAError(OA_ERR_INVALID, "q, k, v must be [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
+        raise OAError(OA_ERR_INVALID, "k and v must be [B, H, Nk, d] matching q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise OAError(OA_ERR_INVALID, "q, k, v must share a dtype")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise OAError(OA_ERR_INVALID, "q, k, v must be contiguous")
+    return B, H, Nq, Nk, d
+
+
+def _kv_len_arg(kv_len, B, device):
+    if kv_len is None:
+        return None
+    if kv_len.dtype != torch.int32 or kv_len.shape != (B,) or not kv_len.is_cuda or kv_len.device != device:
+        raise OAError(OA_ERR_INVALID, "kv_len must be an int32 CUDA tensor of shape [B] on q's device")
+    return kv_len.contiguous()
+
+
+def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None, out=None, lse=None,
+             want_lse: bool = True):
+    """O = softmax(Q K^T * scale) V with per-row LSE; q/k/v [B,H,N,d] bf16 or fp32 on CUDA."""
+    _require_cuda(q, k, v, out, lse)
+    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kv = _kv_len_arg(kv_len, B, q.device)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H, Nq,
+                                  Nk, d, int(bool(causal)), float(scale), _ptr(kv), _stream(q.device)))
+    return out, lse
+
+
+def attn_fwd_f32_tiles(q, k, v, Br: int, Bc: int, causal: bool = False, scale: float | None = None, kv_len=None,
+                       out=None, lse=None):
+    """fp32 attention forward with explicit tile sizes (Br query rows, Bc keys per step)."""
+    _require_cuda(q, k, v, out, lse)
+    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    if q.dtype != torch.float32:
+        raise OAError(OA_ERR_INVALID, "attn_fwd_f32_tiles needs float32 inputs")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kv = _kv_len_arg(kv_len, B, q.device)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_fwd_f32_tiles(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, Nq, Nk, d,
+                                            int(bool(causal)), float(scale), _ptr(kv), int(Br), int(Bc),
+                                            _stream(q.device)))
+    return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(load().oa_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
+
+
+def attn_splitkv(q, k, v, num_splits: int, scale: float | None = None, kv_len=None, out=None, lse=None,
+                 workspace=None):
+    """Split-KV attention: per-chunk partials, then the LSE merge.  workspace: optional uint8 CUDA tensor."""
+    _require_cuda(q, k, v, out, lse, workspace)
+    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kv = _kv_len_arg(kv_len, B, q.device)
+    need = splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H,
+                                      Nq, Nk, d, float(scale), _ptr(kv), int(num_splits), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(q.device)))
+    return out, lse
+
+
+def lse_merge(part_o, part_lse, out_dtype=torch.float32, out=None, lse=None):
+    """Merge S partials: part_o fp32 [S, R, d] (or None for d = 0), part_lse fp32 [S, R]."""
+    _require_cuda(part_o, part_lse, out, lse)
+    if part_lse.dim() != 2 or part_lse.dtype != torch.float32 or not part_lse.is_contiguous():
+        raise OAError(OA_ERR_INVALID, "part_lse must be a contiguous float32 [S, R] tensor")
+    S, R = part_lse.shape
+    d = 0
+    if part_o is not None:
+        if part_o.dim() != 3 or tuple(part_o.shape[:2]) != (S, R) or part_o.dtype != torch.float32 or \
+                not part_o.is_contiguous():
+            raise OAError(OA_ERR_INVALID, "part_o must be a contiguous float32 [S, R, d] tensor")
+        d = part_o.shape[2]
+    if d > 0 and out is None:
+        out = torch.empty((R, d), dtype=out_dtype, device=part_lse.device)
+    if lse is None:
+        lse = torch.empty(R, dtype=torch.float32, device=part_lse.device)
+    code = _dtype_code(out.dtype if out is not None else out_dtype)
+    with torch.cuda.device(part_lse.device):
+        _check(load().oa_lse_merge(_ptr(part_o), _ptr(part_lse), S, R, d, _ptr(out), code, _ptr(lse),
+                                   _stream(part_lse.device)))
+    return out, lse
+
+
+def sync_status(device=None):
+    """Synchronise the current stream and raise OAError if a device wait expired."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(load().oa_sync_status(_stream(dev)))
+
+
+def set_wait_limit_ns(ns: int):
+    load().oa_set_wait_limit_ns(int(ns))
+
+
+def selftest_wait_timeout(limit_ns: int = 1_000_000, device=None):
+    """Launch a wait that nothing satisfies; it must give up after limit_ns (see oa.h)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check(load().oa_selftest_wait_timeout(int(limit_ns), _stream(dev)))

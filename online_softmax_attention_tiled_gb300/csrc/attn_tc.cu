@@ -1,0 +1,463 @@
+// attn_tc.cu -- fused attention forward on the 5th-generation tensor cores
+// (tcgen05, tensor memory) for bf16 inputs, fp32 accumulation, d = 64 / 128.
+//
+// Method: the attention promotion of the online softmax (roadmap page s.5;
+// research-hub page "Key math"): per query row a running max m, running
+// denominator l and unnormalised output o; for each key/value tile
+//   m_new = max(m_old, rowmax(S)), alpha = exp(m_old - m_new),
+//   P = exp(S - m_new), l = alpha l + rowsum(P), o = alpha o + P V,
+// and o / l, LSE = m + ln l once at the end.  The loop order is Q-outer
+// (interview lesson Step 3): one CTA owns 256 query rows of one (b, h) and
+// streams the key/value tiles past them; the score tile never leaves the
+// chip.  Causal tiles above the diagonal are never loaded or computed; only
+// the diagonal tile and the ragged key tail are masked (Step 4).
+//
+// GB300 mapping (one CTA per SM, 320 threads):
+//   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
+//               row t, i.e. TMEM lane t, so row max / sum are thread-local
+//   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
+//   warp 8      TMA producer: Q once, then K and V tiles into 2-4 stage
+//               shared-memory rings (128-byte swizzle), mbarrier complete_tx
+//   warp 9      MMA issuer (one thread): S_i = Q_i K^T (SMEM x SMEM -> TMEM)
+//               and O_i += P_i V (P from TMEM, V from SMEM -> TMEM); owns the
+//               TMEM allocation
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+d), O_1 [256+d, 256+2d).  P_i (bf16, two per column) is
+// written over the first 64 columns of S_i; the next S_i is issued after
+// the PV MMA that reads P_i, and tcgen05 MMAs of one thread run in order.
+// MMA issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
+// each softmax group works while the tensor core runs the other group's
+// MMAs.
+//
+// Every mbarrier wait is bounded (oa_common.cuh); a wait that expires sets
+// the CTA abort flag, every role falls through to the teardown, in-flight
+// TMA loads and MMAs are drained (bounded), and TMEM is always freed.
+#include "oa_internal.h"
+
+namespace oa {
+namespace {
+
+constexpr int BM = 128;  // rows per query tile (= TMEM lanes)
+constexpr int BN = 128;  // keys per key/value tile
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct Cfg {
+  static constexpr int SLABS = D / 64;               // 128-byte swizzle atoms along d
+  static constexpr int SLAB_BYTES = BM * 128;        // 128 rows x 128 bytes
+  static constexpr int TILE_BYTES = SLABS * SLAB_BYTES;
+  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  static constexpr int Q_OFF = 0;
+  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
+  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
+  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NUM_BARS = 1 + 4 * STAGES + 6 + 1;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
+  __host__ __device__ static constexpr uint32_t o_col(int i) { return 256u + (uint32_t)(i * D); }
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);  // Q K^T, both K-major
+  static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);    // P V, V is MN-major
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct TcParams {
+  __nv_bfloat16* o;
+  float* lse;
+  const int32_t* kv_len;
+  int H, Nq, Nk, causal, num_qblocks, BH;
+  float scale_log2;
+  DevStatus st;
+};
+
+enum WaitSite : unsigned {
+  W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_s + pad;
+
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  auto bar_q = [&]() { return bar0; };
+  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
+  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
+  auto bar_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * C::STAGES + s); };
+  auto bar_vempty = [&](int s) { return bar0 + 8u * (1 + 3 * C::STAGES + s); };
+  auto bar_sfull = [&](int i) { return bar0 + 8u * (1 + 4 * C::STAGES + i); };
+  auto bar_pfull = [&](int i) { return bar0 + 8u * (3 + 4 * C::STAGES + i); };
+  auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 4 * C::STAGES + i); };
+  const uint32_t bar_drain = bar0 + 8u * (7 + 4 * C::STAGES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work assignment: last (heaviest, for causal) query blocks first ----
+  const int qb = p.num_qblocks - 1 - (int)(blockIdx.x / p.BH);
+  const int bh = (int)(blockIdx.x % p.BH);
+  const int b = bh / p.H;
+  const int q0 = qb * 2 * BM;
+  int kvl = p.Nk;
+  if (p.kv_len != nullptr) kvl = min(max(p.kv_len[b], 0), p.Nk);
+  const int nk_tiles = (kvl + BN - 1) / BN;
+  int n_kv[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = q0 + i * BM;
+    n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
+    if (r0 >= p.Nq) n_kv[i] = 0;  // query tile entirely past the end
+  }
+  const int n_all = max(n_kv[0], n_kv[1]);
+
+  // ---- set-up: barriers, TMEM ----
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q(), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar_kfull(s), 1);
+      mbar_init(bar_kempty(s), 1);
+      mbar_init(bar_vfull(s), 1);
+      mbar_init(bar_vempty(s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_sfull(i), 1);
+      mbar_init(bar_pfull(i), 4);  // one arrival per softmax warp
+      mbar_init(bar_odone(i), 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == kProducerWarp) {
+    // =================== TMA producer ===================
+    if (lane == 0) {
+      int issued_k = 0, issued_v = 0;
+      if (n_all > 0) {
+        mbar_arrive_expect_tx(bar_q(), 2 * C::TILE_BYTES);
+        for (int i = 0; i < 2; ++i)
+          for (int s = 0; s < C::SLABS; ++s)
+            tma_load_3d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q(), s * 64,
+                        q0 + i * BM, bh);
+      }
+      for (int j = 0; j < n_all; ++j) {
+        const int st = j % C::STAGES;
+        const uint32_t ph = (uint32_t)(j / C::STAGES) & 1u;
+        if (!mbar_wait(bar_kempty(st), ph ^ 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_KEMPTY)) break;
+        mbar_arrive_expect_tx(bar_kfull(st), C::TILE_BYTES);
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d(sbase + C::K_OFF + st * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_k, bar_kfull(st), s * 64,
+                      j * BN, bh);
+        ++issued_k;
+        if (!mbar_wait(bar_vempty(st), ph ^ 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_VEMPTY)) break;
+        mbar_arrive_expect_tx(bar_vfull(st), C::TILE_BYTES);
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d(sbase + C::V_OFF + st * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_v, bar_vfull(st), s * 64,
+                      j * BN, bh);
+        ++issued_v;
+      }
+      // drain: every load issued must have landed before the CTA can exit
+      DevStatus quiet = p.st;
+      for (int j = max(0, issued_k - C::STAGES); j < issued_k; ++j)
+        mbar_wait(bar_kfull(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, quiet, nullptr,
+                  (K_ATTN_TC << 8) | W_DRAIN);
+      for (int j = max(0, issued_v - C::STAGES); j < issued_v; ++j)
+        mbar_wait(bar_vfull(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, quiet, nullptr,
+                  (K_ATTN_TC << 8) | W_DRAIN);
+      if (n_all > 0) mbar_wait(bar_q(), 0, quiet, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    }
+  } else if (warp == kMmaWarp) {
+    // =================== MMA issuer ===================
+    if (lane == 0 && n_all > 0) {
+      const uint32_t q_s = sbase + C::Q_OFF;
+      auto issue_s = [&](int i, int st) {
+        const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
+        const uint32_t a0 = q_s + i * C::TILE_BYTES;
+        const uint32_t b0 = sbase + C::K_OFF + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * C::SLAB_BYTES + (kk % 4) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024), C::IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int i, int st, bool accumulate) {
+        const uint32_t d_tmem = tmem_base + C::o_col(i);
+        const uint32_t a_tmem = tmem_base + (uint32_t)(i * BN);  // P_i over S_i's first 64 columns
+        const uint32_t b0 = sbase + C::V_OFF + st * C::TILE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b0 + kk * 2048, C::SLAB_BYTES, 1024), C::IDESC_O,
+                 (accumulate || kk > 0) ? 1u : 0u);
+      };
+      bool ok = mbar_wait(bar_q(), 0, p.st, abort_flag, (K_ATTN_TC << 8) | W_Q);
+      if (ok) ok = mbar_wait(bar_kfull(0), 0, p.st, abort_flag, (K_ATTN_TC << 8) | W_KFULL);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int i = 0; i < 2; ++i)
+          if (n_kv[i] > 0) {
+            issue_s(i, 0);
+            mma_commit(bar_sfull(i));
+          }
+        mma_commit(bar_kempty(0));
+      }
+      for (int j = 0; ok && j < n_all; ++j) {
+        const int st = j % C::STAGES;
+        const uint32_t ph = (uint32_t)(j / C::STAGES) & 1u;
+        const int st1 = (j + 1) % C::STAGES;
+        const uint32_t ph1 = (uint32_t)((j + 1) / C::STAGES) & 1u;
+        bool k_next_ready = false;
+        if (!(ok = mbar_wait(bar_vfull(st), ph, p.st, abort_flag, (K_ATTN_TC << 8) | W_VFULL))) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j >= n_kv[i]) continue;
+          if (!(ok = mbar_wait(bar_pfull(i), (uint32_t)j & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_PFULL)))
+            break;
+          tc_fence_after_sync();
+          issue_pv(i, st, j > 0);
+          mma_commit(bar_odone(i));
+          if (j + 1 < n_kv[i]) {
+            if (!k_next_ready) {
+              if (!(ok = mbar_wait(bar_kfull(st1), ph1, p.st, abort_flag, (K_ATTN_TC << 8) | W_KFULL))) break;
+              tc_fence_after_sync();
+              k_next_ready = true;
+            }
+            issue_s(i, st1);
+            mma_commit(bar_sfull(i));
+          }
+        }
+        if (!ok) break;
+        mma_commit(bar_vempty(st));
+        if (k_next_ready) mma_commit(bar_kempty(st1));
+      }
+    }
+    if (lane == 0) {
+      // drain: all MMAs issued by this thread complete before TMEM is freed
+      mma_commit(bar_drain);
+      DevStatus quiet = p.st;
+      mbar_wait(bar_drain, 0, quiet, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    }
+  } else {
+    // =================== softmax groups ===================
+    const int i = warp >> 2;                 // query tile of this group
+    const int tt = threadIdx.x & 127;        // row within the tile = TMEM lane
+    const int r0 = q0 + i * BM;
+    const int row = r0 + tt;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_addr = tmem_base + lane_base + (uint32_t)(i * BN);
+    const uint32_t o_addr = tmem_base + lane_base + C::o_col(i);
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;  // running max of the scaled scores, log2 units
+    float l = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < n_kv[i]; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull(i), (uint32_t)j & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_SFULL));
+      if (!ok) break;
+      tc_fence_after_sync();
+      uint32_t sr[128];
+      tmem_ld64(s_addr, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
+      tmem_ld64(s_addr + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      const int col0 = j * BN;
+      if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const int col = col0 + c;
+          if (col >= kvl || (p.causal && col > row)) s[c] = -INFINITY;
+        }
+      }
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+      for (int c = 4; c < 128; c += 4) {
+        mx0 = fmaxf(mx0, s[c]);
+        mx1 = fmaxf(mx1, s[c + 1]);
+        mx2 = fmaxf(mx2, s[c + 2]);
+        mx3 = fmaxf(mx3, s[c + 3]);
+      }
+      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
+      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(m - ref);
+      float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(s[64 * h + 2 * c], sl2, -ref));
+          const float p1 = ex2(fmaf(s[64 * h + 2 * c + 1], sl2, -ref));
+          sum0 += p0;
+          sum1 += p1;
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(s_addr + 32 * h, pk);
+      }
+      l = alpha * l + (sum0 + sum1);
+      m = m_new;
+      if (j > 0) {
+        // O_i must hold PV_i(j-1) before it is rescaled
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_ODONE));
+        if (!ok) break;
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + c, orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            tmem_st32(o_addr + c, orr);
+          }
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_pfull(i));
+    }
+
+    // ---- epilogue: O / l, LSE ----
+    const bool have_o = ok && n_kv[i] > 0;
+    if (have_o)
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(n_kv[i] - 1) & 1u, p.st, abort_flag,
+                                             (K_ATTN_TC << 8) | W_ODONE));
+    if (ok) {
+      tc_fence_after_sync();
+      const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = p.o + ((int64_t)bh * p.Nq + row) * D;
+#pragma unroll 1
+      for (int c = 0; c < D; c += 32) {
+        uint32_t orr[32];
+        if (have_o) {
+          tmem_ld32(o_addr + c, orr);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) orr[e] = 0u;
+        }
+        uint4 pk[4];
+        uint32_t* w = reinterpret_cast<uint32_t*>(pk);
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l, __uint_as_float(orr[2 * e + 1]) * inv_l);
+        if (row < p.Nq) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c);
+          dst[0] = pk[0];
+          dst[1] = pk[1];
+          dst[2] = pk[2];
+          dst[3] = pk[3];
+        }
+      }
+      if (p.lse != nullptr && row < p.Nq)
+        p.lse[(int64_t)bh * p.Nq + row] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); box 64 x 128 x 1
+// with the 128-byte swizzle; rows past N read as zero.
+bool make_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
+                     cudaStream_t s) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const unsigned grid = (unsigned)p.num_qblocks * (unsigned)p.BH;
+  attn_fwd_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                           int Nk, int d, int causal, float scale, const int32_t* kv_len, const DevStatus& st,
+                           cudaStream_t s, const char** why) {
+  const int BH = B * H;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, q, d, Nq, BH) || !make_map(&mk, k, d, Nk, BH) || !make_map(&mv, v, d, Nk, BH)) {
+    if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
+    return cudaErrorInvalidValue;
+  }
+  TcParams p;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.lse = lse;
+  p.kv_len = kv_len;
+  p.H = H;
+  p.Nq = Nq;
+  p.Nk = Nk;
+  p.causal = causal;
+  p.num_qblocks = (Nq + 2 * BM - 1) / (2 * BM);
+  p.BH = BH;
+  p.scale_log2 = scale * kLog2e;
+  p.st = st;
+  return d == 128 ? launch_d<128>(mq, mk, mv, p, s) : launch_d<64>(mq, mk, mv, p, s);
+}
+
+}  // namespace oa

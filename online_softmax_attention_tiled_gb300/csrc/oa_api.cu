@@ -1,0 +1,256 @@
+// oa_api.cu -- the C ABI declared in include/oa.h: host-side validation,
+// dispatch to the kernels, the device status word and the wait-limit
+// self-test.  Nothing here computes results; every step of the path runs in
+// the kernels of this directory.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "oa.h"
+#include "oa_internal.h"
+
+namespace {
+
+// Status word written by kernels when a bounded wait expires (site code).
+__device__ unsigned int g_status_word;
+
+thread_local char g_last_error[512] = "";
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+constexpr unsigned long long kDefaultLimitNs = 2000000000ull;
+
+oa_status fail(oa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+oa_status ok() {
+  g_last_error[0] = '\0';
+  return OA_OK;
+}
+
+oa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(OA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+// Device address of the status word for the current device; looked up once
+// per device with that device current.
+bool status_word(unsigned int** out) {
+  constexpr int kMaxDev = 64;
+  static unsigned int* cache[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return false;
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return false;
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = cache[dev];
+  return true;
+}
+
+bool dev_status(oa::DevStatus* st) {
+  if (!status_word(&st->word)) return false;
+  st->limit_ns = g_wait_limit_ns.load();
+  return true;
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+constexpr int64_t kMaxGrid = 2147483647;
+
+__global__ void selftest_wait_kernel(oa::DevStatus st) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  const uint32_t b = oa::smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    oa::mbar_init(b, 1);
+    abort_flag = 0;
+    oa::fence_barrier_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on `bar`: the wait must give up after st.limit_ns
+  if (threadIdx.x == 0)
+    oa::mbar_wait(b, 0, st, reinterpret_cast<volatile int*>(&abort_flag), (oa::K_SELFTEST << 8) | 1);
+  __syncthreads();
+}
+
+}  // namespace
+
+namespace oa {
+cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s) {
+  selftest_wait_kernel<<<1, 32, 0, s>>>(st);
+  return cudaGetLastError();
+}
+}  // namespace oa
+
+extern "C" {
+
+const char* oa_status_string(int status) {
+  switch (status) {
+    case OA_OK: return "OA_OK";
+    case OA_ERR_INVALID: return "OA_ERR_INVALID: invalid argument";
+    case OA_ERR_UNSUPPORTED: return "OA_ERR_UNSUPPORTED: not supported by this build";
+    case OA_ERR_CUDA: return "OA_ERR_CUDA: CUDA call failed";
+    case OA_ERR_TIMEOUT: return "OA_ERR_TIMEOUT: a bounded device wait expired";
+    default: return "unknown oa_status";
+  }
+}
+
+const char* oa_last_error(void) { return g_last_error; }
+
+int oa_version(void) { return 100; }
+
+void oa_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns == 0 ? kDefaultLimitNs : ns); }
+
+oa_status oa_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
+                          float* lse, oa_stream_t stream) {
+  if (x == nullptr) return fail(OA_ERR_INVALID, "softmax_rows: x is NULL");
+  if (rows < 1 || cols < 1) return fail(OA_ERR_INVALID, "softmax_rows: rows and cols must be >= 1");
+  if (ld_x < cols) return fail(OA_ERR_INVALID, "softmax_rows: ld_x < cols");
+  if (y == nullptr && lse == nullptr) return fail(OA_ERR_INVALID, "softmax_rows: y and lse both NULL");
+  if (y != nullptr && ld_y < cols) return fail(OA_ERR_INVALID, "softmax_rows: ld_y < cols");
+  if (!aligned(x, 4) || !aligned(y, 4) || !aligned(lse, 4))
+    return fail(OA_ERR_INVALID, "softmax_rows: pointers must be 4-byte aligned");
+  if (y != nullptr && static_cast<const void*>(y) == static_cast<const void*>(x) && ld_y != ld_x)
+    return fail(OA_ERR_INVALID, "softmax_rows: in-place needs ld_y == ld_x");
+  if (rows > kMaxGrid / 8) return fail(OA_ERR_INVALID, "softmax_rows: too many rows");
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "softmax_rows: no current CUDA device");
+  cudaError_t e = oa::launch_softmax_rows(x, rows, cols, ld_x, y, ld_y, lse, st, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "softmax_rows launch");
+}
+
+static oa_status check_attn(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
+                            int Nk, int d, int causal, float scale, const char* who) {
+  if (!q || !k || !v || !o) return fail(OA_ERR_INVALID, "%s: q, k, v and o must be non-NULL", who);
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1) return fail(OA_ERR_INVALID, "%s: sizes must be >= 1", who);
+  if (!(std::isfinite(scale) && scale > 0.f)) return fail(OA_ERR_INVALID, "%s: scale must be finite and > 0", who);
+  if (causal != 0 && causal != 1) return fail(OA_ERR_INVALID, "%s: causal must be 0 or 1", who);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return fail(OA_ERR_INVALID, "%s: q/k/v/o must be 16-byte aligned, lse 4-byte", who);
+  if ((int64_t)B * H > (int64_t)1 << 30) return fail(OA_ERR_INVALID, "%s: B*H too large", who);
+  return OA_OK;
+}
+
+oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
+                      int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, oa_stream_t stream) {
+  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, "attn_fwd");
+  if (s != OA_OK) return s;
+  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "attn_fwd: causal needs Nq == Nk");
+  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_fwd: kv_len must be 4-byte aligned");
+  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "attn_fwd: unknown dtype %d", (int)dt);
+  if (dt == OA_BF16 && d != 64 && d != 128)
+    return fail(OA_ERR_UNSUPPORTED, "attn_fwd: bf16 supports d = 64 or 128 (got %d)", d);
+  if (dt == OA_F32 && d > 256) return fail(OA_ERR_UNSUPPORTED, "attn_fwd: fp32 supports d <= 256 (got %d)", d);
+  const int64_t grid = (int64_t)B * H * (dt == OA_BF16 ? (Nq + 255) / 256 : (Nq + 15) / 16);
+  if (grid > kMaxGrid) return fail(OA_ERR_INVALID, "attn_fwd: grid too large");
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "attn_fwd: no current CUDA device");
+  if (dt == OA_BF16) {
+    const char* why = nullptr;
+    cudaError_t e = oa::launch_attn_tc(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, kv_len, st,
+                                       (cudaStream_t)stream, &why);
+    if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "attn_fwd: %s", why) : cuda_fail(e, "attn_fwd launch");
+    return ok();
+  }
+  {
+    cudaError_t e = oa::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                        static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, Nq, Nk, d,
+                                        causal, scale, kv_len, 0, 0, (cudaStream_t)stream);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd launch");
+  }
+}
+
+oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
+                                int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, int Br,
+                                int Bc, oa_stream_t stream) {
+  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, "attn_fwd_f32_tiles");
+  if (s != OA_OK) return s;
+  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: causal needs Nq == Nk");
+  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: kv_len must be 4-byte aligned");
+  if (d > 256) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: d <= 256");
+  if (Br < 1 || Br > 64 || Bc < 1 || Bc > 64) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: 1 <= Br, Bc <= 64");
+  const size_t smem = sizeof(float) * ((size_t)2 * Br * d + (size_t)2 * Bc * d + (size_t)Br * Bc + 3 * (size_t)Br);
+  if (smem > 227 * 1024) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: tiles need %zu bytes of smem", smem);
+  if ((int64_t)B * H * ((Nq + Br - 1) / Br) > kMaxGrid) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: grid");
+  cudaError_t e =
+      oa::launch_attn_f32(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, kv_len, Br, Bc, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd_f32_tiles launch");
+}
+
+size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1) return 0;
+  const size_t floats = (size_t)num_splits * (size_t)B * H * Nq * ((size_t)d + 1);
+  return (floats * sizeof(float) + 255) / 256 * 256;
+}
+
+oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                          int H, int Nq, int Nk, int d, float scale, const int32_t* kv_len, int num_splits,
+                          void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, 0, scale, "attn_splitkv");
+  if (s != OA_OK) return s;
+  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "attn_splitkv: unknown dtype %d", (int)dt);
+  if (!oa::splitkv_supported(dt == OA_BF16, d))
+    return fail(OA_ERR_UNSUPPORTED, "attn_splitkv: unsupported (dtype %d, d %d)", (int)dt, d);
+  if (num_splits < 1 || num_splits > 1024) return fail(OA_ERR_INVALID, "attn_splitkv: 1 <= num_splits <= 1024");
+  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_splitkv: kv_len must be 4-byte aligned");
+  const int64_t R = (int64_t)B * H * Nq;
+  if (R * num_splits > kMaxGrid) return fail(OA_ERR_INVALID, "attn_splitkv: rows * num_splits too large");
+  const size_t need = oa_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
+    return fail(OA_ERR_INVALID, "attn_splitkv: workspace must be 16-byte aligned and >= %zu bytes", need);
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = part_o + (size_t)num_splits * R * d;
+  cudaError_t e = oa::launch_splitkv_partial(q, k, v, dt == OA_BF16, B, H, Nq, Nk, d, scale, kv_len, num_splits,
+                                             part_o, part_lse, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_splitkv partial launch");
+  e = oa::launch_lse_merge(part_o, part_lse, num_splits, R, d, o, dt == OA_BF16, lse, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "attn_splitkv merge launch");
+}
+
+oa_status oa_lse_merge(const float* part_o, const float* part_lse, int S, int64_t R, int d, void* o, oa_dtype o_dt,
+                       float* lse, oa_stream_t stream) {
+  if (part_lse == nullptr) return fail(OA_ERR_INVALID, "lse_merge: part_lse is NULL");
+  if (S < 1 || S > 65535 || R < 1 || d < 0 || d > 1024)
+    return fail(OA_ERR_INVALID, "lse_merge: need 1 <= S <= 65535, R >= 1, 0 <= d <= 1024");
+  if (d > 0 && (part_o == nullptr || o == nullptr))
+    return fail(OA_ERR_INVALID, "lse_merge: part_o and o are required when d > 0");
+  if (d == 0 && lse == nullptr) return fail(OA_ERR_INVALID, "lse_merge: nothing to compute (d == 0, lse NULL)");
+  if (o_dt != OA_F32 && o_dt != OA_BF16) return fail(OA_ERR_INVALID, "lse_merge: unknown dtype %d", (int)o_dt);
+  if (!aligned(part_o, 4) || !aligned(part_lse, 4) || !aligned(lse, 4) || !aligned(o, o_dt == OA_BF16 ? 2 : 4))
+    return fail(OA_ERR_INVALID, "lse_merge: misaligned pointer");
+  if ((R + 7) / 8 > kMaxGrid) return fail(OA_ERR_INVALID, "lse_merge: R too large");
+  cudaError_t e = oa::launch_lse_merge(part_o, part_lse, S, R, d, d > 0 ? o : nullptr, o_dt == OA_BF16, lse,
+                                       (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "lse_merge launch");
+}
+
+oa_status oa_sync_status(oa_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "sync_status: stream synchronize");
+  unsigned int word = 0;
+  e = cudaMemcpyFromSymbol(&word, g_status_word, sizeof word);
+  if (e != cudaSuccess) return cuda_fail(e, "sync_status: read status word");
+  if (word == 0) return ok();
+  const unsigned int zero = 0;
+  e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
+  if (e != cudaSuccess) return cuda_fail(e, "sync_status: clear status word");
+  return fail(OA_ERR_TIMEOUT, "device wait expired: kernel %u, wait site %u", word >> 8, word & 0xFFu);
+}
+
+oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream) {
+  if (limit_ns < 1000ull || limit_ns > 10000000000ull)
+    return fail(OA_ERR_INVALID, "selftest_wait_timeout: limit_ns must be in [1e3, 1e10]");
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "selftest_wait_timeout: no current CUDA device");
+  st.limit_ns = limit_ns;
+  cudaError_t e = oa::launch_selftest_wait(st, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "selftest_wait_timeout launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,37 @@
+// oa_internal.h -- launchers implemented by each kernel translation unit
+// and called by the C ABI layer (oa_api.cu).  Arguments have already been
+// validated there; launchers only pick a configuration and launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "oa_common.cuh"
+
+namespace oa {
+
+cudaError_t launch_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y,
+                                int64_t ld_y, float* lse, const DevStatus& st, cudaStream_t s);
+
+cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int S, int64_t R, int d, void* o,
+                             bool o_bf16, float* lse, cudaStream_t s);
+
+cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
+                            int H, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                            int Br, int Bc, cudaStream_t s);
+
+// True if (bf16, d) / (fp32, d) has a split-KV partial kernel.
+bool splitkv_supported(bool bf16, int d);
+cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, bool bf16, int B, int H,
+                                   int Nq, int Nk, int d, float scale, const int32_t* kv_len,
+                                   int num_splits, float* part_o, float* part_lse, cudaStream_t s);
+
+// Tensor-core attention (tcgen05 + TMA), bf16, d in {64, 128}.  `why` gets
+// a static message when the host-side set-up (tensor maps) fails.
+cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                           int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                           const DevStatus& st, cudaStream_t s, const char** why);
+
+cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s);
+
+}  // namespace oa

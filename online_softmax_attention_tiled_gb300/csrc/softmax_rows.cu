@@ -1,0 +1,272 @@
+// softmax_rows.cu -- bandwidth-bound row softmax with per-row log-sum-exp.
+//
+// One read of x per element when the row fits on chip (the common case):
+//   1. each thread keeps its E elements in registers and forms its own
+//      (m, l): m = max, l = sum exp(x - m)  (tile recurrence of the
+//      roadmap page s.4, with the thread's elements as the tile);
+//   2. the (m, l) pairs are merged with warp shuffles, then across the
+//      CTA's warps, then across the CTAs of a thread-block cluster through
+//      distributed shared memory (interview lesson Step 1: the merge is
+//      associative and commutative, so any tree works);
+//   3. y = exp(x - m) / l is written from the registers.
+// Loads and stores are 128-bit and coalesced when the rows are 16-byte
+// aligned.  Rows wider than the cluster's register capacity stream their
+// slice twice (statistics pass, then output pass).
+// A row whose elements are all -inf has l = 0: it writes y = +0.0 and
+// lse = -inf without forming -inf - -inf anywhere.
+#include <cooperative_groups.h>
+
+#include "oa_internal.h"
+
+namespace oa {
+namespace {
+
+constexpr int kMaxThreads = 256;
+
+struct ML {
+  float m, l;
+};
+
+// (m, l) merge with 0 as the reference when both maxima are -inf.
+__device__ __forceinline__ ML ml_merge(ML a, ML b) {
+  const float m = fmaxf(a.m, b.m);
+  const float ref = (m == -INFINITY) ? 0.f : m;
+  return {m, a.l * expf(a.m - ref) + b.l * expf(b.m - ref)};
+}
+
+__device__ __forceinline__ ML warp_merge(ML v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ML o{__shfl_xor_sync(0xffffffffu, v.m, off), __shfl_xor_sync(0xffffffffu, v.l, off)};
+    v = ml_merge(v, o);
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+// Loads the E elements this thread owns in the piece starting at column
+// `base` (relative to the row), -inf outside [.., end).  VEC: groups of four
+// consecutive columns, group g at base + (g*T + t)*4.  Scalar: column
+// base + i*T + t.
+template <int E, bool VEC, bool STREAM>
+__device__ __forceinline__ void load_piece(const float* __restrict__ xr, int64_t base, int64_t end, float (&v)[E]) {
+  const int T = blockDim.x, t = threadIdx.x;
+  if constexpr (VEC) {
+#pragma unroll
+    for (int g = 0; g < E / 4; ++g) {
+      const int64_t c = base + ((int64_t)g * T + t) * 4;
+      if (c + 3 < end) {
+        const float4 f = STREAM ? __ldcs(reinterpret_cast<const float4*>(xr + c))
+                                : __ldg(reinterpret_cast<const float4*>(xr + c));
+        v[4 * g] = f.x, v[4 * g + 1] = f.y, v[4 * g + 2] = f.z, v[4 * g + 3] = f.w;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[4 * g + e] = (c + e < end) ? xr[c + e] : -INFINITY;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int64_t c = base + (int64_t)i * T + t;
+      v[i] = (c < end) ? (STREAM ? __ldcs(xr + c) : __ldg(xr + c)) : -INFINITY;
+    }
+  }
+}
+
+template <int E>
+__device__ __forceinline__ ML thread_stats(const float (&v)[E]) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < E; ++i) m = fmaxf(m, v[i]);
+  if (m == -INFINITY) return {m, 0.f};
+  float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    l0 += ex2((v[i] - m) * kLog2e);
+    if (i + 1 < E) l1 += ex2((v[i + 1] - m) * kLog2e);
+  }
+  return {m, l0 + l1};
+}
+
+// exp(x - m) / l with the rounding error of x - m carried to first order:
+// s + err == x - m exactly (two-sum), exp(x - m) ~= exp(s) * (1 + err).
+__device__ __forceinline__ float softmax_value(float x, float m, float inv_l) {
+  if (x == -INFINITY) return 0.f;
+  const float s = x - m;
+  const float bb = s - x;
+  const float err = (x - (s - bb)) + (-m - bb);
+  const float e = expf(s);
+  return fmaf(e, err, e) * inv_l;
+}
+
+template <int E, bool VEC>
+__device__ __forceinline__ void store_piece(float* __restrict__ yr, int64_t base, int64_t end, const float (&v)[E],
+                                            float m, float inv_l) {
+  const int T = blockDim.x, t = threadIdx.x;
+  if constexpr (VEC) {
+#pragma unroll
+    for (int g = 0; g < E / 4; ++g) {
+      const int64_t c = base + ((int64_t)g * T + t) * 4;
+      if (c + 3 < end) {
+        float4 f;
+        f.x = softmax_value(v[4 * g], m, inv_l);
+        f.y = softmax_value(v[4 * g + 1], m, inv_l);
+        f.z = softmax_value(v[4 * g + 2], m, inv_l);
+        f.w = softmax_value(v[4 * g + 3], m, inv_l);
+        __stcs(reinterpret_cast<float4*>(yr + c), f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (c + e < end) yr[c + e] = softmax_value(v[4 * g + e], m, inv_l);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      const int64_t c = base + (int64_t)i * T + t;
+      if (c < end) __stcs(yr + c, softmax_value(v[i], m, inv_l));
+    }
+  }
+}
+
+// grid.x = rows * cluster; the `cluster` CTAs of a row split its columns into
+// slices of `slice` columns (a multiple of 4).
+template <int E, bool VEC>
+__global__ void __launch_bounds__(kMaxThreads) softmax_rows_kernel(const float* __restrict__ x, int64_t cols,
+                                                                    int64_t ld_x, float* __restrict__ y,
+                                                                    int64_t ld_y, float* __restrict__ lse,
+                                                                    int cluster, int64_t slice) {
+  __shared__ ML warp_ml[kMaxThreads / 32];
+  __shared__ ML cta_ml;  // this CTA's merged statistics (read by peers)
+  __shared__ ML row_ml;  // statistics of the whole row
+
+  const int T = blockDim.x, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t rank = (cluster > 1) ? cluster_rank() : 0u;
+  const int64_t row = blockIdx.x / cluster;
+  const float* xr = x + row * ld_x;
+  const int64_t c0 = (int64_t)rank * slice;
+  const int64_t c1 = (c0 + slice < cols) ? c0 + slice : cols;
+  const int64_t piece = (int64_t)T * E;
+  const bool resident = (c1 - c0) <= piece;
+
+  float v[E];
+  ML st{-INFINITY, 0.f};
+  if (resident) {
+    load_piece<E, VEC, true>(xr, c0, c1, v);
+    st = thread_stats<E>(v);
+  } else {
+    for (int64_t b = c0; b < c1; b += piece) {
+      load_piece<E, VEC, false>(xr, b, c1, v);
+      st = ml_merge(st, thread_stats<E>(v));
+    }
+  }
+
+  // warps -> CTA
+  st = warp_merge(st);
+  if (lane == 0) warp_ml[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    ML w = (lane < T / 32) ? warp_ml[lane] : ML{-INFINITY, 0.f};
+    w = warp_merge(w);
+    if (lane == 0) cta_ml = w;
+  }
+  __syncthreads();
+
+  // CTAs of the cluster -> row (every CTA merges the slices in rank order,
+  // so all of them hold bit-identical statistics)
+  if (cluster > 1) {
+    cluster_barrier();
+    if (t == 0) {
+      const uint32_t a = smem_addr(&cta_ml);
+      ML tot{-INFINITY, 0.f};
+      for (int r = 0; r < cluster; ++r) tot = ml_merge(tot, ML{ld_dsmem_f32(a, r), ld_dsmem_f32(a + 4, r)});
+      row_ml = tot;
+    }
+  } else if (t == 0) {
+    row_ml = cta_ml;
+  }
+  __syncthreads();
+  const ML rs = row_ml;
+
+  if (lse != nullptr && rank == 0 && t == 0) lse[row] = (rs.l > 0.f) ? rs.m + logf(rs.l) : -INFINITY;
+
+  if (y != nullptr) {
+    const float inv_l = (rs.l > 0.f) ? 1.f / rs.l : 0.f;
+    float* yr = y + row * ld_y;
+    if (resident) {
+      store_piece<E, VEC>(yr, c0, c1, v, rs.m, inv_l);
+    } else {
+      for (int64_t b = c0; b < c1; b += piece) {
+        load_piece<E, VEC, false>(xr, b, c1, v);
+        store_piece<E, VEC>(yr, b, c1, v, rs.m, inv_l);
+      }
+    }
+  }
+  // keep this CTA's shared memory alive until every peer has read it
+  if (cluster > 1) cluster_barrier();
+}
+
+template <int E, bool VEC>
+cudaError_t launch_cfg(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
+                       float* lse, int threads, int cluster, int64_t slice, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(rows * cluster), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  if (cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, softmax_rows_kernel<E, VEC>, x, cols, ld_x, y, ld_y, lse, cluster, slice);
+}
+
+template <bool VEC>
+cudaError_t launch_vec(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
+                       float* lse, cudaStream_t s) {
+  // Register capacity of one CTA: 256 threads x 32 fp32.  Up to 8 CTAs
+  // (a portable cluster) share a row; beyond that each CTA streams.
+  constexpr int64_t kCtaCap = (int64_t)kMaxThreads * 32;
+  if (cols <= 1024) {
+    const int threads = (int)(((cols + 3) / 4 + 31) / 32 * 32);
+    return launch_cfg<4, VEC>(x, rows, cols, ld_x, y, ld_y, lse, threads, 1, (cols + 3) / 4 * 4, s);
+  }
+  if (cols <= 2048) return launch_cfg<8, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
+  if (cols <= 4096) return launch_cfg<16, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
+  int cluster = (int)((cols + kCtaCap - 1) / kCtaCap);
+  if (cluster > 8) cluster = 8;
+  const int64_t slice = ((cols + cluster - 1) / cluster + 3) / 4 * 4;
+  return launch_cfg<32, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, s);
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y,
+                                int64_t ld_y, float* lse, const DevStatus& /*st*/, cudaStream_t s) {
+  const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld_x % 4 == 0) &&
+                   (y == nullptr || ((reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ld_y % 4 == 0)));
+  return vec ? launch_vec<true>(x, rows, cols, ld_x, y, ld_y, lse, s)
+             : launch_vec<false>(x, rows, cols, ld_x, y, ld_y, lse, s);
+}
+
+}  // namespace oa

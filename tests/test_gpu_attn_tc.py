@@ -1,0 +1,95 @@
+"""bf16 tensor-core attention kernel (tcgen05 / TMEM / TMA) vs the fp64 oracle (gpu)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from parity import BF16_O_ATOL, assert_lse_close, assert_out_close, bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(oa, q, k, v, causal=False, kv_len=None, scale=None):
+    kvd = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int32).cuda()
+    o, lse = oa.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, kv_len=kvd, scale=scale)
+    torch.cuda.synchronize()
+    oa.sync_status()
+    return o, lse
+
+
+def _check(oa, q, k, v, causal=False, kv_len=None, scale=None):
+    o, lse = _run(oa, q, k, v, causal, kv_len, scale)
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=causal, kv_len=kv_len,
+                              scale=scale)
+    assert_lse_close(lse, rl)
+    return assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_tile(cuda_lib, d):
+    q, k, v = si.attn_inputs(1, 1, 128, 128, d, torch.bfloat16, seed=d)
+    _check(cuda_lib, q, k, v)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [1, 77, 128, 129, 256, 300, 640])
+def test_square_ragged(cuda_lib, d, causal, N):
+    q, k, v = si.attn_inputs(2, 3, N, N, d, torch.bfloat16, seed=N * 7 + d)
+    _check(cuda_lib, q, k, v, causal=causal)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq,Nk", [(200, 333), (513, 64), (1, 1000), (256, 1)])
+def test_rectangular_noncausal(cuda_lib, d, Nq, Nk):
+    q, k, v = si.attn_inputs(2, 2, Nq, Nk, d, torch.bfloat16, seed=Nq + Nk)
+    _check(cuda_lib, q, k, v)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_len_masks(cuda_lib, d, causal):
+    N = 384
+    q, k, v = si.attn_inputs(4, 2, N, N, d, torch.bfloat16, seed=11)
+    _check(cuda_lib, q, k, v, causal=causal, kv_len=[N, 1, 0, 200])
+
+
+def test_scale_and_large_scores(cuda_lib):
+    q, k, v = si.attn_inputs(1, 2, 300, 300, 128, torch.bfloat16, seed=12)
+    _check(cuda_lib, q, k, v, scale=1.0)  # scores ~N(0, 128): exercises large max shifts
+    _check(cuda_lib, q, k, v, scale=0.01)
+
+
+def test_causal_row0_closed_form(cuda_lib):
+    q, k, v = si.attn_inputs(1, 4, 256, 256, 128, torch.bfloat16, seed=13)
+    o, lse = _run(cuda_lib, q, k, v, causal=True)
+    assert torch.allclose(o[:, :, 0].float().cpu(), v[:, :, 0].float(), atol=1e-2)
+    ref = (q[:, :, 0].double() * k[:, :, 0].double()).sum(-1) / math.sqrt(128)
+    assert torch.allclose(lse[:, :, 0].double().cpu(), ref, atol=1e-4)
+
+
+def _sampled_full_size(oa, B, H, N, d, causal, seed, per_head):
+    q, k, v = si.attn_inputs(B, H, N, N, d, torch.bfloat16, seed=seed)
+    o, lse = _run(oa, q, k, v, causal=causal)
+    local = si.sample_rows(N, per_head, seed=seed)
+    rows = (torch.arange(B * H)[:, None] * N + local[None, :]).reshape(-1).numpy()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=causal, rows=rows)
+    og = o.reshape(-1, d)[torch.from_numpy(rows).cuda()]
+    lg = lse.reshape(-1)[torch.from_numpy(rows).cuda()]
+    assert_lse_close(lg, rl)
+    err = assert_out_close(og, ro, BF16_O_ATOL)
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    return err
+
+
+@pytest.mark.slow
+def test_full_size_noncausal_b4_h16_n4096_d64(cuda_lib):
+    _sampled_full_size(cuda_lib, 4, 16, 4096, 64, False, seed=0, per_head=96)
+
+
+@pytest.mark.slow
+def test_full_size_causal_b1_h32_n8192_d128(cuda_lib):
+    _sampled_full_size(cuda_lib, 1, 32, 8192, 128, True, seed=0, per_head=160)
