@@ -1,0 +1,502 @@
+"""Benchmark of the online-softmax tiled attention library on GB300.
+
+Prints ONE JSON line (rank 0).  The headline workload is the fused causal
+attention forward, bf16, B=1 H=32 N=8192 d=128 (one "step" = one forward
+over that batch); the row softmax + LSE on fp32 [4096, 32768] (the metric's
+second half), the non-causal B4 H16 N4096 d64 forward and the split-KV
+decode B32 H32 Nk32768 d128 are measured in the same run and reported under
+"components", each against its own roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--components/--no-components] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle (the only reference this method has:
+the pages carry no implementation) on a bounded sample of the same workload.
+For N > 1 (torchrun) every rank runs its own replica of the workload on its
+own GPU (independent batches, no collective on the data path); timing is the
+max over ranks and "value" counts the work of all ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd TFLOP/s (bf16, causal N=8192 d=128) & % tensor peak; softmax GB/s % HBM"
+WORKLOAD = "causal attention fwd bf16 B=1 H=32 Nq=Nk=8192 d=128 scale=1/sqrt(128)"
+B, H, N, D = 1, 32, 8192, 128
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------
+# work accounting (algorithmic, per launch)
+# --------------------------------------------------------------------------
+def causal_attn_flops(b, h, n, d):
+    """4*d FLOPs (QK^T and PV) per visible (query, key) pair; n(n+1)/2 pairs per head."""
+    return 4.0 * b * h * d * n * (n + 1) / 2
+
+
+def dense_attn_flops(b, h, nq, nk, d):
+    return 4.0 * b * h * nq * nk * d
+
+
+def softmax_bytes(rows, cols):
+    """Read X once, write Y and LSE (fp32)."""
+    return 4.0 * rows * cols * 2 + 4.0 * rows
+
+
+def decode_bytes(b, h, d, kv_len_sum, esize=2):
+    """q, the visible K and V rows, O and LSE."""
+    return esize * (2.0 * h * d * kv_len_sum + b * h * d * 2) + 4.0 * b * h
+
+
+# --------------------------------------------------------------------------
+# environment helpers
+# --------------------------------------------------------------------------
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_digest():
+    h = hashlib.sha256()
+    for f in ("attn_tc.cu", "oa_common.cuh"):
+        with open(os.path.join(ROOT, "online_softmax_attention_tiled_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """dram bytes per launch of the attention kernel from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    p = os.path.join(ROOT, "profiles", "attn_fwd_tc_causal_b1h32n8192d128.md")
+    try:
+        text = open(p).read()
+    except OSError:
+        return None
+    m_src = re.search(r"kernel_source_digest:\s*([0-9a-f]+)", text)
+    m_b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_b or m_src.group(1) != kernel_source_digest():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 50 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 <= r[0] <= t1] or sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
+        reasons = set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in inside:
+            for name, val in zip(names, r[3][1:]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (weak scaling: every rank runs its own replica)
+# --------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float across the process group (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------
+# GPU timing helpers
+# --------------------------------------------------------------------------
+def time_launches(fn, steps, warmup, flush=None):
+    """Run fn() warmup times, then `steps` times with CUDA events around each launch on the
+    current stream; returns per-launch milliseconds.  flush() (outside the events) evicts L2."""
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return times
+
+
+def components(oa, dev, peaks, peak_kind, steps):
+    """Each hot-path kernel other than the headline one, timed alone (L2 flushed between launches)."""
+    import torch
+
+    import synth_inputs as si
+
+    out = {}
+    flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_buf.fill_(1.0)
+
+    # row softmax + LSE, fp32 [4096, 32768]
+    x, *_ = si.softmax_input(4096, 32768, seed=0)
+    x = x.to(dev)
+    y = torch.empty_like(x)
+    lse = torch.empty(4096, dtype=torch.float32, device=dev)
+    t = time_launches(lambda: oa.softmax_rows(x, y=y, lse=lse), steps, 3, flush)
+    ms = statistics.mean(t)
+    gbs = softmax_bytes(4096, 32768) / (ms * 1e-3) / 1e9
+    out["softmax_rows"] = {"workload": "row softmax + LSE fp32 [4096, 32768], N(0,1)*4, 1% rows -inf, 10% -inf prefix",
+                           "ms": ms, "value": gbs, "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
+                           "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                           "algorithmic_bytes": softmax_bytes(4096, 32768)}
+    del x, y, lse
+    # non-causal attention B4 H16 N4096 d64
+    q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((4, 16, 4096), dtype=torch.float32, device=dev)
+    t = time_launches(lambda: oa.attn_fwd(q, k, v, out=o, lse=lse), steps, 3, flush)
+    ms = statistics.mean(t)
+    tf = dense_attn_flops(4, 16, 4096, 4096, 64) / (ms * 1e-3) / 1e12
+    out["attn_noncausal_d64"] = {"workload": "non-causal attention fwd bf16 B=4 H=16 N=4096 d=64", "ms": ms,
+                                 "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
+                                 "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind}
+    del q, k, v, o, lse
+    # split-KV decode B32 H32 Nk32768 d128, 64 chunks of 512, 5% of sequences truncated
+    q, k, v = si.attn_inputs(32, 32, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+    kv_len = si.decode_kv_len(32, 32768, seed=0)
+    kvd = kv_len.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((32, 32, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(oa.splitkv_workspace_bytes(32, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+    t = time_launches(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws), steps, 3, None)
+    ms = statistics.mean(t)
+    nbytes = decode_bytes(32, 32, 128, int(kv_len.sum()))
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["attn_splitkv_decode"] = {"workload": "split-KV decode bf16 B=32 H=32 Nq=1 Nk=32768 d=128, 64 chunks of 512, "
+                                              "5% of sequences truncated (inputs 17 GB > L2)", "ms": ms, "value": gbs,
+                                  "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
+                                  "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                                  "algorithmic_bytes": nbytes, "launches_per_call": 2}
+    del q, k, v, o, lse, ws, flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the headline workload)
+# --------------------------------------------------------------------------
+def oracle_sample(budget_s=12.0, seed=0):
+    """Times the fp64 oracle on randomly sampled rows of the causal workload, growing the
+    sample until it runs for a few seconds.  Returns (TFLOP/s, threads, description)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth_inputs as si
+
+    q, k, v = si.attn_inputs(B, H, N, N, D, torch.bfloat16, seed=seed)
+    bits = [t.contiguous().view(torch.int16).numpy().view(np.uint16) for t in (q, k, v)]
+    threads = os.cpu_count() or 1
+    g = torch.Generator().manual_seed(seed + 99)
+    nrows = 256
+    spent = 0.0
+    while True:
+        rows = torch.randint(0, B * H * N, (nrows,), generator=g).numpy()
+        i = rows % N
+        flops = float(np.sum(4.0 * D * (i + 1)))
+        t0 = time.perf_counter()
+        oracle.attention(*bits, causal=True, rows=rows, nthreads=threads)
+        dt = time.perf_counter() - t0
+        spent += dt
+        if dt >= budget_s / 3 or spent >= budget_s or nrows >= 1 << 22:
+            break
+        nrows *= 4
+    desc = (f"{nrows} random query rows of the causal B1 H32 N8192 d128 workload, "
+            f"{flops / 1e9:.2f} GFLOP, {dt:.2f} s, {threads} threads")
+    return flops / dt / 1e12, threads, desc
+
+
+# --------------------------------------------------------------------------
+# main
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--components", dest="components", action="store_true", default=True)
+    ap.add_argument("--no-components", dest="components", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_env()
+    if world != args.gpus:
+        if world > 1 or args.gpus > 1:
+            ap.error(f"--gpus {args.gpus} but WORLD_SIZE={world}; launch N>1 with torchrun")
+
+    if args.impl == "reference":
+        return main_reference(args, world, rank)
+
+    import torch
+
+    import online_softmax_attention_tiled_gb300 as oa
+    import synth_inputs as si
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    oa.load()
+    peaks, peak_kind = load_peaks()
+
+    q, k, v = si.attn_inputs(B, H, N, N, D, torch.bfloat16, seed=rank)
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    oa.sync_status()
+
+    # ---- timed region: K steps, one event pair per launch on the launching stream ----
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        start.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier(world)
+    oa.sync_status()
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), world, dev)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    launch_ms = statistics.mean(per_launch)
+    flops = causal_attn_flops(B, H, N, D)
+    value = world * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
+    achieved = flops / (launch_ms * 1e-3) / 1e12
+    clock_summary = clocks.summary(t_wall0, t_wall1)
+
+    # ---- end to end through the public API: pinned host in, pinned host out ----
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world, dev) / e2e_steps
+    oa.sync_status()
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh))
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    del qh, kh, vh, oh, lh
+
+    comps = None
+    if args.components and rank == 0:
+        del q, k, v, o, lse
+        torch.cuda.empty_cache()
+        comps = components(oa, dev, peaks, peak_kind, max(5, min(args.steps, 20)))
+
+    cpu = None
+    if args.cpu_baseline and rank == 0 and world == 1:
+        tf, threads, desc = oracle_sample()
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    barrier(world)
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": elapsed_ms / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1) Q/K/V cast to bf16 (no dataset is named)",
+            "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": True,
+                       "per_gpu_batch": "one (B=1, H=32) batch per rank",
+                       "l2": "inputs larger than L2 (Q+K+V+O = 256 MiB > 129 MB); no flush in the timed loop",
+                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": achieved / peaks["bf16_tflops"], "traffic": profiled_traffic(),
+                         "peak_kind": f"{peak_kind} bf16 dense burst", "launch_ms": launch_ms,
+                         "algorithmic_flops_per_launch": flops},
+            "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clock_summary,
+            "cpu_baseline": cpu,
+            "components": comps,
+            "kernel_source_digest": kernel_source_digest(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+def main_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle, each step a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import numpy as np
+    import torch
+
+    import oracle
+    import synth_inputs as si
+
+    q, k, v = si.attn_inputs(B, H, N, N, D, torch.bfloat16, seed=0)
+    bits = [t.contiguous().view(torch.int16).numpy().view(np.uint16) for t in (q, k, v)]
+    threads = os.cpu_count() or 1
+    g = torch.Generator().manual_seed(7)
+    rows_per_step = 512
+
+    def step():
+        rows = torch.randint(0, B * H * N, (rows_per_step,), generator=g).numpy()
+        oracle.attention(*bits, causal=True, rows=rows, nthreads=threads)
+        return float(np.sum(4.0 * D * (rows % N + 1)))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    flops = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    desc = f"each step: {rows_per_step} random query rows of the causal workload ({threads} threads, fp64)"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": True},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+if __name__ == "__main__":
+    main()

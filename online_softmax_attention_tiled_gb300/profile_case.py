@@ -1,0 +1,76 @@
+"""Runs one kernel case a few times on cuda:0, for use under a profiler.
+
+  python -m online_softmax_attention_tiled_gb300.profile_case CASE [--reps R] [--batch B]
+
+Cases (inputs seeded as in the benchmark):
+  attn_causal      causal attention fwd bf16, B=1 H=32 N=8192 d=128 (~256 MiB on the device)
+  attn_noncausal   non-causal attention fwd bf16, B=4 H=16 N=4096 d=64
+  softmax          row softmax + LSE fp32 [4096, 32768] (1 GiB)
+  decode           split-KV decode bf16, B (default 4) x H=32, Nk=32768, d=128, 64 chunks
+                   (--batch 32 is the full 17 GB benchmark shape)
+Prints the mean CUDA-event time per launch.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import online_softmax_attention_tiled_gb300 as oa  # noqa: E402
+import synth_inputs as si  # noqa: E402
+
+
+def make_case(name, dev, batch):
+    if name == "attn_causal":
+        q, k, v = si.attn_inputs(1, 32, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
+        o, lse = torch.empty_like(q), torch.empty((1, 32, 8192), device=dev)
+        return lambda: oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
+    if name == "attn_noncausal":
+        q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
+        o, lse = torch.empty_like(q), torch.empty((4, 16, 4096), device=dev)
+        return lambda: oa.attn_fwd(q, k, v, out=o, lse=lse)
+    if name == "softmax":
+        x, *_ = si.softmax_input(4096, 32768, seed=0)
+        x = x.to(dev)
+        y, lse = torch.empty_like(x), torch.empty(4096, device=dev)
+        return lambda: oa.softmax_rows(x, y=y, lse=lse)
+    if name == "decode":
+        q, k, v = si.attn_inputs(batch, 32, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+        kv = si.decode_kv_len(batch, 32768, seed=0).to(dev)
+        o, lse = torch.empty_like(q), torch.empty((batch, 32, 1), device=dev)
+        ws = torch.empty(oa.splitkv_workspace_bytes(batch, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+        return lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kv, out=o, lse=lse, workspace=ws)
+    raise SystemExit(f"unknown case {name}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--reps", type=int, default=5)
+    ap.add_argument("--batch", type=int, default=4)
+    a = ap.parse_args()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fn = make_case(a.case, dev, a.batch)
+    fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(a.reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    oa.sync_status()
+    print(f"{a.case}: {sum(times) / len(times):.4f} ms per launch over {a.reps} launches")
+
+
+if __name__ == "__main__":
+    main()
