@@ -158,6 +158,29 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
                           size_t workspace_bytes, oa_stream_t stream);
 
 /*
+ * Split-KV attention that allocates nothing -- a library addition with no
+ * counterpart on the source pages.  Same arguments, result and support
+ * matrix as oa_attn_splitkv, minus the workspace: the partials live in one
+ * 16 MiB scratch array built into the library (held on every GPU that
+ * loads the library, until the process exits).  For callers that cannot
+ * allocate device memory when they call -- code inside a host application
+ * that owns all device memory through its own allocator, or a
+ * latency-critical path where an allocation could block or fail.
+ *   Limit: num_splits * B*H*Nq * (d + 1) * 4 bytes <= 16 MiB; larger
+ *          requests return OA_ERR_INVALID and launch nothing.
+ *   Set-up: the first call on a device looks up the array's device address
+ *          (cudaGetSymbolAddress) with that device current; make that first
+ *          call before any stream capture.
+ *   Sharing: every call uses the same array.  Calls whose work overlaps on
+ *          the GPU (other streams, other host threads) race on it; the
+ *          caller must serialise them.  Nothing in the array needs to start
+ *          at zero: each call writes every partial it reads.
+ */
+oa_status oa_attn_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 oa_dtype dt, int B, int H, int Nq, int Nk, int d, float scale,
+                                 const int32_t* kv_len, int num_splits, oa_stream_t stream);
+
+/*
  * Merge of S split partials per row (interview lesson Step 1 merge and
  * Step 2 normalised-output rule; log-sum-exp form):
  *   L = max_c lse_c,  w_c = exp(lse_c - L),  W = sum_c w_c,

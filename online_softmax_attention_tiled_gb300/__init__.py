@@ -8,7 +8,7 @@ PyTorch fallback -- if the library is missing or cannot load, calls raise.
 
 Entry points (same names as the C ABI, without the ``oa_`` prefix):
   softmax_rows, attn_fwd, attn_fwd_f32_tiles, attn_splitkv,
-  splitkv_workspace_bytes, lse_merge, sync_status, set_wait_limit_ns,
+  splitkv_workspace_bytes, attn_splitkv_static, lse_merge, sync_status, set_wait_limit_ns,
   selftest_wait_timeout.
 """
 from __future__ import annotations
@@ -28,7 +28,8 @@ OA_F32, OA_BF16 = 0, 1
 
 EXPORTS = (
     "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd",
-    "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv", "oa_lse_merge",
+    "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv", "oa_attn_splitkv_static",
+    "oa_lse_merge",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -73,6 +74,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                       i32),
             "oa_splitkv_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
             "oa_attn_splitkv": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp], i32),
+            "oa_attn_splitkv_static": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp], i32),
             "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
             "oa_sync_status": ([vp], i32),
             "oa_set_wait_limit_ns": ([u64], None),
@@ -225,6 +227,26 @@ def attn_splitkv(q, k, v, num_splits: int, scale: float | None = None, kv_len=No
         _check(load().oa_attn_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H,
                                       Nq, Nk, d, float(scale), _ptr(kv), int(num_splits), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(q.device)))
+    return out, lse
+
+
+def attn_splitkv_static(q, k, v, num_splits: int, scale: float | None = None, kv_len=None, out=None, lse=None):
+    """Split-KV attention whose partials live in the library's fixed 16 MiB device scratch (no
+    workspace).  For callers that cannot allocate device memory at call time: pass `out` and `lse`
+    to allocate nothing here either.  Calls that overlap on the GPU share the scratch and race."""
+    _require_cuda(q, k, v, out, lse)
+    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    kv = _kv_len_arg(kv_len, B, q.device)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_splitkv_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype),
+                                             B, H, Nq, Nk, d, float(scale), _ptr(kv), int(num_splits),
+                                             _stream(q.device)))
     return out, lse
 
 

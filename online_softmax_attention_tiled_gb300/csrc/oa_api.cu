@@ -254,3 +254,11 @@ oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream) {
 }
 
 }  // extern "C"
+
+// Helpers for entry points defined in other files of the library: record the
+// last error / success for oa_last_error(), and fetch the status word.
+namespace oa {
+oa_status api_fail(oa_status s, const char* msg) { return fail(s, "%s", msg); }
+oa_status api_ok() { return ok(); }
+bool api_dev_status(DevStatus* st) { return dev_status(st); }
+}  // namespace oa
