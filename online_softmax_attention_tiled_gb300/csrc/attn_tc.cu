@@ -43,6 +43,9 @@ constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
+// A row's running max is only moved (and O, l rescaled) when a tile raises it
+// by more than this many log2 units, i.e. a factor 2^8.
+constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct Cfg {
@@ -278,11 +281,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after_sync();
       uint32_t sr[128];
-      tmem_ld64(s_addr, *reinterpret_cast<uint32_t(*)[64]>(&sr[0]));
-      tmem_ld64(s_addr + 64, *reinterpret_cast<uint32_t(*)[64]>(&sr[64]));
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) s[c] = __uint_as_float(sr[c]);
+      tmem_ld128(s_addr, sr);
+      float* s = reinterpret_cast<float*>(sr);
       const int col0 = j * BN;
       if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
 #pragma unroll
@@ -291,48 +291,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (col >= kvl || (p.causal && col > row)) s[c] = -INFINITY;
         }
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      // row max of the raw scores (scale > 0 commutes with max)
+      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, s[c]);
-        mx1 = fmaxf(mx1, s[c + 1]);
-        mx2 = fmaxf(mx2, s[c + 2]);
-        mx3 = fmaxf(mx3, s[c + 3]);
+      for (int c = 8; c < 128; c += 8) {
+        mx0 = max3(mx0, s[c], s[c + 1]);
+        mx1 = max3(mx1, s[c + 2], s[c + 3]);
+        mx2 = max3(mx2, s[c + 4], s[c + 5]);
+        mx3 = max3(mx3, s[c + 6], s[c + 7]);
       }
-      const float m_new = fmaxf(m, fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2);
-      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - ref);
-      float sum0 = 0.f, sum1 = 0.f;
+      const float m_tile = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+      // Lazy rescale: keep the running reference m unless the row max grew by
+      // more than kRescaleLog2 (P stays <= 2^kRescaleLog2, exact in fp32/bf16
+      // range).  O and l always share the reference, so O / l is unchanged.
+      const bool grow = m_tile > m + kRescaleLog2;
+      const float alpha = grow ? ex2(m - m_tile) : 1.f;  // 0 when m was -inf
+      if (grow) m = m_tile;
+      const float ref = (m == -INFINITY) ? 0.f : m;
+      const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
+      uint64_t acc0 = 0, acc1 = 0;  // packed partial row sums (bit pattern 0 == {+0.f, +0.f})
+      // P = exp2(S * scale * log2 e - ref): pair c (columns 2c, 2c+1) is written as
+      // one bf16x2 word into sr[c], whose scores have already been consumed.
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(s[64 * h + 2 * c], sl2, -ref));
-          const float p1 = ex2(fmaf(s[64 * h + 2 * c + 1], sl2, -ref));
-          sum0 += p0;
-          sum1 += p1;
-          pk[c] = pack_bf16x2(p0, p1);
-        }
-        tmem_st32(s_addr + 32 * h, pk);
+      for (int c = 0; c < 64; ++c) {
+        float e0, e1;
+        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, nref2), e0, e1);
+        const float p0 = ex2(e0), p1 = ex2(e1);
+        if (c & 1)
+          acc1 = f2_add(acc1, f2_pack(p0, p1));
+        else
+          acc0 = f2_add(acc0, f2_pack(p0, p1));
+        sr[c] = pack_bf16x2(p0, p1);
+        if (c == 31) tmem_st32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
       }
-      l = alpha * l + (sum0 + sum1);
-      m = m_new;
-      if (j > 0) {
+      tmem_st32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+      float a0, a1, a2, a3;
+      f2_unpack(acc0, a0, a1);
+      f2_unpack(acc1, a2, a3);
+      l = alpha * l + ((a0 + a1) + (a2 + a3));
+      if (j > 0 && __any_sync(0xffffffffu, grow)) {
         // O_i must hold PV_i(j-1) before it is rescaled
         ok = __all_sync(0xffffffffu,
                         mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_ODONE));
         if (!ok) break;
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t orr[32];
-            tmem_ld32(o_addr + c, orr);
+        for (int c = 0; c < D; c += 32) {
+          uint32_t orr[32];
+          tmem_ld32(o_addr + c, orr);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st32(o_addr + c, orr);
+          for (int e = 0; e < 32; e += 2) {
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al2), o0, o1);
+            orr[e] = __float_as_uint(o0);
+            orr[e + 1] = __float_as_uint(o1);
           }
+          tmem_st32(o_addr + c, orr);
         }
       }
       tmem_st_wait();
