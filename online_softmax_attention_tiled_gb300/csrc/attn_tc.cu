@@ -16,8 +16,9 @@
 //   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
 //               row t, i.e. TMEM lane t, so row max / sum are thread-local
 //   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
-//   warp 8      TMA producer: Q once, then K and V tiles into 2-4 stage
-//               shared-memory rings (128-byte swizzle), mbarrier complete_tx
+//   warp 8      TMA producer: Q once, then K and V tiles into one 5-slot
+//               (d=128) / 10-slot (d=64) shared-memory ring in consumption
+//               order K0,V0,K1,V1,... (128-byte swizzle), mbarrier complete_tx
 //   warp 9      MMA issuer (one thread): S_i = Q_i K^T (SMEM x SMEM -> TMEM)
 //               and O_i += P_i V (P from TMEM, V from SMEM -> TMEM); owns the
 //               TMEM allocation
@@ -52,13 +53,14 @@ struct Cfg {
   static constexpr int SLABS = D / 64;               // 128-byte swizzle atoms along d
   static constexpr int SLAB_BYTES = BM * 128;        // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = SLABS * SLAB_BYTES;
-  static constexpr int STAGES = (D == 128) ? 2 : 4;
+  // One ring of key/value tiles, filled in the order the MMAs consume them:
+  // K_0, V_0, K_1, V_1, ... (load t = 2j for K_j, 2j + 1 for V_j, slot t % SLOTS).
+  static constexpr int SLOTS = (D == 128) ? 5 : 10;
   static constexpr int Q_OFF = 0;
-  static constexpr int K_OFF = Q_OFF + 2 * TILE_BYTES;
-  static constexpr int V_OFF = K_OFF + STAGES * TILE_BYTES;
-  static constexpr int BAR_OFF = V_OFF + STAGES * TILE_BYTES;
-  // q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NUM_BARS = 1 + 4 * STAGES + 6 + 1;
+  static constexpr int RING_OFF = Q_OFF + 2 * TILE_BYTES;
+  static constexpr int BAR_OFF = RING_OFF + SLOTS * TILE_BYTES;
+  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   __host__ __device__ static constexpr uint32_t o_col(int i) { return 256u + (uint32_t)(i * D); }
@@ -93,14 +95,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t bar0 = sbase + C::BAR_OFF;
   auto bar_q = [&]() { return bar0; };
-  auto bar_kfull = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto bar_kempty = [&](int s) { return bar0 + 8u * (1 + C::STAGES + s); };
-  auto bar_vfull = [&](int s) { return bar0 + 8u * (1 + 2 * C::STAGES + s); };
-  auto bar_vempty = [&](int s) { return bar0 + 8u * (1 + 3 * C::STAGES + s); };
-  auto bar_sfull = [&](int i) { return bar0 + 8u * (1 + 4 * C::STAGES + i); };
-  auto bar_pfull = [&](int i) { return bar0 + 8u * (3 + 4 * C::STAGES + i); };
-  auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 4 * C::STAGES + i); };
-  const uint32_t bar_drain = bar0 + 8u * (7 + 4 * C::STAGES);
+  auto bar_full = [&](int t) { return bar0 + 8u * (1 + t % C::SLOTS); };             // ring load t landed
+  auto bar_empty = [&](int t) { return bar0 + 8u * (1 + C::SLOTS + t % C::SLOTS); };  // slot of load t free
+  auto ring_phase = [&](int t) { return (uint32_t)(t / C::SLOTS) & 1u; };
+  auto ring_addr = [&](int t) { return sbase + C::RING_OFF + (uint32_t)((t % C::SLOTS) * C::TILE_BYTES); };
+  auto bar_sfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::SLOTS + i); };
+  auto bar_pfull = [&](int i) { return bar0 + 8u * (3 + 2 * C::SLOTS + i); };
+  auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 2 * C::SLOTS + i); };
+  const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -126,11 +128,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, TMEM ----
   if (threadIdx.x == 0) {
     mbar_init(bar_q(), 1);
-    for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_kfull(s), 1);
-      mbar_init(bar_kempty(s), 1);
-      mbar_init(bar_vfull(s), 1);
-      mbar_init(bar_vempty(s), 1);
+    for (int t = 0; t < C::SLOTS; ++t) {
+      mbar_init(bar_full(t), 1);
+      mbar_init(bar_empty(t), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_sfull(i), 1);
@@ -156,112 +156,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == kProducerWarp) {
-    // =================== TMA producer ===================
-    if (lane == 0) {
-      int issued_k = 0, issued_v = 0;
-      if (n_all > 0) {
-        mbar_arrive_expect_tx(bar_q(), 2 * C::TILE_BYTES);
-        for (int i = 0; i < 2; ++i)
-          for (int s = 0; s < C::SLABS; ++s)
-            tma_load_3d(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q(), s * 64,
-                        q0 + i * BM, bh);
-      }
-      for (int j = 0; j < n_all; ++j) {
-        const int st = j % C::STAGES;
-        const uint32_t ph = (uint32_t)(j / C::STAGES) & 1u;
-        if (!mbar_wait(bar_kempty(st), ph ^ 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_KEMPTY)) break;
-        mbar_arrive_expect_tx(bar_kfull(st), C::TILE_BYTES);
+    // =================== TMA producer (whole warp, one elected lane issues) ===================
+    int issued = 0;
+    if (n_all > 0) {
+      mbar_arrive_expect_tx_elect(bar_q(), 2 * C::TILE_BYTES);
+      for (int i = 0; i < 2; ++i)
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sbase + C::K_OFF + st * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_k, bar_kfull(st), s * 64,
-                      j * BN, bh);
-        ++issued_k;
-        if (!mbar_wait(bar_vempty(st), ph ^ 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_VEMPTY)) break;
-        mbar_arrive_expect_tx(bar_vfull(st), C::TILE_BYTES);
-        for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d(sbase + C::V_OFF + st * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_v, bar_vfull(st), s * 64,
-                      j * BN, bh);
-        ++issued_v;
-      }
-      // drain: every load issued must have landed before the CTA can exit
-      DevStatus quiet = p.st;
-      for (int j = max(0, issued_k - C::STAGES); j < issued_k; ++j)
-        mbar_wait(bar_kfull(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, quiet, nullptr,
-                  (K_ATTN_TC << 8) | W_DRAIN);
-      for (int j = max(0, issued_v - C::STAGES); j < issued_v; ++j)
-        mbar_wait(bar_vfull(j % C::STAGES), (uint32_t)(j / C::STAGES) & 1u, quiet, nullptr,
-                  (K_ATTN_TC << 8) | W_DRAIN);
-      if (n_all > 0) mbar_wait(bar_q(), 0, quiet, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+          tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q(), s * 64,
+                            q0 + i * BM, bh);
     }
+    for (int t = 0; t < 2 * n_all; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_empty(t), ring_phase(t) ^ 1u, p.st, abort_flag,
+                                               (K_ATTN_TC << 8) | W_KEMPTY)))
+        break;
+      mbar_arrive_expect_tx_elect(bar_full(t), C::TILE_BYTES);
+      const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+      for (int s = 0; s < C::SLABS; ++s)
+        tma_load_3d_elect(ring_addr(t) + s * C::SLAB_BYTES, map, bar_full(t), s * 64, (t >> 1) * BN, bh);
+      ++issued;
+    }
+    // drain: every load issued must have landed before the CTA can exit
+    for (int t = max(0, issued - C::SLOTS); t < issued; ++t)
+      mbar_wait(bar_full(t), ring_phase(t), p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    if (n_all > 0) mbar_wait(bar_q(), 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
   } else if (warp == kMmaWarp) {
-    // =================== MMA issuer ===================
-    if (lane == 0 && n_all > 0) {
-      const uint32_t q_s = sbase + C::Q_OFF;
-      auto issue_s = [&](int i, int st) {
-        const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
-        const uint32_t a0 = q_s + i * C::TILE_BYTES;
-        const uint32_t b0 = sbase + C::K_OFF + st * C::TILE_BYTES;
+    // =================== MMA issuer (whole warp, one elected lane issues) ===================
+    // Descriptors are built once; per MMA only a compile-time offset is added,
+    // so every operand stays warp-uniform.
+    const uint64_t q_desc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
+    const uint64_t q_desc1 = smem_desc_sw128(sbase + C::Q_OFF + C::TILE_BYTES, 16, 1024);
+    const uint64_t k_desc0 = smem_desc_sw128(sbase + C::RING_OFF, 16, 1024);            // K: K-major
+    const uint64_t v_desc0 = smem_desc_sw128(sbase + C::RING_OFF, C::SLAB_BYTES, 1024);  // V: MN-major
+    auto slot_off = [&](int t) { return (uint64_t)(((t % C::SLOTS) * C::TILE_BYTES) >> 4); };
+    auto issue_s = [&](int i, int t) {  // S_i = Q_i K^T, K from ring load t
+      const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
+      const uint64_t a = i ? q_desc1 : q_desc0;
+      const uint64_t b = k_desc0 + slot_off(t);
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::SLAB_BYTES + (kk % 4) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(a0 + off, 16, 1024), smem_desc_sw128(b0 + off, 16, 1024), C::IDESC_S,
-                 kk > 0 ? 1u : 0u);
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk / 4) * C::SLAB_BYTES + (kk % 4) * 32) >> 4);
+        mma_ss_elect(d_tmem, a + off, b + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+      }
+    };
+    auto issue_pv = [&](int i, int t, bool accumulate) {  // O_i += P_i V, V from ring load t
+      const uint32_t d_tmem = tmem_base + C::o_col(i);
+      const uint32_t a_tmem = tmem_base + (uint32_t)(i * BN);  // P_i over S_i's first 64 columns
+      const uint64_t b = v_desc0 + slot_off(t);
+#pragma unroll
+      for (int kk = 0; kk < BN / 16; ++kk)
+        mma_ts_elect(d_tmem, a_tmem + kk * 8, b + (uint64_t)((kk * 2048) >> 4), C::IDESC_O,
+                     (accumulate || kk > 0) ? 1u : 0u);
+    };
+    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_TC << 8) | site));
+    };
+    bool ok = n_all > 0 && wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
+    if (ok) {
+      tc_fence_after_sync();
+      for (int i = 0; i < 2; ++i)
+        if (n_kv[i] > 0) {
+          issue_s(i, 0);
+          mma_commit_elect(bar_sfull(i));
         }
-      };
-      auto issue_pv = [&](int i, int st, bool accumulate) {
-        const uint32_t d_tmem = tmem_base + C::o_col(i);
-        const uint32_t a_tmem = tmem_base + (uint32_t)(i * BN);  // P_i over S_i's first 64 columns
-        const uint32_t b0 = sbase + C::V_OFF + st * C::TILE_BYTES;
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(d_tmem, a_tmem + kk * 8, smem_desc_sw128(b0 + kk * 2048, C::SLAB_BYTES, 1024), C::IDESC_O,
-                 (accumulate || kk > 0) ? 1u : 0u);
-      };
-      bool ok = mbar_wait(bar_q(), 0, p.st, abort_flag, (K_ATTN_TC << 8) | W_Q);
-      if (ok) ok = mbar_wait(bar_kfull(0), 0, p.st, abort_flag, (K_ATTN_TC << 8) | W_KFULL);
-      if (ok) {
+      mma_commit_elect(bar_empty(0));
+    }
+    for (int j = 0; ok && j < n_all; ++j) {
+      const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
+      bool k_next_ready = false;
+      if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (j >= n_kv[i]) continue;
+        if (!(ok = wait_all(bar_pfull(i), (uint32_t)j & 1u, W_PFULL))) break;
         tc_fence_after_sync();
-        for (int i = 0; i < 2; ++i)
-          if (n_kv[i] > 0) {
-            issue_s(i, 0);
-            mma_commit(bar_sfull(i));
+        issue_pv(i, tv, j > 0);
+        mma_commit_elect(bar_odone(i));
+        if (j + 1 < n_kv[i]) {
+          if (!k_next_ready) {
+            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+            tc_fence_after_sync();
+            k_next_ready = true;
           }
-        mma_commit(bar_kempty(0));
-      }
-      for (int j = 0; ok && j < n_all; ++j) {
-        const int st = j % C::STAGES;
-        const uint32_t ph = (uint32_t)(j / C::STAGES) & 1u;
-        const int st1 = (j + 1) % C::STAGES;
-        const uint32_t ph1 = (uint32_t)((j + 1) / C::STAGES) & 1u;
-        bool k_next_ready = false;
-        if (!(ok = mbar_wait(bar_vfull(st), ph, p.st, abort_flag, (K_ATTN_TC << 8) | W_VFULL))) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j >= n_kv[i]) continue;
-          if (!(ok = mbar_wait(bar_pfull(i), (uint32_t)j & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_PFULL)))
-            break;
-          tc_fence_after_sync();
-          issue_pv(i, st, j > 0);
-          mma_commit(bar_odone(i));
-          if (j + 1 < n_kv[i]) {
-            if (!k_next_ready) {
-              if (!(ok = mbar_wait(bar_kfull(st1), ph1, p.st, abort_flag, (K_ATTN_TC << 8) | W_KFULL))) break;
-              tc_fence_after_sync();
-              k_next_ready = true;
-            }
-            issue_s(i, st1);
-            mma_commit(bar_sfull(i));
-          }
+          issue_s(i, tk);
+          mma_commit_elect(bar_sfull(i));
         }
-        if (!ok) break;
-        mma_commit(bar_vempty(st));
-        if (k_next_ready) mma_commit(bar_kempty(st1));
       }
+      if (!ok) break;
+      mma_commit_elect(bar_empty(tv));
+      if (k_next_ready) mma_commit_elect(bar_empty(tk));
     }
-    if (lane == 0) {
-      // drain: all MMAs issued by this thread complete before TMEM is freed
-      mma_commit(bar_drain);
-      DevStatus quiet = p.st;
-      mbar_wait(bar_drain, 0, quiet, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
-    }
+    // drain: all MMAs issued by this warp complete before TMEM is freed
+    mma_commit_elect(bar_drain);
+    mbar_wait(bar_drain, 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
   } else {
     // =================== softmax groups ===================
     const int i = warp >> 2;                 // query tile of this group
