@@ -51,6 +51,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_barrier() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// Split exit barrier: arrive (no release: it orders nothing but the peers'
+// finished reads of this CTA's shared memory) as soon as the remote reads are
+// done, wait just before exiting -- so no CTA waits for its output stores.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
   uint32_t remote;
   float v;
@@ -103,20 +110,17 @@ __device__ __forceinline__ ML thread_stats(const float (&v)[E]) {
   return {m, l0 + l1};
 }
 
-// exp(x - m) / l with the rounding error of x - m carried to first order:
-// s + err == x - m exactly (two-sum), exp(x - m) ~= exp(s) * (1 + err).
-__device__ __forceinline__ float softmax_value(float x, float m, float inv_l) {
-  if (x == -INFINITY) return 0.f;
-  const float s = x - m;
-  const float bb = s - x;
-  const float err = (x - (s - bb)) + (-m - bb);
-  const float e = expf(s);
-  return fmaf(e, err, e) * inv_l;
-}
+// exp(x - m) / l.  Relative error bound for every output that is a normal
+// fp32 number (x - m > -87.4): rounding x - m costs |x - m| * 2^-24 <= 5.2e-6,
+// expf ~1 ulp, the product with 1/l two roundings, and l itself (a sum of
+// terms <= 1 with one dominant 1) carries ~1e-6 -- together under 1e-5.
+// `ref` is the row max, or 0 for a row that is entirely -inf (then 1/l is 0):
+// x = -inf gives exp(-inf) = +0.0 exactly and -inf - -inf never forms.
+__device__ __forceinline__ float softmax_value(float x, float ref, float inv_l) { return expf(x - ref) * inv_l; }
 
 template <int E, bool VEC>
 __device__ __forceinline__ void store_piece(float* __restrict__ yr, int64_t base, int64_t end, const float (&v)[E],
-                                            float m, float inv_l) {
+                                            float ref, float inv_l) {
   const int T = blockDim.x, t = threadIdx.x;
   if constexpr (VEC) {
 #pragma unroll
@@ -124,22 +128,22 @@ __device__ __forceinline__ void store_piece(float* __restrict__ yr, int64_t base
       const int64_t c = base + ((int64_t)g * T + t) * 4;
       if (c + 3 < end) {
         float4 f;
-        f.x = softmax_value(v[4 * g], m, inv_l);
-        f.y = softmax_value(v[4 * g + 1], m, inv_l);
-        f.z = softmax_value(v[4 * g + 2], m, inv_l);
-        f.w = softmax_value(v[4 * g + 3], m, inv_l);
+        f.x = softmax_value(v[4 * g], ref, inv_l);
+        f.y = softmax_value(v[4 * g + 1], ref, inv_l);
+        f.z = softmax_value(v[4 * g + 2], ref, inv_l);
+        f.w = softmax_value(v[4 * g + 3], ref, inv_l);
         __stcs(reinterpret_cast<float4*>(yr + c), f);
       } else {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (c + e < end) yr[c + e] = softmax_value(v[4 * g + e], m, inv_l);
+          if (c + e < end) yr[c + e] = softmax_value(v[4 * g + e], ref, inv_l);
       }
     }
   } else {
 #pragma unroll
     for (int i = 0; i < E; ++i) {
       const int64_t c = base + (int64_t)i * T + t;
-      if (c < end) __stcs(yr + c, softmax_value(v[i], m, inv_l));
+      if (c < end) __stcs(yr + c, softmax_value(v[i], ref, inv_l));
     }
   }
 }
@@ -201,24 +205,26 @@ __global__ void __launch_bounds__(kMaxThreads) softmax_rows_kernel(const float* 
     row_ml = cta_ml;
   }
   __syncthreads();
+  if (cluster > 1) cluster_arrive_relaxed();  // thread 0's remote reads are complete
   const ML rs = row_ml;
 
   if (lse != nullptr && rank == 0 && t == 0) lse[row] = (rs.l > 0.f) ? rs.m + logf(rs.l) : -INFINITY;
 
   if (y != nullptr) {
     const float inv_l = (rs.l > 0.f) ? 1.f / rs.l : 0.f;
+    const float ref = (rs.m == -INFINITY) ? 0.f : rs.m;
     float* yr = y + row * ld_y;
     if (resident) {
-      store_piece<E, VEC>(yr, c0, c1, v, rs.m, inv_l);
+      store_piece<E, VEC>(yr, c0, c1, v, ref, inv_l);
     } else {
       for (int64_t b = c0; b < c1; b += piece) {
         load_piece<E, VEC, false>(xr, b, c1, v);
-        store_piece<E, VEC>(yr, b, c1, v, rs.m, inv_l);
+        store_piece<E, VEC>(yr, b, c1, v, ref, inv_l);
       }
     }
   }
   // keep this CTA's shared memory alive until every peer has read it
-  if (cluster > 1) cluster_barrier();
+  if (cluster > 1) cluster_wait();
 }
 
 template <int E, bool VEC>
