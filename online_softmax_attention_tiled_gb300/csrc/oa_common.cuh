@@ -76,9 +76,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // completed.  Gives up -- returning false -- when `abort` (a CTA-shared
 // flag) becomes nonzero, or after st.limit_ns nanoseconds, in which case it
 // records `site` in the status word and raises `abort` for the whole CTA.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const DevStatus& st,
-                                       volatile int* abort, unsigned site) {
-  if (mbar_try_wait(bar, parity)) return true;
+// The first probe is inlined: a phase that has already completed costs a
+// few cycles, with no call.  Only a wait that has to spin enters the
+// out-of-line bounded loop below, so registers live across the wait are
+// saved around the call on that slow path alone.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, const DevStatus& st,
+                                                   volatile int* abort, unsigned site) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -91,6 +94,11 @@ static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, con
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const DevStatus& st,
+                                          volatile int* abort, unsigned site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, st, abort, site);
 }
 
 // ---------------------------------------------------------------------------
