@@ -12,23 +12,28 @@
 // chip.  Causal tiles above the diagonal are never loaded or computed; only
 // the diagonal tile and the ragged key tail are masked (Step 4).
 //
-// GB300 mapping (one CTA per SM, 320 threads):
+// GB300 mapping (one CTA per SM; 320 threads at d=128, 352 at d=64):
 //   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
 //               row t, i.e. TMEM lane t, so row max / sum are thread-local
 //   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
 //   warp 8      TMA producer: Q once, then K and V tiles into one 5-slot
-//               (d=128) / 10-slot (d=64) shared-memory ring in consumption
-//               order K0,V0,K1,V1,... (128-byte swizzle), mbarrier complete_tx
-//   warp 9      MMA issuer (one thread): S_i = Q_i K^T (SMEM x SMEM -> TMEM)
-//               and O_i += P_i V (P from TMEM, V from SMEM -> TMEM); owns the
-//               TMEM allocation
+//               (d=128) / 10-slot (d=64) shared-memory ring in load order
+//               K0,V0,K1,V1,... (128-byte swizzle), mbarrier complete_tx
+//   warp 9(,10) MMA issue (whole warp, one elected lane): S_i = Q_i K^T
+//               (SMEM x SMEM -> TMEM) and O_i += P_i V (P from TMEM, V from
+//               SMEM -> TMEM); warp 9 owns the TMEM allocation
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
-// O_0 [256, 256+d), O_1 [256+d, 256+2d).  P_i (bf16, two per column) is
-// written over the first 64 columns of S_i; the next S_i is issued after
-// the PV MMA that reads P_i, and tcgen05 MMAs of one thread run in order.
-// MMA issue order per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), so
-// each softmax group works while the tensor core runs the other group's
-// MMAs.
+// O_0 [256, 256+d), O_1 [256+d, 256+2d).
+//   d = 128: P_i (bf16, two per column) is written over the first 64 columns
+//   of S_i, so S_i(j+1) can only follow the PV MMA that reads P_i(j).  One
+//   warp issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): each tile's own MMAs
+//   run back to back, and each softmax group works while the tensor core
+//   runs the other group's.
+//   d = 64: P_i gets its own columns [384 + 64 i, +64), so the group frees
+//   S_i as soon as it has read it and S_i(j+1) is computed during the
+//   softmax of S_i(j).  Warp 9 issues tile 0's MMAs and warp 10 tile 1's, in
+//   the order S_i(j+1), PV_i(j); before writing P_i(j) a group waits for
+//   PV_i(j-1).
 //
 // Every mbarrier wait is bounded (oa_common.cuh); a wait that expires sets
 // the CTA abort flag, every role falls through to the teardown, in-flight
@@ -40,9 +45,8 @@ namespace {
 
 constexpr int BM = 128;  // rows per query tile (= TMEM lanes)
 constexpr int BN = 128;  // keys per key/value tile
-constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp0 = 9;  // MMA issuer of query tile 0; warp 10 issues for tile 1
 constexpr uint32_t kTmemCols = 512;
 // A row's running max is only moved (and O, l rescaled) when a tile raises it
 // by more than this many log2 units, i.e. a factor 2^8.
@@ -56,14 +60,27 @@ struct Cfg {
   // One ring of key/value tiles, filled in the order the MMAs consume them:
   // K_0, V_0, K_1, V_1, ... (load t = 2j for K_j, 2j + 1 for V_j, slot t % SLOTS).
   static constexpr int SLOTS = (D == 128) ? 5 : 10;
+  // d = 64 leaves 128 TMEM columns free: P_i gets its own 64 columns, so S_i(j+1)
+  // can be computed while the softmax of S_i(j) runs (the group frees S_i as soon
+  // as it has read it).  At d = 128 P_i is written over S_i.
+  static constexpr bool SEP_P = (D == 64);
+  // With P_i separate each query tile's MMAs come from a warp of its own; with P_i over
+  // S_i one warp issues both tiles' PV and S back to back, which keeps each tile's
+  // critical loop (softmax -> PV_i -> S_i -> softmax) short.
+  static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
+  static constexpr int THREADS = 32 * (9 + MMA_WARPS);  // 8 softmax warps, producer, MMA warp(s)
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + SLOTS * TILE_BYTES;
-  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1;
+  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2]
+  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   __host__ __device__ static constexpr uint32_t o_col(int i) { return 256u + (uint32_t)(i * D); }
+  // first TMEM column of P_i (bf16 pairs, 64 columns)
+  __host__ __device__ static constexpr uint32_t p_col(int i) {
+    return SEP_P ? 256u + 2u * (uint32_t)D + 64u * (uint32_t)i : (uint32_t)(i * BN);
+  }
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);  // Q K^T, both K-major
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);    // P V, V is MN-major
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -79,11 +96,11 @@ struct TcParams {
 };
 
 enum WaitSite : unsigned {
-  W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN
+  W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN, W_SFREE
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   using C = Cfg<D>;
@@ -103,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_pfull = [&](int i) { return bar0 + 8u * (3 + 2 * C::SLOTS + i); };
   auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 2 * C::SLOTS + i); };
   const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
+  auto bar_sfree = [&](int i) { return bar0 + 8u * (8 + 2 * C::SLOTS + i); };  // S_i read by its group
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -130,18 +148,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_q(), 1);
     for (int t = 0; t < C::SLOTS; ++t) {
       mbar_init(bar_full(t), 1);
-      mbar_init(bar_empty(t), 1);
+      mbar_init(bar_empty(t), C::MMA_WARPS);  // released by every MMA warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_sfull(i), 1);
       mbar_init(bar_pfull(i), 4);  // one arrival per softmax warp
       mbar_init(bar_odone(i), 1);
+      mbar_init(bar_sfree(i), 4);  // one arrival per softmax warp
     }
-    mbar_init(bar_drain, 1);
+    mbar_init(bar_drain, C::MMA_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -179,18 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = max(0, issued - C::SLOTS); t < issued; ++t)
       mbar_wait(bar_full(t), ring_phase(t), p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
     if (n_all > 0) mbar_wait(bar_q(), 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
-  } else if (warp == kMmaWarp) {
-    // =================== MMA issuer (whole warp, one elected lane issues) ===================
-    // Descriptors are built once; per MMA only a compile-time offset is added,
-    // so every operand stays warp-uniform.
+  } else if (warp >= kMmaWarp0) {
+    // =================== MMA issuers (whole warp, one elected lane issues) ===================
+    // Descriptors are built once; per MMA only a compile-time offset is added, so every
+    // operand stays warp-uniform.
     const uint64_t q_desc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
-    const uint64_t q_desc1 = smem_desc_sw128(sbase + C::Q_OFF + C::TILE_BYTES, 16, 1024);
     const uint64_t k_desc0 = smem_desc_sw128(sbase + C::RING_OFF, 16, 1024);            // K: K-major
     const uint64_t v_desc0 = smem_desc_sw128(sbase + C::RING_OFF, C::SLAB_BYTES, 1024);  // V: MN-major
     auto slot_off = [&](int t) { return (uint64_t)(((t % C::SLOTS) * C::TILE_BYTES) >> 4); };
     auto issue_s = [&](int i, int t) {  // S_i = Q_i K^T, K from ring load t
       const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
-      const uint64_t a = i ? q_desc1 : q_desc0;
+      const uint64_t a = q_desc0 + (uint64_t)((i * C::TILE_BYTES) >> 4);
       const uint64_t b = k_desc0 + slot_off(t);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -200,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_pv = [&](int i, int t, bool accumulate) {  // O_i += P_i V, V from ring load t
       const uint32_t d_tmem = tmem_base + C::o_col(i);
-      const uint32_t a_tmem = tmem_base + (uint32_t)(i * BN);  // P_i over S_i's first 64 columns
+      const uint32_t a_tmem = tmem_base + C::p_col(i);
       const uint64_t b = v_desc0 + slot_off(t);
 #pragma unroll
       for (int kk = 0; kk < BN / 16; ++kk)
@@ -210,43 +228,89 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_TC << 8) | site));
     };
-    bool ok = n_all > 0 && wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
-    if (ok) {
-      tc_fence_after_sync();
-      for (int i = 0; i < 2; ++i)
-        if (n_kv[i] > 0) {
+    if constexpr (C::SEP_P) {
+      // ---- one warp per query tile: warp 9 for tile 0, warp 10 for tile 1 ----
+      const int i = warp - kMmaWarp0;
+      const int n = n_kv[i];
+      // Loads 2j (K_j) and 2j + 1 (V_j) for j < n are this tile's; it releases each with a
+      // commit after the MMAs that read it.
+      bool ok = true;
+      if (n > 0) {
+        ok = wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
+        if (ok) {
+          tc_fence_after_sync();
           issue_s(i, 0);
           mma_commit_elect(bar_sfull(i));
+          mma_commit_elect(bar_empty(0));
         }
-      mma_commit_elect(bar_empty(0));
-    }
-    for (int j = 0; ok && j < n_all; ++j) {
-      const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
-      bool k_next_ready = false;
-      if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-      for (int i = 0; i < 2 && ok; ++i) {
-        if (j >= n_kv[i]) continue;
+      }
+      for (int j = 0; ok && j < n; ++j) {
+        const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
+        if (j + 1 < n) {  // S_i(j+1) as soon as the softmax group has read S_i(j)
+          if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+          if (!(ok = wait_all(bar_sfree(i), (uint32_t)j & 1u, W_SFREE))) break;
+          tc_fence_after_sync();
+          issue_s(i, tk);
+          mma_commit_elect(bar_sfull(i));
+          mma_commit_elect(bar_empty(tk));
+        }
+        if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
         if (!(ok = wait_all(bar_pfull(i), (uint32_t)j & 1u, W_PFULL))) break;
         tc_fence_after_sync();
         issue_pv(i, tv, j > 0);
         mma_commit_elect(bar_odone(i));
-        if (j + 1 < n_kv[i]) {
-          if (!k_next_ready) {
-            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-            tc_fence_after_sync();
-            k_next_ready = true;
-          }
-          issue_s(i, tk);
-          mma_commit_elect(bar_sfull(i));
-        }
+        mma_commit_elect(bar_empty(tv));
       }
-      if (!ok) break;
-      mma_commit_elect(bar_empty(tv));
-      if (k_next_ready) mma_commit_elect(bar_empty(tk));
+      // Loads this tile does not use (the other tile's last key tile, or every load for an
+      // empty tile) are released by a plain arrival once they have landed, which keeps each
+      // arrival in its slot's current phase.
+      for (int t = 2 * n; ok && t < 2 * n_all; ++t) {
+        if (!(ok = wait_all(bar_full(t), ring_phase(t), W_DRAIN))) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty(t));
+      }
+    } else {
+      // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
+      bool ok = n_all > 0 && wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
+      if (ok) {
+        tc_fence_after_sync();
+        for (int i = 0; i < 2; ++i)
+          if (n_kv[i] > 0) {
+            issue_s(i, 0);
+            mma_commit_elect(bar_sfull(i));
+          }
+        mma_commit_elect(bar_empty(0));
+      }
+      for (int j = 0; ok && j < n_all; ++j) {
+        const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
+        bool k_next_ready = false;
+        if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j >= n_kv[i]) continue;
+          if (!(ok = wait_all(bar_pfull(i), (uint32_t)j & 1u, W_PFULL))) break;
+          tc_fence_after_sync();
+          issue_pv(i, tv, j > 0);
+          mma_commit_elect(bar_odone(i));
+          if (j + 1 < n_kv[i]) {  // P_i lives in S_i's columns: S_i(j+1) after PV_i(j)
+            if (!k_next_ready) {
+              if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+              tc_fence_after_sync();
+              k_next_ready = true;
+            }
+            issue_s(i, tk);
+            mma_commit_elect(bar_sfull(i));
+          }
+        }
+        if (!ok) break;
+        mma_commit_elect(bar_empty(tv));
+        if (k_next_ready) mma_commit_elect(bar_empty(tk));
+      }
     }
-    // drain: all MMAs issued by this warp complete before TMEM is freed
-    mma_commit_elect(bar_drain);
-    mbar_wait(bar_drain, 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    {
+      // drain: every MMA issued completes before TMEM is freed
+      mma_commit_elect(bar_drain);
+      mbar_wait(bar_drain, 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    }
   } else {
     // =================== softmax groups ===================
     const int i = warp >> 2;                 // query tile of this group
@@ -256,6 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem_base + lane_base + (uint32_t)(i * BN);
     const uint32_t o_addr = tmem_base + lane_base + C::o_col(i);
+    const uint32_t p_addr = tmem_base + lane_base + C::p_col(i);
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running max of the scaled scores, log2 units
     float l = 0.f;
@@ -267,6 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       uint32_t sr[128];
       tmem_ld128(s_addr, sr);
+      if constexpr (C::SEP_P) {  // S_i may now be overwritten by S_i(j+1)
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_sfree(i));
+      }
       float* s = reinterpret_cast<float*>(sr);
       const int col0 = j * BN;
       if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
@@ -307,19 +377,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           acc0 = f2_add(acc0, f2_pack(p0, p1));
         sr[c] = pack_bf16x2(p0, p1);
-        if (c == 31) tmem_st32(s_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+        if (c == 31) {
+          if (C::SEP_P && j > 0) {
+            // P_i(j) goes where PV_i(j-1) reads P_i(j-1): wait for that MMA (and O_i)
+            ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag,
+                                                   (K_ATTN_TC << 8) | W_ODONE));
+            tc_fence_after_sync();
+          }
+          if (ok) tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+        }
       }
-      tmem_st32(s_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+      if (!ok) break;
+      tmem_st32(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
       float a0, a1, a2, a3;
       f2_unpack(acc0, a0, a1);
       f2_unpack(acc1, a2, a3);
       l = alpha * l + ((a0 + a1) + (a2 + a3));
       if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_i must hold PV_i(j-1) before it is rescaled
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_ODONE));
-        if (!ok) break;
-        tc_fence_after_sync();
+        // O_i must hold PV_i(j-1) before it is rescaled (already waited for when P_i is separate)
+        if (!C::SEP_P) {
+          ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag,
+                                                 (K_ATTN_TC << 8) | W_ODONE));
+          if (!ok) break;
+          tc_fence_after_sync();
+        }
         const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
@@ -380,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown ----
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kMmaWarp0) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -430,7 +511,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     attr_set = true;
   }
   const unsigned grid = (unsigned)p.num_qblocks * (unsigned)p.BH;
-  attn_fwd_tc_kernel<D><<<grid, kThreads, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
