@@ -12,7 +12,13 @@
 // chip.  Causal tiles above the diagonal are never loaded or computed; only
 // the diagonal tile and the ragged key tail are masked (Step 4).
 //
-// GB300 mapping (one CTA per SM; 320 threads at d=128, 352 at d=64):
+// Persistent: one CTA per SM, each working through items (2 x 128 query rows of one
+// (b, h)) numbered heaviest first and dealt out in rounds of one per CTA, alternating
+// direction between rounds.  Barriers, TMEM and descriptors are set up once; ring loads
+// and barrier phases run on across items, so the next item's Q, K and V are loaded and
+// its first score tiles computed while the current item finishes.
+//
+// GB300 mapping (320 threads at d=128, 352 at d=64):
 //   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
 //               row t, i.e. TMEM lane t, so row max / sum are thread-local
 //   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
@@ -72,8 +78,8 @@ struct Cfg {
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = Q_OFF + 2 * TILE_BYTES;
   static constexpr int BAR_OFF = RING_OFF + SLOTS * TILE_BYTES;
-  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2]
-  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2;
+  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2], q_empty
+  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   __host__ __device__ static constexpr uint32_t o_col(int i) { return 256u + (uint32_t)(i * D); }
@@ -96,11 +102,48 @@ struct TcParams {
 };
 
 enum WaitSite : unsigned {
-  W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN, W_SFREE
+  W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN, W_SFREE, W_QEMPTY
 };
 
+// One work item: 2 x 128 query rows of one (b, h).
+struct Item {
+  int bh, q0, kvl, n_kv[2], n_all;
+};
+
+// Items are numbered heaviest first (for causal: the last query blocks); item idx covers
+// query block num_qblocks - 1 - idx / BH of head idx % BH.
+__device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
+  Item it;
+  const int qb = p.num_qblocks - 1 - idx / p.BH;
+  it.bh = idx % p.BH;
+  const int b = it.bh / p.H;
+  it.q0 = qb * 2 * BM;
+  it.kvl = p.Nk;
+  if (p.kv_len != nullptr) it.kvl = min(max(p.kv_len[b], 0), p.Nk);
+  const int nk_tiles = (it.kvl + BN - 1) / BN;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = it.q0 + i * BM;
+    it.n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
+    if (r0 >= p.Nq) it.n_kv[i] = 0;  // query tile entirely past the end
+  }
+  it.n_all = max(it.n_kv[0], it.n_kv[1]);
+  return it;
+}
+
+// The k-th item of this CTA: round k of the persistent grid takes items [k G, k G + G), in
+// CTA order on even rounds and in reverse on odd ones, so the heavy and light ends of the
+// list pair up across rounds.  Negative past the end of the list.
+__device__ __forceinline__ int item_of_round(int k, int total) {
+  const int G = (int)gridDim.x, c = (int)blockIdx.x;
+  const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
+  return idx < total ? idx : -1;
+}
+
 template <int D>
-__global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
+// No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
+// and the hint made ptxas spill more on this kernel.
+__global__ void __launch_bounds__(Cfg<D>::THREADS)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   using C = Cfg<D>;
@@ -111,7 +154,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   const uint32_t sbase = raw_s + pad;
 
   const uint32_t bar0 = sbase + C::BAR_OFF;
-  auto bar_q = [&]() { return bar0; };
+  const uint32_t bar_q = bar0;
   auto bar_full = [&](int t) { return bar0 + 8u * (1 + t % C::SLOTS); };             // ring load t landed
   auto bar_empty = [&](int t) { return bar0 + 8u * (1 + C::SLOTS + t % C::SLOTS); };  // slot of load t free
   auto ring_phase = [&](int t) { return (uint32_t)(t / C::SLOTS) & 1u; };
@@ -121,31 +164,16 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 2 * C::SLOTS + i); };
   const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
   auto bar_sfree = [&](int i) { return bar0 + 8u * (8 + 2 * C::SLOTS + i); };  // S_i read by its group
+  const uint32_t bar_qempty = bar0 + 8u * (10 + 2 * C::SLOTS);               // Q read by the last S MMAs
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = p.num_qblocks * p.BH;
 
-  // ---- work assignment: last (heaviest, for causal) query blocks first ----
-  const int qb = p.num_qblocks - 1 - (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
-  const int b = bh / p.H;
-  const int q0 = qb * 2 * BM;
-  int kvl = p.Nk;
-  if (p.kv_len != nullptr) kvl = min(max(p.kv_len[b], 0), p.Nk);
-  const int nk_tiles = (kvl + BN - 1) / BN;
-  int n_kv[2];
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r0 = q0 + i * BM;
-    n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
-    if (r0 >= p.Nq) n_kv[i] = 0;  // query tile entirely past the end
-  }
-  const int n_all = max(n_kv[0], n_kv[1]);
-
-  // ---- set-up: barriers, TMEM ----
+  // ---- set-up: barriers, TMEM (once; the CTA then works through its items) ----
   if (threadIdx.x == 0) {
-    mbar_init(bar_q(), 1);
+    mbar_init(bar_q, 1);
     for (int t = 0; t < C::SLOTS; ++t) {
       mbar_init(bar_full(t), 1);
       mbar_init(bar_empty(t), C::MMA_WARPS);  // released by every MMA warp
@@ -157,6 +185,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       mbar_init(bar_sfree(i), 4);  // one arrival per softmax warp
     }
     mbar_init(bar_drain, C::MMA_WARPS);
+    mbar_init(bar_qempty, C::MMA_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -173,31 +202,40 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_TC << 8) | site));
+  };
 
   if (warp == kProducerWarp) {
     // =================== TMA producer (whole warp, one elected lane issues) ===================
-    int issued = 0;
-    if (n_all > 0) {
-      mbar_arrive_expect_tx_elect(bar_q(), 2 * C::TILE_BYTES);
+    // Ring loads are numbered across items (tg), so slots and phases run on.
+    int tg = 0, nq = 0;
+    bool ok = true;
+    for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+      const int idx = item_of_round(k, total);
+      if (idx < 0) continue;
+      const Item it = item_at(p, idx);
+      if (it.n_all == 0) continue;
+      // the previous item's S MMAs must have finished reading Q
+      if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
+      mbar_arrive_expect_tx_elect(bar_q, 2 * C::TILE_BYTES);
       for (int i = 0; i < 2; ++i)
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q(), s * 64,
-                            q0 + i * BM, bh);
-    }
-    for (int t = 0; t < 2 * n_all; ++t) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_empty(t), ring_phase(t) ^ 1u, p.st, abort_flag,
-                                               (K_ATTN_TC << 8) | W_KEMPTY)))
-        break;
-      mbar_arrive_expect_tx_elect(bar_full(t), C::TILE_BYTES);
-      const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
-      for (int s = 0; s < C::SLABS; ++s)
-        tma_load_3d_elect(ring_addr(t) + s * C::SLAB_BYTES, map, bar_full(t), s * 64, (t >> 1) * BN, bh);
-      ++issued;
+          tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q, s * 64,
+                            it.q0 + i * BM, it.bh);
+      ++nq;
+      for (int t = 0; t < 2 * it.n_all; ++t, ++tg) {
+        if (!(ok = wait_all(bar_empty(tg), ring_phase(tg) ^ 1u, W_KEMPTY))) break;
+        mbar_arrive_expect_tx_elect(bar_full(tg), C::TILE_BYTES);
+        const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
+        for (int s = 0; s < C::SLABS; ++s)
+          tma_load_3d_elect(ring_addr(tg) + s * C::SLAB_BYTES, map, bar_full(tg), s * 64, (t >> 1) * BN, it.bh);
+      }
     }
     // drain: every load issued must have landed before the CTA can exit
-    for (int t = max(0, issued - C::SLOTS); t < issued; ++t)
+    for (int t = max(0, tg - C::SLOTS); t < tg; ++t)
       mbar_wait(bar_full(t), ring_phase(t), p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
-    if (n_all > 0) mbar_wait(bar_q(), 0, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
+    if (nq > 0) mbar_wait(bar_q, (uint32_t)(nq - 1) & 1u, p.st, nullptr, (K_ATTN_TC << 8) | W_DRAIN);
   } else if (warp >= kMmaWarp0) {
     // =================== MMA issuers (whole warp, one elected lane issues) ===================
     // Descriptors are built once; per MMA only a compile-time offset is added, so every
@@ -225,85 +263,110 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
         mma_ts_elect(d_tmem, a_tmem + kk * 8, b + (uint64_t)((kk * 2048) >> 4), C::IDESC_O,
                      (accumulate || kk > 0) ? 1u : 0u);
     };
-    auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_TC << 8) | site));
-    };
+    // Running counters across items: tg = first ring load of the item, nq = Q loads so far,
+    // st_i = score tiles of query tile i so far (the phase of s_full / p_full / o_done / s_free).
+    int tg = 0, nq = 0, st0 = 0, st1 = 0;
+    bool ok = true;
     if constexpr (C::SEP_P) {
       // ---- one warp per query tile: warp 9 for tile 0, warp 10 for tile 1 ----
       const int i = warp - kMmaWarp0;
-      const int n = n_kv[i];
-      // Loads 2j (K_j) and 2j + 1 (V_j) for j < n are this tile's; it releases each with a
-      // commit after the MMAs that read it.
-      bool ok = true;
-      if (n > 0) {
-        ok = wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
-        if (ok) {
+      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+        const int idx = item_of_round(k, total);
+        if (idx < 0) continue;
+        const Item it = item_at(p, idx);
+        if (it.n_all == 0) continue;
+        const int n = it.n_kv[i], sb = i ? st1 : st0;
+        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
+        ++nq;
+        // Loads tg + 2j (K_j) and tg + 2j + 1 (V_j) for j < n are this tile's; it releases
+        // each with a commit after the MMAs that read it.
+        if (n > 0) {
+          if (!(ok = wait_all(bar_full(tg), ring_phase(tg), W_KFULL))) break;
           tc_fence_after_sync();
-          issue_s(i, 0);
+          issue_s(i, tg);
           mma_commit_elect(bar_sfull(i));
-          mma_commit_elect(bar_empty(0));
+          mma_commit_elect(bar_empty(tg));
+          if (n == 1) mma_commit_elect(bar_qempty);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_qempty);  // Q(this item) has landed: the arrival is in phase
         }
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
-        if (j + 1 < n) {  // S_i(j+1) as soon as the softmax group has read S_i(j)
-          if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-          if (!(ok = wait_all(bar_sfree(i), (uint32_t)j & 1u, W_SFREE))) break;
-          tc_fence_after_sync();
-          issue_s(i, tk);
-          mma_commit_elect(bar_sfull(i));
-          mma_commit_elect(bar_empty(tk));
-        }
-        if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-        if (!(ok = wait_all(bar_pfull(i), (uint32_t)j & 1u, W_PFULL))) break;
-        tc_fence_after_sync();
-        issue_pv(i, tv, j > 0);
-        mma_commit_elect(bar_odone(i));
-        mma_commit_elect(bar_empty(tv));
-      }
-      // Loads this tile does not use (the other tile's last key tile, or every load for an
-      // empty tile) are released by a plain arrival once they have landed, which keeps each
-      // arrival in its slot's current phase.
-      for (int t = 2 * n; ok && t < 2 * n_all; ++t) {
-        if (!(ok = wait_all(bar_full(t), ring_phase(t), W_DRAIN))) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty(t));
-      }
-    } else {
-      // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
-      bool ok = n_all > 0 && wait_all(bar_q(), 0, W_Q) && wait_all(bar_full(0), ring_phase(0), W_KFULL);
-      if (ok) {
-        tc_fence_after_sync();
-        for (int i = 0; i < 2; ++i)
-          if (n_kv[i] > 0) {
-            issue_s(i, 0);
+        for (int j = 0; ok && j < n; ++j) {
+          const int tv = tg + 2 * j + 1, tk = tg + 2 * j + 2;  // loads holding V_j and K_{j+1}
+          const uint32_t ph = (uint32_t)(sb + j) & 1u;
+          if (j + 1 < n) {  // S_i(j+1) as soon as the softmax group has read S_i(j)
+            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+            if (!(ok = wait_all(bar_sfree(i), ph, W_SFREE))) break;
+            tc_fence_after_sync();
+            issue_s(i, tk);
             mma_commit_elect(bar_sfull(i));
+            mma_commit_elect(bar_empty(tk));
+            if (j + 2 == n) mma_commit_elect(bar_qempty);
           }
-        mma_commit_elect(bar_empty(0));
-      }
-      for (int j = 0; ok && j < n_all; ++j) {
-        const int tv = 2 * j + 1, tk = 2 * j + 2;  // loads holding V_j and K_{j+1}
-        bool k_next_ready = false;
-        if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j >= n_kv[i]) continue;
-          if (!(ok = wait_all(bar_pfull(i), (uint32_t)j & 1u, W_PFULL))) break;
+          if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+          if (!(ok = wait_all(bar_pfull(i), ph, W_PFULL))) break;
           tc_fence_after_sync();
           issue_pv(i, tv, j > 0);
           mma_commit_elect(bar_odone(i));
-          if (j + 1 < n_kv[i]) {  // P_i lives in S_i's columns: S_i(j+1) after PV_i(j)
-            if (!k_next_ready) {
-              if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-              tc_fence_after_sync();
-              k_next_ready = true;
-            }
-            issue_s(i, tk);
+          mma_commit_elect(bar_empty(tv));
+        }
+        // Loads this tile does not use (the other tile's last key tile, or every load for an
+        // empty tile) are released by a plain arrival once they have landed, which keeps each
+        // arrival in its slot's current phase.
+        for (int t = tg + 2 * n; ok && t < tg + 2 * it.n_all; ++t) {
+          if (!(ok = wait_all(bar_full(t), ring_phase(t), W_DRAIN))) break;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_empty(t));
+        }
+        tg += 2 * it.n_all;
+        if (i) st1 += n; else st0 += n;
+      }
+    } else {
+      // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
+      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+        const int idx = item_of_round(k, total);
+        if (idx < 0) continue;
+        const Item it = item_at(p, idx);
+        if (it.n_all == 0) continue;
+        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
+        ++nq;
+        if (!(ok = wait_all(bar_full(tg), ring_phase(tg), W_KFULL))) break;
+        tc_fence_after_sync();
+        for (int i = 0; i < 2; ++i)
+          if (it.n_kv[i] > 0) {
+            issue_s(i, tg);
             mma_commit_elect(bar_sfull(i));
           }
+        mma_commit_elect(bar_empty(tg));
+        if (it.n_all == 1) mma_commit_elect(bar_qempty);
+        for (int j = 0; ok && j < it.n_all; ++j) {
+          const int tv = tg + 2 * j + 1, tk = tg + 2 * j + 2;  // loads holding V_j and K_{j+1}
+          bool k_next_ready = false;
+          if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (j >= it.n_kv[i]) continue;
+            if (!(ok = wait_all(bar_pfull(i), (uint32_t)((i ? st1 : st0) + j) & 1u, W_PFULL))) break;
+            tc_fence_after_sync();
+            issue_pv(i, tv, j > 0);
+            mma_commit_elect(bar_odone(i));
+            if (j + 1 < it.n_kv[i]) {  // P_i lives in S_i's columns: S_i(j+1) after PV_i(j)
+              if (!k_next_ready) {
+                if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+                tc_fence_after_sync();
+                k_next_ready = true;
+              }
+              issue_s(i, tk);
+              mma_commit_elect(bar_sfull(i));
+            }
+          }
+          if (!ok) break;
+          mma_commit_elect(bar_empty(tv));
+          if (k_next_ready) mma_commit_elect(bar_empty(tk));
+          if (j + 2 == it.n_all) mma_commit_elect(bar_qempty);  // the item's last S MMAs are issued
         }
-        if (!ok) break;
-        mma_commit_elect(bar_empty(tv));
-        if (k_next_ready) mma_commit_elect(bar_empty(tk));
+        tg += 2 * it.n_all;
+        st0 += it.n_kv[0];
+        st1 += it.n_kv[1];
       }
     }
     {
@@ -315,119 +378,121 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
     // =================== softmax groups ===================
     const int i = warp >> 2;                 // query tile of this group
     const int tt = threadIdx.x & 127;        // row within the tile = TMEM lane
-    const int r0 = q0 + i * BM;
-    const int row = r0 + tt;
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_addr = tmem_base + lane_base + (uint32_t)(i * BN);
     const uint32_t o_addr = tmem_base + lane_base + C::o_col(i);
     const uint32_t p_addr = tmem_base + lane_base + C::p_col(i);
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of the scaled scores, log2 units
-    float l = 0.f;
+    int sb = 0;  // score tiles of this group in earlier items (barrier phases run on)
     bool ok = true;
+    for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+      const int idx = item_of_round(k, total);
+      if (idx < 0) continue;
+      const Item it = item_at(p, idx);
+      const int n = it.n_kv[i], kvl = it.kvl, bh = it.bh;
+      const int r0 = it.q0 + i * BM;
+      const int row = r0 + tt;
+      float m = -INFINITY;  // running max of the scaled scores, log2 units
+      float l = 0.f;
 
-    for (int j = 0; j < n_kv[i]; ++j) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_sfull(i), (uint32_t)j & 1u, p.st, abort_flag, (K_ATTN_TC << 8) | W_SFULL));
-      if (!ok) break;
-      tc_fence_after_sync();
-      uint32_t sr[128];
-      tmem_ld128(s_addr, sr);
-      if constexpr (C::SEP_P) {  // S_i may now be overwritten by S_i(j+1)
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_sfree(i));
-      }
-      float* s = reinterpret_cast<float*>(sr);
-      const int col0 = j * BN;
-      if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const int col = col0 + c;
-          if (col >= kvl || (p.causal && col > row)) s[c] = -INFINITY;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t ph = (uint32_t)(sb + j) & 1u;
+        if (!(ok = wait_all(bar_sfull(i), ph, W_SFULL))) break;
+        tc_fence_after_sync();
+        uint32_t sr[128];
+        tmem_ld128(s_addr, sr);
+        if constexpr (C::SEP_P) {  // S_i may now be overwritten by S_i(j+1)
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_sfree(i));
         }
-      }
-      // row max of the raw scores (scale > 0 commutes with max)
-      float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
+        float* s = reinterpret_cast<float*>(sr);
+        const int col0 = j * BN;
+        if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
 #pragma unroll
-      for (int c = 8; c < 128; c += 8) {
-        mx0 = max3(mx0, s[c], s[c + 1]);
-        mx1 = max3(mx1, s[c + 2], s[c + 3]);
-        mx2 = max3(mx2, s[c + 4], s[c + 5]);
-        mx3 = max3(mx3, s[c + 6], s[c + 7]);
-      }
-      const float m_tile = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
-      // Lazy rescale: keep the running reference m unless the row max grew by
-      // more than kRescaleLog2 (P stays <= 2^kRescaleLog2, exact in fp32/bf16
-      // range).  O and l always share the reference, so O / l is unchanged.
-      const bool grow = m_tile > m + kRescaleLog2;
-      const float alpha = grow ? ex2(m - m_tile) : 1.f;  // 0 when m was -inf
-      if (grow) m = m_tile;
-      const float ref = (m == -INFINITY) ? 0.f : m;
-      const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
-      uint64_t acc0 = 0, acc1 = 0;  // packed partial row sums (bit pattern 0 == {+0.f, +0.f})
-      // P = exp2(S * scale * log2 e - ref): pair c (columns 2c, 2c+1) is written as
-      // one bf16x2 word into sr[c], whose scores have already been consumed.
+          for (int c = 0; c < 128; ++c) {
+            const int col = col0 + c;
+            if (col >= kvl || (p.causal && col > row)) s[c] = -INFINITY;
+          }
+        }
+        // row max of the raw scores (scale > 0 commutes with max)
+        float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float e0, e1;
-        f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, nref2), e0, e1);
-        const float p0 = ex2(e0), p1 = ex2(e1);
-        if (c & 1)
-          acc1 = f2_add(acc1, f2_pack(p0, p1));
-        else
-          acc0 = f2_add(acc0, f2_pack(p0, p1));
-        sr[c] = pack_bf16x2(p0, p1);
-        if (c == 31) {
-          if (C::SEP_P && j > 0) {
-            // P_i(j) goes where PV_i(j-1) reads P_i(j-1): wait for that MMA (and O_i)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag,
-                                                   (K_ATTN_TC << 8) | W_ODONE));
+        for (int c = 8; c < 128; c += 8) {
+          mx0 = max3(mx0, s[c], s[c + 1]);
+          mx1 = max3(mx1, s[c + 2], s[c + 3]);
+          mx2 = max3(mx2, s[c + 4], s[c + 5]);
+          mx3 = max3(mx3, s[c + 6], s[c + 7]);
+        }
+        const float m_tile = max3(mx0, mx1, fmaxf(mx2, mx3)) * sl2;
+        // Lazy rescale: keep the running reference m unless the row max grew by
+        // more than kRescaleLog2 (P stays <= 2^kRescaleLog2, exact in fp32/bf16
+        // range).  O and l always share the reference, so O / l is unchanged.
+        const bool grow = m_tile > m + kRescaleLog2;
+        const float alpha = grow ? ex2(m - m_tile) : 1.f;  // 0 when m was -inf
+        if (grow) m = m_tile;
+        const float ref = (m == -INFINITY) ? 0.f : m;
+        const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
+        uint64_t acc0 = 0, acc1 = 0;  // packed partial row sums (bit pattern 0 == {+0.f, +0.f})
+        // P = exp2(S * scale * log2 e - ref): pair c (columns 2c, 2c+1) is written as
+        // one bf16x2 word into sr[c], whose scores have already been consumed.
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float e0, e1;
+          f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, nref2), e0, e1);
+          const float p0 = ex2(e0), p1 = ex2(e1);
+          if (c & 1)
+            acc1 = f2_add(acc1, f2_pack(p0, p1));
+          else
+            acc0 = f2_add(acc0, f2_pack(p0, p1));
+          sr[c] = pack_bf16x2(p0, p1);
+          if (c == 31) {
+            if (C::SEP_P && j > 0) {
+              // P_i(j) goes where PV_i(j-1) reads P_i(j-1): wait for that MMA (and O_i).
+              // (At j = 0 the previous item's epilogue already waited for its last PV.)
+              ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE);
+              tc_fence_after_sync();
+            }
+            if (ok) tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+          }
+        }
+        if (!ok) break;
+        tmem_st32(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+        float a0, a1, a2, a3;
+        f2_unpack(acc0, a0, a1);
+        f2_unpack(acc1, a2, a3);
+        l = alpha * l + ((a0 + a1) + (a2 + a3));
+        if (j > 0 && __any_sync(0xffffffffu, grow)) {
+          // O_i must hold PV_i(j-1) before it is rescaled (already waited for when P_i is separate)
+          if (!C::SEP_P) {
+            if (!(ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE))) break;
             tc_fence_after_sync();
           }
-          if (ok) tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+          const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + c, orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float o0, o1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al2), o0, o1);
+              orr[e] = __float_as_uint(o0);
+              orr[e + 1] = __float_as_uint(o1);
+            }
+            tmem_st32(o_addr + c, orr);
+          }
         }
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_pfull(i));
       }
       if (!ok) break;
-      tmem_st32(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
-      float a0, a1, a2, a3;
-      f2_unpack(acc0, a0, a1);
-      f2_unpack(acc1, a2, a3);
-      l = alpha * l + ((a0 + a1) + (a2 + a3));
-      if (j > 0 && __any_sync(0xffffffffu, grow)) {
-        // O_i must hold PV_i(j-1) before it is rescaled (already waited for when P_i is separate)
-        if (!C::SEP_P) {
-          ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(j - 1) & 1u, p.st, abort_flag,
-                                                 (K_ATTN_TC << 8) | W_ODONE));
-          if (!ok) break;
-          tc_fence_after_sync();
-        }
-        const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          uint32_t orr[32];
-          tmem_ld32(o_addr + c, orr);
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float o0, o1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al2), o0, o1);
-            orr[e] = __float_as_uint(o0);
-            orr[e + 1] = __float_as_uint(o1);
-          }
-          tmem_st32(o_addr + c, orr);
-        }
-      }
-      tmem_st_wait();
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_pfull(i));
-    }
 
-    // ---- epilogue: O / l, LSE ----
-    const bool have_o = ok && n_kv[i] > 0;
-    if (have_o)
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_odone(i), (uint32_t)(n_kv[i] - 1) & 1u, p.st, abort_flag,
-                                             (K_ATTN_TC << 8) | W_ODONE));
-    if (ok) {
+      // ---- epilogue: O / l, LSE ----
+      const bool have_o = n > 0;
+      if (have_o && !(ok = wait_all(bar_odone(i), (uint32_t)(sb + n - 1) & 1u, W_ODONE))) break;
       tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + ((int64_t)bh * p.Nq + row) * D;
@@ -455,6 +520,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS, 1)
       }
       if (p.lse != nullptr && row < p.Nq)
         p.lse[(int64_t)bh * p.Nq + row] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+      // O_i has been read out: the next item's PV_i(0) (issued after this group's next P)
+      // may overwrite it
+      tc_fence_before_sync();
+      sb += n;
     }
   }
 
@@ -500,17 +569,28 @@ bool make_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+constexpr int kMaxDevices = 64;
+
+// Persistent grid: one CTA per SM (the kernel holds an SM's TMEM and most of its shared
+// memory), never more CTAs than work items.
 template <int D>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                      cudaStream_t s) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::SMEM_BYTES);
+  static bool attr_set[kMaxDevices] = {};
+  static int sm_count[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
   }
-  const unsigned grid = (unsigned)p.num_qblocks * (unsigned)p.BH;
+  const long long total = (long long)p.num_qblocks * p.BH;
+  const unsigned grid = (unsigned)(total < sm_count[dev] ? total : sm_count[dev]);
   attn_fwd_tc_kernel<D><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }

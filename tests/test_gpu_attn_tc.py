@@ -60,6 +60,18 @@ def test_kv_len_masks(cuda_lib, d, causal):
     _check(cuda_lib, q, k, v, causal=causal, kv_len=[N, 1, 0, 200])
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_items_per_cta(cuda_lib, d, causal):
+    # B*H = 160 heads x 3 query blocks = 480 work items: more than one SM's worth each, so
+    # every CTA of the persistent grid runs several items in turn.  The last query block's
+    # second tile lies past Nq, one sequence has no keys at all (an item with no work
+    # between items with work) and the others end mid-tile.
+    N = 640
+    q, k, v = si.attn_inputs(4, 40, N, N, d, torch.bfloat16, seed=21 + d)
+    _check(cuda_lib, q, k, v, causal=causal, kv_len=[N, 0, 129, 511])
+
+
 def test_scale_and_large_scores(cuda_lib):
     q, k, v = si.attn_inputs(1, 2, 300, 300, 128, torch.bfloat16, seed=12)
     _check(cuda_lib, q, k, v, scale=1.0)  # scores ~N(0, 128): exercises large max shifts
