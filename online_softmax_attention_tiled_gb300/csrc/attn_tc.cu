@@ -22,7 +22,7 @@
 //   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
 //               row t, i.e. TMEM lane t, so row max / sum are thread-local
 //   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
-//   warp 8      TMA producer: Q once, then K and V tiles into one 5-slot
+//   warp 8      TMA producer: Q per item, then K and V tiles into one 4-slot
 //               (d=128) / 10-slot (d=64) shared-memory ring in load order
 //               K0,V0,K1,V1,... (128-byte swizzle), mbarrier complete_tx
 //   warp 9(,10) MMA issue (whole warp, one elected lane): S_i = Q_i K^T
@@ -65,7 +65,7 @@ struct Cfg {
   static constexpr int TILE_BYTES = SLABS * SLAB_BYTES;
   // One ring of key/value tiles, filled in the order the MMAs consume them:
   // K_0, V_0, K_1, V_1, ... (load t = 2j for K_j, 2j + 1 for V_j, slot t % SLOTS).
-  static constexpr int SLOTS = (D == 128) ? 5 : 10;
+  static constexpr int SLOTS = (D == 128) ? 4 : 10;
   // d = 64 leaves 128 TMEM columns free: P_i gets its own 64 columns, so S_i(j+1)
   // can be computed while the softmax of S_i(j) runs (the group frees S_i as soon
   // as it has read it).  At d = 128 P_i is written over S_i.
@@ -97,6 +97,7 @@ struct TcParams {
   float* lse;
   const int32_t* kv_len;
   int H, Nq, Nk, causal, num_qblocks, BH;
+  int o_v8;  // o is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;
   DevStatus st;
 };
@@ -510,12 +511,19 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l, __uint_as_float(orr[2 * e + 1]) * inv_l);
+        // Each thread writes its own row: a warp's store touches 32 rows, so whole 32-byte
+        // sectors per thread (half as many requests as 16-byte stores) matter here.
         if (row < p.Nq) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c);
-          dst[0] = pk[0];
-          dst[1] = pk[1];
-          dst[2] = pk[2];
-          dst[3] = pk[3];
+          if (p.o_v8) {
+            st_global_v8(orow + c, w);
+            st_global_v8(orow + c + 16, w + 8);
+          } else {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c);
+            dst[0] = pk[0];
+            dst[1] = pk[1];
+            dst[2] = pk[2];
+            dst[3] = pk[3];
+          }
         }
       }
       if (p.lse != nullptr && row < p.Nq)
@@ -608,6 +616,7 @@ cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o,
   }
   TcParams p;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_v8 = (reinterpret_cast<uintptr_t>(o) % 32u) == 0 ? 1 : 0;
   p.lse = lse;
   p.kv_len = kv_len;
   p.H = H;

@@ -60,6 +60,23 @@ def test_kv_len_masks(cuda_lib, d, causal):
     _check(cuda_lib, q, k, v, causal=causal, kv_len=[N, 1, 0, 200])
 
 
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_16_byte_aligned(cuda_lib, d):
+    # O rows are written with 32-byte stores when o is 32-byte aligned; an o that is only
+    # 16-byte aligned (the documented minimum) takes the 16-byte store path.
+    B, H, N = 1, 3, 300
+    q, k, v = si.attn_inputs(B, H, N, N, d, torch.bfloat16, seed=31 + d)
+    flat = torch.empty(B * H * N * d + 8, dtype=torch.bfloat16, device="cuda")
+    out = flat[8:].view(B, H, N, d)  # 16 bytes past a 256-byte aligned allocation
+    assert out.data_ptr() % 32 == 16
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True, out=out)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
 def test_many_items_per_cta(cuda_lib, d, causal):
