@@ -116,6 +116,51 @@ oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
                       const int32_t* kv_len, oa_stream_t stream);
 
 /*
+ * oa_attn_fwd with grouped key/value heads: k and v are [B, H_kv, Nk, d]
+ * and query head h reads key/value head h / (H / H_kv).  H_kv == H is
+ * oa_attn_fwd.  The pages' attention has one key/value head per query head;
+ * the grouping is the library generalisation that the interview lesson's
+ * "In Real Systems" list of library entry points (fixed-length, variable-
+ * length and KV-cache calls) is read to ask for.
+ *   q, o [B, H, Nq, d]; k, v [B, H_kv, Nk, d]; everything else as in
+ *   oa_attn_fwd (dtype, alignment, lse, causal, scale, kv_len, support).
+ * Errors: those of oa_attn_fwd, plus OA_ERR_INVALID when H_kv < 1 or
+ * H_kv does not divide H.
+ */
+oa_status oa_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                          oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d, int causal,
+                          float scale, const int32_t* kv_len, oa_stream_t stream);
+
+/*
+ * Fused attention forward over packed sequences of different lengths (the
+ * variable-length entry point of the interview lesson's "In Real Systems"
+ * list), tcgen05 tensor-core kernel.  Sequence s owns query tokens
+ * [cu_seqlens_q[s], cu_seqlens_q[s+1]) and key tokens
+ * [cu_seqlens_k[s], cu_seqlens_k[s+1]); each is attended independently,
+ * exactly as oa_attn_fwd does for one (b, h).
+ *   q, o    bf16 [total_q, H, d] (token-major), 16-byte aligned.
+ *   k, v    bf16 [total_k, H_kv, d]; query head h reads head h / (H/H_kv).
+ *   lse     fp32 [total_q, H], or NULL.
+ *   cu_seqlens_q, cu_seqlens_k   device int32 [num_seqs + 1], non-decreasing;
+ *           entries are clamped to [0, total].  A sequence with no keys gets
+ *           O = 0 and lse = -inf; one with no queries writes nothing.
+ *   max_seqlen_q, max_seqlen_k   the longest query / key sequence.  A
+ *           query sequence longer than max_seqlen_q has its tail rows left
+ *           unwritten and the status word records it (oa_sync_status).
+ *   causal  0 or 1: key j of a sequence is visible to its query i iff j <= i.
+ *   d       64 or 128.
+ * The caller keeps every buffer alive until the work has completed on
+ * `stream`; nothing is allocated.
+ * Errors: OA_ERR_INVALID (NULL pointers, sizes, alignment, H_kv not
+ * dividing H, bad scale); OA_ERR_UNSUPPORTED (dtype other than bf16, d).
+ */
+oa_status oa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                             oa_dtype dt, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, int num_seqs, int H, int H_kv,
+                             int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                             int causal, float scale, oa_stream_t stream);
+
+/*
  * The fp32 SIMT attention forward with explicit tile sizes: Br query rows
  * per CTA and Bc keys per step of the online recurrence (1 <= Br, Bc <= 64).
  * Same contract as oa_attn_fwd with dt = OA_F32; the result does not
@@ -156,6 +201,19 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
                           oa_dtype dt, int B, int H, int Nq, int Nk, int d, float scale,
                           const int32_t* kv_len, int num_splits, void* workspace,
                           size_t workspace_bytes, oa_stream_t stream);
+
+/*
+ * oa_attn_splitkv with grouped key/value heads (KV-cache decode with fewer
+ * key/value heads than query heads): k and v are [B, H_kv, Nk, d] and query
+ * head h reads head h / (H / H_kv); kv_len gives each sequence's cache
+ * length.  Same workspace size and support matrix as oa_attn_splitkv.
+ * Errors: those of oa_attn_splitkv, plus OA_ERR_INVALID when H_kv < 1 or
+ * H_kv does not divide H.
+ */
+oa_status oa_attn_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+                              oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d,
+                              float scale, const int32_t* kv_len, int num_splits, void* workspace,
+                              size_t workspace_bytes, oa_stream_t stream);
 
 /*
  * Split-KV attention that allocates nothing -- a library addition with no
@@ -199,8 +257,9 @@ oa_status oa_lse_merge(const float* part_o, const float* part_lse, int S, int64_
 /*
  * Synchronises `stream`, then reads and clears the device status word that
  * kernels set when a bounded wait expires.  Returns OA_OK, OA_ERR_TIMEOUT
- * (with the code of the expired wait in oa_last_error()) or OA_ERR_CUDA if
- * the synchronisation itself failed.
+ * (with the code of the expired wait in oa_last_error()), OA_ERR_INVALID
+ * when oa_attn_fwd_varlen met a query sequence longer than its
+ * max_seqlen_q, or OA_ERR_CUDA if the synchronisation itself failed.
  */
 oa_status oa_sync_status(oa_stream_t stream);
 

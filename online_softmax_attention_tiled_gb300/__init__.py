@@ -27,9 +27,9 @@ OA_OK, OA_ERR_INVALID, OA_ERR_UNSUPPORTED, OA_ERR_CUDA, OA_ERR_TIMEOUT = 0, 1, 2
 OA_F32, OA_BF16 = 0, 1
 
 EXPORTS = (
-    "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd",
-    "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv", "oa_attn_splitkv_static",
-    "oa_lse_merge",
+    "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd", "oa_attn_fwd_gqa",
+    "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
+    "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -70,10 +70,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "oa_version": ([], i32),
             "oa_softmax_rows": ([vp, i64, i64, i64, vp, i64, vp, vp], i32),
             "oa_attn_fwd": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp], i32),
+            "oa_attn_fwd_gqa": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp, vp], i32),
+            "oa_attn_fwd_varlen": ([vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32,
+                                    f32, vp], i32),
             "oa_attn_fwd_f32_tiles": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, i32, vp],
                                       i32),
             "oa_splitkv_workspace_bytes": ([i32, i32, i32, i32, i32], sz),
             "oa_attn_splitkv": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp], i32),
+            "oa_attn_splitkv_gqa": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp, sz, vp],
+                                    i32),
             "oa_attn_splitkv_static": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp], i32),
             "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
             "oa_sync_status": ([vp], i32),
@@ -142,19 +147,23 @@ def softmax_rows(x: torch.Tensor, y: torch.Tensor | None = None, lse: torch.Tens
     return y, lse
 
 
-def _attn_shapes(q, k, v):
+def _attn_shapes(q, k, v, allow_groups=False):
+    """Sizes of q [B, H, Nq, d] and k, v [B, H_kv, Nk, d]; returns (B, H, Nq, Nk, d, H_kv)."""
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise OAError(OA_ERR_INVALID, "q, k, v must be [B, H, N, d]")
     B, H, Nq, d = q.shape
-    Nk = k.shape[2]
-    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape) != (B, H, Nk, d):
-        raise OAError(OA_ERR_INVALID, "k and v must be [B, H, Nk, d] matching q")
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, Hkv, Nk, d) or tuple(v.shape) != (B, Hkv, Nk, d):
+        raise OAError(OA_ERR_INVALID, "k and v must be [B, H_kv, Nk, d] matching q")
+    if Hkv != H and not (allow_groups and Hkv >= 1 and H % Hkv == 0):
+        raise OAError(OA_ERR_INVALID, f"k and v have {Hkv} heads for {H} query heads"
+                      + (" (need a divisor of H)" if allow_groups else " (need the same count)"))
     if not (q.dtype == k.dtype == v.dtype):
         raise OAError(OA_ERR_INVALID, "q, k, v must share a dtype")
     for t in (q, k, v):
         if not t.is_contiguous():
             raise OAError(OA_ERR_INVALID, "q, k, v must be contiguous")
-    return B, H, Nq, Nk, d
+    return B, H, Nq, Nk, d, Hkv
 
 
 def _kv_len_arg(kv_len, B, device):
@@ -167,9 +176,10 @@ def _kv_len_arg(kv_len, B, device):
 
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, kv_len=None, out=None, lse=None,
              want_lse: bool = True):
-    """O = softmax(Q K^T * scale) V with per-row LSE; q/k/v [B,H,N,d] bf16 or fp32 on CUDA."""
+    """O = softmax(Q K^T * scale) V with per-row LSE; q [B,H,Nq,d], k/v [B,H_kv,Nk,d] (H_kv divides H;
+    query head h reads key/value head h // (H // H_kv)), bf16 or fp32 on CUDA."""
     _require_cuda(q, k, v, out, lse)
-    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v, allow_groups=True)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
@@ -178,8 +188,48 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, kv_len=N
     if want_lse and lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        _check(load().oa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H, Nq,
-                                  Nk, d, int(bool(causal)), float(scale), _ptr(kv), _stream(q.device)))
+        _check(load().oa_attn_fwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H,
+                                      Hkv, Nq, Nk, d, int(bool(causal)), float(scale), _ptr(kv), _stream(q.device)))
+    return out, lse
+
+
+def _cu_seqlens_arg(cu, device, name):
+    if cu.dtype != torch.int32 or cu.dim() != 1 or cu.numel() < 2 or not cu.is_cuda or cu.device != device:
+        raise OAError(OA_ERR_INVALID, f"{name} must be an int32 CUDA tensor of num_seqs + 1 offsets on q's device")
+    return cu.contiguous()
+
+
+def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                    causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True):
+    """Attention over packed sequences: q [Tq, H, d], k/v [Tk, H_kv, d] bf16 (token-major); sequence s is
+    tokens [cu_seqlens_q[s], cu_seqlens_q[s+1]) of q and [cu_seqlens_k[s], cu_seqlens_k[s+1]) of k/v.
+    Returns (o [Tq, H, d], lse [Tq, H])."""
+    _require_cuda(q, k, v, out, lse)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise OAError(OA_ERR_INVALID, "q must be [Tq, H, d] and k, v [Tk, H_kv, d]")
+    Tq, H, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (Tk, Hkv, d) or tuple(v.shape) != (Tk, Hkv, d):
+        raise OAError(OA_ERR_INVALID, "k and v must be [Tk, H_kv, d] matching q")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise OAError(OA_ERR_INVALID, "q, k, v must share a dtype")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise OAError(OA_ERR_INVALID, "q, k, v must be contiguous")
+    cq = _cu_seqlens_arg(cu_seqlens_q, q.device, "cu_seqlens_q")
+    ck = _cu_seqlens_arg(cu_seqlens_k, q.device, "cu_seqlens_k")
+    if cq.numel() != ck.numel():
+        raise OAError(OA_ERR_INVALID, "cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((Tq, H, d), dtype=q.dtype, device=q.device)
+    if want_lse and lse is None:
+        lse = torch.empty((Tq, H), dtype=torch.float32, device=q.device)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype),
+                                         _ptr(cq), _ptr(ck), cq.numel() - 1, H, Hkv, Tq, Tk, int(max_seqlen_q),
+                                         int(max_seqlen_k), d, int(bool(causal)), float(scale), _stream(q.device)))
     return out, lse
 
 
@@ -187,7 +237,7 @@ def attn_fwd_f32_tiles(q, k, v, Br: int, Bc: int, causal: bool = False, scale: f
                        out=None, lse=None):
     """fp32 attention forward with explicit tile sizes (Br query rows, Bc keys per step)."""
     _require_cuda(q, k, v, out, lse)
-    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v)
     if q.dtype != torch.float32:
         raise OAError(OA_ERR_INVALID, "attn_fwd_f32_tiles needs float32 inputs")
     if scale is None:
@@ -210,9 +260,11 @@ def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) ->
 
 def attn_splitkv(q, k, v, num_splits: int, scale: float | None = None, kv_len=None, out=None, lse=None,
                  workspace=None):
-    """Split-KV attention: per-chunk partials, then the LSE merge.  workspace: optional uint8 CUDA tensor."""
+    """Split-KV attention: per-chunk partials, then the LSE merge.  q [B,H,Nq,d], k/v [B,H_kv,Nk,d] (H_kv
+    divides H: grouped key/value heads, e.g. a KV cache with fewer heads).  workspace: optional uint8 CUDA
+    tensor."""
     _require_cuda(q, k, v, out, lse, workspace)
-    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v, allow_groups=True)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
@@ -224,9 +276,10 @@ def attn_splitkv(q, k, v, num_splits: int, scale: float | None = None, kv_len=No
     if lse is None:
         lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
     with torch.cuda.device(q.device):
-        _check(load().oa_attn_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H,
-                                      Nq, Nk, d, float(scale), _ptr(kv), int(num_splits), _ptr(workspace),
-                                      workspace.numel() * workspace.element_size(), _stream(q.device)))
+        _check(load().oa_attn_splitkv_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype),
+                                          B, H, Hkv, Nq, Nk, d, float(scale), _ptr(kv), int(num_splits),
+                                          _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                          _stream(q.device)))
     return out, lse
 
 
@@ -235,7 +288,7 @@ def attn_splitkv_static(q, k, v, num_splits: int, scale: float | None = None, kv
     workspace).  For callers that cannot allocate device memory at call time: pass `out` and `lse`
     to allocate nothing here either.  Calls that overlap on the GPU share the scratch and race."""
     _require_cuda(q, k, v, out, lse)
-    B, H, Nq, Nk, d = _attn_shapes(q, k, v)
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)

@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const float* __restr
                                                             float* __restrict__ lse, int H, int Nq, int Nk, int d,
                                                             int causal, float scale,
                                                             const int32_t* __restrict__ kv_len, int Br, int Bc,
-                                                            int n_qblocks) {
+                                                            int n_qblocks, int group) {
   extern __shared__ float sm[];
   float* Qs = sm;                 // [Br][d]
   float* Os = Qs + Br * d;        // [Br][d]
@@ -45,8 +45,10 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const float* __restr
   const int kv_end = causal ? min(kvl, q0 + br) : kvl;
 
   const float* qb = q + (bh * Nq + q0) * d;
-  const float* kb = k + bh * (int64_t)Nk * d;
-  const float* vb = v + bh * (int64_t)Nk * d;
+  // query head h reads key/value head h / group
+  const int64_t kvbh = (int64_t)b * (H / group) + (int)(bh % H) / group;
+  const float* kb = k + kvbh * (int64_t)Nk * d;
+  const float* vb = v + kvbh * (int64_t)Nk * d;
 
   for (int i = t; i < br * d; i += kThreads) {
     Qs[i] = qb[i];
@@ -132,7 +134,7 @@ size_t smem_bytes(int Br, int Bc, int d) {
 }  // namespace
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
-                            int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, int Br,
+                            int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, int Br,
                             int Bc, cudaStream_t s) {
   if (Br <= 0 || Bc <= 0) {  // library default tiles
     Br = 16;
@@ -146,7 +148,7 @@ cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, floa
   const int n_qblocks = (Nq + Br - 1) / Br;
   const int64_t grid = (int64_t)B * H * n_qblocks;
   attn_f32_kernel<<<(unsigned)grid, kThreads, smem, s>>>(q, k, v, o, lse, H, Nq, Nk, d, causal, scale, kv_len,
-                                                         Br, Bc, n_qblocks);
+                                                         Br, Bc, n_qblocks, H / Hkv);
   return cudaGetLastError();
 }
 

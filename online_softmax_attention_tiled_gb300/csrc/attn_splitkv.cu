@@ -79,7 +79,7 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32) splitkv_partial_kernel(
     const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, float* __restrict__ part_o,
     float* __restrict__ part_lse, int H, int Nq, int Nk, int chunk, int S, float scale_log2,
-    const int32_t* __restrict__ kv_len, int64_t R) {
+    const int32_t* __restrict__ kv_len, int64_t R, int group) {
   constexpr int EPL = Lanes<T>::kPerLane;  // elements per lane (16 bytes)
   constexpr int LPK = D / EPL;             // lanes per key row
   constexpr int G = 32 / LPK;              // key rows per warp load
@@ -120,8 +120,10 @@ __global__ void __launch_bounds__(kWarps * 32) splitkv_partial_kernel(
 #pragma unroll
   for (int e = 0; e < EPL; ++e) st.o[e] = 0.f;
 
-  const T* kb = k + (bh * Nk) * (int64_t)D + sub * EPL;
-  const T* vb = v + (bh * Nk) * (int64_t)D + sub * EPL;
+  // query head h reads key/value head h / group
+  const int64_t kvbh = (int64_t)b * (H / group) + (int)(bh % H) / group;
+  const T* kb = k + (kvbh * Nk) * (int64_t)D + sub * EPL;
+  const T* vb = v + (kvbh * Nk) * (int64_t)D + sub * EPL;
 
   for (int base = j0; base < j1; base += NG * kU) {
     uint4 kr[kU], vr[kU];
@@ -211,11 +213,11 @@ __global__ void __launch_bounds__(kWarps * 32) splitkv_partial_kernel(
 
 template <typename T, int D>
 cudaError_t launch_t(const void* q, const void* k, const void* v, int64_t R, int H, int Nq, int Nk, int S,
-                     float scale, const int32_t* kv_len, float* part_o, float* part_lse, cudaStream_t s) {
+                     float scale, const int32_t* kv_len, float* part_o, float* part_lse, int group, cudaStream_t s) {
   const int chunk = (Nk + S - 1) / S;
   splitkv_partial_kernel<T, D><<<(unsigned)(R * S), kWarps * 32, 0, s>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), part_o, part_lse, H, Nq, Nk,
-      chunk, S, scale * kLog2e, kv_len, R);
+      chunk, S, scale * kLog2e, kv_len, R, group);
   return cudaGetLastError();
 }
 
@@ -226,28 +228,29 @@ bool splitkv_supported(bool bf16, int d) {
   return d == 4 || d == 8 || d == 16 || d == 32 || d == 64 || d == 128;
 }
 
-cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, bool bf16, int B, int H, int Nq,
-                                   int Nk, int d, float scale, const int32_t* kv_len, int S, float* part_o,
+cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, bool bf16, int B, int H, int Hkv,
+                                   int Nq, int Nk, int d, float scale, const int32_t* kv_len, int S, float* part_o,
                                    float* part_lse, cudaStream_t s) {
   const int64_t R = (int64_t)B * H * Nq;
+  const int group = H / Hkv;
   using bf = __nv_bfloat16;
   if (bf16) {
     switch (d) {
-      case 8: return launch_t<bf, 8>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 16: return launch_t<bf, 16>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 32: return launch_t<bf, 32>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 64: return launch_t<bf, 64>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 128: return launch_t<bf, 128>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 256: return launch_t<bf, 256>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
+      case 8: return launch_t<bf, 8>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 16: return launch_t<bf, 16>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 32: return launch_t<bf, 32>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 64: return launch_t<bf, 64>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 128: return launch_t<bf, 128>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 256: return launch_t<bf, 256>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
     }
   } else {
     switch (d) {
-      case 4: return launch_t<float, 4>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 8: return launch_t<float, 8>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 16: return launch_t<float, 16>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 32: return launch_t<float, 32>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 64: return launch_t<float, 64>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
-      case 128: return launch_t<float, 128>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, s);
+      case 4: return launch_t<float, 4>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 8: return launch_t<float, 8>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 16: return launch_t<float, 16>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 32: return launch_t<float, 32>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 64: return launch_t<float, 64>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 128: return launch_t<float, 128>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
     }
   }
   return cudaErrorInvalidValue;

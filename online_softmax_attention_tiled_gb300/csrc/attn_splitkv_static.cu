@@ -93,7 +93,7 @@ extern "C" oa_status oa_attn_splitkv_static(const void* q, const void* k, const 
   float* part_o = scratch_address(&e);
   if (part_o == nullptr) return api_fail(OA_ERR_CUDA, "attn_splitkv_static: cudaGetSymbolAddress failed");
   float* part_lse = part_o + (size_t)num_splits * R * d;
-  e = oa::launch_splitkv_partial(q, k, v, dt == OA_BF16, B, H, Nq, Nk, d, scale, kv_len, num_splits, part_o, part_lse,
+  e = oa::launch_splitkv_partial(q, k, v, dt == OA_BF16, B, H, H, Nq, Nk, d, scale, kv_len, num_splits, part_o, part_lse,
                                  (cudaStream_t)stream);
   if (e != cudaSuccess) return api_fail(OA_ERR_CUDA, "attn_splitkv_static: partial kernel launch failed");
   e = oa::launch_lse_merge(part_o, part_lse, num_splits, R, d, o, dt == OA_BF16, lse, (cudaStream_t)stream);

@@ -95,8 +95,16 @@ struct Cfg {
 struct TcParams {
   __nv_bfloat16* o;
   float* lse;
-  const int32_t* kv_len;
-  int H, Nq, Nk, causal, num_qblocks, BH;
+  const int32_t* kv_len;  // dense layout: keys per batch entry, or NULL
+  // Packed sequences (NULL: the dense [B, H, N, d] layout): sequence s has query tokens
+  // [cu_q[s], cu_q[s+1]) of q [Tq, H, d] and key tokens [cu_k[s], cu_k[s+1]) of k/v [Tk, H_kv, d].
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int Tq, Tk;
+  int H, Nq, Nk, causal, num_qblocks, BH;  // packed: Nq = longest query sequence, BH = sequences x H
+  int group;             // query heads per key/value head (H / H_kv)
+  int64_t o_rs;          // O row stride (elements): d dense, H d packed
+  int l_rs;              // LSE row stride: 1 dense, H packed
   int o_v8;  // o is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;
   DevStatus st;
@@ -106,27 +114,61 @@ enum WaitSite : unsigned {
   W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN, W_SFREE, W_QEMPTY
 };
 
-// One work item: 2 x 128 query rows of one (b, h).
+// One work item: 2 x 128 query rows of one (sequence, head).
 struct Item {
-  int bh, q0, kvl, n_kv[2], n_all;
+  int zq, zkv;      // tensor-map head plane of Q/O and of K/V
+  int yq, ykv;      // tensor-map row of the sequence's first query / key
+  int q0;           // first query row of the item within its sequence
+  int nq, kvl;      // query rows and keys of the sequence
+  int n_kv[2], n_all;
+  int64_t ob, lb;   // offsets of the sequence's row 0 (this head) in O (elements) and in LSE
 };
 
 // Items are numbered heaviest first (for causal: the last query blocks); item idx covers
-// query block num_qblocks - 1 - idx / BH of head idx % BH.
+// query block num_qblocks - 1 - idx / BH of (sequence, head) idx % BH.  Query head h reads
+// key/value head h / group.
+template <int D, bool PACKED>
 __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   Item it;
   const int qb = p.num_qblocks - 1 - idx / p.BH;
-  it.bh = idx % p.BH;
-  const int b = it.bh / p.H;
+  const int sh = idx % p.BH;
+  const int sq = sh / p.H, h = sh % p.H, hk = h / p.group;
+  const int Hkv = p.H / p.group;
   it.q0 = qb * 2 * BM;
-  it.kvl = p.Nk;
-  if (p.kv_len != nullptr) it.kvl = min(max(p.kv_len[b], 0), p.Nk);
+  if constexpr (PACKED) {
+    // lengths are clamped to the tensors, so a bad offset can only drop rows, never
+    // address outside q, k, v, o or lse
+    const int q_beg = min(max(p.cu_q[sq], 0), p.Tq), q_end = min(max(p.cu_q[sq + 1], q_beg), p.Tq);
+    const int k_beg = min(max(p.cu_k[sq], 0), p.Tk), k_end = min(max(p.cu_k[sq + 1], k_beg), p.Tk);
+    it.nq = q_end - q_beg;
+    it.kvl = k_end - k_beg;
+    if (it.nq > p.Nq) {  // longer than the declared maximum: its tail has no items
+      if (qb == 0 && h == 0) record_failure(p.st, kSiteBadSeqlen);
+      it.nq = p.Nq;
+    }
+    it.zq = h;
+    it.zkv = hk;
+    it.yq = q_beg;
+    it.ykv = k_beg;
+    it.ob = ((int64_t)q_beg * p.H + h) * D;
+    it.lb = (int64_t)q_beg * p.H + h;
+  } else {
+    it.nq = p.Nq;
+    it.kvl = p.Nk;
+    if (p.kv_len != nullptr) it.kvl = min(max(p.kv_len[sq], 0), p.Nk);
+    it.zq = sh;
+    it.zkv = sq * Hkv + hk;
+    it.yq = 0;
+    it.ykv = 0;
+    it.ob = (int64_t)sh * p.Nq * D;
+    it.lb = (int64_t)sh * p.Nq;
+  }
   const int nk_tiles = (it.kvl + BN - 1) / BN;
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
     const int r0 = it.q0 + i * BM;
     it.n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
-    if (r0 >= p.Nq) it.n_kv[i] = 0;  // query tile entirely past the end
+    if (r0 >= it.nq) it.n_kv[i] = 0;  // query tile entirely past the end
   }
   it.n_all = max(it.n_kv[0], it.n_kv[1]);
   return it;
@@ -141,9 +183,10 @@ __device__ __forceinline__ int item_of_round(int k, int total) {
   return idx < total ? idx : -1;
 }
 
-template <int D>
 // No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
-// and the hint made ptxas spill more on this kernel.
+// and the hint made ptxas spill more on this kernel.  PACKED: token-major packed sequences
+// (a separate instance, so the dense layout pays nothing for them).
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(Cfg<D>::THREADS)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -215,7 +258,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
       const int idx = item_of_round(k, total);
       if (idx < 0) continue;
-      const Item it = item_at(p, idx);
+      const Item it = item_at<D, PACKED>(p, idx);
       if (it.n_all == 0) continue;
       // the previous item's S MMAs must have finished reading Q
       if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
@@ -223,14 +266,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int i = 0; i < 2; ++i)
         for (int s = 0; s < C::SLABS; ++s)
           tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q, s * 64,
-                            it.q0 + i * BM, it.bh);
+                            it.yq + it.q0 + i * BM, it.zq);
       ++nq;
       for (int t = 0; t < 2 * it.n_all; ++t, ++tg) {
         if (!(ok = wait_all(bar_empty(tg), ring_phase(tg) ^ 1u, W_KEMPTY))) break;
         mbar_arrive_expect_tx_elect(bar_full(tg), C::TILE_BYTES);
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(ring_addr(tg) + s * C::SLAB_BYTES, map, bar_full(tg), s * 64, (t >> 1) * BN, it.bh);
+          tma_load_3d_elect(ring_addr(tg) + s * C::SLAB_BYTES, map, bar_full(tg), s * 64, it.ykv + (t >> 1) * BN,
+                            it.zkv);
       }
     }
     // drain: every load issued must have landed before the CTA can exit
@@ -274,7 +318,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at(p, idx);
+        const Item it = item_at<D, PACKED>(p, idx);
         if (it.n_all == 0) continue;
         const int n = it.n_kv[i], sb = i ? st1 : st0;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
@@ -327,7 +371,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at(p, idx);
+        const Item it = item_at<D, PACKED>(p, idx);
         if (it.n_all == 0) continue;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
         ++nq;
@@ -389,9 +433,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
       const int idx = item_of_round(k, total);
       if (idx < 0) continue;
-      const Item it = item_at(p, idx);
-      const int n = it.n_kv[i], kvl = it.kvl, bh = it.bh;
-      const int r0 = it.q0 + i * BM;
+      // only what the score loop needs stays live through it; the epilogue looks the item up
+      // again for its output offsets
+      int n, kvl, r0;
+      {
+        const Item it = item_at<D, PACKED>(p, idx);
+        n = it.n_kv[i];
+        kvl = it.kvl;
+        r0 = it.q0 + i * BM;
+      }
       const int row = r0 + tt;
       float m = -INFINITY;  // running max of the scaled scores, log2 units
       float l = 0.f;
@@ -496,7 +546,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       if (have_o && !(ok = wait_all(bar_odone(i), (uint32_t)(sb + n - 1) & 1u, W_ODONE))) break;
       tc_fence_after_sync();
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = p.o + ((int64_t)bh * p.Nq + row) * D;
+      const Item it = item_at<D, PACKED>(p, idx);
+      const int64_t o_rs = PACKED ? p.o_rs : D;  // O row stride
+      __nv_bfloat16* orow = p.o + it.ob + (int64_t)row * o_rs;
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t orr[32];
@@ -513,7 +565,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l, __uint_as_float(orr[2 * e + 1]) * inv_l);
         // Each thread writes its own row: a warp's store touches 32 rows, so whole 32-byte
         // sectors per thread (half as many requests as 16-byte stores) matter here.
-        if (row < p.Nq) {
+        if (row < it.nq) {
           if (p.o_v8) {
             st_global_v8(orow + c, w);
             st_global_v8(orow + c + 16, w + 8);
@@ -526,8 +578,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           }
         }
       }
-      if (p.lse != nullptr && row < p.Nq)
-        p.lse[(int64_t)bh * p.Nq + row] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+      if (p.lse != nullptr && row < it.nq)
+        p.lse[it.lb + (int64_t)row * (PACKED ? p.l_rs : 1)] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
       // O_i has been read out: the next item's PV_i(0) (issued after this group's next P)
       // may overwrite it
       tc_fence_before_sync();
@@ -563,13 +615,16 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// [BH, N, D] bf16 viewed as a 3-D tensor (D innermost); box 64 x 128 x 1
-// with the 128-byte swizzle; rows past N read as zero.
-bool make_map(CUtensorMap* map, const void* base, int D, int N, int BH) {
+// bf16 rows of D elements viewed as a 3-D tensor (D innermost, then `rows` rows `row_bytes`
+// apart, then `planes` head planes `plane_bytes` apart); box 64 x 128 x 1 with the 128-byte
+// swizzle; rows past the end read as zero.  Dense [BH, N, D]: rows N, planes BH.  Packed
+// [T, H, D]: rows T (H D elements apart), planes H (D elements apart).
+bool make_map(CUtensorMap* map, const void* base, int D, int rows, int64_t row_bytes, int planes,
+              int64_t plane_bytes) {
   EncodeTiledFn enc = get_encode_fn();
   if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)N * D * 2};
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)(planes > 0 ? planes : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)plane_bytes};
   cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -581,7 +636,7 @@ constexpr int kMaxDevices = 64;
 
 // Persistent grid: one CTA per SM (the kernel holds an SM's TMEM and most of its shared
 // memory), never more CTAs than work items.
-template <int D>
+template <int D, bool PACKED>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                      cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
@@ -591,7 +646,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -599,35 +654,52 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   }
   const long long total = (long long)p.num_qblocks * p.BH;
   const unsigned grid = (unsigned)(total < sm_count[dev] ? total : sm_count[dev]);
-  attn_fwd_tc_kernel<D><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, PACKED><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int Nq,
-                           int Nk, int d, int causal, float scale, const int32_t* kv_len, const DevStatus& st,
-                           cudaStream_t s, const char** why) {
-  const int BH = B * H;
+cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s, const char** why) {
+  const int d = a.d, Hkv = a.Hkv;
+  const bool packed = a.cu_q != nullptr;
+  const int64_t rb = 2 * (int64_t)d;  // bytes per row of one head
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, q, d, Nq, BH) || !make_map(&mk, k, d, Nk, BH) || !make_map(&mv, v, d, Nk, BH)) {
+  bool maps_ok;
+  if (packed)
+    maps_ok = make_map(&mq, a.q, d, a.Tq, rb * a.H, a.H, rb) && make_map(&mk, a.k, d, a.Tk, rb * Hkv, Hkv, rb) &&
+              make_map(&mv, a.v, d, a.Tk, rb * Hkv, Hkv, rb);
+  else
+    maps_ok = make_map(&mq, a.q, d, a.Nq, rb, a.B * a.H, rb * a.Nq) &&
+              make_map(&mk, a.k, d, a.Nk, rb, a.B * Hkv, rb * a.Nk) &&
+              make_map(&mv, a.v, d, a.Nk, rb, a.B * Hkv, rb * a.Nk);
+  if (!maps_ok) {
     if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
   TcParams p;
-  p.o = static_cast<__nv_bfloat16*>(o);
-  p.o_v8 = (reinterpret_cast<uintptr_t>(o) % 32u) == 0 ? 1 : 0;
-  p.lse = lse;
-  p.kv_len = kv_len;
-  p.H = H;
-  p.Nq = Nq;
-  p.Nk = Nk;
-  p.causal = causal;
-  p.num_qblocks = (Nq + 2 * BM - 1) / (2 * BM);
-  p.BH = BH;
-  p.scale_log2 = scale * kLog2e;
+  p.o = static_cast<__nv_bfloat16*>(a.o);
+  p.o_v8 = (reinterpret_cast<uintptr_t>(a.o) % 32u) == 0 ? 1 : 0;
+  p.lse = a.lse;
+  p.kv_len = packed ? nullptr : a.kv_len;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.H = a.H;
+  p.Nq = a.Nq;
+  p.Nk = a.Nk;
+  p.causal = a.causal;
+  p.num_qblocks = (a.Nq + 2 * BM - 1) / (2 * BM);
+  p.BH = a.B * a.H;
+  p.group = a.H / Hkv;
+  p.o_rs = packed ? (int64_t)a.H * d : d;
+  p.l_rs = packed ? a.H : 1;
+  p.scale_log2 = a.scale * kLog2e;
   p.st = st;
-  return d == 128 ? launch_d<128>(mq, mk, mv, p, s) : launch_d<64>(mq, mk, mv, p, s);
+  if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
+  if (packed) return d == 128 ? launch_d<128, true>(mq, mk, mv, p, s) : launch_d<64, true>(mq, mk, mv, p, s);
+  return d == 128 ? launch_d<128, false>(mq, mk, mv, p, s) : launch_d<64, false>(mq, mk, mv, p, s);
 }
 
 }  // namespace oa

@@ -137,33 +137,111 @@ static oa_status check_attn(const void* q, const void* k, const void* v, void* o
   return OA_OK;
 }
 
-oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
-                      int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, oa_stream_t stream) {
-  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, "attn_fwd");
+static oa_status check_heads(int H, int Hkv, const char* who) {
+  if (Hkv < 1 || Hkv > H || H % Hkv != 0)
+    return fail(OA_ERR_INVALID, "%s: H_kv must divide H (H %d, H_kv %d)", who, H, Hkv);
+  return OA_OK;
+}
+
+static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                               int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                               const int32_t* kv_len, oa_stream_t stream, const char* who) {
+  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, who);
   if (s != OA_OK) return s;
-  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "attn_fwd: causal needs Nq == Nk");
-  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_fwd: kv_len must be 4-byte aligned");
-  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "attn_fwd: unknown dtype %d", (int)dt);
+  if ((s = check_heads(H, Hkv, who)) != OA_OK) return s;
+  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "%s: causal needs Nq == Nk", who);
+  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "%s: kv_len must be 4-byte aligned", who);
+  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "%s: unknown dtype %d", who, (int)dt);
   if (dt == OA_BF16 && d != 64 && d != 128)
-    return fail(OA_ERR_UNSUPPORTED, "attn_fwd: bf16 supports d = 64 or 128 (got %d)", d);
-  if (dt == OA_F32 && d > 256) return fail(OA_ERR_UNSUPPORTED, "attn_fwd: fp32 supports d <= 256 (got %d)", d);
+    return fail(OA_ERR_UNSUPPORTED, "%s: bf16 supports d = 64 or 128 (got %d)", who, d);
+  if (dt == OA_F32 && d > 256) return fail(OA_ERR_UNSUPPORTED, "%s: fp32 supports d <= 256 (got %d)", who, d);
   const int64_t grid = (int64_t)B * H * (dt == OA_BF16 ? (Nq + 255) / 256 : (Nq + 15) / 16);
-  if (grid > kMaxGrid) return fail(OA_ERR_INVALID, "attn_fwd: grid too large");
+  if (grid > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);
   oa::DevStatus st;
-  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "attn_fwd: no current CUDA device");
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
   if (dt == OA_BF16) {
+    oa::TcArgs a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.o = o;
+    a.lse = lse;
+    a.B = B;
+    a.H = H;
+    a.Hkv = Hkv;
+    a.Nq = Nq;
+    a.Nk = Nk;
+    a.d = d;
+    a.causal = causal;
+    a.scale = scale;
+    a.kv_len = kv_len;
     const char* why = nullptr;
-    cudaError_t e = oa::launch_attn_tc(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, kv_len, st,
-                                       (cudaStream_t)stream, &why);
-    if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "attn_fwd: %s", why) : cuda_fail(e, "attn_fwd launch");
+    cudaError_t e = oa::launch_attn_tc(a, st, (cudaStream_t)stream, &why);
+    if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_fwd launch");
     return ok();
   }
-  {
-    cudaError_t e = oa::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
-                                        static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, Nq, Nk, d,
-                                        causal, scale, kv_len, 0, 0, (cudaStream_t)stream);
-    return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd launch");
-  }
+  cudaError_t e = oa::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
+                                      static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, Hkv, Nq, Nk,
+                                      d, causal, scale, kv_len, 0, 0, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd launch");
+}
+
+oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
+                      int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len, oa_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, lse, dt, B, H, H, Nq, Nk, d, causal, scale, kv_len, stream, "attn_fwd");
+}
+
+oa_status oa_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                          int H, int H_kv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                          oa_stream_t stream) {
+  return attn_fwd_impl(q, k, v, o, lse, dt, B, H, H_kv, Nq, Nk, d, causal, scale, kv_len, stream, "attn_fwd_gqa");
+}
+
+oa_status oa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,
+                             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int num_seqs, int H,
+                             int H_kv, int total_q, int total_k, int max_seqlen_q, int max_seqlen_k, int d,
+                             int causal, float scale, oa_stream_t stream) {
+  const char* who = "attn_fwd_varlen";
+  if (!q || !k || !v || !o || !cu_seqlens_q || !cu_seqlens_k)
+    return fail(OA_ERR_INVALID, "%s: q, k, v, o and both cu_seqlens must be non-NULL", who);
+  if (num_seqs < 1 || H < 1 || d < 1 || total_q < 1 || total_k < 0 || max_seqlen_q < 1 || max_seqlen_k < 0)
+    return fail(OA_ERR_INVALID, "%s: need num_seqs, H, d, total_q, max_seqlen_q >= 1 and total_k, max_seqlen_k >= 0",
+                who);
+  oa_status s = check_heads(H, H_kv, who);
+  if (s != OA_OK) return s;
+  if (!(std::isfinite(scale) && scale > 0.f)) return fail(OA_ERR_INVALID, "%s: scale must be finite and > 0", who);
+  if (causal != 0 && causal != 1) return fail(OA_ERR_INVALID, "%s: causal must be 0 or 1", who);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return fail(OA_ERR_INVALID, "%s: q/k/v/o must be 16-byte aligned, lse and cu_seqlens 4-byte", who);
+  if (dt != OA_BF16) return fail(OA_ERR_UNSUPPORTED, "%s: bf16 only", who);
+  if (d != 64 && d != 128) return fail(OA_ERR_UNSUPPORTED, "%s: d = 64 or 128 (got %d)", who, d);
+  if ((int64_t)num_seqs * H * ((max_seqlen_q + 255) / 256) > (int64_t)1 << 31)
+    return fail(OA_ERR_INVALID, "%s: too many work items", who);
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  oa::TcArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.lse = lse;
+  a.B = num_seqs;
+  a.H = H;
+  a.Hkv = H_kv;
+  a.Nq = max_seqlen_q;
+  a.Nk = max_seqlen_k;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.Tq = total_q;
+  a.Tk = total_k;
+  const char* why = nullptr;
+  cudaError_t e = oa::launch_attn_tc(a, st, (cudaStream_t)stream, &why);
+  if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_fwd_varlen launch");
+  return ok();
 }
 
 oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, float* o, float* lse, int B, int H,
@@ -179,7 +257,7 @@ oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, 
   if (smem > 227 * 1024) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: tiles need %zu bytes of smem", smem);
   if ((int64_t)B * H * ((Nq + Br - 1) / Br) > kMaxGrid) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: grid");
   cudaError_t e =
-      oa::launch_attn_f32(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, kv_len, Br, Bc, (cudaStream_t)stream);
+      oa::launch_attn_f32(q, k, v, o, lse, B, H, H, Nq, Nk, d, causal, scale, kv_len, Br, Bc, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd_f32_tiles launch");
 }
 
@@ -189,11 +267,12 @@ size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   return (floats * sizeof(float) + 255) / 256 * 256;
 }
 
-oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
-                          int H, int Nq, int Nk, int d, float scale, const int32_t* kv_len, int num_splits,
-                          void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+static oa_status attn_splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,
+                                   int B, int H, int Hkv, int Nq, int Nk, int d, float scale, const int32_t* kv_len,
+                                   int num_splits, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
   oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, 0, scale, "attn_splitkv");
   if (s != OA_OK) return s;
+  if ((s = check_heads(H, Hkv, "attn_splitkv")) != OA_OK) return s;
   if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "attn_splitkv: unknown dtype %d", (int)dt);
   if (!oa::splitkv_supported(dt == OA_BF16, d))
     return fail(OA_ERR_UNSUPPORTED, "attn_splitkv: unsupported (dtype %d, d %d)", (int)dt, d);
@@ -206,11 +285,25 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
     return fail(OA_ERR_INVALID, "attn_splitkv: workspace must be 16-byte aligned and >= %zu bytes", need);
   float* part_o = static_cast<float*>(workspace);
   float* part_lse = part_o + (size_t)num_splits * R * d;
-  cudaError_t e = oa::launch_splitkv_partial(q, k, v, dt == OA_BF16, B, H, Nq, Nk, d, scale, kv_len, num_splits,
+  cudaError_t e = oa::launch_splitkv_partial(q, k, v, dt == OA_BF16, B, H, Hkv, Nq, Nk, d, scale, kv_len, num_splits,
                                              part_o, part_lse, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "attn_splitkv partial launch");
   e = oa::launch_lse_merge(part_o, part_lse, num_splits, R, d, o, dt == OA_BF16, lse, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "attn_splitkv merge launch");
+}
+
+oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                          int H, int Nq, int Nk, int d, float scale, const int32_t* kv_len, int num_splits,
+                          void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  return attn_splitkv_impl(q, k, v, o, lse, dt, B, H, H, Nq, Nk, d, scale, kv_len, num_splits, workspace,
+                           workspace_bytes, stream);
+}
+
+oa_status oa_attn_splitkv_gqa(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                              int H, int H_kv, int Nq, int Nk, int d, float scale, const int32_t* kv_len,
+                              int num_splits, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  return attn_splitkv_impl(q, k, v, o, lse, dt, B, H, H_kv, Nq, Nk, d, scale, kv_len, num_splits, workspace,
+                           workspace_bytes, stream);
 }
 
 oa_status oa_lse_merge(const float* part_o, const float* part_lse, int S, int64_t R, int d, void* o, oa_dtype o_dt,
@@ -240,6 +333,9 @@ oa_status oa_sync_status(oa_stream_t stream) {
   const unsigned int zero = 0;
   e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
   if (e != cudaSuccess) return cuda_fail(e, "sync_status: clear status word");
+  if (word == oa::kSiteBadSeqlen)
+    return fail(OA_ERR_INVALID, "a packed query sequence is longer than the declared max_seqlen_q; "
+                                "its rows past that length were not computed");
   return fail(OA_ERR_TIMEOUT, "device wait expired: kernel %u, wait site %u", word >> 8, word & 0xFFu);
 }
 

@@ -31,6 +31,10 @@ enum KernelId : unsigned {
   K_SELFTEST = 6,
 };
 
+// Not a wait: a packed sequence longer than the maximum its call declared (its tail rows
+// were not computed).  Reported by oa_sync_status as OA_ERR_INVALID.
+constexpr unsigned kSiteBadSeqlen = (K_ATTN_TC << 8) | 0xF0u;
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

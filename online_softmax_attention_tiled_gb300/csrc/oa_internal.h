@@ -17,20 +17,34 @@ cudaError_t launch_lse_merge(const float* part_o, const float* part_lse, int S, 
                              bool o_bf16, float* lse, cudaStream_t s);
 
 cudaError_t launch_attn_f32(const float* q, const float* k, const float* v, float* o, float* lse, int B,
-                            int H, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                            int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
                             int Br, int Bc, cudaStream_t s);
 
 // True if (bf16, d) / (fp32, d) has a split-KV partial kernel.
 bool splitkv_supported(bool bf16, int d);
-cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, bool bf16, int B, int H,
+// K/V have Hkv heads; query head h reads head h / (H / Hkv).
+cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, bool bf16, int B, int H, int Hkv,
                                    int Nq, int Nk, int d, float scale, const int32_t* kv_len,
                                    int num_splits, float* part_o, float* part_lse, cudaStream_t s);
 
-// Tensor-core attention (tcgen05 + TMA), bf16, d in {64, 128}.  `why` gets
-// a static message when the host-side set-up (tensor maps) fails.
-cudaError_t launch_attn_tc(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                           int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
-                           const DevStatus& st, cudaStream_t s, const char** why);
+// Tensor-core attention (tcgen05 + TMA), bf16, d in {64, 128}.
+//   dense  (cu_q == NULL): q/o [B, H, Nq, d], k/v [B, Hkv, Nk, d], kv_len[B] or NULL.
+//   packed (cu_q != NULL): B sequences; q/o [Tq, H, d], k/v [Tk, Hkv, d], lse [Tq, H];
+//          sequence s has query tokens [cu_q[s], cu_q[s+1]) and key tokens [cu_k[s], cu_k[s+1]);
+//          Nq / Nk are the longest query / key sequence.
+// Query head h reads key/value head h / (H / Hkv).
+struct TcArgs {
+  const void *q, *k, *v;
+  void* o;
+  float* lse;
+  int B, H, Hkv, Nq, Nk, d, causal;
+  float scale;
+  const int32_t* kv_len;
+  const int32_t *cu_q, *cu_k;
+  int Tq, Tk;
+};
+// `why` gets a static message when the host-side set-up (tensor maps) fails.
+cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s, const char** why);
 
 cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s);
 

@@ -54,7 +54,7 @@ def _load():
     vp, i64, i32, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.oracle_softmax_rows.argtypes = [vp, i32, i64, i64, i64, vp, i64, vp, i32]
     lib.oracle_softmax_rows.restype = i32
-    lib.oracle_attn.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, dbl, vp, vp, i64, vp, vp, i32]
+    lib.oracle_attn.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32, dbl, vp, vp, i64, vp, vp, i32]
     lib.oracle_attn.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
     lib.oracle_lse_merge.restype = i32
@@ -113,7 +113,8 @@ def softmax_rows(x, nthreads=None):
 def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthreads=None):
     """Materialised softmax(Q K^T * scale) V and per-row LSE, in fp64.
 
-    q [B,H,Nq,d], k/v [B,H,Nk,d] (same dtype code).  kv_len: None or int array [B].
+    q [B,H,Nq,d], k/v [B,Hkv,Nk,d] (same dtype code; Hkv divides H and query head h
+    reads key/value head h // (H // Hkv)).  kv_len: None or int array [B].
     rows: None for every row, else flattened row indices (b*H + h)*Nq + i; then the
     result has shape [len(rows), d] and [len(rows)].
     """
@@ -125,9 +126,11 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthread
     if qa.ndim != 4 or ka.ndim != 4 or va.ndim != 4:
         raise ValueError("q, k, v must be [B,H,N,d]")
     B, H, Nq, d = qa.shape
-    Nk = ka.shape[2]
-    if ka.shape != (B, H, Nk, d) or va.shape != (B, H, Nk, d):
+    Hkv, Nk = ka.shape[1], ka.shape[2]
+    if ka.shape != (B, Hkv, Nk, d) or va.shape != (B, Hkv, Nk, d):
         raise ValueError("k/v shape mismatch")
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError("the key/value head count must divide the query head count")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     kvl = None
@@ -143,12 +146,41 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthread
         n = ra.shape[0]
     o = np.zeros((n, d), np.float64)
     lse = np.empty(n, np.float64)
-    rc = _load().oracle_attn(_ptr(qa), _ptr(ka), _ptr(va), code, B, H, Nq, Nk, d, int(bool(causal)),
+    rc = _load().oracle_attn(_ptr(qa), _ptr(ka), _ptr(va), code, B, H, Hkv, Nq, Nk, d, int(bool(causal)),
                              float(scale), _ptr(kvl), _ptr(ra), n, _ptr(o), _ptr(lse), _threads(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_attn failed")
     if rows is None:
         return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
+    return o, lse
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, nthreads=None):
+    """Attention over packed sequences, in fp64: q [Tq,H,d], k/v [Tk,Hkv,d] (token-major, same dtype
+    code); sequence s is q tokens [cu_q[s], cu_q[s+1]) and k/v tokens [cu_k[s], cu_k[s+1]).  Each
+    sequence is the attention() of its own tokens (the per-(b, h) definition above, one batch entry;
+    causal: key j visible to query i iff j <= i, positions counted within the sequence).  Only
+    slicing and transposes happen here.  Returns (o [Tq,H,d], lse [Tq,H])."""
+    qa, _ = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    cq = np.asarray(cu_seqlens_q, dtype=np.int64)
+    ck = np.asarray(cu_seqlens_k, dtype=np.int64)
+    if cq.shape != ck.shape or cq.ndim != 1 or cq.shape[0] < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be [num_seqs + 1]")
+    Tq, H, d = qa.shape
+    o = np.zeros((Tq, H, d), np.float64)
+    lse = np.full((Tq, H), -np.inf, np.float64)
+    for s in range(cq.shape[0] - 1):
+        q0, q1, k0, k1 = int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])
+        if q1 <= q0:
+            continue
+        qs = np.ascontiguousarray(qa[q0:q1].transpose(1, 0, 2)[None])
+        ks = np.ascontiguousarray(ka[k0:k1].transpose(1, 0, 2)[None])
+        vs = np.ascontiguousarray(va[k0:k1].transpose(1, 0, 2)[None])
+        os_, ls_ = attention(qs, ks, vs, causal=causal, scale=scale, nthreads=nthreads)
+        o[q0:q1] = os_[0].transpose(1, 0, 2)
+        lse[q0:q1] = ls_[0].T
     return o, lse
 
 

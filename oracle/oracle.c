@@ -164,12 +164,14 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t rows, int64_t cols, in
 /* [OS-RM] s.5: A_i = sum_j softmax(Q K^T)_ij V_j;                      */
 /* [OS-PT]: s_t2 = (q_t1 . k_t2) / sqrt(hd), causal t2 <= t1;           */
 /* [OS-IL] Step 2: S = q K^T * scale.                                   */
-/* Layout: q [B,H,Nq,d], k and v [B,H,Nk,d], row-major contiguous.      */
+/* Layout: q [B,H,Nq,d], k and v [B,Hkv,Nk,d], row-major contiguous;  */
+/* query head h reads key/value head h / (H / Hkv) (grouped heads;      */
+/* Hkv == H is one key/value head per query head).                      */
 /* ------------------------------------------------------------------ */
 typedef struct {
   const void *q, *k, *v;
   int dtype;
-  int64_t B, H, Nq, Nk, d;
+  int64_t B, H, Hkv, Nq, Nk, d;
   int causal;
   double scale;
   const int32_t* kv_len;
@@ -190,7 +192,8 @@ static void attn_range(void* p, int64_t t0, int64_t t1, double* s) {
       if (kvl > c->Nk) kvl = c->Nk;
       if (kvl < 0) kvl = 0;
     }
-    const int64_t qbase = row * d, kvbase = bh * c->Nk * d;
+    const int64_t h = bh % c->H, kvh = b * c->Hkv + h / (c->H / c->Hkv);
+    const int64_t qbase = row * d, kvbase = kvh * c->Nk * d;
     /* full score row, -inf where masked */
     for (int64_t j = 0; j < c->Nk; ++j) {
       int visible = (j < kvl) && (!c->causal || j <= i);
@@ -231,10 +234,12 @@ static void attn_range(void* p, int64_t t0, int64_t t1, double* s) {
  * listed flattened rows, o is [nrows, d], lse is [nrows].  kv_len (NULL or
  * int32[B]) hides keys j >= kv_len[b].  Returns 0, or -1 on bad arguments. */
 int oracle_attn(const void* q, const void* k, const void* v, int dtype, int64_t B, int64_t H,
-                int64_t Nq, int64_t Nk, int64_t d, int causal, double scale, const int32_t* kv_len,
-                const int64_t* rows, int64_t nrows, double* o, double* lse, int nthreads) {
+                int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, double scale,
+                const int32_t* kv_len, const int64_t* rows, int64_t nrows, double* o, double* lse,
+                int nthreads) {
   if (!q || !k || !v || B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return -1;
-  attn_ctx c = {q, k, v, dtype, B, H, Nq, Nk, d, causal, scale, kv_len, rows, o, lse};
+  if (Hkv < 1 || H % Hkv != 0) return -1;
+  attn_ctx c = {q, k, v, dtype, B, H, Hkv, Nq, Nk, d, causal, scale, kv_len, rows, o, lse};
   int64_t n = rows ? nrows : B * H * Nq;
   if (rows)
     for (int64_t t = 0; t < nrows; ++t)

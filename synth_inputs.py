@@ -6,7 +6,9 @@ can be fed from it without sharing any of the method's code.
 
 Recipe (all seeded; tensor k of a call uses seed + k):
   * attention Q, K, V: N(0, 1) drawn in fp32, then rounded to nearest-even into
-    the requested dtype (bf16 or fp32);
+    the requested dtype (bf16 or fp32); K and V may have fewer heads than Q
+    (grouped heads), or be packed token-major [tokens, heads, d] with int32
+    offsets of a list of sequence lengths (variable-length batches);
   * row-softmax X: N(0, 1) * 4 in fp32; round(1% of rows) fully -inf; another
     10% of rows (disjoint, chosen by a seeded permutation) get a -inf prefix of
     length uniform in [1, cols - 1];
@@ -17,6 +19,7 @@ Recipe (all seeded; tensor k of a call uses seed + k):
 """
 from __future__ import annotations
 
+import itertools
 import math
 
 import torch
@@ -44,6 +47,31 @@ def attn_inputs(B, H, Nq, Nk, d, dtype=torch.bfloat16, seed=0, device="cpu"):
     k = randn((B, H, Nk, d), seed + 1, dtype, device)
     v = randn((B, H, Nk, d), seed + 2, dtype, device)
     return q, k, v
+
+
+def attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Q [B,H,Nq,d], K and V [B,Hkv,Nk,d] ~ N(0,1) (grouped key/value heads)."""
+    q = randn((B, H, Nq, d), seed, dtype, device)
+    k = randn((B, Hkv, Nk, d), seed + 1, dtype, device)
+    v = randn((B, Hkv, Nk, d), seed + 2, dtype, device)
+    return q, k, v
+
+
+def varlen_lengths(n, max_len, seed=0, min_len=0):
+    """n sequence lengths, uniform on [min_len, max_len], as a Python list."""
+    g = _gen(seed)
+    return torch.randint(min_len, max_len + 1, (n,), generator=g, dtype=torch.int64).tolist()
+
+
+def varlen_inputs(lq, lk, H, Hkv, d, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Packed token-major Q [sum lq, H, d], K and V [sum lk, Hkv, d] ~ N(0,1), and the int32 offsets
+    cu_q = [0, lq0, lq0 + lq1, ...], cu_k likewise."""
+    cu_q = torch.tensor([0] + list(itertools.accumulate(lq)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(lk)), dtype=torch.int32)
+    q = randn((int(cu_q[-1]), H, d), seed, dtype, device)
+    k = randn((int(cu_k[-1]), Hkv, d), seed + 1, dtype, device)
+    v = randn((int(cu_k[-1]), Hkv, d), seed + 2, dtype, device)
+    return q, k, v, cu_q, cu_k
 
 
 def softmax_input(rows, cols, seed=0, mul=4.0, frac_full=0.01, frac_prefix=0.10, device="cpu"):

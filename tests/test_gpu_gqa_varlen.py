@@ -1,0 +1,116 @@
+"""Grouped key/value heads and packed variable-length sequences vs the fp64 oracle (gpu).
+
+Covers the tensor-core forward (oa_attn_fwd_gqa, oa_attn_fwd_varlen), the fp32 forward with grouped
+heads and split-KV decode over a grouped KV cache (oa_attn_splitkv_gqa).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from parity import BF16_O_ATOL, assert_lse_close, assert_out_close, bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _sync(oa):
+    torch.cuda.synchronize()
+    oa.sync_status()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Hkv", [1, 2, 4])
+def test_gqa_tensor_core(cuda_lib, d, causal, Hkv):
+    B, H, N = 2, 8, 300
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, N, N, d, torch.bfloat16, seed=40 + d + Hkv)
+    kv_len = [N, 129]
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal,
+                               kv_len=torch.tensor(kv_len, dtype=torch.int32).cuda())
+    _sync(cuda_lib)
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=causal, kv_len=kv_len)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+def test_gqa_fp32(cuda_lib):
+    B, H, Hkv, Nq, Nk, d = 2, 6, 3, 33, 70, 40
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.float32, seed=50)
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda())
+    _sync(cuda_lib)
+    ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy())
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, 1e-5, lse_ref=rl)
+
+
+def test_gqa_rejects_non_divisor(cuda_lib):
+    q, k, v = si.attn_inputs_gqa(1, 6, 4, 16, 16, 64, torch.bfloat16, seed=1)
+    with pytest.raises(cuda_lib.OAError):
+        cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda())
+
+
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.float32, 64)])
+def test_gqa_splitkv_decode(cuda_lib, dtype, d):
+    # a grouped KV cache of different lengths per sequence, one query token per head
+    B, H, Hkv, Nk, splits = 4, 8, 2, 1000, 8
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, 1, Nk, d, dtype, seed=60 + d)
+    kv_len = [1000, 1, 0, 555]
+    o, lse = cuda_lib.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), splits,
+                                   kv_len=torch.tensor(kv_len, dtype=torch.int32).cuda())
+    _sync(cuda_lib)
+    if dtype == torch.bfloat16:
+        ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), kv_len=kv_len)
+        atol = BF16_O_ATOL
+    else:
+        ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy(), kv_len=kv_len)
+        atol = 2e-5
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, atol, lse_ref=rl)
+
+
+def _varlen_check(oa, lq, lk, H, Hkv, d, causal, seed, max_q=None, max_k=None):
+    q, k, v, cq, ck = si.varlen_inputs(lq, lk, H, Hkv, d, torch.bfloat16, seed=seed)
+    o, lse = oa.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(),
+                                max(lq) if max_q is None else max_q, max(lk) if max_k is None else max_k,
+                                causal=causal)
+    _sync(oa)
+    ro, rl = oracle.attention_varlen(bf16_bits(q), bf16_bits(k), bf16_bits(v), cq.numpy(), ck.numpy(),
+                                     causal=causal)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_self_attention(cuda_lib, d, causal):
+    # lengths crossing tile edges, a 1-token and an empty sequence, one over two tiles of 256 rows
+    lens = [300, 1, 0, 513, 128, 77, 256, 129]
+    _varlen_check(cuda_lib, lens, lens, 4, 2, d, causal, seed=70 + d)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_cross_lengths(cuda_lib, causal):
+    # query and key lengths differ per sequence (a sequence with keys but no queries, and one with
+    # queries but no keys: O = 0, lse = -inf)
+    lq = [100, 0, 257, 40, 3]
+    lk = [333, 50, 129, 0, 700]
+    _varlen_check(cuda_lib, lq, lk, 8, 8, 128, causal, seed=80)
+
+
+def test_varlen_many_sequences(cuda_lib):
+    # more work items than SMs: 64 sequences x 8 heads, lengths in [0, 600]
+    lens = si.varlen_lengths(64, 600, seed=90)
+    _varlen_check(cuda_lib, lens, lens, 8, 2, 64, True, seed=91)
+
+
+def test_varlen_sequence_longer_than_declared_max(cuda_lib):
+    # a query sequence longer than max_seqlen_q is reported through the status word; the kernel
+    # writes the rows it covers and reads or writes nothing outside the tensors
+    lens = [600, 100]
+    q, k, v, cq, ck = si.varlen_inputs(lens, lens, 2, 2, 64, torch.bfloat16, seed=95)
+    cuda_lib.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), 300, 600)
+    torch.cuda.synchronize()
+    with pytest.raises(cuda_lib.OAError):
+        cuda_lib.sync_status()
+    cuda_lib.sync_status()  # the word was cleared: the next call is clean

@@ -361,6 +361,86 @@ def _partials(q, k, v, chunk, kv_len=None):
     return po, pl
 
 
+def _brute_attention_rows(q, k, v, causal, scale):
+    """softmax(q k^T scale) v for one head in plain fp64 numpy, -inf where masked (key j > query i)."""
+    s = (q @ k.T) * scale
+    if causal:
+        s = np.where(np.arange(k.shape[0])[None, :] > np.arange(q.shape[0])[:, None], -np.inf, s)
+    m = s.max(axis=1, keepdims=True) if s.shape[1] else np.full((s.shape[0], 1), -np.inf)
+    o = np.zeros((q.shape[0], v.shape[1]))
+    lse = np.full(q.shape[0], -np.inf)
+    for i in range(q.shape[0]):
+        if not np.isfinite(m[i, 0]):
+            continue
+        w = np.exp(s[i] - m[i, 0])
+        o[i] = (w @ v) / w.sum()
+        lse[i] = m[i, 0] + np.log(w.sum())
+    return o, lse
+
+
+def test_attention_grouped_heads_reduce_to_repeated_heads():
+    # grouped key/value heads: query head h reads head h // (H // Hkv).  Pinned to the per-head
+    # oracle with K and V repeated across each group, and to brute force for one head.
+    rng = np.random.default_rng(5)
+    B, H, Hkv, Nq, Nk, d = 2, 6, 2, 7, 9, 8
+    q = rng.standard_normal((B, H, Nq, d))
+    k = rng.standard_normal((B, Hkv, Nk, d))
+    v = rng.standard_normal((B, Hkv, Nk, d))
+    for causal in (False, True):
+        og, lg = oracle.attention(q, k, v, causal=causal, kv_len=[9, 4])
+        orp, lrp = oracle.attention(q, np.repeat(k, H // Hkv, axis=1), np.repeat(v, H // Hkv, axis=1),
+                                    causal=causal, kv_len=[9, 4])
+        np.testing.assert_array_equal(og, orp)
+        np.testing.assert_array_equal(lg, lrp)
+    # brute force: batch 1, query head 5 uses key/value head 1 over the first 4 keys
+    ob, lb = _brute_attention_rows(q[1, 5], k[1, 1, :4], v[1, 1, :4], False, 1 / math.sqrt(d))
+    og, lg = oracle.attention(q, k, v, kv_len=[9, 4])
+    np.testing.assert_allclose(og[1, 5], ob, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lg[1, 5], lb, rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.attention(q, k[:, :1].repeat(4, axis=1), v[:, :1].repeat(4, axis=1))  # 4 does not divide 6
+
+
+def test_attention_varlen_equal_lengths_is_dense_batch():
+    # packed token-major sequences of one length N equal the dense [B, H, N, d] batch
+    rng = np.random.default_rng(6)
+    B, H, Hkv, N, d = 3, 4, 2, 10, 8
+    q = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    pack = lambda t: np.ascontiguousarray(t.transpose(0, 2, 1, 3).reshape(B * N, t.shape[1], d))
+    cu = np.arange(0, (B + 1) * N, N)
+    for causal in (False, True):
+        od, ld = oracle.attention(q, k, v, causal=causal)
+        ov, lv = oracle.attention_varlen(pack(q), pack(k), pack(v), cu, cu, causal=causal)
+        np.testing.assert_array_equal(ov, pack(od))
+        np.testing.assert_array_equal(lv, ld.transpose(0, 2, 1).reshape(B * N, H))
+
+
+def test_attention_varlen_brute_force_mixed_lengths():
+    # mixed lengths, a sequence without keys (O = 0, lse = -inf), one without queries, and causal
+    # with more keys than queries (key j visible to query i iff j <= i within the sequence)
+    rng = np.random.default_rng(7)
+    H, Hkv, d = 4, 2, 8
+    lq, lk = [5, 3, 0, 6], [7, 0, 2, 6]
+    cq, ck = np.concatenate([[0], np.cumsum(lq)]), np.concatenate([[0], np.cumsum(lk)])
+    q = rng.standard_normal((cq[-1], H, d))
+    k = rng.standard_normal((ck[-1], Hkv, d))
+    v = rng.standard_normal((ck[-1], Hkv, d))
+    sc = 0.3
+    for causal in (False, True):
+        ov, lv = oracle.attention_varlen(q, k, v, cq, ck, causal=causal, scale=sc)
+        for s in range(len(lq)):
+            for h in range(H):
+                ob, lb = _brute_attention_rows(q[cq[s]:cq[s + 1], h], k[ck[s]:ck[s + 1], h // 2],
+                                               v[ck[s]:ck[s + 1], h // 2], causal, sc)
+                np.testing.assert_allclose(ov[cq[s]:cq[s + 1], h], ob, rtol=1e-12, atol=1e-12)
+                np.testing.assert_array_equal(np.isneginf(lv[cq[s]:cq[s + 1], h]), np.isneginf(lb))
+                fin = np.isfinite(lb)
+                np.testing.assert_allclose(lv[cq[s]:cq[s + 1], h][fin], lb[fin], rtol=1e-12, atol=1e-12)
+    assert np.all(ov[cq[1]:cq[2]] == 0) and np.all(np.isneginf(lv[cq[1]:cq[2]]))
+
+
 def test_lse_merge_reaches_unsplit_attention():
     B, H, Nq, Nk, d = 3, 2, 2, 50, 8
     q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=16)
