@@ -3,9 +3,11 @@
 Prints ONE JSON line (rank 0).  The headline workload is the fused causal
 attention forward, bf16, B=1 H=32 N=8192 d=128 (one "step" = one forward
 over that batch); the row softmax + LSE on fp32 [4096, 32768] (the metric's
-second half), the non-causal B4 H16 N4096 d64 forward and the split-KV
-decode B32 H32 Nk32768 d128 are measured in the same run and reported under
-"components", each against its own roofline.
+second half), the non-causal B4 H16 N4096 d64 forward, the split-KV decode
+B32 H32 Nk32768 d128 (and the same over a grouped cache with 8 key/value
+heads) and a causal forward over 16 packed sequences of mixed length are
+measured in the same run and reported under "components", each against its
+own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--components/--no-components] [--no-cpu-baseline]
@@ -57,9 +59,15 @@ def softmax_bytes(rows, cols):
     return 4.0 * rows * cols * 2 + 4.0 * rows
 
 
-def decode_bytes(b, h, d, kv_len_sum, esize=2):
-    """q, the visible K and V rows, O and LSE."""
-    return esize * (2.0 * h * d * kv_len_sum + b * h * d * 2) + 4.0 * b * h
+def decode_bytes(b, h, d, kv_len_sum, esize=2, h_kv=None):
+    """q, the visible K and V rows (h_kv heads; default h), O and LSE."""
+    h_kv = h if h_kv is None else h_kv
+    return esize * (2.0 * h_kv * d * kv_len_sum + b * h * d * 2) + 4.0 * b * h
+
+
+def varlen_causal_flops(lengths, h, d):
+    """4*d FLOPs per visible (query, key) pair, L(L+1)/2 pairs per head of a sequence of length L."""
+    return sum(4.0 * h * d * n * (n + 1) / 2 for n in lengths)
 
 
 # --------------------------------------------------------------------------
@@ -266,7 +274,40 @@ def components(oa, dev, peaks, peak_kind, steps):
                                   "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
                                   "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
                                   "algorithmic_bytes": nbytes, "launches_per_call": 2}
-    del q, k, v, o, lse, ws, flush_buf
+    del q, k, v, o, lse, ws
+    # split-KV decode over a grouped KV cache: B32 H32 with 8 key/value heads, same lengths
+    q, k, v = si.attn_inputs_gqa(32, 32, 8, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((32, 32, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(oa.splitkv_workspace_bytes(32, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+    t = time_launches(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws), steps, 3,
+                      flush)
+    ms = statistics.mean(t)
+    nbytes = decode_bytes(32, 32, 128, int(kv_len.sum()), h_kv=8)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out["attn_splitkv_decode_gqa"] = {"workload": "split-KV decode bf16 B=32 H=32 H_kv=8 Nq=1 Nk=32768 d=128, 64 "
+                                                  "chunks of 512, same truncations (KV 4.3 GB > L2)", "ms": ms,
+                                      "value": gbs, "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
+                                      "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
+                                      "algorithmic_bytes": nbytes, "launches_per_call": 2}
+    del q, k, v, o, lse, ws
+    # causal prefill over packed sequences of mixed length, grouped key/value heads
+    lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
+    q, k, v, cq, ck = si.varlen_inputs(lens, lens, 32, 8, 128, torch.bfloat16, seed=0, device=dev)
+    cq, ck = cq.to(dev), ck.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[0], 32), dtype=torch.float32, device=dev)
+    mx = max(lens)
+    t = time_launches(lambda: oa.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse), steps, 3,
+                      flush)
+    ms = statistics.mean(t)
+    tf = varlen_causal_flops(lens, 32, 128) / (ms * 1e-3) / 1e12
+    out["attn_varlen_causal_gqa"] = {"workload": f"causal attention fwd bf16 over 16 packed sequences, lengths U[1024, "
+                                                 f"8192] (total {sum(lens)} tokens), H=32 H_kv=8 d=128", "ms": ms,
+                                     "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
+                                     "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
+                                     "algorithmic_flops": varlen_causal_flops(lens, 32, 128)}
+    del q, k, v, o, lse, flush_buf
     torch.cuda.empty_cache()
     return out
 

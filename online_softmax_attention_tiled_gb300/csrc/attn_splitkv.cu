@@ -15,7 +15,9 @@
 // warps through shared memory.  Scores are kept in log2 units (the scale is
 // folded with log2 e into q), so each exponential is one ex2.
 // Keys at or beyond kv_len[b] are never read; a chunk with no visible key
-// writes o_c = 0, lse_c = -inf.
+// writes o_c = 0, lse_c = -inf.  With grouped key/value heads (a KV cache
+// with H / H_kv query heads per key/value head) one CTA serves the whole
+// group: every K/V row is read once and scored against each of its queries.
 #include "oa_internal.h"
 
 namespace oa {
@@ -211,9 +213,197 @@ __global__ void __launch_bounds__(kWarps * 32) splitkv_partial_kernel(
   }
 }
 
+// Grouped key/value heads: grid.x = (R / NQ) * S; one (b, key/value head, i) per CTA, whose NQ
+// (= group) query heads share every K/V load, each with its own running (m, l, o).  The same
+// recurrence and merges as splitkv_partial_kernel, NQ-wide.
+template <typename T, int D, int NQ>
+__global__ void __launch_bounds__(kWarps * 32) splitkv_group_kernel(
+    const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, float* __restrict__ part_o,
+    float* __restrict__ part_lse, int H, int Nq, int Nk, int chunk, int S, float scale_log2,
+    const int32_t* __restrict__ kv_len, int64_t R, int group) {
+  constexpr int EPL = Lanes<T>::kPerLane;  // elements per lane (16 bytes)
+  constexpr int LPK = D / EPL;             // lanes per key row
+  constexpr int G = 32 / LPK;              // key rows per warp load
+  constexpr int NG = kWarps * G;           // key groups in the CTA
+  constexpr int KU = NQ >= 8 ? 2 : kU;  // keys per group per step (registers)
+  static_assert(LPK >= 1 && LPK <= 32 && (32 % LPK) == 0, "unsupported head dim");
+
+  __shared__ float sm_m[NQ][kWarps], sm_l[NQ][kWarps];
+  __shared__ float sm_o[NQ][kWarps][D];
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t crow = blockIdx.x / S;
+  const int c = (int)(blockIdx.x % S);
+  int64_t rows[NQ];
+  int b;
+  int64_t kvbh;  // key/value plane b H_kv + head
+  static_assert(NQ > 1, "one query head per CTA is splitkv_partial_kernel");
+  {
+    const int Hkv = H / group;
+    const int qi = (int)(crow % Nq);
+    kvbh = crow / Nq;
+    b = (int)(kvbh / Hkv);
+    const int hkv = (int)(kvbh % Hkv);
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) rows[t] = ((int64_t)b * H + hkv * NQ + t) * Nq + qi;
+  }
+  int kvl = Nk;
+  if (kv_len != nullptr) kvl = min(max(kv_len[b], 0), Nk);
+  const int j0 = c * chunk;
+  const int j1 = min(kvl, j0 + chunk);
+
+  if (j0 >= j1) {  // empty chunk: zero weight in the merge
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+      float* out_o = part_o + ((int64_t)c * R + rows[t]) * D;
+      for (int e = threadIdx.x; e < D; e += kWarps * 32) out_o[e] = 0.f;
+      if (threadIdx.x == 0) part_lse[(int64_t)c * R + rows[t]] = -INFINITY;
+    }
+    return;
+  }
+
+  const int sub = lane % LPK;            // which 16-byte piece of the row
+  const int grp = warp * G + lane / LPK; // key group
+
+  float qv[NQ][EPL];
+  State<EPL> st[NQ];
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    Lanes<T>::unpack(*reinterpret_cast<const uint4*>(q + rows[t] * D + sub * EPL), qv[t]);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) qv[t][e] *= scale_log2;
+    st[t].m = -INFINITY;
+    st[t].l = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) st[t].o[e] = 0.f;
+  }
+
+  const T* kb = k + (kvbh * Nk) * (int64_t)D + sub * EPL;
+  const T* vb = v + (kvbh * Nk) * (int64_t)D + sub * EPL;
+
+  for (int base = j0; base < j1; base += NG * KU) {
+    uint4 kr[KU], vr[KU];
+    bool ok[KU];
+#pragma unroll
+    for (int u = 0; u < KU; ++u) {
+      const int j = base + u * NG + grp;
+      ok[u] = j < j1;
+      if (ok[u]) {
+        kr[u] = ld_stream(kb + (int64_t)j * D);
+        vr[u] = ld_stream(vb + (int64_t)j * D);
+      }
+    }
+    float s[KU][NQ];
+#pragma unroll
+    for (int u = 0; u < KU; ++u) {
+      float kf[EPL];
+      Lanes<T>::unpack(ok[u] ? kr[u] : make_uint4(0, 0, 0, 0), kf);
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qv[t][e], kf[e], dot);
+#pragma unroll
+        for (int off = LPK / 2; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
+        s[u][t] = ok[u] ? dot : -INFINITY;
+      }
+    }
+    float vf[KU][EPL];  // each V row unpacked once for all the group's query heads
+#pragma unroll
+    for (int u = 0; u < KU; ++u) Lanes<T>::unpack(ok[u] ? vr[u] : make_uint4(0, 0, 0, 0), vf[u]);
+#pragma unroll
+    for (int t = 0; t < NQ; ++t) {
+      float mt = s[0][t];
+#pragma unroll
+      for (int u = 1; u < KU; ++u) mt = fmaxf(mt, s[u][t]);
+      const float m_new = fmaxf(st[t].m, mt);
+      const float ref = (m_new == -INFINITY) ? 0.f : m_new;
+      const float alpha = ex2(st[t].m - ref);
+      st[t].l *= alpha;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) st[t].o[e] *= alpha;
+#pragma unroll
+      for (int u = 0; u < KU; ++u) {
+        const float p = ex2(s[u][t] - ref);
+        st[t].l += p;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) st[t].o[e] = fmaf(p, vf[u][e], st[t].o[e]);
+      }
+      st[t].m = m_new;
+    }
+  }
+
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    // merge the G groups of this warp (lanes with the same `sub`)
+#pragma unroll
+    for (int off = LPK; off < 32; off <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, st[t].m, off);
+      const float l2 = __shfl_xor_sync(0xffffffffu, st[t].l, off);
+      float o2[EPL];
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) o2[e] = __shfl_xor_sync(0xffffffffu, st[t].o[e], off);
+      merge_state(st[t], m2, l2, o2);
+    }
+    if (lane < LPK) {
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) sm_o[t][warp][sub * EPL + e] = st[t].o[e];
+      if (lane == 0) {
+        sm_m[t][warp] = st[t].m;
+        sm_l[t][warp] = st[t].l;
+      }
+    }
+  }
+  __syncthreads();
+  // across warps, in warp order; warp t % kWarps finishes query head t
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    if (warp != t % kWarps) continue;
+    float m = sm_m[t][0];
+    for (int w = 1; w < kWarps; ++w) m = fmaxf(m, sm_m[t][w]);
+    const float ref = (m == -INFINITY) ? 0.f : m;
+    float l = 0.f, sc[kWarps];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      sc[w] = ex2(sm_m[t][w] - ref);
+      l += sm_l[t][w] * sc[w];
+    }
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    float* out_o = part_o + ((int64_t)c * R + rows[t]) * D;
+    for (int e = lane; e < D; e += 32) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) acc += sm_o[t][w][e] * sc[w];
+      out_o[e] = acc * inv_l;
+    }
+    if (lane == 0) part_lse[(int64_t)c * R + rows[t]] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
+  }
+}
+
+template <typename T, int D, int NQ>
+cudaError_t launch_group(const void* q, const void* k, const void* v, int64_t R, int H, int Nq, int Nk, int S,
+                         float scale, const int32_t* kv_len, float* part_o, float* part_lse, int group,
+                         cudaStream_t s) {
+  const int chunk = (Nk + S - 1) / S;
+  splitkv_group_kernel<T, D, NQ><<<(unsigned)(R / NQ * S), kWarps * 32, 0, s>>>(
+      static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), part_o, part_lse, H, Nq, Nk,
+      chunk, S, scale * kLog2e, kv_len, R, group);
+  return cudaGetLastError();
+}
+
+// Query heads of a group share K/V loads for the usual decode head sizes; other sizes (and
+// H_kv == H) run one query head per CTA.
 template <typename T, int D>
 cudaError_t launch_t(const void* q, const void* k, const void* v, int64_t R, int H, int Nq, int Nk, int S,
                      float scale, const int32_t* kv_len, float* part_o, float* part_lse, int group, cudaStream_t s) {
+  if constexpr (D >= 64 && (sizeof(T) == 2 || D <= 128)) {
+    switch (group) {
+      case 2: return launch_group<T, D, 2>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 4: return launch_group<T, D, 4>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      case 8: return launch_group<T, D, 8>(q, k, v, R, H, Nq, Nk, S, scale, kv_len, part_o, part_lse, group, s);
+      default: break;
+    }
+  }
   const int chunk = (Nk + S - 1) / S;
   splitkv_partial_kernel<T, D><<<(unsigned)(R * S), kWarps * 32, 0, s>>>(
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), part_o, part_lse, H, Nq, Nk,
