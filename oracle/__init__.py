@@ -56,6 +56,8 @@ def _load():
     lib.oracle_softmax_rows.restype = i32
     lib.oracle_attn.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32, dbl, vp, vp, i64, vp, vp, i32]
     lib.oracle_attn.restype = i32
+    lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, dbl, vp, vp, vp, i32]
+    lib.oracle_attn_bwd.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_online_stats.argtypes = [vp, i64, _c_dbl_p, _c_dbl_p]
@@ -153,6 +155,34 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthread
     if rows is None:
         return o.reshape(B, H, Nq, d), lse.reshape(B, H, Nq)
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, causal=False, scale=None, nthreads=None):
+    """Gradients (dq, dk, dv) of O = softmax(scale Q K^T) V given dO = dout, in fp64.
+
+    q, dout [B,H,Nq,d]; k, v [B,H,Nk,d] (same dtype code).  Causal: key j visible to query i iff
+    j <= i.  P is recomputed from the scores (no stored attention matrix), as the backward of the
+    forward definition; see oracle.c for the formulas."""
+    qa, code = _as_input(q)
+    ka, kcode = _as_input(k)
+    va, vcode = _as_input(v)
+    da, dcode = _as_input(dout)
+    if not (code == kcode == vcode == dcode):
+        raise ValueError("q, k, v, dout must share a dtype")
+    B, H, Nq, d = qa.shape
+    Nk = ka.shape[2]
+    if ka.shape != (B, H, Nk, d) or va.shape != (B, H, Nk, d) or da.shape != (B, H, Nq, d):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    dq = np.zeros((B, H, Nq, d), np.float64)
+    dk = np.zeros((B, H, Nk, d), np.float64)
+    dv = np.zeros((B, H, Nk, d), np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), code, B, H, Nq, Nk, d, int(bool(causal)),
+                                 float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd failed")
+    return dq, dk, dv
 
 
 def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, nthreads=None):

@@ -248,6 +248,107 @@ int oracle_attn(const void* q, const void* k, const void* v, int dtype, int64_t 
 }
 
 /* ------------------------------------------------------------------ */
+/* Attention backward: the gradients of O = softmax(scale Q K^T) V      */
+/* (the forward definition above) given dO, for one (b, h) at a time.   */
+/* [OS-PT] "Where this is heading: FA2": the backward recomputes the    */
+/* scores instead of reading a stored [T, T] attention matrix; here the */
+/* definition is written out with P materialised in fp64:               */
+/*   P = softmax_row(scale Q K^T) (masked keys 0),  O = P V,            */
+/*   dV = P^T dO,   dP = dO V^T,   D_i = sum_e dO_ie O_ie,              */
+/*   dS = P o (dP - D 1^T),   dQ = scale dS K,   dK = scale dS^T Q.     */
+/* (the softmax Jacobian row i is diag(P_i) - P_i P_i^T, and            */
+/*  P_i . dP_i = dO_i . O_i = D_i).  A row with no visible key has      */
+/* P = 0 and contributes nothing.  Layout: q, dout [B,H,Nq,d]; k, v     */
+/* [B,H,Nk,d]; dq [B,H,Nq,d], dk and dv [B,H,Nk,d], all fp64 out.       */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  const void *q, *k, *v, *dout;
+  int dtype;
+  int64_t H, Nq, Nk, d;
+  int causal;
+  double scale;
+  double *dq, *dk, *dv;
+} bwd_ctx;
+
+static void bwd_range(void* p, int64_t t0, int64_t t1, double* scratch) {
+  const bwd_ctx* c = (const bwd_ctx*)p;
+  const int64_t Nq = c->Nq, Nk = c->Nk, d = c->d;
+  double* P = scratch;            /* [Nq][Nk] */
+  double* dS = P + Nq * Nk;       /* [Nq][Nk] */
+  double* O = dS + Nq * Nk;       /* [Nq][d]  */
+  for (int64_t bh = t0; bh < t1; ++bh) {
+    const int64_t qb = bh * Nq * d, kb = bh * Nk * d;
+    /* P, row by row (safe softmax of the visible scaled scores) */
+    for (int64_t i = 0; i < Nq; ++i) {
+      double m = -INFINITY;
+      for (int64_t j = 0; j < Nk; ++j) {
+        double s = -INFINITY;
+        if (!c->causal || j <= i) {
+          double dot = 0.0;
+          for (int64_t e = 0; e < d; ++e)
+            dot += widen(c->q, c->dtype, qb + i * d + e) * widen(c->k, c->dtype, kb + j * d + e);
+          s = c->scale * dot;
+        }
+        P[i * Nk + j] = s;
+        if (s > m) m = s;
+      }
+      double l = 0.0;
+      for (int64_t j = 0; j < Nk; ++j) {
+        double w = (m == -INFINITY || P[i * Nk + j] == -INFINITY) ? 0.0 : exp(P[i * Nk + j] - m);
+        P[i * Nk + j] = w;
+        l += w;
+      }
+      for (int64_t j = 0; j < Nk; ++j) P[i * Nk + j] = (l > 0.0) ? P[i * Nk + j] / l : 0.0;
+    }
+    /* O = P V; dS = P o (dO V^T - D) */
+    for (int64_t i = 0; i < Nq; ++i) {
+      for (int64_t e = 0; e < d; ++e) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) acc += P[i * Nk + j] * widen(c->v, c->dtype, kb + j * d + e);
+        O[i * d + e] = acc;
+      }
+      double D = 0.0;
+      for (int64_t e = 0; e < d; ++e) D += widen(c->dout, c->dtype, qb + i * d + e) * O[i * d + e];
+      for (int64_t j = 0; j < Nk; ++j) {
+        double dp = 0.0;
+        for (int64_t e = 0; e < d; ++e)
+          dp += widen(c->dout, c->dtype, qb + i * d + e) * widen(c->v, c->dtype, kb + j * d + e);
+        dS[i * Nk + j] = P[i * Nk + j] * (dp - D);
+      }
+    }
+    /* dQ = scale dS K */
+    for (int64_t i = 0; i < Nq; ++i)
+      for (int64_t e = 0; e < d; ++e) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < Nk; ++j) acc += dS[i * Nk + j] * widen(c->k, c->dtype, kb + j * d + e);
+        c->dq[qb + i * d + e] = c->scale * acc;
+      }
+    /* dK = scale dS^T Q,  dV = P^T dO */
+    for (int64_t j = 0; j < Nk; ++j)
+      for (int64_t e = 0; e < d; ++e) {
+        double ak = 0.0, av = 0.0;
+        for (int64_t i = 0; i < Nq; ++i) {
+          ak += dS[i * Nk + j] * widen(c->q, c->dtype, qb + i * d + e);
+          av += P[i * Nk + j] * widen(c->dout, c->dtype, qb + i * d + e);
+        }
+        c->dk[kb + j * d + e] = c->scale * ak;
+        c->dv[kb + j * d + e] = av;
+      }
+  }
+}
+
+/* Gradients of attention for B*H independent heads (see above).  Returns 0,
+ * or -1 on bad arguments. */
+int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, int64_t B,
+                    int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, double scale, double* dq,
+                    double* dk, double* dv, int nthreads) {
+  if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return -1;
+  bwd_ctx c = {q, k, v, dout, dtype, H, Nq, Nk, d, causal, scale, dq, dk, dv};
+  const int64_t scratch = 2 * Nq * Nk + Nq * d + 1;
+  return parallel_for(B * H, nthreads, scratch, bwd_range, &c);
+}
+
+/* ------------------------------------------------------------------ */
 /* Merge of split partials: each partial c of row r holds the output   */
 /* normalised over its own keys, o_c, and its log-sum-exp lse_c.  The   */
 /* merged row is the softmax over the union of the keys:                */

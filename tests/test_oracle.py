@@ -441,6 +441,78 @@ def test_attention_varlen_brute_force_mixed_lengths():
     assert np.all(ov[cq[1]:cq[2]] == 0) and np.all(np.isneginf(lv[cq[1]:cq[2]]))
 
 
+def _autograd_bwd(q, k, v, dout, causal, scale):
+    """fp64 torch autograd of softmax(scale Q K^T, masked) V: the library's derivative."""
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    s = scale * tq @ tk.transpose(-1, -2)
+    if causal:
+        Nq, Nk = s.shape[-2:]
+        hide = torch.arange(Nk)[None, :] > torch.arange(Nq)[:, None]
+        s = s.masked_fill(hide, float("-inf"))
+    o = torch.softmax(s, dim=-1) @ tv
+    o.backward(torch.tensor(dout, dtype=torch.float64))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("Nq,Nk", [(7, 7), (5, 9), (9, 5)])
+def test_attention_bwd_vs_fp64_autograd(causal, Nq, Nk):
+    rng = np.random.default_rng(Nq * 10 + Nk)
+    q = rng.standard_normal((2, 3, Nq, 8))
+    k = rng.standard_normal((2, 3, Nk, 8))
+    v = rng.standard_normal((2, 3, Nk, 8))
+    do = rng.standard_normal((2, 3, Nq, 8))
+    got = oracle.attention_bwd(q, k, v, do, causal=causal, scale=0.4)
+    ref = _autograd_bwd(q, k, v, do, causal, 0.4)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-11, atol=1e-12)
+
+
+def test_attention_bwd_finite_differences():
+    # central differences of L = sum(O * dO) through the (pinned) forward oracle
+    rng = np.random.default_rng(3)
+    q, k, v = (rng.standard_normal((1, 1, n, 3)) for n in (4, 5, 5))
+    do = rng.standard_normal((1, 1, 4, 3))
+    for causal in (False, True):
+        grads = oracle.attention_bwd(q, k, v, do, causal=causal, scale=0.7)
+
+        def loss(qq, kk, vv):
+            o, _ = oracle.attention(qq, kk, vv, causal=causal, scale=0.7)
+            return float(np.sum(o * do))
+
+        h = 1e-6
+        for which, (arr, g) in enumerate(zip((q, k, v), grads)):
+            for idx in np.ndindex(arr.shape):
+                a = [q.copy(), k.copy(), v.copy()]
+                a[which][idx] += h
+                up = loss(*a)
+                a[which][idx] -= 2 * h
+                dn = loss(*a)
+                assert abs((up - dn) / (2 * h) - g[idx]) < 1e-6, (which, idx)
+
+
+def test_attention_bwd_closed_forms():
+    rng = np.random.default_rng(4)
+    q, k, v = (rng.standard_normal((1, 2, 6, 4)) for _ in range(3))
+    do = rng.standard_normal((1, 2, 6, 4))
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do)
+    # every row's weights sum to 1, so the value gradients sum to the output gradients
+    np.testing.assert_allclose(dv.sum(axis=2), do.sum(axis=2), rtol=1e-12, atol=1e-12)
+    # causal with one query per visible key at row 0: a single visible key has weight 1 whatever
+    # the scores, so row 0 of dQ is zero
+    dq, dk, dv = oracle.attention_bwd(q, k, v, do, causal=True)
+    np.testing.assert_array_equal(dq[:, :, 0], 0.0)
+    # the last key is seen only by the last query: dV[last] = P[last, last] dO[last]
+    s5 = np.einsum("bhe,bhje->bhj", q[:, :, 5], k) / math.sqrt(4)
+    p55 = np.exp(s5[..., 5] - s5.max(-1)) / np.exp(s5 - s5.max(-1, keepdims=True)).sum(-1)
+    np.testing.assert_allclose(dv[:, :, 5], p55[..., None] * do[:, :, 5], rtol=1e-12)
+    # a single key overall: no score gradient at all
+    dq, dk, dv = oracle.attention_bwd(q, k[:, :, :1], v[:, :, :1], do)
+    np.testing.assert_array_equal(dq, 0.0)
+    np.testing.assert_array_equal(dk, 0.0)
+    np.testing.assert_allclose(dv[:, :, 0], do.sum(axis=2), rtol=1e-12)
+
+
 def test_lse_merge_reaches_unsplit_attention():
     B, H, Nq, Nk, d = 3, 2, 2, 50, 8
     q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=16)
