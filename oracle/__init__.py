@@ -58,6 +58,9 @@ def _load():
     lib.oracle_attn.restype = i32
     lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, dbl, vp, vp, vp, i32]
     lib.oracle_attn_bwd.restype = i32
+    lib.oracle_attn_bwd_sampled.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, dbl, vp, i64, vp, i64, vp, vp,
+                                            vp, i32]
+    lib.oracle_attn_bwd_sampled.restype = i32
     lib.oracle_lse_merge.argtypes = [vp, vp, i64, i64, i64, vp, vp]
     lib.oracle_lse_merge.restype = i32
     lib.oracle_online_stats.argtypes = [vp, i64, _c_dbl_p, _c_dbl_p]
@@ -182,6 +185,35 @@ def attention_bwd(q, k, v, dout, causal=False, scale=None, nthreads=None):
                                  float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _threads(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_attn_bwd failed")
+    return dq, dk, dv
+
+
+def attention_bwd_sampled(q, k, v, dout, q_rows, k_rows, causal=False, scale=None, nthreads=None):
+    """The gradients of attention_bwd for ONE head at chosen rows, in fp64, without the [Nq, Nk] matrices:
+    q, dout [Nq, d], k, v [Nk, d] (same dtype code); returns dq [len(q_rows), d] and dk, dv [len(k_rows), d]
+    at those query / key rows.  Same formulas as attention_bwd; see oracle.c."""
+    qa, code = _as_input(q)
+    ka, kcode = _as_input(k)
+    va, vcode = _as_input(v)
+    da, dcode = _as_input(dout)
+    if not (code == kcode == vcode == dcode):
+        raise ValueError("q, k, v, dout must share a dtype")
+    Nq, d = qa.shape
+    Nk = ka.shape[0]
+    if ka.shape != (Nk, d) or va.shape != (Nk, d) or da.shape != (Nq, d):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    qi = np.ascontiguousarray(np.asarray(q_rows, dtype=np.int64).reshape(-1))
+    kj = np.ascontiguousarray(np.asarray(k_rows, dtype=np.int64).reshape(-1))
+    dq = np.zeros((qi.size, d), np.float64)
+    dk = np.zeros((kj.size, d), np.float64)
+    dv = np.zeros((kj.size, d), np.float64)
+    rc = _load().oracle_attn_bwd_sampled(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), code, Nq, Nk, d,
+                                         int(bool(causal)), float(scale), _ptr(qi), qi.size, _ptr(kj), kj.size,
+                                         _ptr(dq), _ptr(dk), _ptr(dv), _threads(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attn_bwd_sampled failed")
     return dq, dk, dv
 
 

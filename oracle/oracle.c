@@ -349,6 +349,135 @@ int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dou
 }
 
 /* ------------------------------------------------------------------ */
+/* The same gradients for one head at chosen rows only: dQ at query     */
+/* rows qi[], dK and dV at key rows kj[] (so that a large problem can   */
+/* be checked without the [Nq, Nk] matrices).  The formulas are those   */
+/* of oracle_attn_bwd; P_ij = exp(s_ij - m_i) / l_i from each query     */
+/* row's max m_i and sum l_i, which phase A takes over all query rows   */
+/* together with O_i and D_i = dO_i . O_i.                              */
+/* ------------------------------------------------------------------ */
+typedef struct {
+  const void *q, *k, *v, *dout;
+  int dtype;
+  int64_t Nq, Nk, d;
+  int causal;
+  double scale;
+  double *m, *l, *D;
+  const int64_t *qi, *kj;
+  double *dq, *dk, *dv;
+} bwds_ctx;
+
+static double bwds_score(const bwds_ctx* c, int64_t i, int64_t j) {
+  if (c->causal && j > i) return -INFINITY;
+  double dot = 0.0;
+  for (int64_t e = 0; e < c->d; ++e) dot += widen(c->q, c->dtype, i * c->d + e) * widen(c->k, c->dtype, j * c->d + e);
+  return c->scale * dot;
+}
+
+static double bwds_prob(const bwds_ctx* c, int64_t i, int64_t j) {
+  double s = bwds_score(c, i, j);
+  if (s == -INFINITY || c->l[i] == 0.0) return 0.0;
+  return exp(s - c->m[i]) / c->l[i];
+}
+
+static double bwds_dp(const bwds_ctx* c, int64_t i, int64_t j) {
+  double dp = 0.0;
+  for (int64_t e = 0; e < c->d; ++e)
+    dp += widen(c->dout, c->dtype, i * c->d + e) * widen(c->v, c->dtype, j * c->d + e);
+  return dp;
+}
+
+/* phase A: m_i, l_i, O_i (scratch) and D_i for query rows [t0, t1) */
+static void bwds_rows(void* p, int64_t t0, int64_t t1, double* scratch) {
+  const bwds_ctx* c = (const bwds_ctx*)p;
+  double* S = scratch;        /* [Nk] */
+  double* O = scratch + c->Nk; /* [d] */
+  for (int64_t i = t0; i < t1; ++i) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < c->Nk; ++j) {
+      S[j] = bwds_score(c, i, j);
+      if (S[j] > m) m = S[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j < c->Nk; ++j) {
+      S[j] = (m == -INFINITY || S[j] == -INFINITY) ? 0.0 : exp(S[j] - m);
+      l += S[j];
+    }
+    double D = 0.0;
+    for (int64_t e = 0; e < c->d; ++e) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < c->Nk; ++j) acc += S[j] * widen(c->v, c->dtype, j * c->d + e);
+      O[e] = l > 0.0 ? acc / l : 0.0;
+      D += widen(c->dout, c->dtype, i * c->d + e) * O[e];
+    }
+    c->m[i] = m;
+    c->l[i] = l;
+    c->D[i] = D;
+  }
+}
+
+/* phase B: dQ_i = scale sum_j dS_ij K_j at sampled query rows [t0, t1) */
+static void bwds_dq(void* p, int64_t t0, int64_t t1, double* scratch) {
+  const bwds_ctx* c = (const bwds_ctx*)p;
+  double* dS = scratch; /* [Nk] */
+  for (int64_t t = t0; t < t1; ++t) {
+    const int64_t i = c->qi[t];
+    for (int64_t j = 0; j < c->Nk; ++j) {
+      double P = bwds_prob(c, i, j);
+      dS[j] = P == 0.0 ? 0.0 : P * (bwds_dp(c, i, j) - c->D[i]);
+    }
+    for (int64_t e = 0; e < c->d; ++e) {
+      double acc = 0.0;
+      for (int64_t j = 0; j < c->Nk; ++j) acc += dS[j] * widen(c->k, c->dtype, j * c->d + e);
+      c->dq[t * c->d + e] = c->scale * acc;
+    }
+  }
+}
+
+/* phase C: dV_j = sum_i P_ij dO_i and dK_j = scale sum_i dS_ij Q_i at sampled key rows [t0, t1) */
+static void bwds_dkv(void* p, int64_t t0, int64_t t1, double* scratch) {
+  const bwds_ctx* c = (const bwds_ctx*)p;
+  (void)scratch;
+  for (int64_t t = t0; t < t1; ++t) {
+    const int64_t j = c->kj[t];
+    for (int64_t e = 0; e < c->d; ++e) {
+      c->dk[t * c->d + e] = 0.0;
+      c->dv[t * c->d + e] = 0.0;
+    }
+    for (int64_t i = 0; i < c->Nq; ++i) {
+      double P = bwds_prob(c, i, j);
+      if (P == 0.0) continue;
+      double dS = P * (bwds_dp(c, i, j) - c->D[i]);
+      for (int64_t e = 0; e < c->d; ++e) {
+        c->dk[t * c->d + e] += c->scale * dS * widen(c->q, c->dtype, i * c->d + e);
+        c->dv[t * c->d + e] += P * widen(c->dout, c->dtype, i * c->d + e);
+      }
+    }
+  }
+}
+
+/* One head: q, dout [Nq, d], k, v [Nk, d]; dq [nq, d] at rows qi, dk and
+ * dv [nk, d] at rows kj.  Returns 0, or -1 on bad arguments. */
+int oracle_attn_bwd_sampled(const void* q, const void* k, const void* v, const void* dout, int dtype, int64_t Nq,
+                            int64_t Nk, int64_t d, int causal, double scale, const int64_t* qi, int64_t nq,
+                            const int64_t* kj, int64_t nk, double* dq, double* dk, double* dv, int nthreads) {
+  if (!q || !k || !v || !dout || Nq < 0 || Nk < 0 || d < 0 || nq < 0 || nk < 0) return -1;
+  if ((nq > 0 && (!qi || !dq)) || (nk > 0 && (!kj || !dk || !dv))) return -1;
+  for (int64_t t = 0; t < nq; ++t)
+    if (qi[t] < 0 || qi[t] >= Nq) return -1;
+  for (int64_t t = 0; t < nk; ++t)
+    if (kj[t] < 0 || kj[t] >= Nk) return -1;
+  double* stats = (double*)malloc(sizeof(double) * (size_t)(3 * Nq + 1));
+  if (!stats) return -1;
+  bwds_ctx c = {q, k, v, dout, dtype, Nq, Nk, d, causal, scale, stats, stats + Nq, stats + 2 * Nq, qi, kj, dq, dk, dv};
+  int rc = parallel_for(Nq, nthreads, Nk + d + 1, bwds_rows, &c);
+  if (rc == 0) rc = parallel_for(nq, nthreads, Nk + 1, bwds_dq, &c);
+  if (rc == 0) rc = parallel_for(nk, nthreads, 1, bwds_dkv, &c);
+  free(stats);
+  return rc;
+}
+
+/* ------------------------------------------------------------------ */
 /* Merge of split partials: each partial c of row r holds the output   */
 /* normalised over its own keys, o_c, and its log-sum-exp lse_c.  The   */
 /* merged row is the softmax over the union of the keys:                */

@@ -513,6 +513,35 @@ def test_attention_bwd_closed_forms():
     np.testing.assert_allclose(dv[:, :, 0], do.sum(axis=2), rtol=1e-12)
 
 
+@pytest.mark.parametrize("causal,Nq,Nk", [(False, 9, 13), (True, 11, 11), (False, 1, 1)])
+def test_attention_bwd_sampled_vs_fp64_autograd(causal, Nq, Nk):
+    # the row-sampled gradients against torch's fp64 autograd, at every row and at a shuffled subset
+    rng = np.random.default_rng(100 + Nq)
+    q, k, v = rng.standard_normal((Nq, 6)), rng.standard_normal((Nk, 6)), rng.standard_normal((Nk, 6))
+    do = rng.standard_normal((Nq, 6))
+    rq, rk, rv = _autograd_bwd(q, k, v, do, causal, 0.5)
+    dq, dk, dv = oracle.attention_bwd_sampled(q, k, v, do, np.arange(Nq), np.arange(Nk), causal=causal, scale=0.5)
+    for g, r in ((dq, rq), (dk, rk), (dv, rv)):
+        np.testing.assert_allclose(g, r, rtol=1e-11, atol=1e-12)
+    qi, kj = rng.permutation(Nq)[: max(1, Nq // 2)], rng.permutation(Nk)[: max(1, Nk // 3)]
+    dq, dk, dv = oracle.attention_bwd_sampled(q, k, v, do, qi, kj, causal=causal, scale=0.5)
+    np.testing.assert_allclose(dq, rq[qi], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk, rk[kj], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv, rv[kj], rtol=1e-11, atol=1e-12)
+
+
+def test_attention_bwd_sampled_bf16_matches_full():
+    # bf16 bit patterns widen exactly on both paths, so the sampled rows equal the full gradients
+    q, k, v = si.attn_inputs(1, 1, 40, 40, 16, torch.bfloat16, seed=21)
+    do = si.randn((1, 1, 40, 16), 24, torch.bfloat16)
+    full = oracle.attention_bwd(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(do), causal=True)
+    rows = np.array([0, 17, 39])
+    got = oracle.attention_bwd_sampled(bf16_bits(q[0, 0]), bf16_bits(k[0, 0]), bf16_bits(v[0, 0]),
+                                       bf16_bits(do[0, 0]), rows, rows, causal=True)
+    for g, f in zip(got, full):
+        np.testing.assert_allclose(g, f[0, 0][rows], rtol=1e-12, atol=1e-13)
+
+
 def test_lse_merge_reaches_unsplit_attention():
     B, H, Nq, Nk, d = 3, 2, 2, 50, 8
     q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=16)
