@@ -173,6 +173,49 @@ oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, 
                                 oa_stream_t stream);
 
 /*
+ * Bytes of workspace oa_attn_bwd needs: B*H*Nq * (d + 1) fp32 values (the
+ * fp32 dQ accumulator, then D = rowsum(dO * O)), rounded up to 256 bytes.
+ * 0 for invalid sizes.
+ */
+size_t oa_attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
+
+/*
+ * Fused attention backward (tcgen05 tensor-core kernel): the gradients
+ * dQ, dK, dV of O = softmax(Q K^T * scale) V for a given dO, with the
+ * probabilities recomputed tile by tile from the forward's per-row LSE
+ * instead of read back (page "Online softmax in attention -- why and how",
+ * section "Where this is heading: FA2": on backward, the scores are
+ * recomputed from the cached running max and sum, which the LSE folds into
+ * one number).  The Nq x Nk matrices P and dP never reach memory.  Three
+ * launches on `stream`: D = rowsum(dO * O) (and zeroing of the dQ
+ * accumulator), one CTA per 128-key tile of each (b, h) that accumulates
+ * dK and dV on chip and adds its dQ share to the fp32 accumulator, and the
+ * dQ conversion to bf16.
+ *   q, o, dout, dq  bf16 [B, H, Nq, d]; k, v, dk, dv  bf16 [B, H, Nk, d];
+ *           contiguous row-major, 16-byte aligned.  o and lse are the
+ *           forward's outputs for the same q, k, v, causal and scale.
+ *   lse     fp32 [B, H, Nq], non-NULL.  A row with lse = -inf (no visible
+ *           key) gets dQ = 0 and contributes nothing to dK, dV.
+ *   causal  0 or 1 (key j visible to query i iff j <= i; needs Nq == Nk).
+ *   scale   finite and > 0.
+ *   d       64 or 128.
+ *   workspace  device, >= oa_attn_bwd_workspace_bytes(B, H, Nq, d) bytes,
+ *           16-byte aligned; owned by the caller, who must not touch it (or
+ *           dq, dk, dv) until the call's work has completed on `stream`.
+ *           Its contents on entry do not matter.
+ * dK and dV are written with plain stores, one CTA per key tile, so the
+ * result is deterministic; dQ sums fp32 atomics and may differ in the last
+ * bits from run to run.
+ * Errors: OA_ERR_INVALID (NULL pointers, sizes < 1, misalignment, a bad
+ * scale, workspace too small); OA_ERR_UNSUPPORTED (dtype other than bf16,
+ * d other than 64 / 128, causal with Nq != Nk).
+ */
+oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                      const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, int B, int H,
+                      int Nq, int Nk, int d, int causal, float scale, void* workspace,
+                      size_t workspace_bytes, oa_stream_t stream);
+
+/*
  * Bytes of workspace oa_attn_splitkv needs: num_splits * B*H*Nq * (d + 1)
  * fp32 values (normalised partial outputs, then their LSEs), rounded up to
  * 256 bytes.  0 for invalid sizes.

@@ -29,7 +29,7 @@ OA_F32, OA_BF16 = 0, 1
 EXPORTS = (
     "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd", "oa_attn_fwd_gqa",
     "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
-    "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge",
+    "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge", "oa_attn_bwd_workspace_bytes", "oa_attn_bwd",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -81,6 +81,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                     i32),
             "oa_attn_splitkv_static": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp], i32),
             "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
+            "oa_attn_bwd_workspace_bytes": ([i32, i32, i32, i32], sz),
+            "oa_attn_bwd": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp],
+                            i32),
             "oa_sync_status": ([vp], i32),
             "oa_set_wait_limit_ns": ([u64], None),
             "oa_selftest_wait_timeout": ([u64, vp], i32),
@@ -252,6 +255,41 @@ def attn_fwd_f32_tiles(q, k, v, Br: int, Bc: int, causal: bool = False, scale: f
                                             int(bool(causal)), float(scale), _ptr(kv), int(Br), int(Bc),
                                             _stream(q.device)))
     return out, lse
+
+
+def attn_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
+    return int(load().oa_attn_bwd_workspace_bytes(B, H, Nq, d))
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+             workspace=None):
+    """Gradients (dq, dk, dv) of O = softmax(Q K^T * scale) V for the upstream gradient dout, with P recomputed
+    from the forward's LSE.  q, o, dout [B,H,Nq,d] and k, v [B,H,Nk,d], bf16 on CUDA; lse fp32 [B,H,Nq] (o and
+    lse from attn_fwd on the same inputs).  workspace: optional uint8 CUDA tensor of attn_bwd_workspace_bytes."""
+    _require_cuda(q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    B, H, Nq, Nk, d, _ = _attn_shapes(q, k, v)
+    if tuple(o.shape) != (B, H, Nq, d) or tuple(dout.shape) != (B, H, Nq, d):
+        raise OAError(OA_ERR_INVALID, "o and dout must be [B, H, Nq, d] like q")
+    if o.dtype != q.dtype or dout.dtype != q.dtype or not o.is_contiguous() or not dout.is_contiguous():
+        raise OAError(OA_ERR_INVALID, "o and dout must be contiguous with q's dtype")
+    if lse is None or tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise OAError(OA_ERR_INVALID, "lse must be a contiguous float32 [B, H, Nq] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_bwd_workspace_bytes(B, H, Nq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                  _ptr(dv), _dtype_code(q.dtype), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(q.device)))
+    return dq, dk, dv
 
 
 def splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:

@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "liboa.so")
 
-SOURCES = ["oa_api.cu", "softmax_rows.cu", "lse_merge.cu", "attn_f32.cu", "attn_splitkv.cu", "attn_tc.cu",
-           "attn_splitkv_static.cu"]
+SOURCES = ["oa_api.cu", "tma_map.cu", "softmax_rows.cu", "lse_merge.cu", "attn_f32.cu", "attn_splitkv.cu", "attn_tc.cu",
+           "attn_bwd.cu", "attn_splitkv_static.cu"]
 HEADERS = ["oa_common.cuh", "oa_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -596,42 +596,6 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
-// bf16 rows of D elements viewed as a 3-D tensor (D innermost, then `rows` rows `row_bytes`
-// apart, then `planes` head planes `plane_bytes` apart); box 64 x 128 x 1 with the 128-byte
-// swizzle; rows past the end read as zero.  Dense [BH, N, D]: rows N, planes BH.  Packed
-// [T, H, D]: rows T (H D elements apart), planes H (D elements apart).
-bool make_map(CUtensorMap* map, const void* base, int D, int rows, int64_t row_bytes, int planes,
-              int64_t plane_bytes) {
-  EncodeTiledFn enc = get_encode_fn();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)(rows > 0 ? rows : 1), (cuuint64_t)(planes > 0 ? planes : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)plane_bytes};
-  cuuint32_t box[3] = {64, (cuuint32_t)BM, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int kMaxDevices = 64;
 
 // Persistent grid: one CTA per SM (the kernel holds an SM's TMEM and most of its shared
@@ -667,12 +631,13 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   CUtensorMap mq, mk, mv;
   bool maps_ok;
   if (packed)
-    maps_ok = make_map(&mq, a.q, d, a.Tq, rb * a.H, a.H, rb) && make_map(&mk, a.k, d, a.Tk, rb * Hkv, Hkv, rb) &&
-              make_map(&mv, a.v, d, a.Tk, rb * Hkv, Hkv, rb);
+    maps_ok = make_tile_map(&mq, a.q, d, a.Tq, rb * a.H, a.H, rb) &&
+              make_tile_map(&mk, a.k, d, a.Tk, rb * Hkv, Hkv, rb) &&
+              make_tile_map(&mv, a.v, d, a.Tk, rb * Hkv, Hkv, rb);
   else
-    maps_ok = make_map(&mq, a.q, d, a.Nq, rb, a.B * a.H, rb * a.Nq) &&
-              make_map(&mk, a.k, d, a.Nk, rb, a.B * Hkv, rb * a.Nk) &&
-              make_map(&mv, a.v, d, a.Nk, rb, a.B * Hkv, rb * a.Nk);
+    maps_ok = make_tile_map(&mq, a.q, d, a.Nq, rb, a.B * a.H, rb * a.Nq) &&
+              make_tile_map(&mk, a.k, d, a.Nk, rb, a.B * Hkv, rb * a.Nk) &&
+              make_tile_map(&mv, a.v, d, a.Nk, rb, a.B * Hkv, rb * a.Nk);
   if (!maps_ok) {
     if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;

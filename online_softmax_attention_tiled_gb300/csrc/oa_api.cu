@@ -261,6 +261,52 @@ oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, 
   return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd_f32_tiles launch");
 }
 
+size_t oa_attn_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+  if (B < 1 || H < 1 || Nq < 1 || d < 1) return 0;
+  return (oa::attn_bwd_workspace_floats(B, H, Nq, d) * sizeof(float) + 255) / 256 * 256;
+}
+
+oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      void* dq, void* dk, void* dv, oa_dtype dt, int B, int H, int Nq, int Nk, int d, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  const char* who = "attn_bwd";
+  oa_status s = check_attn(q, k, v, dq, nullptr, B, H, Nq, Nk, d, causal, scale, who);
+  if (s != OA_OK) return s;
+  if (!o || !dout || !lse || !dk || !dv) return fail(OA_ERR_INVALID, "%s: o, dout, lse, dk and dv are required", who);
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
+    return fail(OA_ERR_INVALID, "%s: o/dout/dk/dv must be 16-byte aligned, lse 4-byte", who);
+  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "%s: causal needs Nq == Nk", who);
+  if (dt != OA_BF16) return fail(OA_ERR_UNSUPPORTED, "%s: bf16 only", who);
+  if (d != 64 && d != 128) return fail(OA_ERR_UNSUPPORTED, "%s: d = 64 or 128 (got %d)", who, d);
+  if ((int64_t)B * H * ((Nk + 127) / 128) > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);
+  const size_t need = oa_attn_bwd_workspace_bytes(B, H, Nq, d);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
+    return fail(OA_ERR_INVALID, "%s: workspace must be 16-byte aligned and >= %zu bytes", who, need);
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  oa::BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nk = Nk;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  const char* why = nullptr;
+  cudaError_t e = oa::launch_attn_bwd(a, static_cast<float*>(workspace), st, (cudaStream_t)stream, &why);
+  if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_bwd launch");
+  return ok();
+}
+
 size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1) return 0;
   const size_t floats = (size_t)num_splits * (size_t)B * H * Nq * ((size_t)d + 1);

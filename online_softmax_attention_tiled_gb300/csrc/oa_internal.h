@@ -27,6 +27,13 @@ cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, 
                                    int Nq, int Nk, int d, float scale, const int32_t* kv_len,
                                    int num_splits, float* part_o, float* part_lse, cudaStream_t s);
 
+// bf16 rows of D elements viewed as a 3-D tensor for TMA (D innermost, then `rows` rows
+// `row_bytes` apart, then `planes` planes `plane_bytes` apart); box 64 x 128 x 1 with the
+// 128-byte swizzle; reads past the end return zero.  False if the encoder is unavailable or
+// rejects the layout.
+bool make_tile_map(CUtensorMap* map, const void* base, int D, int rows, int64_t row_bytes, int planes,
+                   int64_t plane_bytes);
+
 // Tensor-core attention (tcgen05 + TMA), bf16, d in {64, 128}.
 //   dense  (cu_q == NULL): q/o [B, H, Nq, d], k/v [B, Hkv, Nk, d], kv_len[B] or NULL.
 //   packed (cu_q != NULL): B sequences; q/o [Tq, H, d], k/v [Tk, Hkv, d], lse [Tq, H];
@@ -45,6 +52,21 @@ struct TcArgs {
 };
 // `why` gets a static message when the host-side set-up (tensor maps) fails.
 cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s, const char** why);
+
+// Attention backward (tcgen05 + TMA), bf16, d in {64, 128}, dense [B, H, N, d] layouts:
+// dq/do/q [B, H, Nq, d], dk/dv/k/v [B, H, Nk, d], lse [B, H, Nq] from the forward.
+struct BwdArgs {
+  const void *q, *k, *v, *o, *dout;
+  const float* lse;
+  void *dq, *dk, *dv;
+  int B, H, Nq, Nk, d, causal;
+  float scale;
+};
+// fp32 values of workspace the backward needs: the dQ accumulator [B H Nq, d] and D [B H Nq].
+size_t attn_bwd_workspace_floats(int B, int H, int Nq, int d);
+// Three launches on `s` (pre-pass, main kernel, dQ conversion).  `why` as for launch_attn_tc.
+cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus& st, cudaStream_t s,
+                            const char** why);
 
 cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s);
 

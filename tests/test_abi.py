@@ -120,6 +120,27 @@ def test_attn_splitkv_validation(lib):
     assert call(dt=oa.OA_F32, d=256) == oa.OA_ERR_UNSUPPORTED
 
 
+def test_attn_bwd_validation(lib):
+    NULL = None
+    need = lib.oa_attn_bwd_workspace_bytes(2, 2, 100, 64)
+    assert need == ((2 * 2 * 100 * 65 * 4 + 255) // 256) * 256
+    assert lib.oa_attn_bwd_workspace_bytes(0, 2, 100, 64) == 0
+
+    def call(q=FAKE, o=FAKE, dout=FAKE, lse=FAKE, dk=FAKE, dt=oa.OA_BF16, Nq=100, Nk=100, d=64, causal=1,
+             scale=0.125, ws=FAKE, ws_bytes=need):
+        return lib.oa_attn_bwd(q, FAKE, FAKE, o, dout, lse, FAKE, dk, FAKE, dt, 2, 2, Nq, Nk, d, causal, scale, ws,
+                               ws_bytes, NULL)
+
+    for bad in (dict(q=NULL), dict(o=NULL), dict(dout=NULL), dict(lse=NULL), dict(dk=NULL), dict(Nq=0),
+                dict(scale=-1.0), dict(causal=3), dict(dout=FAKE_ODD), dict(ws=NULL), dict(ws=FAKE_ODD),
+                dict(ws_bytes=need - 1)):
+        assert call(**bad) == oa.OA_ERR_INVALID, bad
+    assert call(Nk=99) == oa.OA_ERR_UNSUPPORTED  # causal needs Nq == Nk
+    assert call(dt=oa.OA_F32) == oa.OA_ERR_UNSUPPORTED
+    assert call(d=96) == oa.OA_ERR_UNSUPPORTED
+    assert "d = 64 or 128" in _err(lib)
+
+
 def test_lse_merge_validation(lib):
     NULL = None
     assert lib.oa_lse_merge(FAKE, NULL, 2, 4, 8, FAKE, oa.OA_F32, FAKE, NULL) == oa.OA_ERR_INVALID
