@@ -54,6 +54,11 @@ def dense_attn_flops(b, h, nq, nk, d):
     return 4.0 * b * h * nq * nk * d
 
 
+def causal_attn_bwd_flops(b, h, n, d):
+    """10*d FLOPs per visible (query, key) pair: S = QK^T and dP = dO V^T recomputed, then dV, dK, dQ."""
+    return 2.5 * causal_attn_flops(b, h, n, d)
+
+
 def softmax_bytes(rows, cols):
     """Read X once, write Y and LSE (fp32)."""
     return 4.0 * rows * cols * 2 + 4.0 * rows
@@ -307,7 +312,23 @@ def components(oa, dev, peaks, peak_kind, steps):
                                      "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
                                      "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
                                      "algorithmic_flops": varlen_causal_flops(lens, 32, 128)}
-    del q, k, v, o, lse, flush_buf
+    del q, k, v, o, lse
+    # attention backward, causal B1 H32 N8192 d128, O and LSE from the forward
+    q, k, v = si.attn_inputs(1, 32, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
+    do = si.randn((1, 32, 8192, 128), 3, torch.bfloat16, dev)
+    o, lse = oa.attn_fwd(q, k, v, causal=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(oa.attn_bwd_workspace_bytes(1, 32, 8192, 128), dtype=torch.uint8, device=dev)
+    t = time_launches(lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws), steps,
+                      3, flush)
+    ms = statistics.mean(t)
+    fl = causal_attn_bwd_flops(1, 32, 8192, 128)
+    tf = fl / (ms * 1e-3) / 1e12
+    out["attn_bwd_causal"] = {"workload": "causal attention bwd bf16 B=1 H=32 N=8192 d=128 (dQ, dK, dV from Q, K, V, "
+                                          "O, LSE, dO)", "ms": ms, "value": tf, "unit": "TFLOP/s", "bound": "tensor",
+                              "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
+                              "algorithmic_flops": fl, "launches_per_call": 3}
+    del q, k, v, do, o, lse, dq, dk, dv, ws, flush_buf
     torch.cuda.empty_cache()
     return out
 

@@ -33,6 +33,9 @@ cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, 
 // rejects the layout.
 bool make_tile_map(CUtensorMap* map, const void* base, int D, int rows, int64_t row_bytes, int planes,
                    int64_t plane_bytes);
+// fp32 [planes][rows][cols], box {32, box_rows, 1}, 128-byte swizzle (TMA reduce-add targets).
+bool make_f32_tile_map(CUtensorMap* map, const void* base, int cols, int rows, int64_t row_bytes, int planes,
+                       int64_t plane_bytes, int box_rows);
 
 // Tensor-core attention (tcgen05 + TMA), bf16, d in {64, 128}.
 //   dense  (cu_q == NULL): q/o [B, H, Nq, d], k/v [B, Hkv, Nk, d], kv_len[B] or NULL.
