@@ -43,14 +43,16 @@ namespace {
 
 constexpr int BT = 128;                  // keys per CTA tile = query rows per step
 constexpr int kBwdRowWarps = 8;
-constexpr int kBwdThreads = 32 * (kBwdRowWarps + 2);
+constexpr int kBwdThreads = 32 * (kBwdRowWarps + 3);
 constexpr int kBwdProducer = kBwdRowWarps;
 constexpr int kBwdMma = kBwdRowWarps + 1;
+constexpr int kBwdReducer = kBwdRowWarps + 2;
 constexpr uint32_t kBwdTmemCols = 512;
 
 template <int D>
 struct BwdCfg {
   static constexpr int SLABS = D / 64;        // 128-byte swizzle atoms along d
+  static constexpr int DQ_CHUNKS = D / 64;    // 32-column dQ chunks per row warp
   static constexpr int SLAB_BYTES = BT * 128;  // 128 rows x 128 bytes
   static constexpr int TILE_BYTES = SLABS * SLAB_BYTES;
   static constexpr int K_OFF = 0;
@@ -61,16 +63,17 @@ struct BwdCfg {
   // A operand of dQ = dS K read M-major
   static constexpr int ST_OFF = DO_OFF + 2 * TILE_BYTES;
   static constexpr int ST_BYTES = 2 * SLAB_BYTES;
-  // (LSE log2 e, D) of the step's 128 query rows, float2 each (+inf / 0 past the end)
+  // -LSE log2 e of the step's 128 query rows, then -D (-inf / 0 past the end)
   static constexpr int LD_OFF = ST_OFF + ST_BYTES;
   static constexpr int BAR_OFF = LD_OFF + BT * 8;
-  // kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, ds_ready, dq_full, dq_read, done, ld_ready
-  static constexpr int NUM_BARS = 12;
+  // kv_full, qdo_full[2], qdo_empty[2], s_full[2], dp_full[2], ds_ready[2], dq_full, dq_read, done,
+  // ld_ready[2] ([h]: the query half h = queries 64h .. 64h + 63 of the step), dq_staged[2]
+  static constexpr int NUM_BARS = 17;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
-  // S^T = K Q^T and dP^T = V dO^T: both operands K-major
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT, false);
+  // S^T = K Q^T and dP^T = V dO^T for one half of the queries: both operands K-major
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT / 2, false);
   // dV += P^T dO and dK += dS^T Q: A from TMEM, B (dO, Q with d contiguous) N-major
   static constexpr uint32_t IDESC_KV = idesc_bf16_f32(BT, D, true);
   // dQ = dS K: A (staged dS, queries contiguous) M-major, B (K, d contiguous) N-major
@@ -89,7 +92,16 @@ struct BwdParams {
   DevStatus st;
 };
 
-enum BwdWait : unsigned { B_KV = 1, B_QDO, B_QDO_EMPTY, B_S, B_DP, B_DS, B_DQ, B_DQ_READ, B_DONE, B_LD };
+enum BwdWait : unsigned { B_KV = 1, B_QDO, B_QDO_EMPTY, B_S, B_DP, B_DS, B_DQ, B_DQ_READ, B_DONE, B_LD, B_DQ_STAGED };
+
+// Shared-memory offset of the 32 x 32 fp32 dQ block (row warp w, chunk m) of a step: 4 KB each,
+// in that step's Q stage and then its dO stage (8 warps x DQ_CHUNKS x 4 KB = the two tiles),
+// which no MMA reads once the step's dQ MMA is complete.
+template <class C>
+__device__ __forceinline__ uint32_t bwd_dq_block(uint32_t q_stage_off, int w, int m) {
+  const uint32_t off = (uint32_t)((w * C::DQ_CHUNKS + m) * 4096);
+  return q_stage_off + (off < (uint32_t)C::TILE_BYTES ? off : off - C::TILE_BYTES + (C::DO_OFF - C::Q_OFF));
+}
 
 // D[r] = sum_e dO[r, e] O[r, e] for every query row; dq_acc[r, :] = 0.  One warp per row.
 __global__ void bwd_pre_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
@@ -120,26 +132,39 @@ __global__ void bwd_post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16*
 }
 
 // P^T and dS^T for 32 queries q_first .. q_first + 31 of one key row: sr / dr the fp32 S^T and
-// dP^T columns, ld the (LSE log2 e, D) pairs of those queries (two per float4).  MASK applies
-// the key and causal tests as an exponent of -inf (no branch per element).
+// dP^T columns, nl / nd the negated (LSE log2 e, D) of those queries (four per float4), in packed
+// pairs of fp32.  MASK applies the key and causal tests as an exponent of -inf (no branch).
 template <bool MASK>
-__device__ __forceinline__ void bwd_p_ds(const uint32_t (&sr)[32], const uint32_t (&dr)[32], const float4* ld,
-                                         float sl2, int key, int q_first, bool key_ok, bool causal,
+__device__ __forceinline__ void bwd_p_ds(const uint32_t* sr, const uint32_t* dr, const float4* nl, const float4* nd,
+                                         uint64_t sl2x2, int key, int q_first, bool key_ok, bool causal,
                                          uint32_t (&pw)[16], uint32_t (&dw)[16]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 2) {
-    const float4 l = ld[e / 2];  // a broadcast: every lane reads the same 16 bytes
-    // P^T = exp(scale s - LSE) = exp2(s scale log2 e - LSE log2 e)
-    float a0 = fmaf(__uint_as_float(sr[e]), sl2, -l.x);
-    float a1 = fmaf(__uint_as_float(sr[e + 1]), sl2, -l.z);
-    if (MASK) {
-      const int q = q_first + e;
-      a0 = (key_ok && (!causal || key <= q)) ? a0 : -INFINITY;
-      a1 = (key_ok && (!causal || key <= q + 1)) ? a1 : -INFINITY;
+  for (int e = 0; e < 32; e += 4) {
+    // broadcasts: every lane reads the same 16 bytes
+    const ulonglong2 nlv = *reinterpret_cast<const ulonglong2*>(nl + e / 4);
+    const ulonglong2 ndv = *reinterpret_cast<const ulonglong2*>(nd + e / 4);
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+      // P^T = exp(scale s - LSE) = exp2(s scale log2 e - LSE log2 e), two queries at once
+      const uint64_t a = f2_fma(f2_pack(__uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1])), sl2x2,
+                                h ? nlv.y : nlv.x);
+      float a0, a1;
+      f2_unpack(a, a0, a1);
+      if (MASK) {
+        const int q = q_first + e + h;
+        a0 = (key_ok && (!causal || key <= q)) ? a0 : -INFINITY;
+        a1 = (key_ok && (!causal || key <= q + 1)) ? a1 : -INFINITY;
+      }
+      const float p0 = ex2(a0), p1 = ex2(a1);
+      // dS^T = P^T (dP^T - D)
+      const uint64_t ds = f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(dr[e + h]),
+                                                               __uint_as_float(dr[e + h + 1])),
+                                                       h ? ndv.y : ndv.x));
+      float d0, d1;
+      f2_unpack(ds, d0, d1);
+      pw[(e + h) / 2] = pack_bf16x2(p0, p1);
+      dw[(e + h) / 2] = pack_bf16x2(d0, d1);
     }
-    const float p0 = ex2(a0), p1 = ex2(a1);
-    pw[e / 2] = pack_bf16x2(p0, p1);
-    dw[e / 2] = pack_bf16x2(p0 * (__uint_as_float(dr[e]) - l.y), p1 * (__uint_as_float(dr[e + 1]) - l.w));
   }
 }
 
@@ -160,14 +185,18 @@ __global__ void __launch_bounds__(kBwdThreads)
   const uint32_t bar0 = sbase + C::BAR_OFF;
   const uint32_t bar_kv = bar0;
   auto bar_qdo = [&](int s) { return bar0 + 8u * (1 + s); };        // Q_i, dO_i of stage s landed
-  auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (3 + s); };  // stage s read by its MMAs
-  const uint32_t bar_s = bar0 + 8u * 5;        // S^T in TMEM
-  const uint32_t bar_dp = bar0 + 8u * 6;       // dP^T in TMEM
-  const uint32_t bar_ds = bar0 + 8u * 7;       // P^T, dS^T in TMEM and dS staged (4 warps)
-  const uint32_t bar_dq = bar0 + 8u * 8;       // dQ_i in TMEM
-  const uint32_t bar_dq_read = bar0 + 8u * 9;  // dQ_i read out of TMEM (4 warps)
-  const uint32_t bar_done = bar0 + 8u * 10;    // every MMA of the CTA complete
-  const uint32_t bar_ld = bar0 + 8u * 11;      // the step's (LSE, D) block written (4 warps)
+  // stage s free again: its MMAs are complete and the dQ blocks staged in it have been read by
+  // their TMA reduce-adds (the reducer warp)
+  auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (3 + s); };
+  auto bar_s = [&](int h) { return bar0 + 8u * (5 + h); };    // S^T of query half h in TMEM
+  auto bar_dp = [&](int h) { return bar0 + 8u * (7 + h); };   // dP^T of half h in TMEM
+  auto bar_ds = [&](int h) { return bar0 + 8u * (9 + h); };   // P^T, dS^T of half h in TMEM, dS staged
+  const uint32_t bar_dq = bar0 + 8u * 11;                     // dQ_i in TMEM
+  const uint32_t bar_dq_read = bar0 + 8u * 12;                // dQ_i read out of TMEM (8 warps)
+  const uint32_t bar_done = bar0 + 8u * 13;                   // every MMA of the CTA complete
+  auto bar_ld = [&](int h) { return bar0 + 8u * (14 + h); };  // half h's (LSE, D) entries written
+  // the dQ blocks of the step using stage s are staged in it (8 warps)
+  auto bar_dq_staged = [&](int s) { return bar0 + 8u * (16 + s); };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -183,13 +212,16 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qdo(s), 1);
       mbar_init(bar_qdo_empty(s), 1);
+      mbar_init(bar_dq_staged(s), kBwdRowWarps);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_dp, 1);
-    mbar_init(bar_ds, kBwdRowWarps);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar_s(h), 1);
+      mbar_init(bar_dp(h), 1);
+      mbar_init(bar_ds(h), kBwdRowWarps / 2);
+      mbar_init(bar_ld(h), kBwdRowWarps / 2);
+    }
     mbar_init(bar_dq, 1);
     mbar_init(bar_dq_read, kBwdRowWarps);
-    mbar_init(bar_ld, kBwdRowWarps);
     mbar_init(bar_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -260,28 +292,38 @@ __global__ void __launch_bounds__(kBwdThreads)
       // S^T goes where dQ_{i-1} lies: the rows must have read it out first
       if (it > 0 && !(ok = wait_all(bar_dq_read, ph ^ 1u, B_DQ_READ))) break;
       tc_fence_after_sync();
+      // S^T and dP^T per query half (N = 64): the rows of half 0 start while half 1 computes;
+      // the B operands of half h start 64 rows (8192 bytes) into each slab
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_elect(tmem_base + C::S_COL, k_kmaj + kmaj_off(kk), q_kmaj + kmaj_off(kk), C::IDESC_S,
-                     kk > 0 ? 1u : 0u);
-      mma_commit_elect(bar_s);
+      for (int h = 0; h < 2; ++h) {
+        const uint64_t hoff = (uint64_t)((h * 64 * 128) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_elect(tmem_base + C::DP_COL, v_kmaj + kmaj_off(kk), do_kmaj + kmaj_off(kk), C::IDESC_S,
-                     kk > 0 ? 1u : 0u);
-      mma_commit_elect(bar_dp);
-      if (!(ok = wait_all(bar_ds, ph, B_DS))) break;
-      tc_fence_after_sync();
-      // dV += P^T dO_i and dK += dS^T Q_i (K = the 128 queries, 16 per MMA step = 8 TMEM
-      // columns of bf16 pairs; queries 64-127 start at column 64)
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_elect(tmem_base + C::S_COL + h * 64, k_kmaj + kmaj_off(kk), q_kmaj + hoff + kmaj_off(kk), C::IDESC_S,
+                       kk > 0 ? 1u : 0u);
+        mma_commit_elect(bar_s(h));
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), do_nmaj + rows16_off(kk), C::IDESC_KV,
-                     (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ss_elect(tmem_base + C::DP_COL + h * 64, v_kmaj + kmaj_off(kk), do_kmaj + hoff + kmaj_off(kk),
+                       C::IDESC_S, kk > 0 ? 1u : 0u);
+        mma_commit_elect(bar_dp(h));
+      }
+      // dV += P^T dO_i and dK += dS^T Q_i, half by half as the rows finish (K = 16 queries per
+      // MMA step = 8 TMEM columns of bf16 pairs; queries 64-127 start at column 64)
 #pragma unroll
-      for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ts_elect(tmem_base + C::DK_COL, tmem_base + C::DP_COL + pcol(kk), q_nmaj + rows16_off(kk), C::IDESC_KV,
-                     (it > 0 || kk > 0) ? 1u : 0u);
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = wait_all(bar_ds(h), ph, B_DS))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), do_nmaj + rows16_off(kk),
+                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_elect(tmem_base + C::DK_COL, tmem_base + C::DP_COL + pcol(kk), q_nmaj + rows16_off(kk),
+                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!ok) break;
       // dQ_i = dS K_j (K = the 128 keys) into the columns P^T occupied: after the dV MMAs that
       // read it (MMAs of one thread run in order)
 #pragma unroll
@@ -289,11 +331,35 @@ __global__ void __launch_bounds__(kBwdThreads)
         mma_ss_elect(tmem_base + C::S_COL, st_mmaj + rows16_off(kk), k_nmaj + rows16_off(kk), C::IDESC_Q,
                      kk > 0 ? 1u : 0u);
       mma_commit_elect(bar_dq);
-      mma_commit_elect(bar_qdo_empty(s));
     }
     // every MMA complete (for the dK / dV epilogue and before TMEM is freed)
     mma_commit_elect(bar_done);
     mbar_wait(bar_done, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
+  } else if (warp == kBwdReducer) {
+    // ============ dQ reducer (whole warp, one lane issues): TMA reduce-adds of the blocks ============
+    // Step `it` uses stage it & 1 for Q_i, dO_i and then for the row warps' dQ blocks; each block
+    // is added into rows q0 + 32 (w % 4) .. + 31 (clipped at Nq; skipped when wholly past it)
+    // and columns 32 (DQ_CHUNKS (w / 4) + m) of the fp32 accumulator.
+    bool ok = true;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int s = it & 1, q0 = (i_begin + it) * BT;
+      if (!(ok = wait_all(bar_dq_staged(s), (uint32_t)(it >> 1) & 1u, B_DQ_STAGED))) break;
+      if (lane == 0) {
+        const uint32_t stage_base = C::Q_OFF + (uint32_t)s * C::TILE_BYTES;
+        for (int w = 0; w < kBwdRowWarps; ++w) {
+          if (q0 + (w & 3) * 32 >= p.Nq) continue;
+          for (int m = 0; m < C::DQ_CHUNKS; ++m)
+            tma_reduce_add_3d(&tm_dq, sbase + bwd_dq_block<C>(stage_base, w, m), ((w >> 2) * C::DQ_CHUNKS + m) * 32,
+                              q0 + (w & 3) * 32, bh);
+        }
+        bulk_commit_group();
+        bulk_wait_read<0>();  // the stage may be refilled once its blocks have been read
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qdo_empty(s));
+    }
+    if (lane == 0) bulk_wait_all();  // every add performed before the CTA exits
+    __syncwarp();
   } else {
     // =================== rows: warps 0-7, thread t = TMEM lane t % 128 ===================
     const int tt = threadIdx.x & (BT - 1);  // key row of the tile (the dQ tile: query row)
@@ -304,47 +370,59 @@ __global__ void __launch_bounds__(kBwdThreads)
     const float* lse_row = p.lse + (int64_t)bh * p.Nq;
     const float* dsum_row = p.dsum + (int64_t)bh * p.Nq;
     uint8_t* st_row = smem + C::ST_OFF + half * C::SLAB_BYTES + tt * 128;  // key row in slab `half`
-    const float4* ld4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
-    float2* ld_mine = reinterpret_cast<float2*>(smem + C::LD_OFF) + tt;
-    // this warp's own 32 staging rows: its dS rows, then its 32 x 32 fp32 dQ blocks
-    const uint32_t scratch = sbase + C::ST_OFF + half * C::SLAB_BYTES + (warp & 3) * 32 * 128;
-    constexpr int DQ_CHUNKS = D / 64;  // 32-column dQ chunks per warp
-    const float sl2 = p.scale_log2;
+    const float4* nl4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
+    const float4* nd4 = reinterpret_cast<const float4*>(smem + C::LD_OFF + BT * 4);
+    // threads 0-63 of each half own the (LSE, D) entries of that half's queries
+    const int ld_q = 64 * half + tt;
+    float* nl_mine = reinterpret_cast<float*>(smem + C::LD_OFF) + ld_q;
+    float* nd_mine = reinterpret_cast<float*>(smem + C::LD_OFF + BT * 4) + ld_q;
+    constexpr int DQ_CHUNKS = C::DQ_CHUNKS;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    // (LSE, D) of query q0 + ld_q of step `step`, as loaded values (converted when stored)
+    auto load_ld = [&](int step, float& l, float& dd) {
+      const int q = (i_begin + step) * BT + ld_q;
+      l = -INFINITY;
+      dd = 0.f;
+      if (tt < 64 && step < n_it && q < p.Nq) {
+        l = lse_row[q];
+        dd = dsum_row[q];
+      }
+    };
+    // issued one step ahead: the loads' latency hides behind the step's dV / dK / dQ MMAs
+    float next_l, next_d;
+    load_ld(0, next_l, next_d);
     bool ok = true;
     for (int it = 0; ok && it < n_it; ++it) {
       const int i = i_begin + it, q0 = i * BT;
       const uint32_t ph = (uint32_t)it & 1u;
       // every (key, query) pair of the step visible and inside the tensors
       const bool full = (k0 + BT <= p.Nk) && (q0 + BT <= p.Nq) && (!p.causal || i > j);
-      // (LSE log2 e, D) of query q0 + t; a row past the end or with no visible key gets
-      // +inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
-      float2 mine = make_float2(INFINITY, 0.f);
-      if (half == 0 && q0 + tt < p.Nq) {
-        const float l = lse_row[q0 + tt];
-        mine.x = l == -INFINITY ? INFINITY : l * kLog2e;
-        mine.y = dsum_row[q0 + tt];
-      }
-      if (!(ok = wait_all(bar_s, ph, B_S))) break;
+      if (!(ok = wait_all(bar_s(half), ph, B_S))) break;
+      // -LSE log2 e and -D of query q0 + ld_q; a row past the end or with no visible key gets
+      // -inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
       // every row warp is past the previous step's reads of the (LSE, D) block: it arrived on
-      // dq_read, which the S MMA of this step waited for
-      if (half == 0) *ld_mine = mine;
-      // this warp's dQ blocks of the previous step have left the staging rows it rewrites now
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ld);
-      if (!(ok = wait_all(bar_ld, ph, B_LD))) break;
-      if (!(ok = wait_all(bar_dp, ph, B_DP))) break;
+      // dq_read, which the S MMAs of this step waited for
+      if (tt < 64) {
+        *nl_mine = next_l == -INFINITY ? -INFINITY : -next_l * kLog2e;
+        *nd_mine = -next_d;
+      }
+      if (lane == 0) mbar_arrive(bar_ld(half));
+      if (!(ok = wait_all(bar_ld(half), ph, B_LD))) break;
+      if (!(ok = wait_all(bar_dp(half), ph, B_DP))) break;
       tc_fence_after_sync();
-#pragma unroll 1
-      for (int c = 64 * half; c < 64 * half + 64; c += 32) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem_base + lane_base + C::S_COL + c, sr);
-        tmem_ld32(tmem_base + lane_base + C::DP_COL + c, dr);
+      // this half's 64 columns of S^T (sd[0..63]) and dP^T (sd[64..127]), one wait
+      uint32_t sd[128];
+      tmem_ld64x2(tmem_base + lane_base + C::S_COL + 64 * half, tmem_base + lane_base + C::DP_COL + 64 * half, sd);
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 64 * half + 32 * cc;
         uint32_t pw[16], dw[16];
         if (full)
-          bwd_p_ds<false>(sr, dr, ld4 + c / 2, sl2, key, q0 + c, true, false, pw, dw);
+          bwd_p_ds<false>(sd + 32 * cc, sd + 64 + 32 * cc, nl4 + c / 4, nd4 + c / 4, sl2x2, key, q0 + c, true, false,
+                          pw, dw);
         else
-          bwd_p_ds<true>(sr, dr, ld4 + c / 2, sl2, key, q0 + c, key_ok, p.causal != 0, pw, dw);
+          bwd_p_ds<true>(sd + 32 * cc, sd + 64 + 32 * cc, nl4 + c / 4, nd4 + c / 4, sl2x2, key, q0 + c, key_ok,
+                         p.causal != 0, pw, dw);
         // P^T / dS^T as bf16 pairs: queries c .. c+31 to columns c/2 (+32 for the second half),
         // all of them already read by this warp and by no other
         const uint32_t oc = c / 2 + (c >= 64 ? 32 : 0);
@@ -362,7 +440,8 @@ __global__ void __launch_bounds__(kBwdThreads)
       tc_fence_before_sync();
       fence_proxy_async_smem();  // the staged dS is read by the tensor core (async proxy)
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ds);
+      if (lane == 0) mbar_arrive(bar_ds(half));
+      load_ld(it + 1, next_l, next_d);
       // dQ_i = scale dS K_j: thread t holds query row q0 + t % 128.  The warp's columns leave
       // TMEM first (so the next step's S MMA may overwrite them); then per 32 columns the warp
       // stages its 32 x 32 block (swizzled like the map) in its own staging rows, which the dQ
@@ -377,30 +456,20 @@ __global__ void __launch_bounds__(kBwdThreads)
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_read);
-      const bool rows_in = q0 + (warp & 3) * 32 < p.Nq;
-      uint8_t* brow = smem + (scratch - sbase) + lane * 128;
+      const uint32_t stage_base = C::Q_OFF + (uint32_t)(it & 1) * C::TILE_BYTES;  // this step's Q stage
 #pragma unroll
       for (int m = 0; m < DQ_CHUNKS; ++m) {
-        if (m > 0) {  // the previous block has been read out of the staging rows
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-        }
+        uint8_t* brow = smem + bwd_dq_block<C>(stage_base, warp, m) + lane * 128;
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
           *reinterpret_cast<float4*>(brow + ((q4 ^ (lane & 7)) * 16)) =
               make_float4(__uint_as_float(r[m][4 * q4]) * p.scale, __uint_as_float(r[m][4 * q4 + 1]) * p.scale,
                           __uint_as_float(r[m][4 * q4 + 2]) * p.scale, __uint_as_float(r[m][4 * q4 + 3]) * p.scale);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && rows_in) {
-          tma_reduce_add_3d(&tm_dq, scratch, (half * DQ_CHUNKS + m) * 32, q0 + (warp & 3) * 32, bh);
-          bulk_commit_group();
-        }
       }
+      fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_staged(it & 1));
     }
-    // the last dQ blocks: read out of shared memory and added before the CTA may exit
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
     // dK_j, dV_j rows (key rows of the tile), columns [half D/2, half D/2 + D/2)
     if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
     if (ok) {
