@@ -5,6 +5,8 @@
 Cases (inputs seeded as in the benchmark):
   attn_causal      causal attention fwd bf16, B=1 H=32 N=8192 d=128 (~256 MiB on the device)
   attn_noncausal   non-causal attention fwd bf16, B=4 H=16 N=4096 d=64
+  attn_bwd_causal  causal attention bwd bf16, B=1 H=32 N=8192 d=128 (O and LSE from the forward;
+                   ~650 MiB on the device)
   softmax          row softmax + LSE fp32 [4096, 32768] (1 GiB)
   decode           split-KV decode bf16, B (default 4) x H=32, Nk=32768, d=128, 64 chunks
                    (--batch 32 is the full 17 GB benchmark shape)
@@ -35,6 +37,13 @@ def make_case(name, dev, batch):
         q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
         o, lse = torch.empty_like(q), torch.empty((4, 16, 4096), device=dev)
         return lambda: oa.attn_fwd(q, k, v, out=o, lse=lse)
+    if name == "attn_bwd_causal":
+        q, k, v = si.attn_inputs(1, 32, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
+        do = si.randn((1, 32, 8192, 128), 3, torch.bfloat16, dev)
+        o, lse = oa.attn_fwd(q, k, v, causal=True)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(oa.attn_bwd_workspace_bytes(1, 32, 8192, 128), dtype=torch.uint8, device=dev)
+        return lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
     if name == "softmax":
         x, *_ = si.softmax_input(4096, 32768, seed=0)
         x = x.to(dev)
