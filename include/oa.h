@@ -161,6 +161,47 @@ oa_status oa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* 
                              int causal, float scale, oa_stream_t stream);
 
 /*
+ * Bytes of device workspace oa_attn_fwd_host needs: device copies of q, k,
+ * v, o (dtype dt) and lse (fp32), each rounded up to 256 bytes.  0 for
+ * invalid arguments.
+ */
+size_t oa_attn_fwd_host_workspace_bytes(oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d);
+
+/*
+ * oa_attn_fwd_gqa on HOST buffers: copies q, k, v in, runs the forward and
+ * copies o and lse back, overlapping the three.  A library addition with no
+ * counterpart on the source pages, for callers whose tensors live in host
+ * memory (the whole call is what a host-side user pays).  The B * H_kv
+ * key/value planes are cut into `chunks` pieces (0: the library's default of
+ * 4) whose sizes fall linearly, so that little work follows the last copy
+ * in; the copy in of piece c + 1, the kernel of piece c and the copy out of
+ * piece c - 1 run at the same time on three streams the library keeps for
+ * each device (created on the first call on that device; make that call
+ * before any stream capture).  Every piece's result equals that of
+ * oa_attn_fwd_gqa on the whole batch.
+ *   q_host, k_host, v_host, o_host, lse_host: host memory in the layouts of
+ *          oa_attn_fwd_gqa (lse_host may be NULL), 16-byte aligned.  For the
+ *          copies to overlap they must be page-locked (cudaHostAlloc,
+ *          pinned); they must stay valid, and the inputs unchanged, until
+ *          the call's work has completed on `stream`.
+ *   workspace: device memory of >= oa_attn_fwd_host_workspace_bytes(...)
+ *          bytes, 256-byte aligned, owned by the caller.
+ *   chunks: 0 .. 64.  kv_len is not supported here (all keys visible).
+ * Ordering: the work starts after everything queued on `stream` before the
+ * call and `stream` waits for all of it, so a synchronisation of `stream`
+ * covers the outputs.  Calls on one device are serialised by the library
+ * (they share its streams).
+ * Errors: those of oa_attn_fwd_gqa (checked before anything is queued), plus
+ * OA_ERR_INVALID for a bad chunks value or workspace.  A CUDA error after
+ * some pieces were queued returns OA_ERR_CUDA; the queued work still runs.
+ */
+oa_status oa_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                           float* lse_host, oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d,
+                           int causal, float scale, int chunks, void* workspace, size_t workspace_bytes,
+                           oa_stream_t stream);
+
+/*
+ * The fp32 SIMT attention forward with explicit tile sizes/*
  * The fp32 SIMT attention forward with explicit tile sizes: Br query rows
  * per CTA and Bc keys per step of the online recurrence (1 <= Br, Bc <= 64).
  * Same contract as oa_attn_fwd with dt = OA_F32; the result does not

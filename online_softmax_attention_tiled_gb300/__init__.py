@@ -30,6 +30,7 @@ EXPORTS = (
     "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd", "oa_attn_fwd_gqa",
     "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
     "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge", "oa_attn_bwd_workspace_bytes", "oa_attn_bwd",
+    "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -82,6 +83,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "oa_attn_splitkv_static": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, vp, i32, vp], i32),
             "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
             "oa_attn_bwd_workspace_bytes": ([i32, i32, i32, i32], sz),
+            "oa_attn_fwd_host_workspace_bytes": ([i32, i32, i32, i32, i32, i32, i32], sz),
+            "oa_attn_fwd_host": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp],
+                                 i32),
             "oa_attn_bwd": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp],
                             i32),
             "oa_sync_status": ([vp], i32),
@@ -200,6 +204,42 @@ def _cu_seqlens_arg(cu, device, name):
     if cu.dtype != torch.int32 or cu.dim() != 1 or cu.numel() < 2 or not cu.is_cuda or cu.device != device:
         raise OAError(OA_ERR_INVALID, f"{name} must be an int32 CUDA tensor of num_seqs + 1 offsets on q's device")
     return cu.contiguous()
+
+
+def attn_fwd_host_workspace_bytes(dtype, B: int, H: int, H_kv: int, Nq: int, Nk: int, d: int) -> int:
+    return int(load().oa_attn_fwd_host_workspace_bytes(_dtype_code(dtype), B, H, H_kv, Nq, Nk, d))
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+                  chunks: int = 0, workspace=None, device=None):
+    """attn_fwd on host (CPU) tensors, pinned for the copies to overlap: the library copies q, k, v to the
+    device in pieces, runs the forward and copies o and lse back while the next pieces move.  Outputs are
+    CPU tensors (pinned when allocated here), complete once the current stream of `device` is synchronised.
+    workspace: optional uint8 CUDA tensor of attn_fwd_host_workspace_bytes."""
+    for t in (q, k, v, out, lse):
+        if t is not None and t.is_cuda:
+            raise OAError(OA_ERR_INVALID, "attn_fwd_host takes host tensors")
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v, allow_groups=True)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if out is None:
+        out = torch.empty((B, H, Nq, d), dtype=q.dtype).pin_memory()
+    if want_lse and lse is None:
+        lse = torch.empty((B, H, Nq), dtype=torch.float32).pin_memory()
+    if tuple(out.shape) != (B, H, Nq, d) or out.dtype != q.dtype or not out.is_contiguous():
+        raise OAError(OA_ERR_INVALID, "out must be a contiguous [B, H, Nq, d] host tensor of q's dtype")
+    if lse is not None and (tuple(lse.shape) != (B, H, Nq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise OAError(OA_ERR_INVALID, "lse must be a contiguous float32 [B, H, Nq] host tensor")
+    need = attn_fwd_host_workspace_bytes(q.dtype, B, H, Hkv, Nq, Nk, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+    _require_cuda(workspace)
+    with torch.cuda.device(dev):
+        _check(load().oa_attn_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _dtype_code(q.dtype), B, H,
+                                       Hkv, Nq, Nk, d, int(bool(causal)), float(scale), int(chunks), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(dev)))
+    return out, lse
 
 
 def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,

@@ -2,11 +2,13 @@
 // dispatch to the kernels, the device status word and the wait-limit
 // self-test.  Nothing here computes results; every step of the path runs in
 // the kernels of this directory.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "oa.h"
 #include "oa_internal.h"
@@ -143,9 +145,10 @@ static oa_status check_heads(int H, int Hkv, const char* who) {
   return OA_OK;
 }
 
-static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
-                               int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
-                               const int32_t* kv_len, oa_stream_t stream, const char* who) {
+// Every check of the dense forward, before anything is launched or copied.
+static oa_status check_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
+                           int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                           const char* who) {
   oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, who);
   if (s != OA_OK) return s;
   if ((s = check_heads(H, Hkv, who)) != OA_OK) return s;
@@ -157,8 +160,13 @@ static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (dt == OA_F32 && d > 256) return fail(OA_ERR_UNSUPPORTED, "%s: fp32 supports d <= 256 (got %d)", who, d);
   const int64_t grid = (int64_t)B * H * (dt == OA_BF16 ? (Nq + 255) / 256 : (Nq + 15) / 16);
   if (grid > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);
-  oa::DevStatus st;
-  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  return OA_OK;
+}
+
+// The dense forward on `stream`, arguments already checked.
+static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                            int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
+                            const oa::DevStatus& st, cudaStream_t stream, const char* who) {
   if (dt == OA_BF16) {
     oa::TcArgs a{};
     a.q = q;
@@ -176,14 +184,24 @@ static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
     a.scale = scale;
     a.kv_len = kv_len;
     const char* why = nullptr;
-    cudaError_t e = oa::launch_attn_tc(a, st, (cudaStream_t)stream, &why);
+    cudaError_t e = oa::launch_attn_tc(a, st, stream, &why);
     if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_fwd launch");
     return ok();
   }
   cudaError_t e = oa::launch_attn_f32(static_cast<const float*>(q), static_cast<const float*>(k),
                                       static_cast<const float*>(v), static_cast<float*>(o), lse, B, H, Hkv, Nq, Nk,
-                                      d, causal, scale, kv_len, 0, 0, (cudaStream_t)stream);
+                                      d, causal, scale, kv_len, 0, 0, stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd launch");
+}
+
+static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                               int H, int Hkv, int Nq, int Nk, int d, int causal, float scale,
+                               const int32_t* kv_len, oa_stream_t stream, const char* who) {
+  oa_status s = check_fwd(q, k, v, o, lse, dt, B, H, Hkv, Nq, Nk, d, causal, scale, kv_len, who);
+  if (s != OA_OK) return s;
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  return launch_fwd(q, k, v, o, lse, dt, B, H, Hkv, Nq, Nk, d, causal, scale, kv_len, st, (cudaStream_t)stream, who);
 }
 
 oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
@@ -195,6 +213,156 @@ oa_status oa_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
                           int H, int H_kv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
                           oa_stream_t stream) {
   return attn_fwd_impl(q, k, v, o, lse, dt, B, H, H_kv, Nq, Nk, d, causal, scale, kv_len, stream, "attn_fwd_gqa");
+}
+
+// ---------------------------------------------------------------------------
+// Host-buffer forward: chunked copies in, kernels, copies out, overlapped on three streams
+// the library keeps per device, joined back to the caller's stream.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kHostMaxChunks = 64;
+constexpr int kHostDefaultChunks = 4;
+constexpr int kHostMaxDevices = 64;
+
+struct HostPipe {
+  std::mutex mu;  // one call at a time per device: the streams and events are shared
+  bool ready = false;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t landed[kHostMaxChunks] = {}, done[kHostMaxChunks] = {};
+};
+HostPipe g_pipes[kHostMaxDevices];
+
+// The device's streams and events, created on first use (with `dev` current).
+cudaError_t host_pipe(int dev, HostPipe** out) {
+  HostPipe& p = g_pipes[dev];
+  if (!p.ready) {
+    cudaError_t e = cudaSuccess;
+    for (cudaStream_t* st : {&p.in, &p.comp, &p.out})
+      if (e == cudaSuccess && *st == nullptr) e = cudaStreamCreateWithFlags(st, cudaStreamNonBlocking);
+    for (cudaEvent_t* ev : {&p.start, &p.end})
+      if (e == cudaSuccess && *ev == nullptr) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+    for (int c = 0; c < kHostMaxChunks && e == cudaSuccess; ++c) {
+      if (p.landed[c] == nullptr) e = cudaEventCreateWithFlags(&p.landed[c], cudaEventDisableTiming);
+      if (e == cudaSuccess && p.done[c] == nullptr) e = cudaEventCreateWithFlags(&p.done[c], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return e;
+    p.ready = true;
+  }
+  *out = &p;
+  return cudaSuccess;
+}
+
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+
+// First key/value plane of piece c of nch over `units` planes.  The sizes fall linearly (boundaries
+// at units (1 - (1 - c / nch)^2), every piece non-empty): what follows the last copy in -- the last
+// piece's kernel and copy out -- is then short.  Each piece's kernel costs at least its heaviest item
+// (for causal attention, the last query tiles against every key), so a few pieces beat many.
+size_t host_piece_bound(int c, int nch, int units) {
+  if (c >= nch) return (size_t)units;
+  const double t = 1.0 - (double)c / nch;
+  const size_t u = (size_t)(units * (1.0 - t * t) + 0.5);
+  return std::max((size_t)c, std::min(u, (size_t)(units - (nch - c))));
+}
+
+struct HostLayout {
+  size_t esize, q, kv, o, lse, total;  // section bytes (each 256-byte aligned), total
+};
+
+HostLayout host_layout(oa_dtype dt, int B, int H, int Hkv, int Nq, int Nk, int d) {
+  HostLayout L{};
+  L.esize = dt == OA_F32 ? 4 : 2;
+  L.q = round256((size_t)B * H * Nq * d * L.esize);
+  L.kv = round256((size_t)B * Hkv * Nk * d * L.esize);
+  L.o = L.q;
+  L.lse = round256((size_t)B * H * Nq * 4);
+  L.total = L.q + 2 * L.kv + L.o + L.lse;
+  return L;
+}
+
+}  // namespace
+
+size_t oa_attn_fwd_host_workspace_bytes(oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d) {
+  if ((dt != OA_BF16 && dt != OA_F32) || B < 1 || H < 1 || H_kv < 1 || Nq < 1 || Nk < 1 || d < 1) return 0;
+  return host_layout(dt, B, H, H_kv, Nq, Nk, d).total;
+}
+
+oa_status oa_attn_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                           oa_dtype dt, int B, int H, int H_kv, int Nq, int Nk, int d, int causal, float scale,
+                           int chunks, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  const char* who = "attn_fwd_host";
+  oa_status s = check_fwd(q_host, k_host, v_host, o_host, lse_host, dt, B, H, H_kv, Nq, Nk, d, causal, scale,
+                          nullptr, who);
+  if (s != OA_OK) return s;
+  if (chunks < 0 || chunks > kHostMaxChunks)
+    return fail(OA_ERR_INVALID, "%s: chunks must be 0 (default) .. %d", who, kHostMaxChunks);
+  const HostLayout L = host_layout(dt, B, H, H_kv, Nq, Nk, d);
+  if (workspace == nullptr || workspace_bytes < L.total || !aligned(workspace, 256))
+    return fail(OA_ERR_INVALID, "%s: workspace must be 256-byte aligned and >= %zu bytes", who, L.total);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostMaxDevices)
+    return fail(OA_ERR_CUDA, "%s: no usable current CUDA device", who);
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* qd = ws;
+  uint8_t* kd = qd + L.q;
+  uint8_t* vd = kd + L.kv;
+  uint8_t* od = vd + L.kv;
+  float* lsed = lse_host ? reinterpret_cast<float*>(od + L.o) : nullptr;
+  // chunks over the B * H_kv key/value planes; query planes follow in groups of H / H_kv
+  const int units = B * H_kv, g = H / H_kv;
+  const int nch = std::min(chunks > 0 ? chunks : kHostDefaultChunks, units);
+  const size_t qplane = (size_t)Nq * d * L.esize, kvplane = (size_t)Nk * d * L.esize, lplane = (size_t)Nq * 4;
+  const uint8_t* qh = static_cast<const uint8_t*>(q_host);
+  const uint8_t* kh = static_cast<const uint8_t*>(k_host);
+  const uint8_t* vh = static_cast<const uint8_t*>(v_host);
+  uint8_t* oh = static_cast<uint8_t*>(o_host);
+  uint8_t* lh = reinterpret_cast<uint8_t*>(lse_host);
+
+  HostPipe* p = nullptr;
+  std::lock_guard<std::mutex> lock(g_pipes[dev].mu);
+  cudaError_t e = host_pipe(dev, &p);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_fwd_host stream set-up");
+  const cudaStream_t user = (cudaStream_t)stream;
+  // nothing starts before the caller's earlier work on `stream` (which may still use the workspace)
+  if ((e = cudaEventRecord(p->start, user)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host record");
+  if ((e = cudaStreamWaitEvent(p->in, p->start, 0)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host wait");
+  for (int c = 0; c < nch; ++c) {
+    const size_t u0 = host_piece_bound(c, nch, units), u1 = host_piece_bound(c + 1, nch, units);
+    const size_t nu = u1 - u0;
+    // in: this chunk's Q (nu * g planes), K and V (nu planes)
+    if ((e = cudaMemcpyAsync(qd + u0 * g * qplane, qh + u0 * g * qplane, nu * g * qplane, cudaMemcpyHostToDevice,
+                             p->in)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(kd + u0 * kvplane, kh + u0 * kvplane, nu * kvplane, cudaMemcpyHostToDevice, p->in)) !=
+            cudaSuccess ||
+        (e = cudaMemcpyAsync(vd + u0 * kvplane, vh + u0 * kvplane, nu * kvplane, cudaMemcpyHostToDevice, p->in)) !=
+            cudaSuccess ||
+        (e = cudaEventRecord(p->landed[c], p->in)) != cudaSuccess)
+      return cuda_fail(e, "attn_fwd_host copy in");
+    // compute: the chunk as one batch of nu * g query heads over nu key/value heads
+    if ((e = cudaStreamWaitEvent(p->comp, p->landed[c], 0)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host wait");
+    s = launch_fwd(qd + u0 * g * qplane, kd + u0 * kvplane, vd + u0 * kvplane, od + u0 * g * qplane,
+                   lsed ? lsed + u0 * g * Nq : nullptr, dt, 1, (int)(nu * g), (int)nu, Nq, Nk, d, causal, scale,
+                   nullptr, st, p->comp, who);
+    if (s != OA_OK) return s;
+    if ((e = cudaEventRecord(p->done[c], p->comp)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host record");
+    // out: O and LSE of the chunk
+    if ((e = cudaStreamWaitEvent(p->out, p->done[c], 0)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host wait");
+    if ((e = cudaMemcpyAsync(oh + u0 * g * qplane, od + u0 * g * qplane, nu * g * qplane, cudaMemcpyDeviceToHost,
+                             p->out)) != cudaSuccess)
+      return cuda_fail(e, "attn_fwd_host copy out");
+    if (lh && (e = cudaMemcpyAsync(lh + u0 * g * lplane, lsed + u0 * g * Nq, nu * g * lplane, cudaMemcpyDeviceToHost,
+                                   p->out)) != cudaSuccess)
+      return cuda_fail(e, "attn_fwd_host copy out");
+  }
+  // the caller's stream continues after the last copy out (which follows every chunk's kernel)
+  if ((e = cudaEventRecord(p->end, p->out)) != cudaSuccess || (e = cudaStreamWaitEvent(user, p->end, 0)) != cudaSuccess)
+    return cuda_fail(e, "attn_fwd_host join");
+  return ok();
 }
 
 oa_status oa_attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,

@@ -141,6 +141,25 @@ def test_attn_bwd_validation(lib):
     assert "d = 64 or 128" in _err(lib)
 
 
+def test_attn_fwd_host_validation(lib):
+    NULL = None
+    need = lib.oa_attn_fwd_host_workspace_bytes(oa.OA_BF16, 2, 8, 2, 100, 100, 64)
+    r = lambda n: (n + 255) // 256 * 256
+    assert need == 2 * r(2 * 8 * 100 * 64 * 2) + 2 * r(2 * 2 * 100 * 64 * 2) + r(2 * 8 * 100 * 4)
+    assert lib.oa_attn_fwd_host_workspace_bytes(7, 2, 8, 2, 100, 100, 64) == 0
+    WS = ctypes.c_void_p(0x100000)
+
+    def call(q=FAKE, o=FAKE, dt=oa.OA_BF16, H=8, Hkv=2, d=64, causal=1, Nk=100, chunks=0, ws=WS, ws_bytes=need):
+        return lib.oa_attn_fwd_host(q, FAKE, FAKE, o, FAKE, dt, 2, H, Hkv, 100, Nk, d, causal, 0.125, chunks, ws,
+                                    ws_bytes, NULL)
+
+    for bad in (dict(q=NULL), dict(o=NULL), dict(q=FAKE_ODD), dict(Hkv=3), dict(causal=2), dict(chunks=-1),
+                dict(chunks=65), dict(ws=NULL), dict(ws=ctypes.c_void_p(0x100010)), dict(ws_bytes=need - 1)):
+        assert call(**bad) == oa.OA_ERR_INVALID, bad
+    assert call(Nk=99) == oa.OA_ERR_UNSUPPORTED  # causal needs Nq == Nk
+    assert call(d=96) == oa.OA_ERR_UNSUPPORTED
+
+
 def test_lse_merge_validation(lib):
     NULL = None
     assert lib.oa_lse_merge(FAKE, NULL, 2, 4, 8, FAKE, oa.OA_F32, FAKE, NULL) == oa.OA_ERR_INVALID
