@@ -56,7 +56,7 @@ def _load():
     lib.oracle_softmax_rows.restype = i32
     lib.oracle_attn.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32, dbl, vp, vp, i64, vp, vp, i32]
     lib.oracle_attn.restype = i32
-    lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i64, i32, dbl, vp, vp, vp, i32]
+    lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, i64, i64, i32, dbl, vp, vp, vp, i32]
     lib.oracle_attn_bwd.restype = i32
     lib.oracle_attn_bwd_sampled.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i32, dbl, vp, i64, vp, i64, vp, vp,
                                             vp, i32]
@@ -163,9 +163,10 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthread
 def attention_bwd(q, k, v, dout, causal=False, scale=None, nthreads=None):
     """Gradients (dq, dk, dv) of O = softmax(scale Q K^T) V given dO = dout, in fp64.
 
-    q, dout [B,H,Nq,d]; k, v [B,H,Nk,d] (same dtype code).  Causal: key j visible to query i iff
-    j <= i.  P is recomputed from the scores (no stored attention matrix), as the backward of the
-    forward definition; see oracle.c for the formulas."""
+    q, dout [B,H,Nq,d]; k, v [B,Hkv,Nk,d] (same dtype code; Hkv divides H and query head h reads
+    key/value head h // (H // Hkv); the dk, dv of a key/value head sum over its query heads).
+    Causal: key j visible to query i iff j <= i.  P is recomputed from the scores (no stored
+    attention matrix), as the backward of the forward definition; see oracle.c for the formulas."""
     qa, code = _as_input(q)
     ka, kcode = _as_input(k)
     va, vcode = _as_input(v)
@@ -173,16 +174,16 @@ def attention_bwd(q, k, v, dout, causal=False, scale=None, nthreads=None):
     if not (code == kcode == vcode == dcode):
         raise ValueError("q, k, v, dout must share a dtype")
     B, H, Nq, d = qa.shape
-    Nk = ka.shape[2]
-    if ka.shape != (B, H, Nk, d) or va.shape != (B, H, Nk, d) or da.shape != (B, H, Nq, d):
+    Hkv, Nk = ka.shape[1], ka.shape[2]
+    if ka.shape != (B, Hkv, Nk, d) or va.shape != (B, Hkv, Nk, d) or da.shape != (B, H, Nq, d) or H % Hkv:
         raise ValueError("shape mismatch")
     if scale is None:
         scale = 1.0 / np.sqrt(d)
     dq = np.zeros((B, H, Nq, d), np.float64)
-    dk = np.zeros((B, H, Nk, d), np.float64)
-    dv = np.zeros((B, H, Nk, d), np.float64)
-    rc = _load().oracle_attn_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), code, B, H, Nq, Nk, d, int(bool(causal)),
-                                 float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _threads(nthreads))
+    dk = np.zeros((B, Hkv, Nk, d), np.float64)
+    dv = np.zeros((B, Hkv, Nk, d), np.float64)
+    rc = _load().oracle_attn_bwd(_ptr(qa), _ptr(ka), _ptr(va), _ptr(da), code, B, H, Hkv, Nq, Nk, d,
+                                 int(bool(causal)), float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _threads(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_attn_bwd failed")
     return dq, dk, dv

@@ -259,12 +259,15 @@ int oracle_attn(const void* q, const void* k, const void* v, int dtype, int64_t 
 /* (the softmax Jacobian row i is diag(P_i) - P_i P_i^T, and            */
 /*  P_i . dP_i = dO_i . O_i = D_i).  A row with no visible key has      */
 /* P = 0 and contributes nothing.  Layout: q, dout [B,H,Nq,d]; k, v     */
-/* [B,H,Nk,d]; dq [B,H,Nq,d], dk and dv [B,H,Nk,d], all fp64 out.       */
+/* [B,Hkv,Nk,d] (query head h reads key/value head h / (H / Hkv)); dq   */
+/* [B,H,Nq,d], dk and dv [B,Hkv,Nk,d], all fp64 out.  A key/value head  */
+/* used by several query heads receives the sum of their dK, dV (each   */
+/* use is a separate term of the loss).                                 */
 /* ------------------------------------------------------------------ */
 typedef struct {
   const void *q, *k, *v, *dout;
   int dtype;
-  int64_t H, Nq, Nk, d;
+  int64_t H, Hkv, Nq, Nk, d;
   int causal;
   double scale;
   double *dq, *dk, *dv;
@@ -276,8 +279,12 @@ static void bwd_range(void* p, int64_t t0, int64_t t1, double* scratch) {
   double* P = scratch;            /* [Nq][Nk] */
   double* dS = P + Nq * Nk;       /* [Nq][Nk] */
   double* O = dS + Nq * Nk;       /* [Nq][d]  */
-  for (int64_t bh = t0; bh < t1; ++bh) {
-    const int64_t qb = bh * Nq * d, kb = bh * Nk * d;
+  const int64_t g = c->H / c->Hkv;
+  /* one key/value plane per item; its query heads in turn, summing into its dK, dV */
+  for (int64_t kvp = t0; kvp < t1; ++kvp)
+  for (int64_t t = 0; t < g; ++t) {
+    const int64_t bh = kvp * g + t; /* query plane: (b, h) with h = (kvp % Hkv) g + t */
+    const int64_t qb = bh * Nq * d, kb = kvp * Nk * d;
     /* P, row by row (safe softmax of the visible scaled scores) */
     for (int64_t i = 0; i < Nq; ++i) {
       double m = -INFINITY;
@@ -331,8 +338,12 @@ static void bwd_range(void* p, int64_t t0, int64_t t1, double* scratch) {
           ak += dS[i * Nk + j] * widen(c->q, c->dtype, qb + i * d + e);
           av += P[i * Nk + j] * widen(c->dout, c->dtype, qb + i * d + e);
         }
-        c->dk[kb + j * d + e] = c->scale * ak;
-        c->dv[kb + j * d + e] = av;
+        if (t == 0) {
+          c->dk[kb + j * d + e] = 0.0;
+          c->dv[kb + j * d + e] = 0.0;
+        }
+        c->dk[kb + j * d + e] += c->scale * ak;
+        c->dv[kb + j * d + e] += av;
       }
   }
 }
@@ -340,12 +351,13 @@ static void bwd_range(void* p, int64_t t0, int64_t t1, double* scratch) {
 /* Gradients of attention for B*H independent heads (see above).  Returns 0,
  * or -1 on bad arguments. */
 int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* dout, int dtype, int64_t B,
-                    int64_t H, int64_t Nq, int64_t Nk, int64_t d, int causal, double scale, double* dq,
+                    int64_t H, int64_t Hkv, int64_t Nq, int64_t Nk, int64_t d, int causal, double scale, double* dq,
                     double* dk, double* dv, int nthreads) {
   if (!q || !k || !v || !dout || !dq || !dk || !dv || B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 0) return -1;
-  bwd_ctx c = {q, k, v, dout, dtype, H, Nq, Nk, d, causal, scale, dq, dk, dv};
+  if (Hkv < 1 || H % Hkv != 0) return -1;
+  bwd_ctx c = {q, k, v, dout, dtype, H, Hkv, Nq, Nk, d, causal, scale, dq, dk, dv};
   const int64_t scratch = 2 * Nq * Nk + Nq * d + 1;
-  return parallel_for(B * H, nthreads, scratch, bwd_range, &c);
+  return parallel_for(B * Hkv, nthreads, scratch, bwd_range, &c);
 }
 
 /* ------------------------------------------------------------------ */

@@ -468,6 +468,29 @@ def test_attention_bwd_vs_fp64_autograd(causal, Nq, Nk):
         np.testing.assert_allclose(g, r, rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_bwd_grouped_heads_vs_fp64_autograd(causal):
+    # key/value heads shared by groups of query heads: torch's autograd through K, V repeated over each
+    # group sums the gradient of every use, which is the definition the oracle must reach
+    rng = np.random.default_rng(31 + causal)
+    B, H, Hkv, N, d = 2, 6, 2, 7, 5
+    q, do = rng.standard_normal((B, H, N, d)), rng.standard_normal((B, H, N, d))
+    k, v = rng.standard_normal((B, Hkv, N, d)), rng.standard_normal((B, Hkv, N, d))
+    tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+    g = H // Hkv
+    s = 0.3 * tq @ tk.repeat_interleave(g, dim=1).transpose(-1, -2)
+    if causal:
+        s = s.masked_fill(torch.arange(N)[None, :] > torch.arange(N)[:, None], float("-inf"))
+    (torch.softmax(s, dim=-1) @ tv.repeat_interleave(g, dim=1)).backward(torch.tensor(do))
+    got = oracle.attention_bwd(q, k, v, do, causal=causal, scale=0.3)
+    for a, r in zip(got, (tq.grad, tk.grad, tv.grad)):
+        np.testing.assert_allclose(a, r.numpy(), rtol=1e-11, atol=1e-12)
+    # with H_kv = H it is the ungrouped backward of each head
+    full = oracle.attention_bwd(q, np.repeat(k, g, axis=1), np.repeat(v, g, axis=1), do, causal=causal, scale=0.3)
+    np.testing.assert_allclose(got[0], full[0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(got[1], full[1].reshape(B, Hkv, g, N, d).sum(2), rtol=1e-11, atol=1e-12)
+
+
 def test_attention_bwd_finite_differences():
     # central differences of L = sum(O * dO) through the (pinned) forward oracle
     rng = np.random.default_rng(3)
