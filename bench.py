@@ -328,6 +328,19 @@ def components(oa, dev, peaks, peak_kind, steps):
                                           "O, LSE, dO)", "ms": ms, "value": tf, "unit": "TFLOP/s", "bound": "tensor",
                               "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
                               "algorithmic_flops": fl, "launches_per_call": 3}
+    del q, k, v, o, lse, dk, dv
+    # the same backward over grouped key/value heads (H_kv 8): dK, dV sum over each group's 4 query heads
+    q, k, v = si.attn_inputs_gqa(1, 32, 8, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
+    o, lse = oa.attn_fwd(q, k, v, causal=True)
+    dk, dv = torch.empty_like(k), torch.empty_like(v)
+    t = time_launches(lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws), steps,
+                      3, flush)
+    ms = statistics.mean(t)
+    tf = fl / (ms * 1e-3) / 1e12
+    out["attn_bwd_causal_gqa"] = {"workload": "causal attention bwd bf16 B=1 H=32 H_kv=8 N=8192 d=128", "ms": ms,
+                                  "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
+                                  "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
+                                  "algorithmic_flops": fl, "launches_per_call": 3}
     del q, k, v, do, o, lse, dq, dk, dv, ws, flush_buf
     torch.cuda.empty_cache()
     return out

@@ -257,6 +257,22 @@ oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o
                       size_t workspace_bytes, oa_stream_t stream);
 
 /*
+ * oa_attn_bwd with grouped key/value heads: k, v, dk, dv are [B, H_kv, Nk, d]
+ * and query head h reads key/value head h / (H / H_kv), as in
+ * oa_attn_fwd_gqa.  dK and dV of a key/value head sum the contributions of
+ * every query head of its group: one CTA per 128 keys of a key/value head
+ * steps through all query tiles of all the group's heads, so the sums stay
+ * on chip (no atomics) and remain deterministic.  H_kv == H is oa_attn_bwd.
+ * Same workspace (oa_attn_bwd_workspace_bytes(B, H, Nq, d)), support and
+ * errors as oa_attn_bwd, plus OA_ERR_INVALID when H_kv < 1 or does not
+ * divide H.
+ */
+oa_status oa_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, int B, int H,
+                          int H_kv, int Nq, int Nk, int d, int causal, float scale, void* workspace,
+                          size_t workspace_bytes, oa_stream_t stream);
+
+/*
  * Bytes of workspace oa_attn_splitkv needs: num_splits * B*H*Nq * (d + 1)
  * fp32 values (normalised partial outputs, then their LSEs), rounded up to
  * 256 bytes.  0 for invalid sizes.

@@ -30,7 +30,7 @@ EXPORTS = (
     "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd", "oa_attn_fwd_gqa",
     "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
     "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge", "oa_attn_bwd_workspace_bytes", "oa_attn_bwd",
-    "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host",
+    "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host", "oa_attn_bwd_gqa",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -84,6 +84,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "oa_lse_merge": ([vp, vp, i32, i64, i32, vp, i32, vp, vp], i32),
             "oa_attn_bwd_workspace_bytes": ([i32, i32, i32, i32], sz),
             "oa_attn_fwd_host_workspace_bytes": ([i32, i32, i32, i32, i32, i32, i32], sz),
+            "oa_attn_bwd_gqa": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp,
+                                 sz, vp], i32),
             "oa_attn_fwd_host": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp],
                                  i32),
             "oa_attn_bwd": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp],
@@ -304,10 +306,11 @@ def attn_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
 def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
              workspace=None):
     """Gradients (dq, dk, dv) of O = softmax(Q K^T * scale) V for the upstream gradient dout, with P recomputed
-    from the forward's LSE.  q, o, dout [B,H,Nq,d] and k, v [B,H,Nk,d], bf16 on CUDA; lse fp32 [B,H,Nq] (o and
-    lse from attn_fwd on the same inputs).  workspace: optional uint8 CUDA tensor of attn_bwd_workspace_bytes."""
+    from the forward's LSE.  q, o, dout [B,H,Nq,d] and k, v [B,H_kv,Nk,d] (H_kv divides H: grouped key/value
+    heads, whose dk, dv sum over their query heads), bf16 on CUDA; lse fp32 [B,H,Nq] (o and lse from attn_fwd
+    on the same inputs).  workspace: optional uint8 CUDA tensor of attn_bwd_workspace_bytes."""
     _require_cuda(q, k, v, o, lse, dout, dq, dk, dv, workspace)
-    B, H, Nq, Nk, d, _ = _attn_shapes(q, k, v)
+    B, H, Nq, Nk, d, Hkv = _attn_shapes(q, k, v, allow_groups=True)
     if tuple(o.shape) != (B, H, Nq, d) or tuple(dout.shape) != (B, H, Nq, d):
         raise OAError(OA_ERR_INVALID, "o and dout must be [B, H, Nq, d] like q")
     if o.dtype != q.dtype or dout.dtype != q.dtype or not o.is_contiguous() or not dout.is_contiguous():
@@ -326,9 +329,10 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     if dv is None:
         dv = torch.empty_like(v)
     with torch.cuda.device(q.device):
-        _check(load().oa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
-                                  _ptr(dv), _dtype_code(q.dtype), B, H, Nq, Nk, d, int(bool(causal)), float(scale),
-                                  _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(q.device)))
+        _check(load().oa_attn_bwd_gqa(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                      _ptr(dk), _ptr(dv), _dtype_code(q.dtype), B, H, Hkv, Nq, Nk, d,
+                                      int(bool(causal)), float(scale), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _stream(q.device)))
     return dq, dk, dv
 
 

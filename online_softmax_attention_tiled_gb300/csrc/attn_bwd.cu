@@ -87,7 +87,9 @@ struct BwdParams {
   const float* dsum;     // D [B H Nq]
   __nv_bfloat16* dk;     // [B H Nk, d]
   __nv_bfloat16* dv;
-  int Nq, Nk, causal, nkt, nqt, BH;
+  int Nq, Nk, causal, nkt, nqt;
+  int BHkv;   // key/value planes (B * H_kv): the grid covers nkt key tiles of each
+  int group;  // query heads per key/value head (H / H_kv); query plane = kv plane * group + t
   float scale, scale_log2;
   DevStatus st;
 };
@@ -201,11 +203,25 @@ __global__ void __launch_bounds__(kBwdThreads)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = (int)(blockIdx.x / p.BH);
-  const int bh = (int)(blockIdx.x % p.BH);
+  const int j = (int)(blockIdx.x / p.BHkv);
+  const int kvp = (int)(blockIdx.x % p.BHkv);  // key/value plane
   const int k0 = j * BT;
   const int i_begin = p.causal ? j : 0;  // causal: query tile i sees key tile j iff i >= j
-  const int n_it = max(p.nqt - i_begin, 0);
+  const int n_i = max(p.nqt - i_begin, 0);  // visible query tiles of one query head
+  // steps: every visible query tile of every query head of the group, head by head
+  const int n_it = p.group * n_i;
+  // (query head t of the group, query tile i) of consecutive steps, without a division per step
+  struct StepPos {
+    int t, i;
+  };
+  auto next_pos = [&](StepPos s) {
+    if (++s.i == p.nqt) {
+      s.i = i_begin;
+      ++s.t;
+    }
+    return s;
+  };
+  const StepPos first_pos{0, i_begin};
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -250,20 +266,21 @@ __global__ void __launch_bounds__(kBwdThreads)
     bool ok = true;
     mbar_arrive_expect_tx_elect(bar_kv, 2 * C::TILE_BYTES);
     for (int c = 0; c < C::SLABS; ++c) {
-      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, k0, bh);
-      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, k0, bh);
+      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, k0, kvp);
+      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, k0, kvp);
     }
     int issued = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int s = it & 1, q0 = (i_begin + it) * BT;
+    StepPos pos = first_pos;
+    for (int it = 0; it < n_it; ++it, pos = next_pos(pos)) {
+      const int s = it & 1, q0 = pos.i * BT, qp = kvp * p.group + pos.t;
       // stage s was last read by step it - 2
       if (it >= 2 && !(ok = wait_all(bar_qdo_empty(s), (uint32_t)((it >> 1) - 1) & 1u, B_QDO_EMPTY))) break;
       mbar_arrive_expect_tx_elect(bar_qdo(s), 2 * C::TILE_BYTES);
       for (int c = 0; c < C::SLABS; ++c) {
         tma_load_3d_elect(sbase + C::Q_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, bar_qdo(s), c * 64, q0,
-                          bh);
+                          qp);
         tma_load_3d_elect(sbase + C::DO_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_do, bar_qdo(s), c * 64,
-                          q0, bh);
+                          q0, qp);
       }
       ++issued;
     }
@@ -341,8 +358,9 @@ __global__ void __launch_bounds__(kBwdThreads)
     // is added into rows q0 + 32 (w % 4) .. + 31 (clipped at Nq; skipped when wholly past it)
     // and columns 32 (DQ_CHUNKS (w / 4) + m) of the fp32 accumulator.
     bool ok = true;
-    for (int it = 0; ok && it < n_it; ++it) {
-      const int s = it & 1, q0 = (i_begin + it) * BT;
+    StepPos pos = first_pos;
+    for (int it = 0; ok && it < n_it; ++it, pos = next_pos(pos)) {
+      const int s = it & 1, q0 = pos.i * BT, qp = kvp * p.group + pos.t;
       if (!(ok = wait_all(bar_dq_staged(s), (uint32_t)(it >> 1) & 1u, B_DQ_STAGED))) break;
       if (lane == 0) {
         const uint32_t stage_base = C::Q_OFF + (uint32_t)s * C::TILE_BYTES;
@@ -350,7 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads)
           if (q0 + (w & 3) * 32 >= p.Nq) continue;
           for (int m = 0; m < C::DQ_CHUNKS; ++m)
             tma_reduce_add_3d(&tm_dq, sbase + bwd_dq_block<C>(stage_base, w, m), ((w >> 2) * C::DQ_CHUNKS + m) * 32,
-                              q0 + (w & 3) * 32, bh);
+                              q0 + (w & 3) * 32, qp);
         }
         bulk_commit_group();
         bulk_wait_read<0>();  // the stage may be refilled once its blocks have been read
@@ -367,8 +385,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = k0 + tt;
     const bool key_ok = key < p.Nk;
-    const float* lse_row = p.lse + (int64_t)bh * p.Nq;
-    const float* dsum_row = p.dsum + (int64_t)bh * p.Nq;
+
     uint8_t* st_row = smem + C::ST_OFF + half * C::SLAB_BYTES + tt * 128;  // key row in slab `half`
     const float4* nl4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
     const float4* nd4 = reinterpret_cast<const float4*>(smem + C::LD_OFF + BT * 4);
@@ -379,21 +396,23 @@ __global__ void __launch_bounds__(kBwdThreads)
     constexpr int DQ_CHUNKS = C::DQ_CHUNKS;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     // (LSE, D) of query q0 + ld_q of step `step`, as loaded values (converted when stored)
-    auto load_ld = [&](int step, float& l, float& dd) {
-      const int q = (i_begin + step) * BT + ld_q;
+    auto load_ld = [&](int step, StepPos sp, float& l, float& dd) {
       l = -INFINITY;
       dd = 0.f;
+      const int q = sp.i * BT + ld_q;
       if (tt < 64 && step < n_it && q < p.Nq) {
-        l = lse_row[q];
-        dd = dsum_row[q];
+        const int64_t row = (int64_t)(kvp * p.group + sp.t) * p.Nq + q;
+        l = p.lse[row];
+        dd = p.dsum[row];
       }
     };
     // issued one step ahead: the loads' latency hides behind the step's dV / dK / dQ MMAs
     float next_l, next_d;
-    load_ld(0, next_l, next_d);
+    load_ld(0, first_pos, next_l, next_d);
     bool ok = true;
+    StepPos pos = first_pos;
     for (int it = 0; ok && it < n_it; ++it) {
-      const int i = i_begin + it, q0 = i * BT;
+      const int i = pos.i, q0 = i * BT;
       const uint32_t ph = (uint32_t)it & 1u;
       // every (key, query) pair of the step visible and inside the tensors
       const bool full = (k0 + BT <= p.Nk) && (q0 + BT <= p.Nq) && (!p.causal || i > j);
@@ -441,7 +460,8 @@ __global__ void __launch_bounds__(kBwdThreads)
       fence_proxy_async_smem();  // the staged dS is read by the tensor core (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds(half));
-      load_ld(it + 1, next_l, next_d);
+      pos = next_pos(pos);  // the next step's (head, tile); its (LSE, D) load is issued now
+      load_ld(it + 1, pos, next_l, next_d);
       // dQ_i = scale dS K_j: thread t holds query row q0 + t % 128.  The warp's columns leave
       // TMEM first (so the next step's S MMA may overwrite them); then per 32 columns the warp
       // stages its 32 x 32 block (swizzled like the map) in its own staging rows, which the dQ
@@ -474,8 +494,8 @@ __global__ void __launch_bounds__(kBwdThreads)
     if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
     if (ok) {
       tc_fence_after_sync();
-      __nv_bfloat16* dkrow = p.dk + ((int64_t)bh * p.Nk + key) * D;
-      __nv_bfloat16* dvrow = p.dv + ((int64_t)bh * p.Nk + key) * D;
+      __nv_bfloat16* dkrow = p.dk + ((int64_t)kvp * p.Nk + key) * D;
+      __nv_bfloat16* dvrow = p.dv + ((int64_t)kvp * p.Nk + key) * D;
 #pragma unroll 1
       for (int c = half * (D / 2); c < half * (D / 2) + D / 2; c += 32) {
         uint32_t rk[32], rv[32];
@@ -530,7 +550,7 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  const unsigned grid = (unsigned)p.nkt * (unsigned)p.BH;
+  const unsigned grid = (unsigned)p.nkt * (unsigned)p.BHkv;
   attn_bwd_tc_kernel<D><<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
@@ -541,14 +561,14 @@ size_t attn_bwd_workspace_floats(int B, int H, int Nq, int d) { return (size_t)B
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus& st, cudaStream_t s,
                             const char** why) {
-  const int d = a.d, BH = a.B * a.H;
+  const int d = a.d, BH = a.B * a.H, BHkv = a.B * a.Hkv;
   const int64_t rb = 2 * (int64_t)d;  // bytes per row
   const int64_t rows = (int64_t)BH * a.Nq;
   float* dq_acc = workspace;
   float* dsum = workspace + rows * d;
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!make_tile_map(&mq, a.q, d, a.Nq, rb, BH, rb * a.Nq) || !make_tile_map(&mk, a.k, d, a.Nk, rb, BH, rb * a.Nk) ||
-      !make_tile_map(&mv, a.v, d, a.Nk, rb, BH, rb * a.Nk) ||
+  if (!make_tile_map(&mq, a.q, d, a.Nq, rb, BH, rb * a.Nq) || !make_tile_map(&mk, a.k, d, a.Nk, rb, BHkv, rb * a.Nk) ||
+      !make_tile_map(&mv, a.v, d, a.Nk, rb, BHkv, rb * a.Nk) ||
       !make_tile_map(&mdo, a.dout, d, a.Nq, rb, BH, rb * a.Nq) ||
       !make_f32_tile_map(&mdq, dq_acc, d, a.Nq, 2 * rb, BH, 2 * rb * a.Nq, 32)) {
     if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
@@ -570,7 +590,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus&
   p.causal = a.causal;
   p.nkt = (a.Nk + BT - 1) / BT;
   p.nqt = (a.Nq + BT - 1) / BT;
-  p.BH = BH;
+  p.BHkv = BHkv;
+  p.group = a.H / a.Hkv;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;

@@ -434,19 +434,20 @@ size_t oa_attn_bwd_workspace_bytes(int B, int H, int Nq, int d) {
   return (oa::attn_bwd_workspace_floats(B, H, Nq, d) * sizeof(float) + 255) / 256 * 256;
 }
 
-oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                      void* dq, void* dk, void* dv, oa_dtype dt, int B, int H, int Nq, int Nk, int d, int causal,
-                      float scale, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
-  const char* who = "attn_bwd";
+static oa_status attn_bwd_impl(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                               const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, int B, int H, int Hkv,
+                               int Nq, int Nk, int d, int causal, float scale, void* workspace,
+                               size_t workspace_bytes, oa_stream_t stream, const char* who) {
   oa_status s = check_attn(q, k, v, dq, nullptr, B, H, Nq, Nk, d, causal, scale, who);
   if (s != OA_OK) return s;
+  if ((s = check_heads(H, Hkv, who)) != OA_OK) return s;
   if (!o || !dout || !lse || !dk || !dv) return fail(OA_ERR_INVALID, "%s: o, dout, lse, dk and dv are required", who);
   if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return fail(OA_ERR_INVALID, "%s: o/dout/dk/dv must be 16-byte aligned, lse 4-byte", who);
   if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "%s: causal needs Nq == Nk", who);
   if (dt != OA_BF16) return fail(OA_ERR_UNSUPPORTED, "%s: bf16 only", who);
   if (d != 64 && d != 128) return fail(OA_ERR_UNSUPPORTED, "%s: d = 64 or 128 (got %d)", who, d);
-  if ((int64_t)B * H * ((Nk + 127) / 128) > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);
+  if ((int64_t)B * Hkv * ((Nk + 127) / 128) > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);
   const size_t need = oa_attn_bwd_workspace_bytes(B, H, Nq, d);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
     return fail(OA_ERR_INVALID, "%s: workspace must be 16-byte aligned and >= %zu bytes", who, need);
@@ -464,6 +465,7 @@ oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o
   a.dv = dv;
   a.B = B;
   a.H = H;
+  a.Hkv = Hkv;
   a.Nq = Nq;
   a.Nk = Nk;
   a.d = d;
@@ -473,6 +475,21 @@ oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o
   cudaError_t e = oa::launch_attn_bwd(a, static_cast<float*>(workspace), st, (cudaStream_t)stream, &why);
   if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_bwd launch");
   return ok();
+}
+
+oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
+                      void* dq, void* dk, void* dv, oa_dtype dt, int B, int H, int Nq, int Nk, int d, int causal,
+                      float scale, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
+  return attn_bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, dt, B, H, H, Nq, Nk, d, causal, scale, workspace,
+                       workspace_bytes, stream, "attn_bwd");
+}
+
+oa_status oa_attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, int B, int H, int H_kv, int Nq,
+                          int Nk, int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                          oa_stream_t stream) {
+  return attn_bwd_impl(q, k, v, o, dout, lse, dq, dk, dv, dt, B, H, H_kv, Nq, Nk, d, causal, scale, workspace,
+                       workspace_bytes, stream, "attn_bwd_gqa");
 }
 
 size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {

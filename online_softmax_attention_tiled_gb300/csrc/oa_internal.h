@@ -62,7 +62,7 @@ struct BwdArgs {
   const void *q, *k, *v, *o, *dout;
   const float* lse;
   void *dq, *dk, *dv;
-  int B, H, Nq, Nk, d, causal;
+  int B, H, Hkv, Nq, Nk, d, causal;  // query head h reads key/value head h / (H / Hkv)
   float scale;
 };
 // fp32 values of workspace the backward needs: the dQ accumulator [B H Nq, d] and D [B H Nq].

@@ -139,6 +139,9 @@ def test_attn_bwd_validation(lib):
     assert call(dt=oa.OA_F32) == oa.OA_ERR_UNSUPPORTED
     assert call(d=96) == oa.OA_ERR_UNSUPPORTED
     assert "d = 64 or 128" in _err(lib)
+    # grouped heads: H_kv must divide H
+    assert lib.oa_attn_bwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, oa.OA_BF16, 2, 2, 3, 100, 100, 64,
+                               1, 0.125, FAKE, need, NULL) == oa.OA_ERR_INVALID
 
 
 def test_attn_fwd_host_validation(lib):

@@ -120,6 +120,33 @@ def test_attn_bwd_matches_oracle(B, H, Nq, Nk, d, causal, scale):
             _assert_within(dv[b, h], rv[b, h], tv, f"dV[{b},{h}]")
 
 
+@pytest.mark.parametrize("B,H,Hkv,N,d,causal", [
+    (1, 4, 2, 300, 128, True),
+    (2, 8, 2, 200, 64, False),
+    (1, 3, 1, 129, 64, True),
+])
+def test_attn_bwd_grouped_heads_match_oracle(B, H, Hkv, N, d, causal):
+    # dK, dV of a key/value head sum over its query heads: their first-order bounds add up
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, N, N, d, torch.bfloat16, seed=60 + N)
+    do = si.randn((B, H, N, d), 64 + N, torch.bfloat16)
+    sc = 1.0 / np.sqrt(d)
+    dq, dk, dv = _run(q, k, v, do, causal, sc)
+    rq, rk, rv = oracle.attention_bwd(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(do), causal=causal,
+                                      scale=sc)
+    g = H // Hkv
+    for b in range(B):
+        for hk in range(Hkv):
+            tk_sum, tv_sum = 0.0, 0.0
+            for t in range(g):
+                h = hk * g + t
+                f64 = [x.to(torch.float64) for x in (q[b, h], k[b, hk], v[b, hk], do[b, h])]
+                tq, tk, tv = _bounds(*f64, causal, sc, np.arange(N), np.arange(N))
+                _assert_within(dq[b, h], rq[b, h], tq, f"dQ[{b},{h}]")
+                tk_sum, tv_sum = tk_sum + tk, tv_sum + tv
+            _assert_within(dk[b, hk], rk[b, hk], tk_sum, f"dK[{b},{hk}]")
+            _assert_within(dv[b, hk], rv[b, hk], tv_sum, f"dV[{b},{hk}]")
+
+
 def test_attn_bwd_single_key_has_no_score_gradient():
     # one key: every weight is 1 whatever the scores, so dQ and dK vanish and dV is the sum of dO
     q, k, v, do = _inputs(1, 2, 200, 1, 64, seed=5)
