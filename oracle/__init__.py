@@ -247,6 +247,35 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=No
     return o, lse
 
 
+def attention_bwd_varlen(q, k, v, dout, cu_seqlens_q, cu_seqlens_k, causal=False, scale=None, nthreads=None):
+    """The gradients of attention_varlen, in fp64: q, dout [Tq,H,d], k/v [Tk,Hkv,d] token-major (same dtype
+    code).  Each sequence's tokens get the attention_bwd of that sequence alone (a sequence without keys has
+    a constant output, so zero gradients; keys no query sees get zero).  Only slicing and transposes happen
+    here.  Returns (dq [Tq,H,d], dk [Tk,Hkv,d], dv [Tk,Hkv,d])."""
+    qa, _ = _as_input(q)
+    ka, _ = _as_input(k)
+    va, _ = _as_input(v)
+    da, _ = _as_input(dout)
+    cq = np.asarray(cu_seqlens_q, dtype=np.int64)
+    ck = np.asarray(cu_seqlens_k, dtype=np.int64)
+    if cq.shape != ck.shape or cq.ndim != 1 or cq.shape[0] < 2:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must be [num_seqs + 1]")
+    dq = np.zeros(qa.shape, np.float64)
+    dk = np.zeros(ka.shape, np.float64)
+    dv = np.zeros(va.shape, np.float64)
+    heads_first = lambda a: np.ascontiguousarray(a.transpose(1, 0, 2)[None])
+    for s in range(cq.shape[0] - 1):
+        q0, q1, k0, k1 = int(cq[s]), int(cq[s + 1]), int(ck[s]), int(ck[s + 1])
+        if q1 <= q0 or k1 <= k0:
+            continue
+        g = attention_bwd(heads_first(qa[q0:q1]), heads_first(ka[k0:k1]), heads_first(va[k0:k1]),
+                          heads_first(da[q0:q1]), causal=causal, scale=scale, nthreads=nthreads)
+        dq[q0:q1] = g[0][0].transpose(1, 0, 2)
+        dk[k0:k1] = g[1][0].transpose(1, 0, 2)
+        dv[k0:k1] = g[2][0].transpose(1, 0, 2)
+    return dq, dk, dv
+
+
 def lse_merge(part_o, part_lse):
     """Merge split partials (normalised o_c [S,R,d], lse_c [S,R]) into (o [R,d], lse [R])."""
     pl = np.ascontiguousarray(np.asarray(part_lse, np.float64))

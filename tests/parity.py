@@ -63,7 +63,8 @@ def assert_out_close(o, o_ref, atol, lse_ref=None, what="O"):
     assert a.shape == r.shape, (a.shape, r.shape)
     assert_no_nan(a, what)
     err = np.abs(a - r)
-    assert err.max() <= atol, f"{what}: max abs err {err.max():.3e} > {atol} at {np.unravel_index(np.argmax(err), err.shape)}"
+    worst = np.unravel_index(np.argmax(err), err.shape)
+    assert err.max() <= atol, f"{what}: max abs err {err.max():.3e} > {atol} at {worst}"
     if lse_ref is not None:
         empty = np.isneginf(np.asarray(lse_ref).reshape(-1))
         if empty.any():

@@ -4,8 +4,8 @@ Inputs: Q, K, V, dO ~ N(0, 1) in bf16 (seeded); O and LSE come from this library
 same Q, K, V, as a training step passes them.  The oracle differentiates the exact attention of
 the same bf16 values in fp64.
 
-Tolerance, element by element, from the kernel's arithmetic (u = 2^-8, the unit roundoff of bf16's 8-bit significand).  The
-kernel rounds P and dS = P (dP - D) to bf16 before the tensor-core products; D_i = dO_i . O_i uses
+Tolerance, element by element, from the kernel's arithmetic (u = 2^-8, the unit roundoff of bf16's
+8-bit significand).  The kernel rounds P and dS = P (dP - D) to bf16 before the tensor-core products; D_i = dO_i . O_i uses
 the forward's bf16 O, which lies within 2u A_ic of the exact output, A_ic = sum_j P_ij |V_jc|; all
 sums run in fp32 and the results are rounded to bf16 once.  To first order:
     dD_i  = 2u sum_c |dO_ic| A_ic                 (error of D_i)

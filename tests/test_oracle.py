@@ -491,6 +491,36 @@ def test_attention_bwd_grouped_heads_vs_fp64_autograd(causal):
     np.testing.assert_allclose(got[1], full[1].reshape(B, Hkv, g, N, d).sum(2), rtol=1e-11, atol=1e-12)
 
 
+def test_attention_bwd_varlen_vs_fp64_autograd():
+    # packed sequences of mixed lengths (one without keys, one without queries, causal with more keys than
+    # queries): every token's gradient is that of its own sequence, computed here by torch autograd
+    lq, lk = [5, 0, 7, 3, 6], [5, 4, 7, 0, 9]
+    H, Hkv, d = 4, 2, 6
+    rng = np.random.default_rng(77)
+    Tq, Tk = sum(lq), sum(lk)
+    q, do = rng.standard_normal((Tq, H, d)), rng.standard_normal((Tq, H, d))
+    k, v = rng.standard_normal((Tk, Hkv, d)), rng.standard_normal((Tk, Hkv, d))
+    cq, ck = np.cumsum([0] + lq), np.cumsum([0] + lk)
+    for causal in (False, True):
+        dq, dk, dv = oracle.attention_bwd_varlen(q, k, v, do, cq, ck, causal=causal, scale=0.4)
+        rq, rk, rv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+        for s in range(len(lq)):
+            if lq[s] == 0 or lk[s] == 0:
+                continue
+            sl_q, sl_k = slice(cq[s], cq[s + 1]), slice(ck[s], ck[s + 1])
+            tq, tk, tv = (torch.tensor(a.transpose(1, 0, 2), requires_grad=True) for a in (q[sl_q], k[sl_k], v[sl_k]))
+            sc = 0.4 * tq @ tk.repeat_interleave(H // Hkv, 0).transpose(-1, -2)
+            if causal:
+                sc = sc.masked_fill(torch.arange(lk[s])[None, :] > torch.arange(lq[s])[:, None], float("-inf"))
+            out = torch.softmax(sc, -1) @ tv.repeat_interleave(H // Hkv, 0)
+            out.backward(torch.tensor(do[sl_q].transpose(1, 0, 2)))
+            rq[sl_q], rk[sl_k], rv[sl_k] = (t.grad.numpy().transpose(1, 0, 2) for t in (tq, tk, tv))
+        for a, r in ((dq, rq), (dk, rk), (dv, rv)):
+            np.testing.assert_allclose(a, r, rtol=1e-11, atol=1e-12)
+        # the key-less sequence's queries and the query-less sequence's keys get exactly zero
+        assert np.all(dq[cq[3]:cq[4]] == 0.0) and np.all(dk[ck[1]:ck[2]] == 0.0) and np.all(dv[ck[1]:ck[2]] == 0.0)
+
+
 def test_attention_bwd_finite_differences():
     # central differences of L = sum(O * dO) through the (pinned) forward oracle
     rng = np.random.default_rng(3)
