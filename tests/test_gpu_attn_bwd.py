@@ -5,9 +5,9 @@ same Q, K, V, as a training step passes them.  The oracle differentiates the exa
 the same bf16 values in fp64.
 
 Tolerance, element by element, from the kernel's arithmetic (u = 2^-8, the unit roundoff of bf16's
-8-bit significand).  The kernel rounds P and dS = P (dP - D) to bf16 before the tensor-core products; D_i = dO_i . O_i uses
-the forward's bf16 O, which lies within 2u A_ic of the exact output, A_ic = sum_j P_ij |V_jc|; all
-sums run in fp32 and the results are rounded to bf16 once.  To first order:
+8-bit significand).  The kernel rounds P and dS = P (dP - D) to bf16 before the tensor-core products;
+D_i = dO_i . O_i uses the forward's bf16 O, which lies within 2u A_ic of the exact output,
+A_ic = sum_j P_ij |V_jc|; all sums run in fp32 and the results are rounded to bf16 once.  To first order:
     dD_i  = 2u sum_c |dO_ic| A_ic                 (error of D_i)
     E_ij  = u |dS_ij| + P_ij dD_i                 (error of the bf16 dS_ij)
     |dV_j - ref| <= 2 (u sum_i P_ij |dO_i| + u |dV_j|)
