@@ -273,6 +273,35 @@ oa_status oa_attn_bwd_gqa(const void* q, const void* k, const void* v, const voi
                           size_t workspace_bytes, oa_stream_t stream);
 
 /*
+ * oa_attn_bwd over packed sequences of different lengths (the gradients of
+ * oa_attn_fwd_varlen): sequence s owns query tokens [cu_seqlens_q[s],
+ * cu_seqlens_q[s+1]) and key tokens [cu_seqlens_k[s], cu_seqlens_k[s+1]),
+ * each differentiated on its own, with grouped key/value heads as in
+ * oa_attn_bwd_gqa.
+ *   q, o, dout, dq  bf16 [total_q, H, d] (token-major), 16-byte aligned.
+ *   k, v, dk, dv    bf16 [total_k, H_kv, d].
+ *   lse     fp32 [total_q, H] from oa_attn_fwd_varlen on the same inputs.
+ *   cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k: as in
+ *           oa_attn_fwd_varlen.  One CTA per 128 keys up to max_seqlen_k
+ *           of each (sequence, key/value head); a key sequence longer than
+ *           max_seqlen_k has its tail keys' dK, dV left unwritten and the
+ *           status word records it (oa_sync_status returns
+ *           OA_ERR_INVALID).  max_seqlen_q is accepted for symmetry with the
+ *           forward and not needed.  Keys that no query sees get dK = dV = 0;
+ *           queries of a sequence without keys get dQ = 0.
+ *   workspace: >= oa_attn_bwd_workspace_bytes(1, H, total_q, d) bytes.
+ * Errors: those of oa_attn_bwd_gqa, plus OA_ERR_INVALID for NULL or
+ * misaligned cu_seqlens, num_seqs < 1 or max_seqlen_k outside
+ * [1, total_k].
+ */
+oa_status oa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             oa_dtype dt, const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                             int num_seqs, int H, int H_kv, int total_q, int total_k,
+                             int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale,
+                             void* workspace, size_t workspace_bytes, oa_stream_t stream);
+
+/*
  * Bytes of workspace oa_attn_splitkv needs: num_splits * B*H*Nq * (d + 1)
  * fp32 values (normalised partial outputs, then their LSEs), rounded up to
  * 256 bytes.  0 for invalid sizes.

@@ -30,7 +30,7 @@ EXPORTS = (
     "oa_status_string", "oa_last_error", "oa_version", "oa_softmax_rows", "oa_attn_fwd", "oa_attn_fwd_gqa",
     "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
     "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge", "oa_attn_bwd_workspace_bytes", "oa_attn_bwd",
-    "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host", "oa_attn_bwd_gqa",
+    "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host", "oa_attn_bwd_gqa", "oa_attn_bwd_varlen",
     "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
 )
 
@@ -86,6 +86,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "oa_attn_fwd_host_workspace_bytes": ([i32, i32, i32, i32, i32, i32, i32], sz),
             "oa_attn_bwd_gqa": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, vp,
                                  sz, vp], i32),
+            "oa_attn_bwd_varlen": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                    i32, i32, f32, vp, sz, vp], i32),
             "oa_attn_fwd_host": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp],
                                  i32),
             "oa_attn_bwd": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, vp, sz, vp],
@@ -333,6 +335,45 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
                                       _ptr(dk), _ptr(dv), _dtype_code(q.dtype), B, H, Hkv, Nq, Nk, d,
                                       int(bool(causal)), float(scale), _ptr(workspace),
                                       workspace.numel() * workspace.element_size(), _stream(q.device)))
+    return dq, dk, dv
+
+
+def attn_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int,
+                    causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None, workspace=None):
+    """Gradients of attn_fwd_varlen: q, o, dout [Tq, H, d] and k, v [Tk, H_kv, d] bf16 (token-major), lse fp32
+    [Tq, H] from attn_fwd_varlen on the same inputs.  Returns (dq, dk, dv) in the layouts of q, k, v."""
+    _require_cuda(q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise OAError(OA_ERR_INVALID, "q must be [Tq, H, d] and k, v [Tk, H_kv, d]")
+    Tq, H, d = q.shape
+    Tk, Hkv = k.shape[0], k.shape[1]
+    if tuple(k.shape) != (Tk, Hkv, d) or tuple(v.shape) != (Tk, Hkv, d):
+        raise OAError(OA_ERR_INVALID, "k and v must be [Tk, H_kv, d] matching q")
+    for t in (q, k, v, o, dout):
+        if t.dtype != q.dtype or not t.is_contiguous():
+            raise OAError(OA_ERR_INVALID, "q, k, v, o, dout must be contiguous with one dtype")
+    if tuple(o.shape) != (Tq, H, d) or tuple(dout.shape) != (Tq, H, d):
+        raise OAError(OA_ERR_INVALID, "o and dout must be [Tq, H, d] like q")
+    if lse is None or tuple(lse.shape) != (Tq, H) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise OAError(OA_ERR_INVALID, "lse must be a contiguous float32 [Tq, H] tensor")
+    cq = _cu_seqlens_arg(cu_seqlens_q, q.device, "cu_seqlens_q")
+    ck = _cu_seqlens_arg(cu_seqlens_k, q.device, "cu_seqlens_k")
+    if cq.numel() != ck.numel():
+        raise OAError(OA_ERR_INVALID, "cu_seqlens_q and cu_seqlens_k must have the same length")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    need = attn_bwd_workspace_bytes(1, H, Tq, d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    with torch.cuda.device(q.device):
+        _check(load().oa_attn_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), _dtype_code(q.dtype), _ptr(cq), _ptr(ck), cq.numel() - 1,
+                                         H, Hkv, Tq, Tk, int(max_seqlen_q), int(max_seqlen_k), d, int(bool(causal)),
+                                         float(scale), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                         _stream(q.device)))
     return dq, dk, dv
 
 

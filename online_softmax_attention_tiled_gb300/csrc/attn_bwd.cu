@@ -87,9 +87,13 @@ struct BwdParams {
   const float* dsum;     // D [B H Nq]
   __nv_bfloat16* dk;     // [B H Nk, d]
   __nv_bfloat16* dv;
-  int Nq, Nk, causal, nkt, nqt;
-  int BHkv;   // key/value planes (B * H_kv): the grid covers nkt key tiles of each
-  int group;  // query heads per key/value head (H / H_kv); query plane = kv plane * group + t
+  int Nq, Nk, causal, nkt, nqt;  // dense: lengths and tiles; packed: the longest key sequence's tiles (nkt)
+  int BHkv;   // dense: key/value planes (B * H_kv); packed: sequences * H_kv.  The grid covers nkt key
+              // tiles of each
+  int group;  // query heads per key/value head (H / H_kv)
+  int H, Hkv;                       // packed: head counts of the token-major rows
+  const int32_t *cu_q, *cu_k;       // packed: sequence offsets [num_seqs + 1] (NULL: dense)
+  int total_q, total_k;             // packed: tokens in the Q / K tensors
   float scale, scale_log2;
   DevStatus st;
 };
@@ -170,9 +174,11 @@ __device__ __forceinline__ void bwd_p_ds(const uint32_t* sr, const uint32_t* dr,
   }
 }
 
-// grid.x = nkt * BH: blockIdx.x / BH is the key tile j (low j first: for causal those have
-// the most query tiles), blockIdx.x % BH the (b, h) plane.
-template <int D>
+// grid.x = nkt * BHkv: blockIdx.x / BHkv is the key tile j (low j first: for causal those have
+// the most query tiles), blockIdx.x % BHkv the key/value plane -- dense: (b, key/value head);
+// PACKED: (sequence, key/value head) of token-major [tokens, heads, d] tensors, whose sequence s
+// owns rows [cu[s], cu[s+1]) (a CTA past its sequence's keys exits at once).
+template <int D, bool PACKED>
 __global__ void __launch_bounds__(kBwdThreads)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -204,10 +210,47 @@ __global__ void __launch_bounds__(kBwdThreads)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int j = (int)(blockIdx.x / p.BHkv);
-  const int kvp = (int)(blockIdx.x % p.BHkv);  // key/value plane
   const int k0 = j * BT;
+  // The CTA's geometry.  Rows: Q / dO / dQ row of query q is qrow0 + q, K / V / dK / dV row of key
+  // k is krow0 + k (TMA coordinates); query head t of the group is TMA plane qplane0 + t; the LSE / D
+  // entry of (q, t) is lbase + q lq + t lt; the dK / dV row of key k starts at (dkbase + k dks) D.
+  int Nq, Nk, nqt, qrow0, krow0, qplane0, kplane;
+  int64_t lbase, lq, lt, dkbase, dks;
+  if constexpr (PACKED) {
+    const int r = (int)(blockIdx.x % p.BHkv), seq = r / p.Hkv, hkv = r % p.Hkv;
+    const int qb = min(max(p.cu_q[seq], 0), p.total_q), qe = min(max(p.cu_q[seq + 1], qb), p.total_q);
+    const int kb = min(max(p.cu_k[seq], 0), p.total_k), ke = min(max(p.cu_k[seq + 1], kb), p.total_k);
+    Nq = qe - qb;
+    Nk = ke - kb;
+    // a key sequence longer than the grid covers: its tail gets no gradient; report it
+    if (j == p.nkt - 1 && hkv == 0 && threadIdx.x == 0 && Nk > p.nkt * BT)
+      record_failure(p.st, kSiteBwdBadSeqlen);
+    if (k0 >= Nk) return;  // no key of this sequence in the tile (uniform over the CTA; nothing set up yet)
+    qrow0 = qb;
+    krow0 = kb;
+    qplane0 = hkv * p.group;
+    kplane = hkv;
+    lbase = (int64_t)qb * p.H + (int64_t)hkv * p.group;
+    lq = p.H;
+    lt = 1;
+    dkbase = (int64_t)kb * p.Hkv + hkv;
+    dks = p.Hkv;
+  } else {
+    const int kvp = (int)(blockIdx.x % p.BHkv);  // (b, key/value head)
+    Nq = p.Nq;
+    Nk = p.Nk;
+    qrow0 = krow0 = 0;
+    qplane0 = kvp * p.group;
+    kplane = kvp;
+    lbase = (int64_t)kvp * p.group * p.Nq;
+    lq = 1;
+    lt = p.Nq;
+    dkbase = (int64_t)kvp * p.Nk;
+    dks = 1;
+  }
+  nqt = (Nq + BT - 1) / BT;
   const int i_begin = p.causal ? j : 0;  // causal: query tile i sees key tile j iff i >= j
-  const int n_i = max(p.nqt - i_begin, 0);  // visible query tiles of one query head
+  const int n_i = max(nqt - i_begin, 0);  // visible query tiles of one query head
   // steps: every visible query tile of every query head of the group, head by head
   const int n_it = p.group * n_i;
   // (query head t of the group, query tile i) of consecutive steps, without a division per step
@@ -215,7 +258,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     int t, i;
   };
   auto next_pos = [&](StepPos s) {
-    if (++s.i == p.nqt) {
+    if (++s.i == nqt) {
       s.i = i_begin;
       ++s.t;
     }
@@ -266,21 +309,21 @@ __global__ void __launch_bounds__(kBwdThreads)
     bool ok = true;
     mbar_arrive_expect_tx_elect(bar_kv, 2 * C::TILE_BYTES);
     for (int c = 0; c < C::SLABS; ++c) {
-      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, k0, kvp);
-      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, k0, kvp);
+      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, krow0 + k0, kplane);
+      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, krow0 + k0, kplane);
     }
     int issued = 0;
     StepPos pos = first_pos;
     for (int it = 0; it < n_it; ++it, pos = next_pos(pos)) {
-      const int s = it & 1, q0 = pos.i * BT, qp = kvp * p.group + pos.t;
+      const int s = it & 1, q0 = pos.i * BT, qp = qplane0 + pos.t, qy = qrow0 + q0;
       // stage s was last read by step it - 2
       if (it >= 2 && !(ok = wait_all(bar_qdo_empty(s), (uint32_t)((it >> 1) - 1) & 1u, B_QDO_EMPTY))) break;
       mbar_arrive_expect_tx_elect(bar_qdo(s), 2 * C::TILE_BYTES);
       for (int c = 0; c < C::SLABS; ++c) {
-        tma_load_3d_elect(sbase + C::Q_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, bar_qdo(s), c * 64, q0,
+        tma_load_3d_elect(sbase + C::Q_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, bar_qdo(s), c * 64, qy,
                           qp);
         tma_load_3d_elect(sbase + C::DO_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_do, bar_qdo(s), c * 64,
-                          q0, qp);
+                          qy, qp);
       }
       ++issued;
     }
@@ -360,15 +403,15 @@ __global__ void __launch_bounds__(kBwdThreads)
     bool ok = true;
     StepPos pos = first_pos;
     for (int it = 0; ok && it < n_it; ++it, pos = next_pos(pos)) {
-      const int s = it & 1, q0 = pos.i * BT, qp = kvp * p.group + pos.t;
+      const int s = it & 1, q0 = pos.i * BT, qp = qplane0 + pos.t, qy = qrow0 + q0;
       if (!(ok = wait_all(bar_dq_staged(s), (uint32_t)(it >> 1) & 1u, B_DQ_STAGED))) break;
       if (lane == 0) {
         const uint32_t stage_base = C::Q_OFF + (uint32_t)s * C::TILE_BYTES;
         for (int w = 0; w < kBwdRowWarps; ++w) {
-          if (q0 + (w & 3) * 32 >= p.Nq) continue;
+          if (q0 + (w & 3) * 32 >= Nq) continue;
           for (int m = 0; m < C::DQ_CHUNKS; ++m)
             tma_reduce_add_3d(&tm_dq, sbase + bwd_dq_block<C>(stage_base, w, m), ((w >> 2) * C::DQ_CHUNKS + m) * 32,
-                              q0 + (w & 3) * 32, qp);
+                              qy + (w & 3) * 32, qp);
         }
         bulk_commit_group();
         bulk_wait_read<0>();  // the stage may be refilled once its blocks have been read
@@ -384,7 +427,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     const int half = warp >> 2;             // queries (dQ / dK / dV columns) [64 half, 64 half + 64)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int key = k0 + tt;
-    const bool key_ok = key < p.Nk;
+    const bool key_ok = key < Nk;
 
     uint8_t* st_row = smem + C::ST_OFF + half * C::SLAB_BYTES + tt * 128;  // key row in slab `half`
     const float4* nl4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
@@ -400,8 +443,8 @@ __global__ void __launch_bounds__(kBwdThreads)
       l = -INFINITY;
       dd = 0.f;
       const int q = sp.i * BT + ld_q;
-      if (tt < 64 && step < n_it && q < p.Nq) {
-        const int64_t row = (int64_t)(kvp * p.group + sp.t) * p.Nq + q;
+      if (tt < 64 && step < n_it && q < Nq) {
+        const int64_t row = lbase + (int64_t)q * lq + (int64_t)sp.t * lt;
         l = p.lse[row];
         dd = p.dsum[row];
       }
@@ -415,7 +458,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int i = pos.i, q0 = i * BT;
       const uint32_t ph = (uint32_t)it & 1u;
       // every (key, query) pair of the step visible and inside the tensors
-      const bool full = (k0 + BT <= p.Nk) && (q0 + BT <= p.Nq) && (!p.causal || i > j);
+      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || i > j);
       if (!(ok = wait_all(bar_s(half), ph, B_S))) break;
       // -LSE log2 e and -D of query q0 + ld_q; a row past the end or with no visible key gets
       // -inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
@@ -494,8 +537,8 @@ __global__ void __launch_bounds__(kBwdThreads)
     if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
     if (ok) {
       tc_fence_after_sync();
-      __nv_bfloat16* dkrow = p.dk + ((int64_t)kvp * p.Nk + key) * D;
-      __nv_bfloat16* dvrow = p.dv + ((int64_t)kvp * p.Nk + key) * D;
+      __nv_bfloat16* dkrow = p.dk + (dkbase + (int64_t)key * dks) * D;
+      __nv_bfloat16* dvrow = p.dv + (dkbase + (int64_t)key * dks) * D;
 #pragma unroll 1
       for (int c = half * (D / 2); c < half * (D / 2) + D / 2; c += 32) {
         uint32_t rk[32], rv[32];
@@ -536,7 +579,7 @@ __global__ void __launch_bounds__(kBwdThreads)
 
 constexpr int kMaxDevices = 64;
 
-template <int D>
+template <int D, bool PACKED>
 cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mdo, const CUtensorMap& mdq, const BwdParams& p, cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
@@ -545,13 +588,13 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              BwdCfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   const unsigned grid = (unsigned)p.nkt * (unsigned)p.BHkv;
-  attn_bwd_tc_kernel<D><<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
+  attn_bwd_tc_kernel<D, PACKED><<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
   return cudaGetLastError();
 }
 
@@ -561,16 +604,22 @@ size_t attn_bwd_workspace_floats(int B, int H, int Nq, int d) { return (size_t)B
 
 cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus& st, cudaStream_t s,
                             const char** why) {
+  // dense: [B, H, N, d] (planes of N rows); packed: [tokens, H, d] (rows of H d elements, heads as
+  // planes), B = 1 and Nq, Nk the token counts
+  const bool packed = a.cu_q != nullptr;
   const int d = a.d, BH = a.B * a.H, BHkv = a.B * a.Hkv;
-  const int64_t rb = 2 * (int64_t)d;  // bytes per row
+  const int64_t eb = 2 * (int64_t)d;  // bytes per row of one head
   const int64_t rows = (int64_t)BH * a.Nq;
   float* dq_acc = workspace;
   float* dsum = workspace + rows * d;
+  const int64_t q_row = packed ? eb * a.H : eb, q_plane = packed ? eb : eb * a.Nq;
+  const int64_t k_row = packed ? eb * a.Hkv : eb, k_plane = packed ? eb : eb * a.Nk;
   CUtensorMap mq, mk, mv, mdo, mdq;
-  if (!make_tile_map(&mq, a.q, d, a.Nq, rb, BH, rb * a.Nq) || !make_tile_map(&mk, a.k, d, a.Nk, rb, BHkv, rb * a.Nk) ||
-      !make_tile_map(&mv, a.v, d, a.Nk, rb, BHkv, rb * a.Nk) ||
-      !make_tile_map(&mdo, a.dout, d, a.Nq, rb, BH, rb * a.Nq) ||
-      !make_f32_tile_map(&mdq, dq_acc, d, a.Nq, 2 * rb, BH, 2 * rb * a.Nq, 32)) {
+  if (!make_tile_map(&mq, a.q, d, a.Nq, q_row, BH, q_plane) ||
+      !make_tile_map(&mk, a.k, d, a.Nk, k_row, BHkv, k_plane) ||
+      !make_tile_map(&mv, a.v, d, a.Nk, k_row, BHkv, k_plane) ||
+      !make_tile_map(&mdo, a.dout, d, a.Nq, q_row, BH, q_plane) ||
+      !make_f32_tile_map(&mdq, dq_acc, d, a.Nq, 2 * q_row, BH, 2 * q_plane, 32)) {
     if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;
   }
@@ -588,14 +637,26 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus&
   p.Nq = a.Nq;
   p.Nk = a.Nk;
   p.causal = a.causal;
-  p.nkt = (a.Nk + BT - 1) / BT;
+  p.nkt = ((packed ? a.max_seqlen_k : a.Nk) + BT - 1) / BT;
   p.nqt = (a.Nq + BT - 1) / BT;
-  p.BHkv = BHkv;
+  p.BHkv = packed ? a.num_seqs * a.Hkv : BHkv;
   p.group = a.H / a.Hkv;
+  p.H = a.H;
+  p.Hkv = a.Hkv;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.total_q = a.Nq;
+  p.total_k = a.Nk;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;
-  e = d == 128 ? launch_bwd_d<128>(mq, mk, mv, mdo, mdq, p, s) : launch_bwd_d<64>(mq, mk, mv, mdo, mdq, p, s);
+  if (p.nkt < 1) p.nkt = 1;
+  if (packed)
+    e = d == 128 ? launch_bwd_d<128, true>(mq, mk, mv, mdo, mdq, p, s)
+                 : launch_bwd_d<64, true>(mq, mk, mv, mdo, mdq, p, s);
+  else
+    e = d == 128 ? launch_bwd_d<128, false>(mq, mk, mv, mdo, mdq, p, s)
+                 : launch_bwd_d<64, false>(mq, mk, mv, mdo, mdq, p, s);
   if (e != cudaSuccess) return e;
   const int64_t n = rows * d;
   bwd_post_kernel<<<(unsigned)((n / 4 + 255) / 256), 256, 0, s>>>(dq_acc, static_cast<__nv_bfloat16*>(a.dq), n);

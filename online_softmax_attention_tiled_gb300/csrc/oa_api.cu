@@ -492,6 +492,59 @@ oa_status oa_attn_bwd_gqa(const void* q, const void* k, const void* v, const voi
                        workspace_bytes, stream, "attn_bwd_gqa");
 }
 
+oa_status oa_attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                             const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, int num_seqs, int H, int H_kv, int total_q, int total_k,
+                             int max_seqlen_q, int max_seqlen_k, int d, int causal, float scale, void* workspace,
+                             size_t workspace_bytes, oa_stream_t stream) {
+  const char* who = "attn_bwd_varlen";
+  oa_status s = check_attn(q, k, v, dq, nullptr, 1, H, total_q, total_k, d, causal, scale, who);
+  if (s != OA_OK) return s;
+  if ((s = check_heads(H, H_kv, who)) != OA_OK) return s;
+  if (!o || !dout || !lse || !dk || !dv || !cu_seqlens_q || !cu_seqlens_k)
+    return fail(OA_ERR_INVALID, "%s: o, dout, lse, dk, dv and both cu_seqlens are required", who);
+  if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4) ||
+      !aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4))
+    return fail(OA_ERR_INVALID, "%s: o/dout/dk/dv must be 16-byte aligned, lse and cu_seqlens 4-byte", who);
+  if (num_seqs < 1 || max_seqlen_q < 0 || max_seqlen_k < 1 || max_seqlen_k > total_k)
+    return fail(OA_ERR_INVALID, "%s: need num_seqs >= 1 and 1 <= max_seqlen_k <= total_k", who);
+  if (dt != OA_BF16) return fail(OA_ERR_UNSUPPORTED, "%s: bf16 only", who);
+  if (d != 64 && d != 128) return fail(OA_ERR_UNSUPPORTED, "%s: d = 64 or 128 (got %d)", who, d);
+  if ((int64_t)num_seqs * H_kv * ((max_seqlen_k + 127) / 128) > kMaxGrid)
+    return fail(OA_ERR_INVALID, "%s: grid too large", who);
+  const size_t need = oa_attn_bwd_workspace_bytes(1, H, total_q, d);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
+    return fail(OA_ERR_INVALID, "%s: workspace must be 16-byte aligned and >= %zu bytes", who, need);
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  oa::BwdArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.o = o;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = 1;
+  a.H = H;
+  a.Hkv = H_kv;
+  a.Nq = total_q;
+  a.Nk = total_k;
+  a.d = d;
+  a.causal = causal;
+  a.scale = scale;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.num_seqs = num_seqs;
+  a.max_seqlen_k = max_seqlen_k;
+  const char* why = nullptr;
+  cudaError_t e = oa::launch_attn_bwd(a, static_cast<float*>(workspace), st, (cudaStream_t)stream, &why);
+  if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_bwd_varlen launch");
+  return ok();
+}
+
 size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   if (B < 1 || H < 1 || Nq < 1 || d < 1 || num_splits < 1) return 0;
   const size_t floats = (size_t)num_splits * (size_t)B * H * Nq * ((size_t)d + 1);
@@ -567,6 +620,9 @@ oa_status oa_sync_status(oa_stream_t stream) {
   if (word == oa::kSiteBadSeqlen)
     return fail(OA_ERR_INVALID, "a packed query sequence is longer than the declared max_seqlen_q; "
                                 "its rows past that length were not computed");
+  if (word == oa::kSiteBwdBadSeqlen)
+    return fail(OA_ERR_INVALID, "a packed key sequence is longer than the declared max_seqlen_k; "
+                                "its keys past that length got no dK, dV");
   return fail(OA_ERR_TIMEOUT, "device wait expired: kernel %u, wait site %u", word >> 8, word & 0xFFu);
 }
 

@@ -35,6 +35,8 @@ enum KernelId : unsigned {
 // Not a wait: a packed sequence longer than the maximum its call declared (its tail rows
 // were not computed).  Reported by oa_sync_status as OA_ERR_INVALID.
 constexpr unsigned kSiteBadSeqlen = (K_ATTN_TC << 8) | 0xF0u;
+// a packed key sequence longer than the declared maximum (attention backward)
+constexpr unsigned kSiteBwdBadSeqlen = (K_ATTN_BWD << 8) | 0xF0u;
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

@@ -64,6 +64,10 @@ struct BwdArgs {
   void *dq, *dk, *dv;
   int B, H, Hkv, Nq, Nk, d, causal;  // query head h reads key/value head h / (H / Hkv)
   float scale;
+  // packed sequences (NULL for the dense layout): token-major [Nq, H, d] / [Nk, Hkv, d] tensors with
+  // B = 1 and Nq, Nk the token counts; sequence s owns rows [cu[s], cu[s + 1])
+  const int32_t *cu_q = nullptr, *cu_k = nullptr;
+  int num_seqs = 0, max_seqlen_k = 0;
 };
 // fp32 values of workspace the backward needs: the dQ accumulator [B H Nq, d] and D [B H Nq].
 size_t attn_bwd_workspace_floats(int B, int H, int Nq, int d);

@@ -139,6 +139,11 @@ def test_attn_bwd_validation(lib):
     assert call(dt=oa.OA_F32) == oa.OA_ERR_UNSUPPORTED
     assert call(d=96) == oa.OA_ERR_UNSUPPORTED
     assert "d = 64 or 128" in _err(lib)
+    # packed sequences: the offsets are required, and max_seqlen_k must lie in [1, total_k]
+    assert lib.oa_attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, oa.OA_BF16, NULL, FAKE, 2, 2, 2,
+                                  100, 100, 50, 50, 64, 1, 0.125, FAKE, need, NULL) == oa.OA_ERR_INVALID
+    assert lib.oa_attn_bwd_varlen(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, oa.OA_BF16, FAKE, FAKE, 2, 2, 2,
+                                  100, 100, 50, 101, 64, 1, 0.125, FAKE, need, NULL) == oa.OA_ERR_INVALID
     # grouped heads: H_kv must divide H
     assert lib.oa_attn_bwd_gqa(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, oa.OA_BF16, 2, 2, 3, 100, 100, 64,
                                1, 0.125, FAKE, need, NULL) == oa.OA_ERR_INVALID

@@ -206,3 +206,49 @@ def test_attn_bwd_full_size_sampled_rows():
         _assert_within(dq[0, h][rows], rq, tq, f"dQ[0,{h}] sampled")
         _assert_within(dk[0, h][rows], rk, tk, f"dK[0,{h}] sampled")
         _assert_within(dv[0, h][rows], rv, tv, f"dV[0,{h}] sampled")
+
+
+@pytest.mark.parametrize("lq,lk,H,Hkv,d,causal", [
+    ([300, 129, 1, 257], [300, 129, 1, 257], 4, 2, 128, True),
+    ([100, 0, 200, 64, 33], [150, 80, 0, 64, 200], 2, 2, 64, False),
+    ([130, 70], [200, 70], 4, 1, 128, True),   # causal with more keys than queries
+])
+def test_attn_bwd_varlen_matches_oracle(lq, lk, H, Hkv, d, causal):
+    q, k, v, cq, ck = si.varlen_inputs(lq, lk, H, Hkv, d, torch.bfloat16, seed=80 + sum(lq))
+    do = si.randn(tuple(q.shape), 90 + sum(lq), torch.bfloat16)
+    sc = 1.0 / np.sqrt(d)
+    qd, kd, vd, dod, cqd, ckd = (t.to(DEV) for t in (q, k, v, do, cq, ck))
+    o, lse = oa.attn_fwd_varlen(qd, kd, vd, cqd, ckd, max(lq), max(lk), causal=causal, scale=sc)
+    dq, dk, dv = oa.attn_bwd_varlen(qd, kd, vd, o, lse, dod, cqd, ckd, max(lq), max(lk), causal=causal, scale=sc)
+    oa.sync_status()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    rq, rk, rv = oracle.attention_bwd_varlen(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(do), cq.numpy(),
+                                             ck.numpy(), causal=causal, scale=sc)
+    g = H // Hkv
+    for s in range(len(lq)):
+        sq, sk = slice(int(cq[s]), int(cq[s + 1])), slice(int(ck[s]), int(ck[s + 1]))
+        if lq[s] == 0 or lk[s] == 0:  # no query or no key: the gradients there are exactly zero
+            assert torch.all(dq[sq] == 0) and torch.all(dk[sk] == 0) and torch.all(dv[sk] == 0)
+            continue
+        for hk in range(Hkv):
+            tk_sum, tv_sum = 0.0, 0.0
+            for t in range(g):
+                h = hk * g + t
+                f64 = [x.to(torch.float64) for x in (q[sq, h], k[sk, hk], v[sk, hk], do[sq, h])]
+                tq, tk, tv = _bounds(*f64, causal, sc, np.arange(lq[s]), np.arange(lk[s]))
+                _assert_within(dq[sq, h], rq[sq, h], tq, f"dQ seq {s} head {h}")
+                tk_sum, tv_sum = tk_sum + tk, tv_sum + tv
+            _assert_within(dk[sk, hk], rk[sk, hk], tk_sum, f"dK seq {s} head {hk}")
+            _assert_within(dv[sk, hk], rv[sk, hk], tv_sum, f"dV seq {s} head {hk}")
+
+
+def test_attn_bwd_varlen_reports_a_key_sequence_longer_than_declared():
+    lq = lk = [200, 300]
+    q, k, v, cq, ck = si.varlen_inputs(lq, lk, 2, 2, 64, torch.bfloat16, seed=3)
+    qd, kd, vd, cqd, ckd = (t.to(DEV) for t in (q, k, v, cq, ck))
+    o, lse = oa.attn_fwd_varlen(qd, kd, vd, cqd, ckd, 300, 300)
+    oa.attn_bwd_varlen(qd, kd, vd, o, lse, torch.ones_like(qd), cqd, ckd, 300, 256)  # 300 keys > 256 declared
+    with pytest.raises(oa.OAError) as e:
+        oa.sync_status()
+    assert e.value.status == oa.OA_ERR_INVALID
+    oa.sync_status()  # cleared
