@@ -252,3 +252,30 @@ def test_attn_bwd_varlen_reports_a_key_sequence_longer_than_declared():
         oa.sync_status()
     assert e.value.status == oa.OA_ERR_INVALID
     oa.sync_status()  # cleared
+
+
+def test_attn_bwd_full_size_grouped_heads_sampled_rows():
+    # causal B=1 H=32 H_kv=8 N=8192 d=128 (the benchmarked grouped backward): dK, dV of two key/value
+    # heads at sampled rows are the sums of the row-sampled oracle over each group's four query heads
+    B, H, Hkv, N, d = 1, 32, 8, 8192, 128
+    sc = 1.0 / np.sqrt(d)
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, N, N, d, torch.bfloat16, seed=79)
+    do = si.randn((B, H, N, d), 82, torch.bfloat16)
+    dq, dk, dv = _run(q, k, v, do, True, sc)
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+    rows = si.sample_rows(N, 96, seed=5).numpy()
+    g = H // Hkv
+    for hk in (0, Hkv - 1):
+        sum_k, sum_v, tk_sum, tv_sum = 0.0, 0.0, 0.0, 0.0
+        for t in range(g):
+            h = hk * g + t
+            rq, rk, rv = oracle.attention_bwd_sampled(*(bf16_bits(x[0, i]) for x, i in
+                                                        ((q, h), (k, hk), (v, hk), (do, h))), rows, rows,
+                                                      causal=True, scale=sc)
+            tq, tk, tv = _bounds(*(x[0, i].to(torch.float64) for x, i in ((q, h), (k, hk), (v, hk), (do, h))),
+                                 True, sc, rows, rows)
+            _assert_within(dq[0, h][rows], rq, tq, f"dQ[0,{h}] sampled")
+            sum_k, sum_v, tk_sum, tv_sum = sum_k + rk, sum_v + rv, tk_sum + tk, tv_sum + tv
+        _assert_within(dk[0, hk][rows], sum_k, tk_sum, f"dK[0,{hk}] sampled")
+        _assert_within(dv[0, hk][rows], sum_v, tv_sum, f"dV[0,{hk}] sampled")

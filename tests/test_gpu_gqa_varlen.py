@@ -114,3 +114,48 @@ def test_varlen_sequence_longer_than_declared_max(cuda_lib):
     with pytest.raises(cuda_lib.OAError):
         cuda_lib.sync_status()
     cuda_lib.sync_status()  # the word was cleared: the next call is clean
+
+
+@pytest.mark.slow
+def test_full_size_decode_grouped_cache(cuda_lib):
+    """The benchmarked grouped decode: B32 H32 H_kv8 Nq1 Nk32768 d128 bf16, 64 chunks of 512, the same
+    truncated sequences; sampled (b, h) rows against the oracle on their key/value head."""
+    B, H, Hkv, Nk, d = 32, 32, 8, 32768, 128
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, 1, Nk, d, torch.bfloat16, seed=0, device="cuda")
+    kv_len = si.decode_kv_len(B, Nk, seed=0)
+    o, lse = cuda_lib.attn_splitkv(q, k, v, 64, kv_len=kv_len.cuda())
+    _sync(cuda_lib)
+    trunc = torch.nonzero(kv_len < Nk).reshape(-1).tolist()
+    for b in sorted(set([0, B - 1] + trunc + list(range(3, B, 9)))):
+        n = int(kv_len[b])
+        for h in (0, 5, H - 1):
+            hk = h // (H // Hkv)
+            ro, rl = oracle.attention(bf16_bits(q[b:b + 1, h:h + 1]), bf16_bits(k[b:b + 1, hk:hk + 1, :n]),
+                                      bf16_bits(v[b:b + 1, hk:hk + 1, :n]))
+            assert_lse_close(lse[b, h], rl)
+            assert_out_close(o[b, h], ro[0, 0], BF16_O_ATOL)
+    assert not torch.isnan(o).any()
+
+
+@pytest.mark.slow
+def test_full_size_varlen_causal_grouped(cuda_lib):
+    """The benchmarked packed prefill: 16 causal sequences of U[1024, 8192] tokens, H32 H_kv8 d128;
+    sampled rows (both sides of every tile boundary) of three sequences and two heads."""
+    H, Hkv, d = 32, 8, 128
+    lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
+    q, k, v, cq, ck = si.varlen_inputs(lens, lens, H, Hkv, d, torch.bfloat16, seed=0)
+    o, lse = cuda_lib.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(lens), max(lens),
+                                      causal=True)
+    _sync(cuda_lib)
+    o, lse = o.cpu(), lse.cpu()
+    for s in (0, 7, len(lens) - 1):
+        L, a = lens[s], int(cq[s])
+        rows = si.sample_rows(L, 64, seed=s)
+        for h in (0, H - 1):
+            hk = h // (H // Hkv)
+            qs = q[a:a + L, h].reshape(1, 1, L, d)
+            ks, vs = k[a:a + L, hk].reshape(1, 1, L, d), v[a:a + L, hk].reshape(1, 1, L, d)
+            ro, rl = oracle.attention(bf16_bits(qs), bf16_bits(ks), bf16_bits(vs), causal=True, rows=rows.numpy())
+            assert_lse_close(lse[a + rows, h], rl)
+            assert_out_close(o[a + rows, h], ro, BF16_O_ATOL)
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
