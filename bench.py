@@ -290,8 +290,9 @@ def components(oa, dev, peaks, peak_kind, steps):
     ms = statistics.mean(t)
     nbytes = decode_bytes(32, 32, 128, int(kv_len.sum()), h_kv=8)
     gbs = nbytes / (ms * 1e-3) / 1e9
-    out["attn_splitkv_decode_gqa"] = {"workload": "split-KV decode bf16 B=32 H=32 H_kv=8 Nq=1 Nk=32768 d=128, 64 "
-                                                  "chunks of 512, same truncations (KV 4.3 GB > L2)", "ms": ms,
+    out["attn_splitkv_decode_gqa"] = {"workload": "decode bf16 B=32 H=32 H_kv=8 Nq=1 Nk=32768 d=128 through "
+                                                  "oa_attn_splitkv_gqa (each group's 4 queries as rows of the "
+                                                  "tensor-core forward), same truncations (KV 4.3 GB > L2)", "ms": ms,
                                       "value": gbs, "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
                                       "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
                                       "algorithmic_bytes": nbytes, "launches_per_call": 2}

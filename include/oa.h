@@ -124,6 +124,9 @@ oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  * length and KV-cache calls) is read to ask for.
  *   q, o [B, H, Nq, d]; k, v [B, H_kv, Nk, d]; everything else as in
  *   oa_attn_fwd (dtype, alignment, lse, causal, scale, kv_len, support).
+ * With one query per row (Nq = 1, not causal, bf16), the query heads of a
+ * group are run as the rows of one [B, H_kv, H / H_kv, d] problem, so each
+ * group's K/V is read once (the decode case).
  * Errors: those of oa_attn_fwd, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */
@@ -336,6 +339,11 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
  * key/value heads than query heads): k and v are [B, H_kv, Nk, d] and query
  * head h reads head h / (H / H_kv); kv_len gives each sequence's cache
  * length.  Same workspace size and support matrix as oa_attn_splitkv.
+ * With one query per row (Nq = 1), bf16 and d = 64 / 128, the H / H_kv
+ * query heads of a group are consecutive rows of q, o and lse and are
+ * computed together by the tensor-core forward kernel, every K/V row read
+ * once for the whole group and no split taken (num_splits and the workspace
+ * are then checked but not used); the result is the same attention.
  * Errors: those of oa_attn_splitkv, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */

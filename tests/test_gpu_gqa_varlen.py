@@ -69,6 +69,27 @@ def test_gqa_splitkv_decode(cuda_lib, dtype, d):
     assert_out_close(o, ro, atol, lse_ref=rl)
 
 
+@pytest.mark.parametrize("H,Hkv", [(16, 8), (16, 4), (16, 2), (16, 1)])
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("nq", [1, 2])
+def test_gqa_decode_groups(cuda_lib, H, Hkv, d, nq):
+    # one query per head runs each group as the rows of one plane (forward kernel); two queries per head
+    # take the split-KV group kernel; both entry points, every group size, against the oracle
+    B, Nk = 3, 700
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, nq, Nk, d, torch.bfloat16, seed=70 + H // Hkv + d + nq)
+    kv_len = [700, 129, 0]
+    kvd = torch.tensor(kv_len, dtype=torch.int32).cuda()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), kv_len=kv_len)
+    o, lse = cuda_lib.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), 6, kv_len=kvd)
+    _sync(cuda_lib)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+    o2, lse2 = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), kv_len=kvd)
+    _sync(cuda_lib)
+    assert_lse_close(lse2, rl)
+    assert_out_close(o2, ro, BF16_O_ATOL, lse_ref=rl)
+
+
 def _varlen_check(oa, lq, lk, H, Hkv, d, causal, seed, max_q=None, max_k=None):
     q, k, v, cq, ck = si.varlen_inputs(lq, lk, H, Hkv, d, torch.bfloat16, seed=seed)
     o, lse = oa.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(),
