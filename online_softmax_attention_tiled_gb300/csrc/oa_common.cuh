@@ -64,9 +64,6 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -109,19 +106,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const D
 }
 
 // ---------------------------------------------------------------------------
-// TMA (cp.async.bulk.tensor) -- tiled loads from a 3-D tensor map into this
-// CTA's shared memory, completing transaction bytes on an mbarrier.
+// TMA (cp.async.bulk.tensor): the tensor-map prefetch here; the tiled load is one of the
+// warp-wide forms below.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
-                                            int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
 }
 
 // ---------------------------------------------------------------------------
@@ -147,38 +136,17 @@ __device__ __forceinline__ void tc_fence_after_sync() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]   (kind::f16: bf16 x bf16 -> fp32)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// Arrive (once) on an mbarrier when every tcgen05 operation issued so far by
-// this thread has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-
 // Warp-wide forms: every lane of a converged warp executes the call with the
 // same (warp-uniform) operands and one lane, chosen by elect.sync, issues the
 // instruction.  Keeping the operands uniform lets them live in uniform
-// registers; a single-lane branch around the plain forms above costs about
+// registers; a single-lane branch around single-thread forms costs about
 // 40 extra cycles per tcgen05.mma and starves the tensor core.
+//   mma_ss_elect      D[tmem] (+)= A[smem] * B[smem]   (kind::f16: bf16 x bf16 -> fp32)
+//   mma_ts_elect      D[tmem] (+)= A[tmem] * B[smem]
+//   mma_commit_elect  arrive (once) on an mbarrier when every tcgen05 operation issued so far
+//                     by the electing thread has completed
+//   tma_load_3d_elect a tiled load from a 3-D tensor map into this CTA's shared memory,
+//                     completing its bytes on an mbarrier
 __device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                              uint32_t accumulate) {
   asm volatile(
@@ -265,21 +233,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       "tcgen05.wait::ld.sync.aligned;\n"
       : OA_R8(0), OA_R8(8), OA_R8(16), OA_R8(24)
       : "r"(taddr)
-      : "memory");
-}
-
-// 64 consecutive columns in two loads, one wait.
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;\n"
-      : OA_R8(0), OA_R8(8), OA_R8(16), OA_R8(24), OA_R8(32), OA_R8(40), OA_R8(48), OA_R8(56)
-      : "r"(taddr), "r"(taddr + 32)
       : "memory");
 }
 
