@@ -13,26 +13,30 @@
 // kernel, and a post-pass (dQ to bf16).  Main kernel, key-tile outer: one CTA per (b, h,
 // 128 keys); K_j and V_j stay in shared memory while the query tiles i (causal: i >= j)
 // stream through a 2-stage TMA ring with their dO tiles.  Per query tile:
-//   S^T  = K_j Q_i^T,   dP^T = V_j dO_i^T           (SS MMAs into TMEM, lanes = keys)
-//   P^T, dS^T  elementwise, one thread per key row  (P^T, dS^T as bf16 back into TMEM;
-//                                                     dS^T also into shared memory)
-//   dV_j += P^T dO_i,   dK_j += dS^T Q_i           (TS MMAs: A from TMEM, accumulate in TMEM)
+//   S^T  = K_j Q_i^T,   dP^T = V_j dO_i^T           (SS MMAs into TMEM, lanes = keys, N = 128)
+//   P^T  elementwise as soon as S^T is in, while dP^T computes (P^T as bf16 back into TMEM)
+//   dV_j += P^T dO_i                                 (TS MMA: A from TMEM), while the rows
+//   dS^T elementwise from dP^T and the P^T kept in registers (bf16 into TMEM and shared memory)
+//   dK_j += dS^T Q_i                                 (TS MMA, accumulates in TMEM)
 //   dQ_i  = dS K_j                                   (SS MMA: A = the staged dS, read M-major)
 // and the dQ_i tile is added into the fp32 accumulator in global memory (the tiles of
 // other key blocks add into the same rows) by TMA reduce-adds of 32 x 32 blocks staged in
 // shared memory.  dK_j, dV_j leave TMEM once, at the end.  The 128 (LSE log2 e, D) pairs
 // of a query tile are loaded once per step into shared memory and read as broadcasts.
 //
-// GB300 mapping (320 threads, one CTA per SM):
+// GB300 mapping (352 threads, one CTA per SM):
 //   warps 0-7  warp w reaches TMEM lanes 32 (w % 4) .. +31, so thread t owns key row t % 128
-//              of the tile for the elementwise pass and the dK/dV epilogue, and query row
+//              of the tile for the elementwise passes and the dK/dV epilogue, and query row
 //              t % 128 of the dQ tile; warps 0-3 take queries (or columns) [0, 64), warps 4-7
 //              [64, 128): two row warps per SM sub-partition
 //   warp 8     TMA producer (K_j, V_j once; Q_i, dO_i per step)
 //   warp 9     MMA issue (whole warp, one elected lane); owns the TMEM allocation
-// TMEM (512 columns): S^T [0, 128) -> P^T bf16 (queries 0-63 in [0, 32), 64-127 in [64, 96),
-// so neither half overwrites scores the other still reads) -> dQ_i fp32 [0, d); dP^T
-// [128, 256) -> dS^T bf16 likewise at +128; dV [256, 256 + d); dK [256 + d, 256 + 2d).
+//   warp 10    dQ reducer: issues the TMA reduce-adds of the staged dQ blocks
+// TMEM (512 columns): S^T [0, 128) -> P^T bf16 (queries 0-63 in [0, 32), 64-127 in [64, 96):
+// each warp overwrites only scores it has read); dP^T [128, 256) -> dS^T bf16 likewise at +128
+// -> dQ_i fp32 [128, 128 + d), written after the dK MMAs have read dS^T, so that the next
+// step's S^T MMAs need not wait for the dQ read-out (only its dP^T MMAs do); dV [256, 256 + d);
+// dK [256 + d, 256 + 2d).
 //
 // Every wait is bounded (oa_common.cuh); a wait that expires aborts the CTA, which falls
 // through to its teardown with TMEM freed.
@@ -48,6 +52,10 @@ constexpr int kBwdProducer = kBwdRowWarps;
 constexpr int kBwdMma = kBwdRowWarps + 1;
 constexpr int kBwdReducer = kBwdRowWarps + 2;
 constexpr uint32_t kBwdTmemCols = 512;
+// Key/value planes per dispatch group: the CTAs of kBwdPlaneGroup planes come before those of the
+// next planes, so the dQ accumulator rows and the Q / dO tiles that the running CTAs share stay in
+// L2 (key tile order over all planes at once spreads them over every head's rows).
+constexpr int kBwdPlaneGroup = 4;
 
 template <int D>
 struct BwdCfg {
@@ -67,13 +75,14 @@ struct BwdCfg {
   static constexpr int LD_OFF = ST_OFF + ST_BYTES;
   static constexpr int BAR_OFF = LD_OFF + BT * 8;
   // kv_full, qdo_full[2], qdo_empty[2], s_full[2], dp_full[2], ds_ready[2], dq_full, dq_read, done,
-  // ld_ready[2] ([h]: the query half h = queries 64h .. 64h + 63 of the step), dq_staged[2]
-  static constexpr int NUM_BARS = 17;
+  // ld_ready[2], dq_staged[2], p_ready[2] ([h]: the query half h = queries 64h .. 64h + 63 of the
+  // step; s_full and dp_full complete together for both halves)
+  static constexpr int NUM_BARS = 20;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
-  // S^T = K Q^T and dP^T = V dO^T for one half of the queries: both operands K-major
-  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT / 2, false);
+  // S^T = K Q^T and dP^T = V dO^T for the 128 queries: both operands K-major
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT, false);
   // dV += P^T dO and dK += dS^T Q: A from TMEM, B (dO, Q with d contiguous) N-major
   static constexpr uint32_t IDESC_KV = idesc_bf16_f32(BT, D, true);
   // dQ = dS K: A (staged dS, queries contiguous) M-major, B (K, d contiguous) N-major
@@ -137,21 +146,18 @@ __global__ void bwd_post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16*
   *reinterpret_cast<uint2*>(dq + i) = w;
 }
 
-// P^T and dS^T for 32 queries q_first .. q_first + 31 of one key row: sr / dr the fp32 S^T and
-// dP^T columns, nl / nd the negated (LSE log2 e, D) of those queries (four per float4), in packed
-// pairs of fp32.  MASK applies the key and causal tests as an exponent of -inf (no branch).
+// P^T for 64 queries q_first .. q_first + 63 of one key row: sr the fp32 S^T columns, nl the
+// negated LSE log2 e of those queries (four per float4).  pp keeps P^T in fp32 pairs for the dS^T
+// pass, pw the bf16 pairs that the dV MMA reads.  MASK applies the key and causal tests as an
+// exponent of -inf (no branch).
 template <bool MASK>
-__device__ __forceinline__ void bwd_p_ds(const uint32_t* sr, const uint32_t* dr, const float4* nl, const float4* nd,
-                                         uint64_t sl2x2, int key, int q_first, bool key_ok, bool causal,
-                                         uint32_t (&pw)[16], uint32_t (&dw)[16]) {
+__device__ __forceinline__ void bwd_p(const uint32_t (&sr)[64], const float4* nl, uint64_t sl2x2, int key, int q_first,
+                                      bool key_ok, bool causal, uint64_t (&pp)[32], uint32_t (&pw)[32]) {
 #pragma unroll
-  for (int e = 0; e < 32; e += 4) {
-    // broadcasts: every lane reads the same 16 bytes
+  for (int e = 0; e < 64; e += 4) {
     const ulonglong2 nlv = *reinterpret_cast<const ulonglong2*>(nl + e / 4);
-    const ulonglong2 ndv = *reinterpret_cast<const ulonglong2*>(nd + e / 4);
 #pragma unroll
     for (int h = 0; h < 4; h += 2) {
-      // P^T = exp(scale s - LSE) = exp2(s scale log2 e - LSE log2 e), two queries at once
       const uint64_t a = f2_fma(f2_pack(__uint_as_float(sr[e + h]), __uint_as_float(sr[e + h + 1])), sl2x2,
                                 h ? nlv.y : nlv.x);
       float a0, a1;
@@ -162,20 +168,33 @@ __device__ __forceinline__ void bwd_p_ds(const uint32_t* sr, const uint32_t* dr,
         a1 = (key_ok && (!causal || key <= q + 1)) ? a1 : -INFINITY;
       }
       const float p0 = ex2(a0), p1 = ex2(a1);
-      // dS^T = P^T (dP^T - D)
-      const uint64_t ds = f2_mul(f2_pack(p0, p1), f2_add(f2_pack(__uint_as_float(dr[e + h]),
-                                                               __uint_as_float(dr[e + h + 1])),
-                                                       h ? ndv.y : ndv.x));
+      pp[(e + h) / 2] = f2_pack(p0, p1);
+      pw[(e + h) / 2] = pack_bf16x2(p0, p1);
+    }
+  }
+}
+// dS^T = P^T (dP^T - D) for the same 64 queries: dr the fp32 dP^T columns, nd the negated D of
+// those queries, pp the fp32 P^T of bwd_p; dw the bf16 pairs.
+__device__ __forceinline__ void bwd_ds(const uint32_t (&dr)[64], const float4* nd, const uint64_t (&pp)[32],
+                                       uint32_t (&dw)[32]) {
+#pragma unroll
+  for (int e = 0; e < 64; e += 4) {
+    const ulonglong2 ndv = *reinterpret_cast<const ulonglong2*>(nd + e / 4);
+#pragma unroll
+    for (int h = 0; h < 4; h += 2) {
+      const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1])),
+                                  h ? ndv.y : ndv.x);
+      const uint64_t ds = f2_mul(pp[(e + h) / 2], dpd);
       float d0, d1;
       f2_unpack(ds, d0, d1);
-      pw[(e + h) / 2] = pack_bf16x2(p0, p1);
       dw[(e + h) / 2] = pack_bf16x2(d0, d1);
     }
   }
 }
 
-// grid.x = nkt * BHkv: blockIdx.x / BHkv is the key tile j (low j first: for causal those have
-// the most query tiles), blockIdx.x % BHkv the key/value plane -- dense: (b, key/value head);
+// grid.x = nkt * BHkv CTAs in groups of kBwdPlaneGroup key/value planes (the last group may be
+// smaller); inside a group the key tile j is the slow index (low j first: for causal those have
+// the most query tiles) and the plane the fast one.  A plane is -- dense: (b, key/value head);
 // PACKED: (sequence, key/value head) of token-major [tokens, heads, d] tensors, whose sequence s
 // owns rows [cu[s], cu[s+1]) (a CTA past its sequence's keys exits at once).
 template <int D, bool PACKED>
@@ -196,8 +215,8 @@ __global__ void __launch_bounds__(kBwdThreads)
   // stage s free again: its MMAs are complete and the dQ blocks staged in it have been read by
   // their TMA reduce-adds (the reducer warp)
   auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (3 + s); };
-  auto bar_s = [&](int h) { return bar0 + 8u * (5 + h); };    // S^T of query half h in TMEM
-  auto bar_dp = [&](int h) { return bar0 + 8u * (7 + h); };   // dP^T of half h in TMEM
+  auto bar_s = [&](int h) { return bar0 + 8u * (5 + h); };    // S^T (waited on by the rows of half h)
+  auto bar_dp = [&](int h) { return bar0 + 8u * (7 + h); };   // dP^T (likewise)
   auto bar_ds = [&](int h) { return bar0 + 8u * (9 + h); };   // P^T, dS^T of half h in TMEM, dS staged
   const uint32_t bar_dq = bar0 + 8u * 11;                     // dQ_i in TMEM
   const uint32_t bar_dq_read = bar0 + 8u * 12;                // dQ_i read out of TMEM (8 warps)
@@ -205,11 +224,16 @@ __global__ void __launch_bounds__(kBwdThreads)
   auto bar_ld = [&](int h) { return bar0 + 8u * (14 + h); };  // half h's (LSE, D) entries written
   // the dQ blocks of the step using stage s are staged in it (8 warps)
   auto bar_dq_staged = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto bar_p = [&](int h) { return bar0 + 8u * (18 + h); };   // P^T of half h in TMEM (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = (int)(blockIdx.x / p.BHkv);
+  const int g0 = (int)(blockIdx.x / (unsigned)(kBwdPlaneGroup * p.nkt)) * kBwdPlaneGroup;  // first plane
+  const int gsz = min(kBwdPlaneGroup, p.BHkv - g0);
+  const int g_local = (int)blockIdx.x - g0 * p.nkt;
+  const int j = g_local / gsz;
+  const int plane = g0 + g_local % gsz;
   const int k0 = j * BT;
   // The CTA's geometry.  Rows: Q / dO / dQ row of query q is qrow0 + q, K / V / dK / dV row of key
   // k is krow0 + k (TMA coordinates); query head t of the group is TMA plane qplane0 + t; the LSE / D
@@ -217,7 +241,7 @@ __global__ void __launch_bounds__(kBwdThreads)
   int Nq, Nk, nqt, qrow0, krow0, qplane0, kplane;
   int64_t lbase, lq, lt, dkbase, dks;
   if constexpr (PACKED) {
-    const int r = (int)(blockIdx.x % p.BHkv), seq = r / p.Hkv, hkv = r % p.Hkv;
+    const int seq = plane / p.Hkv, hkv = plane % p.Hkv;
     const int qb = min(max(p.cu_q[seq], 0), p.total_q), qe = min(max(p.cu_q[seq + 1], qb), p.total_q);
     const int kb = min(max(p.cu_k[seq], 0), p.total_k), ke = min(max(p.cu_k[seq + 1], kb), p.total_k);
     Nq = qe - qb;
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     dkbase = (int64_t)kb * p.Hkv + hkv;
     dks = p.Hkv;
   } else {
-    const int kvp = (int)(blockIdx.x % p.BHkv);  // (b, key/value head)
+    const int kvp = plane;  // (b, key/value head)
     Nq = p.Nq;
     Nk = p.Nk;
     qrow0 = krow0 = 0;
@@ -277,6 +301,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       mbar_init(bar_s(h), 1);
       mbar_init(bar_dp(h), 1);
       mbar_init(bar_ds(h), kBwdRowWarps / 2);
+      mbar_init(bar_p(h), kBwdRowWarps / 2);
       mbar_init(bar_ld(h), kBwdRowWarps / 2);
     }
     mbar_init(bar_dq, 1);
@@ -349,46 +374,50 @@ __global__ void __launch_bounds__(kBwdThreads)
       const uint64_t q_nmaj = smem_desc_sw128(sbase + C::Q_OFF + s * C::TILE_BYTES, C::SLAB_BYTES, 1024);
       const uint64_t do_nmaj = smem_desc_sw128(sbase + C::DO_OFF + s * C::TILE_BYTES, C::SLAB_BYTES, 1024);
       if (!(ok = wait_all(bar_qdo(s), (uint32_t)(it >> 1) & 1u, B_QDO))) break;
-      // S^T goes where dQ_{i-1} lies: the rows must have read it out first
+      tc_fence_after_sync();
+      // S^T into columns that nothing reads any more (the previous step's P^T was read by its dV
+      // MMAs, issued earlier); dP^T into the columns of the previous step's dQ, once the rows have
+      // read it out
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(tmem_base + C::S_COL, k_kmaj + kmaj_off(kk), q_kmaj + kmaj_off(kk), C::IDESC_S, kk > 0 ? 1u : 0u);
+      mma_commit_elect(bar_s(0));
+      mma_commit_elect(bar_s(1));
       if (it > 0 && !(ok = wait_all(bar_dq_read, ph ^ 1u, B_DQ_READ))) break;
       tc_fence_after_sync();
-      // S^T and dP^T per query half (N = 64): the rows of half 0 start while half 1 computes;
-      // the B operands of half h start 64 rows (8192 bytes) into each slab
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(tmem_base + C::DP_COL, v_kmaj + kmaj_off(kk), do_kmaj + kmaj_off(kk), C::IDESC_S, kk > 0 ? 1u : 0u);
+      mma_commit_elect(bar_dp(0));
+      mma_commit_elect(bar_dp(1));
+      // dV += P^T dO_i half by half as the rows write P^T (K = 16 queries per MMA step = 8 TMEM
+      // columns of bf16 pairs; queries 64-127 start at column 64), while dP^T computes; then
+      // dK += dS^T Q_i likewise
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint64_t hoff = (uint64_t)((h * 64 * 128) >> 4);
+        if (!(ok = wait_all(bar_p(h), ph, B_DS))) break;
+        tc_fence_after_sync();
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_elect(tmem_base + C::S_COL + h * 64, k_kmaj + kmaj_off(kk), q_kmaj + hoff + kmaj_off(kk), C::IDESC_S,
-                       kk > 0 ? 1u : 0u);
-        mma_commit_elect(bar_s(h));
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_ss_elect(tmem_base + C::DP_COL + h * 64, v_kmaj + kmaj_off(kk), do_kmaj + hoff + kmaj_off(kk),
-                       C::IDESC_S, kk > 0 ? 1u : 0u);
-        mma_commit_elect(bar_dp(h));
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), do_nmaj + rows16_off(kk),
+                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
       }
-      // dV += P^T dO_i and dK += dS^T Q_i, half by half as the rows finish (K = 16 queries per
-      // MMA step = 8 TMEM columns of bf16 pairs; queries 64-127 start at column 64)
+      if (!ok) break;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         if (!(ok = wait_all(bar_ds(h), ph, B_DS))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-          mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), do_nmaj + rows16_off(kk),
-                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
           mma_ts_elect(tmem_base + C::DK_COL, tmem_base + C::DP_COL + pcol(kk), q_nmaj + rows16_off(kk),
                        C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
       }
       if (!ok) break;
-      // dQ_i = dS K_j (K = the 128 keys) into the columns P^T occupied: after the dV MMAs that
+      // dQ_i = dS K_j (K = the 128 keys) into the columns dS^T occupied: after the dK MMAs that
       // read it (MMAs of one thread run in order)
 #pragma unroll
       for (int kk = 0; kk < BT / 16; ++kk)
-        mma_ss_elect(tmem_base + C::S_COL, st_mmaj + rows16_off(kk), k_nmaj + rows16_off(kk), C::IDESC_Q,
+        mma_ss_elect(tmem_base + C::DP_COL, st_mmaj + rows16_off(kk), k_nmaj + rows16_off(kk), C::IDESC_Q,
                      kk > 0 ? 1u : 0u);
       mma_commit_elect(bar_dq);
     }
@@ -462,41 +491,46 @@ __global__ void __launch_bounds__(kBwdThreads)
       if (!(ok = wait_all(bar_s(half), ph, B_S))) break;
       // -LSE log2 e and -D of query q0 + ld_q; a row past the end or with no visible key gets
       // -inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
-      // every row warp is past the previous step's reads of the (LSE, D) block: it arrived on
-      // dq_read, which the S MMAs of this step waited for
+      // every row warp is past the previous step's reads of the (LSE, D) block: this warp waited
+      // for that step's dQ MMA, issued only after all eight warps had arrived on ds_ready
       if (tt < 64) {
         *nl_mine = next_l == -INFINITY ? -INFINITY : -next_l * kLog2e;
         *nd_mine = -next_d;
       }
       if (lane == 0) mbar_arrive(bar_ld(half));
       if (!(ok = wait_all(bar_ld(half), ph, B_LD))) break;
+      tc_fence_after_sync();
+      // this warp's 64 columns of S^T (then of dP^T); P^T and dS^T go as bf16 pairs into the first
+      // 32 of them, which this warp has read and no other warp touches
+      const uint32_t sc = tmem_base + lane_base + C::S_COL + 64 * half;
+      const uint32_t dc = tmem_base + lane_base + C::DP_COL + 64 * half;
+      uint64_t pp[32];  // P^T of the 64 queries in fp32, for the dS^T pass
+      {
+        uint32_t sr[64], pw[32];
+        tmem_ld32x2(sc, sc + 32, sr);
+        if (full)
+          bwd_p<false>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, true, false, pp, pw);
+        else
+          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
+        tmem_st32(sc, pw);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(half));
       if (!(ok = wait_all(bar_dp(half), ph, B_DP))) break;
       tc_fence_after_sync();
-      // this half's 64 columns of S^T (sd[0..63]) and dP^T (sd[64..127]), one wait
-      uint32_t sd[128];
-      tmem_ld64x2(tmem_base + lane_base + C::S_COL + 64 * half, tmem_base + lane_base + C::DP_COL + 64 * half, sd);
+      {
+        uint32_t dr[64], dw[32];
+        tmem_ld32x2(dc, dc + 32, dr);
+        bwd_ds(dr, nd4 + 16 * half, pp, dw);
+        tmem_st32(dc, dw);
+        // dS^T row `key`, queries 64 half .. +63: the 128-byte row of slab `half`, 16-byte chunk q
+        // stored at position q ^ (row % 8) (128-byte swizzle)
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 64 * half + 32 * cc;
-        uint32_t pw[16], dw[16];
-        if (full)
-          bwd_p_ds<false>(sd + 32 * cc, sd + 64 + 32 * cc, nl4 + c / 4, nd4 + c / 4, sl2x2, key, q0 + c, true, false,
-                          pw, dw);
-        else
-          bwd_p_ds<true>(sd + 32 * cc, sd + 64 + 32 * cc, nl4 + c / 4, nd4 + c / 4, sl2x2, key, q0 + c, key_ok,
-                         p.causal != 0, pw, dw);
-        // P^T / dS^T as bf16 pairs: queries c .. c+31 to columns c/2 (+32 for the second half),
-        // all of them already read by this warp and by no other
-        const uint32_t oc = c / 2 + (c >= 64 ? 32 : 0);
-        tmem_st16(tmem_base + lane_base + C::S_COL + oc, pw);
-        tmem_st16(tmem_base + lane_base + C::DP_COL + oc, dw);
-        // dS^T row `key`, queries c .. c+31: 16-byte chunks (c % 64) / 8 .. +3 of slab c / 64,
-        // chunk q of row r stored at position q ^ (r % 8) (128-byte swizzle)
-        const int cq0 = (c % 64) / 8;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          *reinterpret_cast<uint4*>(st_row + (((cq0 + q4) ^ (tt & 7)) * 16)) =
-              make_uint4(dw[4 * q4], dw[4 * q4 + 1], dw[4 * q4 + 2], dw[4 * q4 + 3]);
+        for (int q8 = 0; q8 < 8; ++q8)
+          *reinterpret_cast<uint4*>(st_row + ((q8 ^ (tt & 7)) * 16)) =
+              make_uint4(dw[4 * q8], dw[4 * q8 + 1], dw[4 * q8 + 2], dw[4 * q8 + 3]);
       }
       tmem_st_wait();
       tc_fence_before_sync();
@@ -506,7 +540,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       pos = next_pos(pos);  // the next step's (head, tile); its (LSE, D) load is issued now
       load_ld(it + 1, pos, next_l, next_d);
       // dQ_i = scale dS K_j: thread t holds query row q0 + t % 128.  The warp's columns leave
-      // TMEM first (so the next step's S MMA may overwrite them); then per 32 columns the warp
+      // TMEM first (so the next step's dP MMA may overwrite them); then per 32 columns the warp
       // stages its 32 x 32 block (swizzled like the map) in its own staging rows, which the dQ
       // MMA has finished reading, and one lane adds it into the accumulator with a TMA
       // reduce-add (rows past Nq are clipped by the map; a block wholly past the end is skipped).
@@ -515,7 +549,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       uint32_t r[DQ_CHUNKS][32];
 #pragma unroll
       for (int m = 0; m < DQ_CHUNKS; ++m)
-        tmem_ld32(tmem_base + lane_base + C::S_COL + (half * DQ_CHUNKS + m) * 32, r[m]);
+        tmem_ld32(tmem_base + lane_base + C::DP_COL + (half * DQ_CHUNKS + m) * 32, r[m]);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_read);

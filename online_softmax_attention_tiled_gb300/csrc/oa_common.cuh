@@ -236,25 +236,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
-// 64 consecutive columns at each of two addresses (r[0..63] from ta, r[64..127] from tb), one wait.
-__device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, uint32_t (&r)[128]) {
+// 64 consecutive columns, r[0..31] from ta and r[32..63] from tb (tb = ta + 32 for a contiguous
+// block), two loads and one wait.
+__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, uint32_t (&r)[64]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%128];\n\t"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%129];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,"
-      "%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95}, [%130];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,"
-      "%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%131];\n\t"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
       "tcgen05.wait::ld.sync.aligned;\n"
-      : OA_R8(0), OA_R8(8), OA_R8(16), OA_R8(24), OA_R8(32), OA_R8(40), OA_R8(48), OA_R8(56), OA_R8(64),
-        OA_R8(72), OA_R8(80), OA_R8(88), OA_R8(96), OA_R8(104), OA_R8(112), OA_R8(120)
-      : "r"(ta), "r"(ta + 32), "r"(tb), "r"(tb + 32)
+      : OA_R8(0), OA_R8(8), OA_R8(16), OA_R8(24), OA_R8(32), OA_R8(40), OA_R8(48), OA_R8(56)
+      : "r"(ta), "r"(tb)
       : "memory");
 }
 
