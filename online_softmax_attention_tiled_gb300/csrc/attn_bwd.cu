@@ -74,10 +74,11 @@ struct BwdCfg {
   // -LSE log2 e of the step's 128 query rows, then -D (-inf / 0 past the end)
   static constexpr int LD_OFF = ST_OFF + ST_BYTES;
   static constexpr int BAR_OFF = LD_OFF + BT * 8;
-  // kv_full, qdo_full[2], qdo_empty[2], s_full[2], dp_full[2], ds_ready[2], dq_full, dq_read, done,
-  // ld_ready[2], dq_staged[2], p_ready[2] ([h]: the query half h = queries 64h .. 64h + 63 of the
-  // step; s_full and dp_full complete together for both halves)
-  static constexpr int NUM_BARS = 20;
+  // kv_full, q_full[2], q_empty[2], s_full[2], dp_full[2], ds_ready[2], dq_full, dq_read, done,
+  // ld_ready[2], dq_staged[2], p_ready[2], do_full[2], do_empty[2], dq_staged_hi[2] ([s]: ring stage
+  // s; [h]: the query half h = queries 64h .. 64h + 63 of the step; s_full and dp_full complete
+  // together for both halves)
+  static constexpr int NUM_BARS = 26;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 256 + D;
@@ -211,9 +212,11 @@ __global__ void __launch_bounds__(kBwdThreads)
 
   const uint32_t bar0 = sbase + C::BAR_OFF;
   const uint32_t bar_kv = bar0;
-  auto bar_qdo = [&](int s) { return bar0 + 8u * (1 + s); };        // Q_i, dO_i of stage s landed
-  // stage s free again: its MMAs are complete and the dQ blocks staged in it have been read by
-  // their TMA reduce-adds (the reducer warp)
+  auto bar_qdo = [&](int s) { return bar0 + 8u * (1 + s); };  // Q_i of stage s landed
+  // the Q buffer of stage s free again: its MMAs are complete and the dQ blocks that warps 0-3
+  // staged in it have been read by their TMA reduce-adds (the reducer warp); bar_do_empty the same
+  // for the dO buffer and warps 4-7.  The reducer adds the Q buffer's blocks first, so the next
+  // Q (needed first, by the S MMAs) can load while the dO buffer's blocks are still being read.
   auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (3 + s); };
   auto bar_s = [&](int h) { return bar0 + 8u * (5 + h); };    // S^T (waited on by the rows of half h)
   auto bar_dp = [&](int h) { return bar0 + 8u * (7 + h); };   // dP^T (likewise)
@@ -223,7 +226,10 @@ __global__ void __launch_bounds__(kBwdThreads)
   const uint32_t bar_done = bar0 + 8u * 13;                   // every MMA of the CTA complete
   auto bar_ld = [&](int h) { return bar0 + 8u * (14 + h); };  // half h's (LSE, D) entries written
   // the dQ blocks of the step using stage s are staged in it (8 warps)
-  auto bar_dq_staged = [&](int s) { return bar0 + 8u * (16 + s); };
+  auto bar_dq_staged = [&](int s) { return bar0 + 8u * (16 + s); };  // warps 0-3 staged (Q buffer)
+  auto bar_do = [&](int s) { return bar0 + 8u * (20 + s); };             // dO_i of stage s landed
+  auto bar_do_empty = [&](int s) { return bar0 + 8u * (22 + s); };
+  auto bar_dq_staged_hi = [&](int s) { return bar0 + 8u * (24 + s); };  // warps 4-7 staged (dO buffer)
   auto bar_p = [&](int h) { return bar0 + 8u * (18 + h); };   // P^T of half h in TMEM (4 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -295,7 +301,10 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qdo(s), 1);
       mbar_init(bar_qdo_empty(s), 1);
-      mbar_init(bar_dq_staged(s), kBwdRowWarps);
+      mbar_init(bar_dq_staged(s), kBwdRowWarps / 2);
+      mbar_init(bar_dq_staged_hi(s), kBwdRowWarps / 2);
+      mbar_init(bar_do(s), 1);
+      mbar_init(bar_do_empty(s), 1);
     }
     for (int h = 0; h < 2; ++h) {
       mbar_init(bar_s(h), 1);
@@ -337,24 +346,30 @@ __global__ void __launch_bounds__(kBwdThreads)
       tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, krow0 + k0, kplane);
       tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, krow0 + k0, kplane);
     }
-    int issued = 0;
+    int issued_q = 0, issued_do = 0;
     StepPos pos = first_pos;
     for (int it = 0; it < n_it; ++it, pos = next_pos(pos)) {
       const int s = it & 1, q0 = pos.i * BT, qp = qplane0 + pos.t, qy = qrow0 + q0;
-      // stage s was last read by step it - 2
-      if (it >= 2 && !(ok = wait_all(bar_qdo_empty(s), (uint32_t)((it >> 1) - 1) & 1u, B_QDO_EMPTY))) break;
-      mbar_arrive_expect_tx_elect(bar_qdo(s), 2 * C::TILE_BYTES);
-      for (int c = 0; c < C::SLABS; ++c) {
+      // stage s was last used by step it - 2: Q first (the S MMAs read it first), then dO
+      const uint32_t par = (uint32_t)((it >> 1) - 1) & 1u;
+      if (it >= 2 && !(ok = wait_all(bar_qdo_empty(s), par, B_QDO_EMPTY))) break;
+      mbar_arrive_expect_tx_elect(bar_qdo(s), C::TILE_BYTES);
+      for (int c = 0; c < C::SLABS; ++c)
         tma_load_3d_elect(sbase + C::Q_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_q, bar_qdo(s), c * 64, qy,
                           qp);
-        tma_load_3d_elect(sbase + C::DO_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_do, bar_qdo(s), c * 64,
+      ++issued_q;
+      if (it >= 2 && !(ok = wait_all(bar_do_empty(s), par, B_QDO_EMPTY))) break;
+      mbar_arrive_expect_tx_elect(bar_do(s), C::TILE_BYTES);
+      for (int c = 0; c < C::SLABS; ++c)
+        tma_load_3d_elect(sbase + C::DO_OFF + s * C::TILE_BYTES + c * C::SLAB_BYTES, &tm_do, bar_do(s), c * 64,
                           qy, qp);
-      }
-      ++issued;
+      ++issued_do;
     }
     // drain: every load issued must have landed before the CTA can exit
-    for (int it = max(0, issued - 2); it < issued; ++it)
+    for (int it = max(0, issued_q - 2); it < issued_q; ++it)
       mbar_wait(bar_qdo(it & 1), (uint32_t)(it >> 1) & 1u, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
+    for (int it = max(0, issued_do - 2); it < issued_do; ++it)
+      mbar_wait(bar_do(it & 1), (uint32_t)(it >> 1) & 1u, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
     mbar_wait(bar_kv, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
   } else if (warp == kBwdMma) {
     // =================== MMA issue (whole warp, one elected lane) ===================
@@ -384,6 +399,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       mma_commit_elect(bar_s(0));
       mma_commit_elect(bar_s(1));
       if (it > 0 && !(ok = wait_all(bar_dq_read, ph ^ 1u, B_DQ_READ))) break;
+      if (!(ok = wait_all(bar_do(s), (uint32_t)(it >> 1) & 1u, B_QDO))) break;  // dO_i landed
       tc_fence_after_sync();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
@@ -433,20 +449,30 @@ __global__ void __launch_bounds__(kBwdThreads)
     StepPos pos = first_pos;
     for (int it = 0; ok && it < n_it; ++it, pos = next_pos(pos)) {
       const int s = it & 1, q0 = pos.i * BT, qp = qplane0 + pos.t, qy = qrow0 + q0;
-      if (!(ok = wait_all(bar_dq_staged(s), (uint32_t)(it >> 1) & 1u, B_DQ_STAGED))) break;
-      if (lane == 0) {
-        const uint32_t stage_base = C::Q_OFF + (uint32_t)s * C::TILE_BYTES;
-        for (int w = 0; w < kBwdRowWarps; ++w) {
-          if (q0 + (w & 3) * 32 >= Nq) continue;
-          for (int m = 0; m < C::DQ_CHUNKS; ++m)
-            tma_reduce_add_3d(&tm_dq, sbase + bwd_dq_block<C>(stage_base, w, m), ((w >> 2) * C::DQ_CHUNKS + m) * 32,
-                              qy + (w & 3) * 32, qp);
+      const uint32_t stage_base = C::Q_OFF + (uint32_t)s * C::TILE_BYTES;
+      const uint32_t par = (uint32_t)(it >> 1) & 1u;
+      // warps 0-3 staged their blocks in the Q buffer, warps 4-7 in the dO buffer: one commit
+      // group each, the Q buffer's first
+      for (int hw = 0; hw < 2 && ok; ++hw) {
+        if (!(ok = wait_all(hw ? bar_dq_staged_hi(s) : bar_dq_staged(s), par, B_DQ_STAGED))) break;
+        if (lane == 0) {
+          for (int w = 4 * hw; w < 4 * hw + 4; ++w) {
+            if (q0 + (w & 3) * 32 >= Nq) continue;
+            for (int m = 0; m < C::DQ_CHUNKS; ++m)
+              tma_reduce_add_3d(&tm_dq, sbase + bwd_dq_block<C>(stage_base, w, m),
+                                ((w >> 2) * C::DQ_CHUNKS + m) * 32, qy + (w & 3) * 32, qp);
+          }
+          bulk_commit_group();
         }
-        bulk_commit_group();
-        bulk_wait_read<0>();  // the stage may be refilled once its blocks have been read
+        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) bulk_wait_read<1>();  // the Q buffer's blocks have been read: refill it
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_qdo_empty(s));
+      if (lane == 0) bulk_wait_read<0>();  // and the dO buffer's
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_do_empty(s));
     }
     if (lane == 0) bulk_wait_all();  // every add performed before the CTA exits
     __syncwarp();
@@ -565,7 +591,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       }
       fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dq_staged(it & 1));
+      if (lane == 0) mbar_arrive(warp < 4 ? bar_dq_staged(it & 1) : bar_dq_staged_hi(it & 1));
     }
     // dK_j, dV_j rows (key rows of the tile), columns [half D/2, half D/2 + D/2)
     if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
