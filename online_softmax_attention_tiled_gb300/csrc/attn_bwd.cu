@@ -193,11 +193,119 @@ __device__ __forceinline__ void bwd_ds(const uint32_t (&dr)[64], const float4* n
   }
 }
 
+// The CTA's geometry.  Rows: Q / dO / dQ row of query q is qrow0 + q, K / V / dK / dV row of key
+// k is krow0 + k (TMA coordinates); query head t of the group is TMA plane qplane0 + t; the LSE / D
+// entry of (q, t) is lbase + q lq + t lt; the dK / dV row of key k starts at (dkbase + k dks) d.
+struct BwdGeom {
+  int j, k0;  // key tile and its first key
+  int Nq, Nk, nqt, qrow0, krow0, qplane0, kplane;
+  int64_t lbase, lq, lt, dkbase, dks;
+  int i_begin;  // first visible query tile (causal: query tile i sees key tile j iff i >= j)
+  int n_it;     // steps: every visible query tile of every query head of the group, head by head
+};
+
 // grid.x = nkt * BHkv CTAs in groups of kBwdPlaneGroup key/value planes (the last group may be
 // smaller); inside a group the key tile j is the slow index (low j first: for causal those have
 // the most query tiles) and the plane the fast one.  A plane is -- dense: (b, key/value head);
 // PACKED: (sequence, key/value head) of token-major [tokens, heads, d] tensors, whose sequence s
 // owns rows [cu[s], cu[s+1]) (a CTA past its sequence's keys exits at once).
+// Returns false for a CTA with nothing to do (its key tile starts past its packed sequence's keys).
+template <bool PACKED>
+__device__ __forceinline__ bool bwd_geometry(const BwdParams& p, BwdGeom& g) {
+  const int g0 = (int)(blockIdx.x / (unsigned)(kBwdPlaneGroup * p.nkt)) * kBwdPlaneGroup;  // first plane
+  const int gsz = min(kBwdPlaneGroup, p.BHkv - g0);
+  const int g_local = (int)blockIdx.x - g0 * p.nkt;
+  g.j = g_local / gsz;
+  const int plane = g0 + g_local % gsz;
+  g.k0 = g.j * BT;
+  if constexpr (PACKED) {
+    const int seq = plane / p.Hkv, hkv = plane % p.Hkv;
+    const int qb = min(max(p.cu_q[seq], 0), p.total_q), qe = min(max(p.cu_q[seq + 1], qb), p.total_q);
+    const int kb = min(max(p.cu_k[seq], 0), p.total_k), ke = min(max(p.cu_k[seq + 1], kb), p.total_k);
+    g.Nq = qe - qb;
+    g.Nk = ke - kb;
+    // a key sequence longer than the grid covers: its tail gets no gradient; report it
+    if (g.j == p.nkt - 1 && hkv == 0 && threadIdx.x == 0 && g.Nk > p.nkt * BT)
+      record_failure(p.st, kSiteBwdBadSeqlen);
+    if (g.k0 >= g.Nk) return false;  // uniform over the CTA; nothing set up yet
+    g.qrow0 = qb;
+    g.krow0 = kb;
+    g.qplane0 = hkv * p.group;
+    g.kplane = hkv;
+    g.lbase = (int64_t)qb * p.H + (int64_t)hkv * p.group;
+    g.lq = p.H;
+    g.lt = 1;
+    g.dkbase = (int64_t)kb * p.Hkv + hkv;
+    g.dks = p.Hkv;
+  } else {
+    const int kvp = plane;  // (b, key/value head)
+    g.Nq = p.Nq;
+    g.Nk = p.Nk;
+    g.qrow0 = g.krow0 = 0;
+    g.qplane0 = kvp * p.group;
+    g.kplane = kvp;
+    g.lbase = (int64_t)kvp * p.group * p.Nq;
+    g.lq = 1;
+    g.lt = p.Nq;
+    g.dkbase = (int64_t)kvp * p.Nk;
+    g.dks = 1;
+  }
+  g.nqt = (g.Nq + BT - 1) / BT;
+  g.i_begin = p.causal ? g.j : 0;
+  g.n_it = p.group * max(g.nqt - g.i_begin, 0);
+  return true;
+}
+
+// (query head t of the group, query tile i) of a step; next() steps to the following one without a
+// division: query tiles i_begin .. nqt - 1 of head t, then of head t + 1
+struct StepPos {
+  int t, i;
+  __device__ __forceinline__ StepPos next(const BwdGeom& g) const {
+    StepPos n{t, i + 1};
+    if (n.i == g.nqt) {
+      n.i = g.i_begin;
+      ++n.t;
+    }
+    return n;
+  }
+};
+
+// dK (times scale) and dV of key row `key` as bf16, columns [half d/2, half d/2 + d/2), from the
+// accumulators at TMEM columns dk_col and dv_col of this thread's lane (tl = TMEM base + the warp's
+// lane quarter); zeros when the CTA had no step; no store for a key past the end.
+template <int D>
+__device__ __forceinline__ void bwd_store_dkdv(const BwdParams& p, const BwdGeom& g, uint32_t tl, uint32_t dk_col,
+                                               uint32_t dv_col, int half, int key, bool key_ok, bool any_step) {
+  __nv_bfloat16* dkrow = p.dk + (g.dkbase + (int64_t)key * g.dks) * D;
+  __nv_bfloat16* dvrow = p.dv + (g.dkbase + (int64_t)key * g.dks) * D;
+#pragma unroll 1
+  for (int c = half * (D / 2); c < half * (D / 2) + D / 2; c += 32) {
+    uint32_t rk[32], rv[32];
+    if (any_step) {
+      tmem_ld32(tl + dk_col + c, rk);
+      tmem_ld32(tl + dv_col + c, rv);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) rk[e] = rv[e] = 0u;
+    }
+    uint4 wk[4], wv[4];
+    uint32_t* k32 = reinterpret_cast<uint32_t*>(wk);
+    uint32_t* v32 = reinterpret_cast<uint32_t*>(wv);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      k32[e] = pack_bf16x2(__uint_as_float(rk[2 * e]) * p.scale, __uint_as_float(rk[2 * e + 1]) * p.scale);
+      v32[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
+    }
+    if (key_ok) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        reinterpret_cast<uint4*>(dkrow + c)[e] = wk[e];
+        reinterpret_cast<uint4*>(dvrow + c)[e] = wv[e];
+      }
+    }
+  }
+}
+
 template <int D, bool PACKED>
 __global__ void __launch_bounds__(kBwdThreads)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -235,66 +343,12 @@ __global__ void __launch_bounds__(kBwdThreads)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g0 = (int)(blockIdx.x / (unsigned)(kBwdPlaneGroup * p.nkt)) * kBwdPlaneGroup;  // first plane
-  const int gsz = min(kBwdPlaneGroup, p.BHkv - g0);
-  const int g_local = (int)blockIdx.x - g0 * p.nkt;
-  const int j = g_local / gsz;
-  const int plane = g0 + g_local % gsz;
-  const int k0 = j * BT;
-  // The CTA's geometry.  Rows: Q / dO / dQ row of query q is qrow0 + q, K / V / dK / dV row of key
-  // k is krow0 + k (TMA coordinates); query head t of the group is TMA plane qplane0 + t; the LSE / D
-  // entry of (q, t) is lbase + q lq + t lt; the dK / dV row of key k starts at (dkbase + k dks) D.
-  int Nq, Nk, nqt, qrow0, krow0, qplane0, kplane;
-  int64_t lbase, lq, lt, dkbase, dks;
-  if constexpr (PACKED) {
-    const int seq = plane / p.Hkv, hkv = plane % p.Hkv;
-    const int qb = min(max(p.cu_q[seq], 0), p.total_q), qe = min(max(p.cu_q[seq + 1], qb), p.total_q);
-    const int kb = min(max(p.cu_k[seq], 0), p.total_k), ke = min(max(p.cu_k[seq + 1], kb), p.total_k);
-    Nq = qe - qb;
-    Nk = ke - kb;
-    // a key sequence longer than the grid covers: its tail gets no gradient; report it
-    if (j == p.nkt - 1 && hkv == 0 && threadIdx.x == 0 && Nk > p.nkt * BT)
-      record_failure(p.st, kSiteBwdBadSeqlen);
-    if (k0 >= Nk) return;  // no key of this sequence in the tile (uniform over the CTA; nothing set up yet)
-    qrow0 = qb;
-    krow0 = kb;
-    qplane0 = hkv * p.group;
-    kplane = hkv;
-    lbase = (int64_t)qb * p.H + (int64_t)hkv * p.group;
-    lq = p.H;
-    lt = 1;
-    dkbase = (int64_t)kb * p.Hkv + hkv;
-    dks = p.Hkv;
-  } else {
-    const int kvp = plane;  // (b, key/value head)
-    Nq = p.Nq;
-    Nk = p.Nk;
-    qrow0 = krow0 = 0;
-    qplane0 = kvp * p.group;
-    kplane = kvp;
-    lbase = (int64_t)kvp * p.group * p.Nq;
-    lq = 1;
-    lt = p.Nq;
-    dkbase = (int64_t)kvp * p.Nk;
-    dks = 1;
-  }
-  nqt = (Nq + BT - 1) / BT;
-  const int i_begin = p.causal ? j : 0;  // causal: query tile i sees key tile j iff i >= j
-  const int n_i = max(nqt - i_begin, 0);  // visible query tiles of one query head
-  // steps: every visible query tile of every query head of the group, head by head
-  const int n_it = p.group * n_i;
-  // (query head t of the group, query tile i) of consecutive steps, without a division per step
-  struct StepPos {
-    int t, i;
-  };
-  auto next_pos = [&](StepPos s) {
-    if (++s.i == nqt) {
-      s.i = i_begin;
-      ++s.t;
-    }
-    return s;
-  };
-  const StepPos first_pos{0, i_begin};
+  BwdGeom g;
+  if (!bwd_geometry<PACKED>(p, g)) return;
+  const int j = g.j, k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
+  const int64_t lbase = g.lbase, lq = g.lq, lt = g.lt;
+  auto next_pos = [&](StepPos sp) { return sp.next(g); };
+  const StepPos first_pos{0, g.i_begin};
 
   if (threadIdx.x == 0) {
     mbar_init(bar_kv, 1);
@@ -343,8 +397,8 @@ __global__ void __launch_bounds__(kBwdThreads)
     bool ok = true;
     mbar_arrive_expect_tx_elect(bar_kv, 2 * C::TILE_BYTES);
     for (int c = 0; c < C::SLABS; ++c) {
-      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, krow0 + k0, kplane);
-      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, krow0 + k0, kplane);
+      tma_load_3d_elect(sbase + C::K_OFF + c * C::SLAB_BYTES, &tm_k, bar_kv, c * 64, g.krow0 + k0, g.kplane);
+      tma_load_3d_elect(sbase + C::V_OFF + c * C::SLAB_BYTES, &tm_v, bar_kv, c * 64, g.krow0 + k0, g.kplane);
     }
     int issued_q = 0, issued_do = 0;
     StepPos pos = first_pos;
@@ -597,34 +651,387 @@ __global__ void __launch_bounds__(kBwdThreads)
     if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
     if (ok) {
       tc_fence_after_sync();
-      __nv_bfloat16* dkrow = p.dk + (dkbase + (int64_t)key * dks) * D;
-      __nv_bfloat16* dvrow = p.dv + (dkbase + (int64_t)key * dks) * D;
-#pragma unroll 1
-      for (int c = half * (D / 2); c < half * (D / 2) + D / 2; c += 32) {
-        uint32_t rk[32], rv[32];
-        if (n_it > 0) {
-          tmem_ld32(tmem_base + lane_base + C::DK_COL + c, rk);
-          tmem_ld32(tmem_base + lane_base + C::DV_COL + c, rv);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) rk[e] = rv[e] = 0u;
-        }
-        uint4 wk[4], wv[4];
-        uint32_t* k32 = reinterpret_cast<uint32_t*>(wk);
-        uint32_t* v32 = reinterpret_cast<uint32_t*>(wv);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          k32[e] = pack_bf16x2(__uint_as_float(rk[2 * e]) * p.scale, __uint_as_float(rk[2 * e + 1]) * p.scale);
-          v32[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
-        }
-        if (key_ok) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            reinterpret_cast<uint4*>(dkrow + c)[e] = wk[e];
-            reinterpret_cast<uint4*>(dvrow + c)[e] = wv[e];
-          }
-        }
+      bwd_store_dkdv<D>(p, g, tmem_base + lane_base, C::DK_COL, C::DV_COL, half, key, key_ok, n_it > 0);
+    }
+  }
+
+  // ---- teardown ----
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kBwdMma) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kBwdTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// d = 64: a deeper pipeline across steps.  At d = 64 TMEM has columns to spare (S^T 128 + dP^T 128
+// + dV 64 + dK 64 = 384 of 512) and shared memory has room (the K, V, Q, dO tiles are half the
+// size), so dQ gets TMEM columns and a staging buffer of its own, and Q / dO a third ring stage.
+// Then the next step's S^T MMAs are issued right after this step's dV MMAs, and the row warps
+// read out and stage the previous step's dQ between their P and dS passes instead of waiting for
+// this step's dK and dQ MMAs:
+//   MMA warp:   dV_n, S_{n+1}, dK_n, dQ_n (once dQ_{n-1} has been read out), dP_{n+1}
+//   row warps:  P pass n, dQ_{n-1} read-out and staging, dS pass n, (LSE, D) of step n + 1
+// Everything else (roles, passes, masks, the dQ reduce-adds, the dK / dV epilogue) is as in
+// attn_bwd_tc_kernel.
+// ---------------------------------------------------------------------------------------------
+struct Bwd64Cfg {
+  static constexpr int D = 64;
+  static constexpr int TILE_BYTES = BT * 128;  // 128 rows x 64 bf16: one 128-byte swizzle slab
+  static constexpr int NST = 3;                // Q / dO ring stages
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + TILE_BYTES;
+  static constexpr int Q_OFF = V_OFF + TILE_BYTES;
+  static constexpr int DO_OFF = Q_OFF + NST * TILE_BYTES;
+  static constexpr int ST_OFF = DO_OFF + NST * TILE_BYTES;  // dS of a step: two 64-query slabs
+  static constexpr int DQB_OFF = ST_OFF + 2 * TILE_BYTES;   // dQ staging: warp w's 32 x 32 fp32 block at w * 4 KB
+  static constexpr int LD_OFF = DQB_OFF + kBwdRowWarps * 4096;  // -LSE log2 e, then -D, of the step's queries
+  static constexpr int BAR_OFF = LD_OFF + BT * 8;
+  // kv_full, qdo_full[3], qdo_empty[3], s_full, dp_full, p_ready[2], ds_ready[2], dq_full, dq_read,
+  // dq_staged, dqb_empty, ld_ready[2], done
+  static constexpr int NUM_BARS = 20;
+  static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384;
+  static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT, false);
+  static constexpr uint32_t IDESC_KV = idesc_bf16_f32(BT, D, true);
+  static constexpr uint32_t IDESC_Q = idesc_bf16_f32(BT, D, true, true);
+  static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+template <bool PACKED>
+__global__ void __launch_bounds__(kBwdThreads)
+    attn_bwd_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = Bwd64Cfg;
+  constexpr int D = C::D, NST = C::NST;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_s = smem_addr(smem_raw);
+  const uint32_t pad = (1024u - (raw_s & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  const uint32_t sbase = raw_s + pad;
+
+  const uint32_t bar0 = sbase + C::BAR_OFF;
+  const uint32_t bar_kv = bar0;
+  auto bar_qdo = [&](int s) { return bar0 + 8u * (1 + s); };        // Q_i, dO_i of stage s landed
+  auto bar_qdo_empty = [&](int s) { return bar0 + 8u * (4 + s); };  // the MMAs reading stage s complete
+  const uint32_t bar_s = bar0 + 8u * 7;                             // S^T in TMEM
+  const uint32_t bar_dp = bar0 + 8u * 8;                            // dP^T in TMEM
+  auto bar_p = [&](int h) { return bar0 + 8u * (9 + h); };          // P^T of query half h in TMEM (4 warps)
+  auto bar_ds = [&](int h) { return bar0 + 8u * (11 + h); };        // dS^T of half h in TMEM, dS staged
+  const uint32_t bar_dq = bar0 + 8u * 13;                           // dQ in TMEM
+  const uint32_t bar_dq_read = bar0 + 8u * 14;                      // dQ read out of TMEM (8 warps)
+  const uint32_t bar_dq_staged = bar0 + 8u * 15;                    // dQ blocks staged (8 warps)
+  const uint32_t bar_dqb_empty = bar0 + 8u * 16;                    // staged blocks read by their adds
+  auto bar_ld = [&](int h) { return bar0 + 8u * (17 + h); };        // half h's (LSE, D) entries written
+  const uint32_t bar_done = bar0 + 8u * 19;                         // every MMA of the CTA complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  BwdGeom g;
+  if (!bwd_geometry<PACKED>(p, g)) return;
+  const int j = g.j, k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
+  const StepPos first_pos{0, g.i_begin};
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(bar_qdo(s), 1);
+      mbar_init(bar_qdo_empty(s), 1);
+    }
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(bar_p(h), kBwdRowWarps / 2);
+      mbar_init(bar_ds(h), kBwdRowWarps / 2);
+      mbar_init(bar_ld(h), kBwdRowWarps / 2);
+    }
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dq_read, kBwdRowWarps);
+    mbar_init(bar_dq_staged, kBwdRowWarps);
+    mbar_init(bar_dqb_empty, 1);
+    mbar_init(bar_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == kBwdMma) {
+    tmem_alloc(smem_addr(tmem_slot), kBwdTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kBwdProducer && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dq);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_BWD << 8) | site));
+  };
+
+  if (warp == kBwdProducer) {
+    // =================== TMA producer (whole warp, one elected lane issues) ===================
+    bool ok = true;
+    mbar_arrive_expect_tx_elect(bar_kv, 2 * C::TILE_BYTES);
+    tma_load_3d_elect(sbase + C::K_OFF, &tm_k, bar_kv, 0, g.krow0 + k0, g.kplane);
+    tma_load_3d_elect(sbase + C::V_OFF, &tm_v, bar_kv, 0, g.krow0 + k0, g.kplane);
+    int issued = 0, st = 0;
+    uint32_t par = 0;  // step it uses stage st = it % NST for the (it / NST)-th time; par = that count & 1
+    StepPos pos = first_pos;
+    for (int it = 0; it < n_it; ++it, pos = pos.next(g)) {
+      const int qp = qplane0 + pos.t, qy = qrow0 + pos.i * BT;
+      // the stage's previous use (step it - NST) must be complete
+      if (it >= NST && !(ok = wait_all(bar_qdo_empty(st), par ^ 1u, B_QDO_EMPTY))) break;
+      mbar_arrive_expect_tx_elect(bar_qdo(st), 2 * C::TILE_BYTES);
+      tma_load_3d_elect(sbase + C::Q_OFF + st * C::TILE_BYTES, &tm_q, bar_qdo(st), 0, qy, qp);
+      tma_load_3d_elect(sbase + C::DO_OFF + st * C::TILE_BYTES, &tm_do, bar_qdo(st), 0, qy, qp);
+      ++issued;
+      if (++st == NST) {
+        st = 0;
+        par ^= 1u;
       }
+    }
+    // drain: every load issued must have landed before the CTA can exit
+    for (int it = max(0, issued - NST); it < issued; ++it)
+      mbar_wait(bar_qdo(it % NST), (uint32_t)(it / NST) & 1u, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
+    mbar_wait(bar_kv, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
+  } else if (warp == kBwdMma) {
+    // =================== MMA issue (whole warp, one elected lane) ===================
+    const uint64_t k_kmaj = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);                 // A of S^T
+    const uint64_t v_kmaj = smem_desc_sw128(sbase + C::V_OFF, 16, 1024);                 // A of dP^T
+    const uint64_t k_nmaj = smem_desc_sw128(sbase + C::K_OFF, C::TILE_BYTES, 1024);      // B of dQ
+    const uint64_t st_mmaj = smem_desc_sw128(sbase + C::ST_OFF, C::TILE_BYTES, 1024);    // A of dQ
+    auto kmaj = [&](int s0, int st, int kk) {  // K-major tile of stage st, K step kk (16 of the 64 dims)
+      return smem_desc_sw128(sbase + s0 + st * C::TILE_BYTES, 16, 1024) + (uint64_t)((kk * 32) >> 4);
+    };
+    auto nmaj = [&](int s0, int st) { return smem_desc_sw128(sbase + s0 + st * C::TILE_BYTES, C::TILE_BYTES, 1024); };
+    auto rows16_off = [](int kk) { return (uint64_t)((kk * 16 * 128) >> 4); };  // 16 rows of 128 bytes
+    auto pcol = [](int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); };  // P^T / dS^T column
+    // S^T (into S_COL, whose P^T the dV MMAs issued before have read) and dP^T (into DP_COL, whose
+    // dS^T the dK MMAs issued before have read) of the step in stage st
+    auto issue_s = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(tmem_base + C::S_COL, k_kmaj + (uint64_t)((kk * 32) >> 4), kmaj(C::Q_OFF, st, kk), C::IDESC_S,
+                     kk > 0 ? 1u : 0u);
+      mma_commit_elect(bar_s);
+    };
+    auto issue_dp = [&](int st) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss_elect(tmem_base + C::DP_COL, v_kmaj + (uint64_t)((kk * 32) >> 4), kmaj(C::DO_OFF, st, kk),
+                     C::IDESC_S, kk > 0 ? 1u : 0u);
+      mma_commit_elect(bar_dp);
+    };
+    bool ok = wait_all(bar_kv, 0, B_KV);
+    if (ok && n_it > 0 && (ok = wait_all(bar_qdo(0), 0, B_QDO))) {
+      tc_fence_after_sync();
+      issue_s(0);
+      issue_dp(0);
+    }
+    int st = 0;
+    uint32_t par = 0;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const uint32_t ph = (uint32_t)it & 1u;
+      const int st1 = st + 1 == NST ? 0 : st + 1;           // stage of step it + 1
+      const uint32_t par1 = st1 == 0 ? par ^ 1u : par;
+      const bool more = it + 1 < n_it;
+      // dV += P^T dO_it, half by half as the rows write P^T
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = wait_all(bar_p(h), ph, B_DS))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), nmaj(C::DO_OFF, st) + rows16_off(kk),
+                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!ok) break;
+      // the next step's S^T, so that the rows' next P pass need not wait for this step's dK / dQ
+      if (more) {
+        if (!(ok = wait_all(bar_qdo(st1), par1, B_QDO))) break;
+        tc_fence_after_sync();
+        issue_s(st1);
+      }
+      // dK += dS^T Q_it
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!(ok = wait_all(bar_ds(h), ph, B_DS))) break;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+          mma_ts_elect(tmem_base + C::DK_COL, tmem_base + C::DP_COL + pcol(kk), nmaj(C::Q_OFF, st) + rows16_off(kk),
+                       C::IDESC_KV, (it > 0 || kk > 0) ? 1u : 0u);
+      }
+      if (!ok) break;
+      // dQ_it = dS K_j into DQ_COL, once the rows have read dQ_{it-1} out of it
+      if (it > 0 && !(ok = wait_all(bar_dq_read, ph ^ 1u, B_DQ_READ))) break;
+      tc_fence_after_sync();
+#pragma unroll
+      for (int kk = 0; kk < BT / 16; ++kk)
+        mma_ss_elect(tmem_base + C::DQ_COL, st_mmaj + rows16_off(kk), k_nmaj + rows16_off(kk), C::IDESC_Q,
+                     kk > 0 ? 1u : 0u);
+      mma_commit_elect(bar_dq);
+      mma_commit_elect(bar_qdo_empty(st));  // stage st free once this step's MMAs are complete
+      if (more) issue_dp(st1);
+      st = st1;
+      par = par1;
+    }
+    // every MMA complete (for the dK / dV epilogue and before TMEM is freed)
+    mma_commit_elect(bar_done);
+    mbar_wait(bar_done, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
+  }
+  else if (warp == kBwdReducer) {
+    // ============ dQ reducer (whole warp, one lane issues): TMA reduce-adds of the blocks ============
+    // Warp w's block of step it is added into rows q0 + 32 (w % 4) .. + 31 (clipped at Nq; skipped
+    // when wholly past it) and columns 32 (w / 4) of the fp32 accumulator.
+    bool ok = true;
+    StepPos pos = first_pos;
+    for (int it = 0; ok && it < n_it; ++it, pos = pos.next(g)) {
+      const int q0 = pos.i * BT, qp = qplane0 + pos.t, qy = qrow0 + q0;
+      if (!(ok = wait_all(bar_dq_staged, (uint32_t)it & 1u, B_DQ_STAGED))) break;
+      if (lane == 0) {
+        for (int w = 0; w < kBwdRowWarps; ++w) {
+          if (q0 + (w & 3) * 32 >= Nq) continue;
+          tma_reduce_add_3d(&tm_dq, sbase + C::DQB_OFF + w * 4096, (w >> 2) * 32, qy + (w & 3) * 32, qp);
+        }
+        bulk_commit_group();
+        bulk_wait_read<0>();  // the buffer may be refilled once its blocks have been read
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dqb_empty);
+    }
+    if (lane == 0) bulk_wait_all();  // every add performed before the CTA exits
+    __syncwarp();
+  } else {
+    // =================== rows: warps 0-7, thread t = TMEM lane t % 128 ===================
+    const int tt = threadIdx.x & (BT - 1);  // key row of the tile (the dQ tile: query row)
+    const int half = warp >> 2;             // queries [64 half, 64 half + 64); dQ / dK / dV columns likewise
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tl = tmem_base + lane_base;
+    const int key = k0 + tt;
+    const bool key_ok = key < Nk;
+    uint8_t* st_row = smem + C::ST_OFF + half * C::TILE_BYTES + tt * 128;  // key row in slab `half`
+    const float4* nl4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
+    const float4* nd4 = reinterpret_cast<const float4*>(smem + C::LD_OFF + BT * 4);
+    // threads 0-63 of each half own the (LSE, D) entries of that half's queries
+    const int ld_q = 64 * half + tt;
+    float* nl_mine = reinterpret_cast<float*>(smem + C::LD_OFF) + ld_q;
+    float* nd_mine = reinterpret_cast<float*>(smem + C::LD_OFF + BT * 4) + ld_q;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    auto load_ld = [&](int step, StepPos sp, float& l, float& dd) {
+      l = -INFINITY;
+      dd = 0.f;
+      const int q = sp.i * BT + ld_q;
+      if (tt < 64 && step < n_it && q < Nq) {
+        const int64_t row = g.lbase + (int64_t)q * g.lq + (int64_t)sp.t * g.lt;
+        l = p.lse[row];
+        dd = p.dsum[row];
+      }
+    };
+    // -LSE log2 e and -D of a step's queries; a row past the end or with no visible key gets -inf,
+    // so that exp2(s scale log2 e - inf) = 0 needs no test
+    auto write_ld = [&](float l, float dd) {
+      if (tt < 64) {
+        *nl_mine = l == -INFINITY ? -INFINITY : -l * kLog2e;
+        *nd_mine = -dd;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ld(half));
+    };
+    // dQ of step m out of TMEM (so that dQ of step m + 1 may follow), then staged as this warp's
+    // 32 x 32 block (swizzled like the map) once the adds of step m - 1 have read the buffer
+    auto drain_dq = [&](int m) {
+      if (!wait_all(bar_dq, (uint32_t)m & 1u, B_DQ)) return false;
+      tc_fence_after_sync();
+      uint32_t r[32];
+      tmem_ld32(tl + C::DQ_COL + half * 32, r);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_read);
+      if (m > 0 && !wait_all(bar_dqb_empty, (uint32_t)(m - 1) & 1u, B_DQ_STAGED)) return false;
+      uint8_t* brow = smem + C::DQB_OFF + warp * 4096 + lane * 128;
+#pragma unroll
+      for (int q4 = 0; q4 < 8; ++q4)
+        *reinterpret_cast<float4*>(brow + ((q4 ^ (lane & 7)) * 16)) =
+            make_float4(__uint_as_float(r[4 * q4]) * p.scale, __uint_as_float(r[4 * q4 + 1]) * p.scale,
+                        __uint_as_float(r[4 * q4 + 2]) * p.scale, __uint_as_float(r[4 * q4 + 3]) * p.scale);
+      fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_dq_staged);
+      return true;
+    };
+    // the entries of step it are written during step it - 1, after every warp of the half is past
+    // its dS pass (the last reader of the previous entries); their loads a step before that
+    StepPos lpos = first_pos;
+    float next_l, next_d;
+    load_ld(0, lpos, next_l, next_d);
+    write_ld(next_l, next_d);
+    lpos = lpos.next(g);
+    load_ld(1, lpos, next_l, next_d);
+    bool ok = true;
+    StepPos pos = first_pos;
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int i = pos.i, q0 = i * BT;
+      const uint32_t ph = (uint32_t)it & 1u;
+      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || i > j);
+      if (!(ok = wait_all(bar_s, ph, B_S))) break;
+      if (!(ok = wait_all(bar_ld(half), ph, B_LD))) break;
+      tc_fence_after_sync();
+      // P^T of this warp's 64 queries over the first 32 of its S^T columns (read by it alone)
+      const uint32_t sc = tl + C::S_COL + 64 * half;
+      const uint32_t dc = tl + C::DP_COL + 64 * half;
+      uint64_t pp[32];
+      {
+        uint32_t sr[64], pw[32];
+        tmem_ld32x2(sc, sc + 32, sr);
+        if (full)
+          bwd_p<false>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, true, false, pp, pw);
+        else
+          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
+        tmem_st32(sc, pw);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p(half));
+      // the previous step's dQ (its MMA ran during this P pass); it also frees the dS buffer
+      if (it > 0 && !(ok = drain_dq(it - 1))) break;
+      if (!(ok = wait_all(bar_dp, ph, B_DP))) break;
+      tc_fence_after_sync();
+      {
+        uint32_t dr[64], dw[32];
+        tmem_ld32x2(dc, dc + 32, dr);
+        bwd_ds(dr, nd4 + 16 * half, pp, dw);
+        tmem_st32(dc, dw);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8)
+          *reinterpret_cast<uint4*>(st_row + ((q8 ^ (tt & 7)) * 16)) =
+              make_uint4(dw[4 * q8], dw[4 * q8 + 1], dw[4 * q8 + 2], dw[4 * q8 + 3]);
+      }
+      tmem_st_wait();
+      tc_fence_before_sync();
+      fence_proxy_async_smem();  // the staged dS is read by the tensor core (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_ds(half));
+      pos = pos.next(g);
+      if (!(ok = wait_all(bar_ds(half), ph, B_DS))) break;
+      write_ld(next_l, next_d);
+      lpos = lpos.next(g);
+      load_ld(it + 2, lpos, next_l, next_d);
+    }
+    if (ok && n_it > 0) ok = drain_dq(n_it - 1);
+    if (ok && n_it > 0) ok = wait_all(bar_done, 0, B_DONE);
+    if (ok) {
+      tc_fence_after_sync();
+      bwd_store_dkdv<D>(p, g, tl, C::DK_COL, C::DV_COL, half, key, key_ok, n_it > 0);
     }
   }
 
@@ -647,14 +1054,24 @@ cudaError_t launch_bwd_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BwdCfg<D>::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   const unsigned grid = (unsigned)p.nkt * (unsigned)p.BHkv;
-  attn_bwd_tc_kernel<D, PACKED><<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
+  if constexpr (D == 64) {
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(attn_bwd_tc64_kernel<PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Bwd64Cfg::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    attn_bwd_tc64_kernel<PACKED><<<grid, kBwdThreads, Bwd64Cfg::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
+  } else {
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               BwdCfg<D>::SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+    attn_bwd_tc_kernel<D, PACKED><<<grid, kBwdThreads, BwdCfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, mdo, mdq, p);
+  }
   return cudaGetLastError();
 }
 
