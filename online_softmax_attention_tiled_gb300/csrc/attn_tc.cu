@@ -599,7 +599,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
 constexpr int kMaxDevices = 64;
 
 // Persistent grid: one CTA per SM (the kernel holds an SM's TMEM and most of its shared
-// memory), never more CTAs than work items.
+// memory), never more CTAs than work items.  Without the causal mask (and without packed
+// sequences) the items weigh alike, so the grid is the fewest CTAs that keep the number of rounds:
+// every CTA then works through the same number of items, and the memory-bound cases (grouped
+// decode) spread the same bytes over fewer, busier CTAs instead of a last round half empty.
 template <int D, bool PACKED>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                      cudaStream_t s) {
@@ -617,7 +620,12 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     attr_set[dev] = true;
   }
   const long long total = (long long)p.num_qblocks * p.BH;
-  const unsigned grid = (unsigned)(total < sm_count[dev] ? total : sm_count[dev]);
+  long long g = total < sm_count[dev] ? total : sm_count[dev];
+  if (!PACKED && !p.causal) {
+    const long long rounds = (total + g - 1) / g;
+    g = (total + rounds - 1) / rounds;
+  }
+  const unsigned grid = (unsigned)g;
   attn_fwd_tc_kernel<D, PACKED><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
