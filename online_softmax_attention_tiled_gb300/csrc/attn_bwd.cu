@@ -7,7 +7,7 @@
 // and how", "Where this is heading: FA2": on backward, recompute the scores from the cached
 // softmax statistics).  With P = exp(scale S - LSE) (S = Q K^T, masked keys 0):
 //   dV = P^T dO,   dP = dO V^T,   D = rowsum(dO o O),   dS = P o (dP - D),
-//   dQ = scale dS K,   dK = scale dS^T Q.
+//   dQ = scale dS K,   dK = scale dS^T Q    (the kernels carry scale dS, formed with one FMA).
 //
 // Three launches: a pre-pass (D per query row; the fp32 dQ accumulator zeroed), the main
 // kernel, and a post-pass (dQ to bf16).  Main kernel, key-tile outer: one CTA per (b, h,
@@ -71,7 +71,7 @@ struct BwdCfg {
   // A operand of dQ = dS K read M-major
   static constexpr int ST_OFF = DO_OFF + 2 * TILE_BYTES;
   static constexpr int ST_BYTES = 2 * SLAB_BYTES;
-  // -LSE log2 e of the step's 128 query rows, then -D (-inf / 0 past the end)
+  // -LSE log2 e of the step's 128 query rows, then -D scale (-inf / 0 past the end)
   static constexpr int LD_OFF = ST_OFF + ST_BYTES;
   static constexpr int BAR_OFF = LD_OFF + BT * 8;
   // kv_full, q_full[2], q_empty[2], s_full[2], dp_full[2], ds_ready[2], dq_full, dq_read, done,
@@ -174,16 +174,17 @@ __device__ __forceinline__ void bwd_p(const uint32_t (&sr)[64], const float4* nl
     }
   }
 }
-// dS^T = P^T (dP^T - D) for the same 64 queries: dr the fp32 dP^T columns, nd the negated D of
-// those queries, pp the fp32 P^T of bwd_p; dw the bf16 pairs.
-__device__ __forceinline__ void bwd_ds(const uint32_t (&dr)[64], const float4* nd, const uint64_t (&pp)[32],
+// scale dS^T = P^T (dP^T scale - D scale) for the same 64 queries, one FMA per pair: dr the fp32 dP^T
+// columns, nd the negated D scale of those queries, s2x2 the scale twice, pp the fp32 P^T of bwd_p;
+// dw the bf16 pairs.  With the scale inside dS, dQ = dS K and dK = dS^T Q need no further scaling.
+__device__ __forceinline__ void bwd_ds(const uint32_t (&dr)[64], const float4* nd, uint64_t s2x2, const uint64_t (&pp)[32],
                                        uint32_t (&dw)[32]) {
 #pragma unroll
   for (int e = 0; e < 64; e += 4) {
     const ulonglong2 ndv = *reinterpret_cast<const ulonglong2*>(nd + e / 4);
 #pragma unroll
     for (int h = 0; h < 4; h += 2) {
-      const uint64_t dpd = f2_add(f2_pack(__uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1])),
+      const uint64_t dpd = f2_fma(f2_pack(__uint_as_float(dr[e + h]), __uint_as_float(dr[e + h + 1])), s2x2,
                                   h ? ndv.y : ndv.x);
       const uint64_t ds = f2_mul(pp[(e + h) / 2], dpd);
       float d0, d1;
@@ -270,7 +271,7 @@ struct StepPos {
   }
 };
 
-// dK (times scale) and dV of key row `key` as bf16, columns [half d/2, half d/2 + d/2), from the
+// dK and dV of key row `key` as bf16, columns [half d/2, half d/2 + d/2), from the
 // accumulators at TMEM columns dk_col and dv_col of this thread's lane (tl = TMEM base + the warp's
 // lane quarter); zeros when the CTA had no step; no store for a key past the end.
 template <int D>
@@ -293,7 +294,7 @@ __device__ __forceinline__ void bwd_store_dkdv(const BwdParams& p, const BwdGeom
     uint32_t* v32 = reinterpret_cast<uint32_t*>(wv);
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      k32[e] = pack_bf16x2(__uint_as_float(rk[2 * e]) * p.scale, __uint_as_float(rk[2 * e + 1]) * p.scale);
+      k32[e] = pack_bf16x2(__uint_as_float(rk[2 * e]), __uint_as_float(rk[2 * e + 1]));
       v32[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
     }
     if (key_ok) {
@@ -547,6 +548,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     float* nd_mine = reinterpret_cast<float*>(smem + C::LD_OFF + BT * 4) + ld_q;
     constexpr int DQ_CHUNKS = C::DQ_CHUNKS;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t sl2 = f2_pack(p.scale, p.scale);
     // (LSE, D) of query q0 + ld_q of step `step`, as loaded values (converted when stored)
     auto load_ld = [&](int step, StepPos sp, float& l, float& dd) {
       l = -INFINITY;
@@ -569,13 +571,13 @@ __global__ void __launch_bounds__(kBwdThreads)
       // every (key, query) pair of the step visible and inside the tensors
       const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || i > j);
       if (!(ok = wait_all(bar_s(half), ph, B_S))) break;
-      // -LSE log2 e and -D of query q0 + ld_q; a row past the end or with no visible key gets
+      // -LSE log2 e and -D scale of query q0 + ld_q; a row past the end or with no visible key gets
       // -inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
       // every row warp is past the previous step's reads of the (LSE, D) block: this warp waited
       // for that step's dQ MMA, issued only after all eight warps had arrived on ds_ready
       if (tt < 64) {
         *nl_mine = next_l == -INFINITY ? -INFINITY : -next_l * kLog2e;
-        *nd_mine = -next_d;
+        *nd_mine = -next_d * p.scale;
       }
       if (lane == 0) mbar_arrive(bar_ld(half));
       if (!(ok = wait_all(bar_ld(half), ph, B_LD))) break;
@@ -603,7 +605,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       {
         uint32_t dr[64], dw[32];
         tmem_ld32x2(dc, dc + 32, dr);
-        bwd_ds(dr, nd4 + 16 * half, pp, dw);
+        bwd_ds(dr, nd4 + 16 * half, sl2, pp, dw);
         tmem_st32(dc, dw);
         // dS^T row `key`, queries 64 half .. +63: the 128-byte row of slab `half`, 16-byte chunk q
         // stored at position q ^ (row % 8) (128-byte swizzle)
@@ -619,7 +621,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       if (lane == 0) mbar_arrive(bar_ds(half));
       pos = next_pos(pos);  // the next step's (head, tile); its (LSE, D) load is issued now
       load_ld(it + 1, pos, next_l, next_d);
-      // dQ_i = scale dS K_j: thread t holds query row q0 + t % 128.  The warp's columns leave
+      // dQ_i = (scale dS) K_j: thread t holds query row q0 + t % 128.  The warp's columns leave
       // TMEM first (so the next step's dP MMA may overwrite them); then per 32 columns the warp
       // stages its 32 x 32 block (swizzled like the map) in its own staging rows, which the dQ
       // MMA has finished reading, and one lane adds it into the accumulator with a TMA
@@ -627,9 +629,20 @@ __global__ void __launch_bounds__(kBwdThreads)
       if (!(ok = wait_all(bar_dq, ph, B_DQ))) break;
       tc_fence_after_sync();
       uint32_t r[DQ_CHUNKS][32];
+      if constexpr (DQ_CHUNKS == 2) {
+        uint32_t r64[64];
+        const uint32_t a0 = tmem_base + lane_base + C::DP_COL + half * 64;
+        tmem_ld32x2(a0, a0 + 32, r64);
 #pragma unroll
-      for (int m = 0; m < DQ_CHUNKS; ++m)
-        tmem_ld32(tmem_base + lane_base + C::DP_COL + (half * DQ_CHUNKS + m) * 32, r[m]);
+        for (int e = 0; e < 32; ++e) {
+          r[0][e] = r64[e];
+          r[1][e] = r64[32 + e];
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < DQ_CHUNKS; ++m)
+          tmem_ld32(tmem_base + lane_base + C::DP_COL + (half * DQ_CHUNKS + m) * 32, r[m]);
+      }
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_read);
@@ -640,8 +653,8 @@ __global__ void __launch_bounds__(kBwdThreads)
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
           *reinterpret_cast<float4*>(brow + ((q4 ^ (lane & 7)) * 16)) =
-              make_float4(__uint_as_float(r[m][4 * q4]) * p.scale, __uint_as_float(r[m][4 * q4 + 1]) * p.scale,
-                          __uint_as_float(r[m][4 * q4 + 2]) * p.scale, __uint_as_float(r[m][4 * q4 + 3]) * p.scale);
+              make_float4(__uint_as_float(r[m][4 * q4]), __uint_as_float(r[m][4 * q4 + 1]),
+                          __uint_as_float(r[m][4 * q4 + 2]), __uint_as_float(r[m][4 * q4 + 3]));
       }
       fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
       __syncwarp();
@@ -686,7 +699,7 @@ struct Bwd64Cfg {
   static constexpr int DO_OFF = Q_OFF + NST * TILE_BYTES;
   static constexpr int ST_OFF = DO_OFF + NST * TILE_BYTES;  // dS of a step: two 64-query slabs
   static constexpr int DQB_OFF = ST_OFF + 2 * TILE_BYTES;   // dQ staging: warp w's 32 x 32 fp32 block at w * 4 KB
-  static constexpr int LD_OFF = DQB_OFF + kBwdRowWarps * 4096;  // -LSE log2 e, then -D, of the step's queries
+  static constexpr int LD_OFF = DQB_OFF + kBwdRowWarps * 4096;  // -LSE log2 e, then -D scale, of the step's queries
   static constexpr int BAR_OFF = LD_OFF + BT * 8;
   // kv_full, qdo_full[3], qdo_empty[3], s_full, dp_full, p_ready[2], ds_ready[2], dq_full, dq_read,
   // dq_staged, dqb_empty, ld_ready[2], done
@@ -926,6 +939,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     float* nl_mine = reinterpret_cast<float*>(smem + C::LD_OFF) + ld_q;
     float* nd_mine = reinterpret_cast<float*>(smem + C::LD_OFF + BT * 4) + ld_q;
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t sl2 = f2_pack(p.scale, p.scale);
     auto load_ld = [&](int step, StepPos sp, float& l, float& dd) {
       l = -INFINITY;
       dd = 0.f;
@@ -936,12 +950,12 @@ __global__ void __launch_bounds__(kBwdThreads)
         dd = p.dsum[row];
       }
     };
-    // -LSE log2 e and -D of a step's queries; a row past the end or with no visible key gets -inf,
+    // -LSE log2 e and -D scale of a step's queries; a row past the end or with no visible key gets -inf,
     // so that exp2(s scale log2 e - inf) = 0 needs no test
     auto write_ld = [&](float l, float dd) {
       if (tt < 64) {
         *nl_mine = l == -INFINITY ? -INFINITY : -l * kLog2e;
-        *nd_mine = -dd;
+        *nd_mine = -dd * p.scale;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ld(half));
@@ -961,8 +975,8 @@ __global__ void __launch_bounds__(kBwdThreads)
 #pragma unroll
       for (int q4 = 0; q4 < 8; ++q4)
         *reinterpret_cast<float4*>(brow + ((q4 ^ (lane & 7)) * 16)) =
-            make_float4(__uint_as_float(r[4 * q4]) * p.scale, __uint_as_float(r[4 * q4 + 1]) * p.scale,
-                        __uint_as_float(r[4 * q4 + 2]) * p.scale, __uint_as_float(r[4 * q4 + 3]) * p.scale);
+            make_float4(__uint_as_float(r[4 * q4]), __uint_as_float(r[4 * q4 + 1]),
+                        __uint_as_float(r[4 * q4 + 2]), __uint_as_float(r[4 * q4 + 3]));
       fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_staged);
@@ -1009,7 +1023,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       {
         uint32_t dr[64], dw[32];
         tmem_ld32x2(dc, dc + 32, dr);
-        bwd_ds(dr, nd4 + 16 * half, pp, dw);
+        bwd_ds(dr, nd4 + 16 * half, sl2, pp, dw);
         tmem_st32(dc, dw);
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8)
