@@ -7,6 +7,8 @@ Cases (inputs seeded as in the benchmark):
   attn_noncausal   non-causal attention fwd bf16, B=4 H=16 N=4096 d=64
   attn_bwd_causal  causal attention bwd bf16, B=1 H=32 N=8192 d=128 (O and LSE from the forward;
                    ~650 MiB on the device)
+  attn_varlen      causal attention fwd bf16 over 16 packed sequences of 1024-8192 tokens (96634 in
+                   all), H=32 H_kv=8 d=128 (~1 GiB on the device)
   softmax          row softmax + LSE fp32 [4096, 32768] (1 GiB)
   decode           split-KV decode bf16, B (default 4) x H=32, Nk=32768, d=128, 64 chunks
                    (--batch 32 is the full 17 GB benchmark shape)
@@ -44,6 +46,13 @@ def make_case(name, dev, batch):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         ws = torch.empty(oa.attn_bwd_workspace_bytes(1, 32, 8192, 128), dtype=torch.uint8, device=dev)
         return lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws)
+    if name == "attn_varlen":
+        lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
+        q, k, v, cq, ck = si.varlen_inputs(lens, lens, 32, 8, 128, torch.bfloat16, seed=0, device=dev)
+        cq, ck = cq.to(dev), ck.to(dev)
+        mx = int(max(lens))
+        o, lse = torch.empty_like(q), torch.empty((q.shape[0], 32), device=dev)
+        return lambda: oa.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse)
     if name == "softmax":
         x, *_ = si.softmax_input(4096, 32768, seed=0)
         x = x.to(dev)
