@@ -10,9 +10,11 @@
 //   dQ = scale dS K,   dK = scale dS^T Q    (the kernels carry scale dS, formed with one FMA).
 //
 // Three launches: a pre-pass (D per query row; the fp32 dQ accumulator zeroed), the main
-// kernel, and a post-pass (dQ to bf16).  Main kernel, key-tile outer: one CTA per (b, h,
-// 128 keys); K_j and V_j stay in shared memory while the query tiles i (causal: i >= j)
-// stream through a 2-stage TMA ring with their dO tiles.  Per query tile:
+// kernel (attn_bwd_tc_kernel at d = 128, described here; attn_bwd_tc64_kernel at d = 64, the
+// same roles pipelined one step deeper, described at its definition), and a post-pass (dQ to
+// bf16).  Main kernel, key-tile outer: one CTA per (b, h, 128 keys); K_j and V_j stay in shared
+// memory while the query tiles i (causal: i >= j) stream through a 2-stage TMA ring with their
+// dO tiles.  Per query tile:
 //   S^T  = K_j Q_i^T,   dP^T = V_j dO_i^T           (SS MMAs into TMEM, lanes = keys, N = 128)
 //   P^T  elementwise as soon as S^T is in, while dP^T computes (P^T as bf16 back into TMEM)
 //   dV_j += P^T dO_i                                 (TS MMA: A from TMEM), while the rows
@@ -312,6 +314,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  static_assert(D == 128, "d = 64 runs attn_bwd_tc64_kernel");
   using C = BwdCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_s = smem_addr(smem_raw);
@@ -628,21 +631,9 @@ __global__ void __launch_bounds__(kBwdThreads)
       // reduce-add (rows past Nq are clipped by the map; a block wholly past the end is skipped).
       if (!(ok = wait_all(bar_dq, ph, B_DQ))) break;
       tc_fence_after_sync();
-      uint32_t r[DQ_CHUNKS][32];
-      if constexpr (DQ_CHUNKS == 2) {
-        uint32_t r64[64];
-        const uint32_t a0 = tmem_base + lane_base + C::DP_COL + half * 64;
-        tmem_ld32x2(a0, a0 + 32, r64);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          r[0][e] = r64[e];
-          r[1][e] = r64[32 + e];
-        }
-      } else {
-#pragma unroll
-        for (int m = 0; m < DQ_CHUNKS; ++m)
-          tmem_ld32(tmem_base + lane_base + C::DP_COL + (half * DQ_CHUNKS + m) * 32, r[m]);
-      }
+      uint32_t r[DQ_CHUNKS * 32];  // this warp's 64 dQ columns, one wait
+      const uint32_t a0 = tmem_base + lane_base + C::DP_COL + half * 64;
+      tmem_ld32x2(a0, a0 + 32, r);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dq_read);
@@ -653,8 +644,8 @@ __global__ void __launch_bounds__(kBwdThreads)
 #pragma unroll
         for (int q4 = 0; q4 < 8; ++q4)
           *reinterpret_cast<float4*>(brow + ((q4 ^ (lane & 7)) * 16)) =
-              make_float4(__uint_as_float(r[m][4 * q4]), __uint_as_float(r[m][4 * q4 + 1]),
-                          __uint_as_float(r[m][4 * q4 + 2]), __uint_as_float(r[m][4 * q4 + 3]));
+              make_float4(__uint_as_float(r[32 * m + 4 * q4]), __uint_as_float(r[32 * m + 4 * q4 + 1]),
+                          __uint_as_float(r[32 * m + 4 * q4 + 2]), __uint_as_float(r[32 * m + 4 * q4 + 3]));
       }
       fence_proxy_async_smem();  // the blocks are read by the reducer warp's TMA (async proxy)
       __syncwarp();
