@@ -12,6 +12,8 @@ Cases (inputs seeded as in the benchmark):
   softmax          row softmax + LSE fp32 [4096, 32768] (1 GiB)
   decode           split-KV decode bf16, B (default 4) x H=32, Nk=32768, d=128, 64 chunks
                    (--batch 32 is the full 17 GB benchmark shape)
+  decode_gqa       decode bf16 over a grouped cache, B (default 4) x H=32, H_kv=8, Nk=32768, d=128,
+                   each group's queries as rows of the tensor-core forward (--batch 32: 4.3 GB)
 Prints the mean CUDA-event time per launch.
 """
 from __future__ import annotations
@@ -60,6 +62,12 @@ def make_case(name, dev, batch):
         return lambda: oa.softmax_rows(x, y=y, lse=lse)
     if name == "decode":
         q, k, v = si.attn_inputs(batch, 32, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+        kv = si.decode_kv_len(batch, 32768, seed=0).to(dev)
+        o, lse = torch.empty_like(q), torch.empty((batch, 32, 1), device=dev)
+        ws = torch.empty(oa.splitkv_workspace_bytes(batch, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+        return lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kv, out=o, lse=lse, workspace=ws)
+    if name == "decode_gqa":
+        q, k, v = si.attn_inputs_gqa(batch, 32, 8, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
         kv = si.decode_kv_len(batch, 32768, seed=0).to(dev)
         o, lse = torch.empty_like(q), torch.empty((batch, 32, 1), device=dev)
         ws = torch.empty(oa.splitkv_workspace_bytes(batch, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
