@@ -204,7 +204,6 @@ oa_status oa_attn_fwd_host(const void* q_host, const void* k_host, const void* v
                            oa_stream_t stream);
 
 /*
- * The fp32 SIMT attention forward with explicit tile sizes/*
  * The fp32 SIMT attention forward with explicit tile sizes: Br query rows
  * per CTA and Bc keys per step of the online recurrence (1 <= Br, Bc <= 64).
  * Same contract as oa_attn_fwd with dt = OA_F32; the result does not
