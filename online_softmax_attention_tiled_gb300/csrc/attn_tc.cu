@@ -126,8 +126,9 @@ struct Item {
 
 // Items are numbered heaviest first (for causal: the last query blocks); item idx covers
 // query block num_qblocks - 1 - idx / BH of (sequence, head) idx % BH.  Query head h reads
-// key/value head h / group.
-template <int D, bool PACKED>
+// key/value head h / group.  SPLIT (at most 128 query rows, no mask): both query-tile slots hold
+// the same rows, slot 0 takes the even key tiles and slot 1 the odd ones.
+template <int D, bool PACKED, bool SPLIT = false>
 __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   Item it;
   const int qb = p.num_qblocks - 1 - idx / p.BH;
@@ -164,15 +165,26 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
     it.lb = (int64_t)sh * p.Nq;
   }
   const int nk_tiles = (it.kvl + BN - 1) / BN;
+  if constexpr (SPLIT) {
+    const bool any = it.q0 < it.nq;
+    it.n_kv[0] = any ? (nk_tiles + 1) / 2 : 0;
+    it.n_kv[1] = any ? nk_tiles / 2 : 0;
+  } else {
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int r0 = it.q0 + i * BM;
-    it.n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
-    if (r0 >= it.nq) it.n_kv[i] = 0;  // query tile entirely past the end
+    for (int i = 0; i < 2; ++i) {
+      const int r0 = it.q0 + i * BM;
+      it.n_kv[i] = p.causal ? min(nk_tiles, r0 / BN + 1) : nk_tiles;
+      if (r0 >= it.nq) it.n_kv[i] = 0;  // query tile entirely past the end
+    }
   }
   it.n_all = max(it.n_kv[0], it.n_kv[1]);
   return it;
 }
+
+// Key tiles an item loads (K_0, V_0, K_1, V_1, ...): each once, shared by both slots, or (SPLIT)
+// split between them.
+template <bool SPLIT>
+__device__ __forceinline__ int n_loads_of(const Item& it) { return SPLIT ? it.n_kv[0] + it.n_kv[1] : it.n_all; }
 
 // The k-th item of this CTA: round k of the persistent grid takes items [k G, k G + G), in
 // CTA order on even rounds and in reverse on odd ones, so the heavy and light ends of the
@@ -186,7 +198,7 @@ __device__ __forceinline__ int item_of_round(int k, int total) {
 // No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
 // and the hint made ptxas spill more on this kernel.  PACKED: token-major packed sequences
 // (a separate instance, so the dense layout pays nothing for them).
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool SPLIT>
 __global__ void __launch_bounds__(Cfg<D>::THREADS)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -209,6 +221,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
   auto bar_sfree = [&](int i) { return bar0 + 8u * (8 + 2 * C::SLOTS + i); };  // S_i read by its group
   const uint32_t bar_qempty = bar0 + 8u * (10 + 2 * C::SLOTS);               // Q read by the last S MMAs
+  static_assert(!SPLIT || (D == 128 && !PACKED), "the split mode serves d = 128, dense layout");
+  // SPLIT: Q tile 1's buffer (never loaded) holds group 1's (m, l) per row and two barriers:
+  // xch (group 1's O_1, m, l ready; 4 warps) and xdone (group 0 has read them; 4 warps)
+  float2* xch_ml = reinterpret_cast<float2*>(smem + C::Q_OFF + C::TILE_BYTES);
+  const uint32_t bar_xch = sbase + C::Q_OFF + C::TILE_BYTES + BM * 8;
+  const uint32_t bar_xdone = bar_xch + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -230,6 +248,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     }
     mbar_init(bar_drain, C::MMA_WARPS);
     mbar_init(bar_qempty, C::MMA_WARPS);
+    if constexpr (SPLIT) {
+      mbar_init(bar_xch, 4);
+      mbar_init(bar_xdone, 4);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -258,17 +280,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
       const int idx = item_of_round(k, total);
       if (idx < 0) continue;
-      const Item it = item_at<D, PACKED>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT>(p, idx);
       if (it.n_all == 0) continue;
       // the previous item's S MMAs must have finished reading Q
       if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
-      mbar_arrive_expect_tx_elect(bar_q, 2 * C::TILE_BYTES);
-      for (int i = 0; i < 2; ++i)
+      mbar_arrive_expect_tx_elect(bar_q, (SPLIT ? 1 : 2) * C::TILE_BYTES);
+      for (int i = 0; i < (SPLIT ? 1 : 2); ++i)
         for (int s = 0; s < C::SLABS; ++s)
           tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q, s * 64,
                             it.yq + it.q0 + i * BM, it.zq);
       ++nq;
-      for (int t = 0; t < 2 * it.n_all; ++t, ++tg) {
+      for (int t = 0; t < 2 * n_loads_of<SPLIT>(it); ++t, ++tg) {
         if (!(ok = wait_all(bar_empty(tg), ring_phase(tg) ^ 1u, W_KEMPTY))) break;
         mbar_arrive_expect_tx_elect(bar_full(tg), C::TILE_BYTES);
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
@@ -289,9 +311,9 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     const uint64_t k_desc0 = smem_desc_sw128(sbase + C::RING_OFF, 16, 1024);            // K: K-major
     const uint64_t v_desc0 = smem_desc_sw128(sbase + C::RING_OFF, C::SLAB_BYTES, 1024);  // V: MN-major
     auto slot_off = [&](int t) { return (uint64_t)(((t % C::SLOTS) * C::TILE_BYTES) >> 4); };
-    auto issue_s = [&](int i, int t) {  // S_i = Q_i K^T, K from ring load t
+    auto issue_s = [&](int i, int t) {  // S_i = Q_i K^T (SPLIT: Q_0 for both), K from ring load t
       const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
-      const uint64_t a = q_desc0 + (uint64_t)((i * C::TILE_BYTES) >> 4);
+      const uint64_t a = q_desc0 + (uint64_t)(((SPLIT ? 0 : i) * C::TILE_BYTES) >> 4);
       const uint64_t b = k_desc0 + slot_off(t);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
@@ -318,7 +340,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
         if (it.n_all == 0) continue;
         const int n = it.n_kv[i], sb = i ? st1 : st0;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
@@ -366,12 +388,59 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         tg += 2 * it.n_all;
         if (i) st1 += n; else st0 += n;
       }
+    } else if constexpr (SPLIT) {
+      // ---- one warp, the two slots on alternate key tiles: slot i's m-th key tile is key tile
+      // 2 m + i (K in load tg + 4 m + 2 i, V in the load after it); per m: PV_0, S_0 of its next
+      // tile, PV_1, S_1 of its next tile.  Every load is read by exactly one MMA, released by a
+      // commit after it.
+      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+        const int idx = item_of_round(k, total);
+        if (idx < 0) continue;
+        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        if (it.n_all == 0) continue;
+        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
+        ++nq;
+        int s_left = it.n_kv[0] + it.n_kv[1];  // S MMAs of the item still to issue
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (it.n_kv[i] == 0) continue;
+          const int tk = tg + 2 * i;
+          if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+          tc_fence_after_sync();
+          issue_s(i, tk);
+          mma_commit_elect(bar_sfull(i));
+          mma_commit_elect(bar_empty(tk));
+          if (--s_left == 0) mma_commit_elect(bar_qempty);
+        }
+        for (int m = 0; ok && m < it.n_all; ++m) {
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (m >= it.n_kv[i]) continue;
+            const int tv = tg + 4 * m + 2 * i + 1, tk = tg + 4 * (m + 1) + 2 * i;
+            if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+            if (!(ok = wait_all(bar_pfull(i), (uint32_t)((i ? st1 : st0) + m) & 1u, W_PFULL))) break;
+            tc_fence_after_sync();
+            issue_pv(i, tv, m > 0);
+            mma_commit_elect(bar_odone(i));
+            mma_commit_elect(bar_empty(tv));
+            if (m + 1 < it.n_kv[i]) {  // P_i lives in S_i's columns: S_i of the next tile after PV_i
+              if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+              tc_fence_after_sync();
+              issue_s(i, tk);
+              mma_commit_elect(bar_sfull(i));
+              mma_commit_elect(bar_empty(tk));
+              if (--s_left == 0) mma_commit_elect(bar_qempty);
+            }
+          }
+        }
+        tg += 2 * n_loads_of<SPLIT>(it);
+        st0 += it.n_kv[0];
+        st1 += it.n_kv[1];
+      }
     } else {
       // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
         if (it.n_all == 0) continue;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
         ++nq;
@@ -409,7 +478,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           if (k_next_ready) mma_commit_elect(bar_empty(tk));
           if (j + 2 == it.n_all) mma_commit_elect(bar_qempty);  // the item's last S MMAs are issued
         }
-        tg += 2 * it.n_all;
+        tg += 2 * n_loads_of<SPLIT>(it);
         st0 += it.n_kv[0];
         st1 += it.n_kv[1];
       }
@@ -429,6 +498,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     const uint32_t p_addr = tmem_base + lane_base + C::p_col(i);
     const float sl2 = p.scale_log2;
     int sb = 0;  // score tiles of this group in earlier items (barrier phases run on)
+    int nx = 0;  // SPLIT: items handed over so far (the phase of xch / xdone)
     bool ok = true;
     for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
       const int idx = item_of_round(k, total);
@@ -437,10 +507,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       // again for its output offsets
       int n, kvl, r0;
       {
-        const Item it = item_at<D, PACKED>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
         n = it.n_kv[i];
         kvl = it.kvl;
-        r0 = it.q0 + i * BM;
+        r0 = it.q0 + (SPLIT ? 0 : i * BM);
       }
       const int row = r0 + tt;
       float m = -INFINITY;  // running max of the scaled scores, log2 units
@@ -458,7 +528,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           if (lane == 0) mbar_arrive(bar_sfree(i));
         }
         float* s = reinterpret_cast<float*>(sr);
-        const int col0 = j * BN;
+        const int col0 = (SPLIT ? 2 * j + i : j) * BN;  // SPLIT: this slot's j-th key tile is 2 j + i
         if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
@@ -545,8 +615,37 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       const bool have_o = n > 0;
       if (have_o && !(ok = wait_all(bar_odone(i), (uint32_t)(sb + n - 1) & 1u, W_ODONE))) break;
       tc_fence_after_sync();
+      // SPLIT: the two slots hold (m, l, O) of the same rows over the even and the odd key tiles.
+      // Slot 1 hands over (m, l) and its finished O_1; slot 0 merges the pairs (the reference
+      // max of the two, each side rescaled to it) and writes the row; slot 1 waits until slot 0
+      // has read O_1 before its next P can let PV_1 overwrite it.
+      bool have_o1 = false;
+      float a0 = 1.f, a1 = 0.f;
+      if constexpr (SPLIT) {
+        const uint32_t xph = (uint32_t)nx & 1u;
+        ++nx;
+        if (i == 1) {
+          xch_ml[tt] = make_float2(m, have_o ? l : 0.f);
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_xch);
+          if (!(ok = wait_all(bar_xdone, xph, W_ODONE))) break;
+          sb += n;
+          continue;
+        }
+        if (!(ok = wait_all(bar_xch, xph, W_ODONE))) break;
+        tc_fence_after_sync();
+        const float2 ml1 = xch_ml[tt];
+        have_o1 = ml1.y > 0.f;
+        const float mm = fmaxf(m, ml1.x);
+        const float ref = (mm == -INFINITY) ? 0.f : mm;
+        a0 = (m == -INFINITY) ? 0.f : ex2(m - ref);
+        a1 = (ml1.x == -INFINITY) ? 0.f : ex2(ml1.x - ref);
+        l = a0 * l + a1 * ml1.y;
+        m = mm;
+      }
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const Item it = item_at<D, PACKED>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT>(p, idx);
       const int64_t o_rs = PACKED ? p.o_rs : D;  // O row stride
       __nv_bfloat16* orow = p.o + it.ob + (int64_t)row * o_rs;
 #pragma unroll 1
@@ -557,6 +656,15 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) orr[e] = 0u;
+        }
+        if constexpr (SPLIT) {  // O = a0 O_0 + a1 O_1 (a side with no keys contributes nothing)
+          uint32_t o1[32];
+          if (have_o1) tmem_ld32(tmem_base + lane_base + C::o_col(1) + c, o1);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float v0 = have_o ? a0 * __uint_as_float(orr[e]) : 0.f;
+            orr[e] = __float_as_uint(have_o1 ? fmaf(a1, __uint_as_float(o1[e]), v0) : v0);
+          }
         }
         uint4 pk[4];
         uint32_t* w = reinterpret_cast<uint32_t*>(pk);
@@ -583,6 +691,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       // O_i has been read out: the next item's PV_i(0) (issued after this group's next P)
       // may overwrite it
       tc_fence_before_sync();
+      if constexpr (SPLIT) {  // and O_1 and slot 1's (m, l) too
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_xdone);
+      }
       sb += n;
     }
   }
@@ -603,7 +715,7 @@ constexpr int kMaxDevices = 64;
 // sequences) the items weigh alike, so the grid is the fewest CTAs that keep the number of rounds:
 // every CTA then works through the same number of items, and the memory-bound cases (grouped
 // decode) spread the same bytes over fewer, busier CTAs instead of a last round half empty.
-template <int D, bool PACKED>
+template <int D, bool PACKED, bool SPLIT = false>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                      cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
@@ -613,7 +725,8 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, PACKED>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, PACKED, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
@@ -626,7 +739,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     g = (total + rounds - 1) / rounds;
   }
   const unsigned grid = (unsigned)g;
-  attn_fwd_tc_kernel<D, PACKED><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, PACKED, SPLIT><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -672,6 +785,10 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.st = st;
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
   if (packed) return d == 128 ? launch_d<128, true>(mq, mk, mv, p, s) : launch_d<64, true>(mq, mk, mv, p, s);
+  // At most 128 query rows without the mask (decode, and grouped decode whose group's queries are
+  // the rows): an item fills only one query-tile slot, so at d = 128 both slots take the same rows
+  // over alternate key tiles and their results are merged (see item_at).
+  if (d == 128 && !a.causal && a.Nq <= BM) return launch_d<128, false, true>(mq, mk, mv, p, s);
   return d == 128 ? launch_d<128, false>(mq, mk, mv, p, s) : launch_d<64, false>(mq, mk, mv, p, s);
 }
 
