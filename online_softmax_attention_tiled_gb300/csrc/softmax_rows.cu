@@ -148,15 +148,19 @@ __device__ __forceinline__ void store_piece(float* __restrict__ yr, int64_t base
   }
 }
 
-// grid.x = rows * cluster; the `cluster` CTAs of a row split its columns into
-// slices of `slice` columns (a multiple of 4).  At most 64 registers per thread, so that four
-// 256-thread CTAs share an SM and hide each other's reduction phases (+0.8 % at 4096 x 32768
-// against 80 registers and three CTAs).
+// CTAs per SM the register budget is cut for: five 256-thread CTAs (48 registers) hide each
+// other's load and reduction phases better than four (64 registers: 0.194 -> 0.187 ms at
+// 4096 x 32768; three at 80 registers were 0.8 % slower than four); the scalar 32-element
+// instance keeps four, at 48 registers it would spill.
 template <int E, bool VEC>
-__global__ void __launch_bounds__(kMaxThreads, 4) softmax_rows_kernel(const float* __restrict__ x, int64_t cols,
-                                                                    int64_t ld_x, float* __restrict__ y,
-                                                                    int64_t ld_y, float* __restrict__ lse,
-                                                                    int cluster, int64_t slice) {
+constexpr int kSoftmaxMinBlocks = (E == 32 && !VEC) ? 4 : 5;
+
+// grid.x = rows * cluster; the `cluster` CTAs of a row split its columns into
+// slices of `slice` columns (a multiple of 4).
+template <int E, bool VEC>
+__global__ void __launch_bounds__(kMaxThreads, kSoftmaxMinBlocks<E, VEC>)
+    softmax_rows_kernel(const float* __restrict__ x, int64_t cols, int64_t ld_x, float* __restrict__ y, int64_t ld_y,
+                        float* __restrict__ lse, int cluster, int64_t slice) {
   __shared__ ML warp_ml[kMaxThreads / 32];
   __shared__ ML cta_ml;  // this CTA's merged statistics (read by peers)
   __shared__ ML row_ml;  // statistics of the whole row
