@@ -40,6 +40,12 @@
 //   softmax of S_i(j).  Warp 9 issues tile 0's MMAs and warp 10 tile 1's, in
 //   the order S_i(j+1), PV_i(j); before writing P_i(j) a group waits for
 //   PV_i(j-1).
+//   SPLIT instance (d = 128, dense, at most 128 query rows, no mask: decode):
+//   an item would fill only query tile 0, so both tiles hold the same rows
+//   and take alternate key tiles (tile 0 the even, tile 1 the odd ones) with
+//   their own (m, l, O); at the end group 1 hands (m, l) to group 0 through
+//   Q tile 1's buffer, which this mode never loads, and group 0 merges the
+//   two partial results (the same (m, l) merge as split-KV) and writes O.
 //
 // Every mbarrier wait is bounded (oa_common.cuh); a wait that expires sets
 // the CTA abort flag, every role falls through to the teardown, in-flight
