@@ -40,7 +40,7 @@
 //   softmax of S_i(j).  Warp 9 issues tile 0's MMAs and warp 10 tile 1's, in
 //   the order S_i(j+1), PV_i(j); before writing P_i(j) a group waits for
 //   PV_i(j-1).
-//   SPLIT instance (d = 128, dense, at most 128 query rows, no mask: decode):
+//   SPLIT instances (dense, at most 128 query rows, no mask: decode):
 //   an item would fill only query tile 0, so both tiles hold the same rows
 //   and take alternate key tiles (tile 0 the even, tile 1 the odd ones) with
 //   their own (m, l, O); at the end group 1 hands (m, l) to group 0 through
@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
   auto bar_sfree = [&](int i) { return bar0 + 8u * (8 + 2 * C::SLOTS + i); };  // S_i read by its group
   const uint32_t bar_qempty = bar0 + 8u * (10 + 2 * C::SLOTS);               // Q read by the last S MMAs
-  static_assert(!SPLIT || (D == 128 && !PACKED), "the split mode serves d = 128, dense layout");
+  static_assert(!SPLIT || !PACKED, "the split mode serves the dense layout");
   // SPLIT: Q tile 1's buffer (never loaded) holds group 1's (m, l) per row and two barriers:
   // xch (group 1's O_1, m, l ready; 4 warps) and xdone (group 0 has read them; 4 warps)
   float2* xch_ml = reinterpret_cast<float2*>(smem + C::Q_OFF + C::TILE_BYTES);
@@ -340,7 +340,68 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     // st_i = score tiles of query tile i so far (the phase of s_full / p_full / o_done / s_free).
     int tg = 0, nq = 0, st0 = 0, st1 = 0;
     bool ok = true;
-    if constexpr (C::SEP_P) {
+    if constexpr (C::SEP_P && SPLIT) {
+      // ---- one warp per slot, the slots on alternate key tiles: slot i's m-th key tile is key
+      // tile 2 m + i (K in load tg + 4 m + 2 i, V in the load after it).  The other slot's loads
+      // are released by a plain arrival once they have landed, in load order as this warp moves
+      // past them, so neither warp holds ring slots the other needs.
+      const int i = warp - kMmaWarp0;
+      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+        const int idx = item_of_round(k, total);
+        if (idx < 0) continue;
+        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        if (it.n_all == 0) continue;
+        const int n = it.n_kv[i], sb = i ? st1 : st0, n_ld = 2 * n_loads_of<SPLIT>(it);
+        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
+        ++nq;
+        int rel = 0;  // loads tg + rel onwards not yet passed
+        auto release_to = [&](int t_end) {  // plain arrivals for the other slot's loads before t_end
+          for (; rel < t_end; ++rel) {
+            if (((rel >> 1) & 1) == i) continue;  // this slot's own load: released by a commit
+            if (!wait_all(bar_full(tg + rel), ring_phase(tg + rel), W_DRAIN)) return false;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty(tg + rel));
+          }
+          return true;
+        };
+        auto k_ld = [&](int m) { return 4 * m + 2 * i; };  // load of slot i's m-th K (V follows)
+        if (n > 0) {
+          if (!(ok = release_to(k_ld(0)))) break;
+          if (!(ok = wait_all(bar_full(tg + k_ld(0)), ring_phase(tg + k_ld(0)), W_KFULL))) break;
+          tc_fence_after_sync();
+          issue_s(i, tg + k_ld(0));
+          mma_commit_elect(bar_sfull(i));
+          mma_commit_elect(bar_empty(tg + k_ld(0)));
+          if (n == 1) mma_commit_elect(bar_qempty);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_qempty);  // Q(this item) has landed: the arrival is in phase
+        }
+        for (int m = 0; ok && m < n; ++m) {
+          const int tv = tg + k_ld(m) + 1, tk = tg + k_ld(m + 1);
+          const uint32_t ph = (uint32_t)(sb + m) & 1u;
+          if (m + 1 < n) {  // S_i of the next tile as soon as the softmax group has read S_i
+            if (!(ok = release_to(k_ld(m + 1)))) break;
+            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
+            if (!(ok = wait_all(bar_sfree(i), ph, W_SFREE))) break;
+            tc_fence_after_sync();
+            issue_s(i, tk);
+            mma_commit_elect(bar_sfull(i));
+            mma_commit_elect(bar_empty(tk));
+            if (m + 2 == n) mma_commit_elect(bar_qempty);
+          }
+          if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
+          if (!(ok = wait_all(bar_pfull(i), ph, W_PFULL))) break;
+          tc_fence_after_sync();
+          issue_pv(i, tv, m > 0);
+          mma_commit_elect(bar_odone(i));
+          mma_commit_elect(bar_empty(tv));
+        }
+        if (ok) ok = release_to(n_ld);
+        tg += n_ld;
+        if (i) st1 += n; else st0 += n;
+      }
+    } else if constexpr (C::SEP_P) {
       // ---- one warp per query tile: warp 9 for tile 0, warp 10 for tile 1 ----
       const int i = warp - kMmaWarp0;
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
@@ -792,9 +853,10 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
   if (packed) return d == 128 ? launch_d<128, true>(mq, mk, mv, p, s) : launch_d<64, true>(mq, mk, mv, p, s);
   // At most 128 query rows without the mask (decode, and grouped decode whose group's queries are
-  // the rows): an item fills only one query-tile slot, so at d = 128 both slots take the same rows
-  // over alternate key tiles and their results are merged (see item_at).
-  if (d == 128 && !a.causal && a.Nq <= BM) return launch_d<128, false, true>(mq, mk, mv, p, s);
+  // the rows): an item fills only one query-tile slot, so both slots take the same rows over
+  // alternate key tiles and their results are merged (see item_at).
+  if (!a.causal && a.Nq <= BM)
+    return d == 128 ? launch_d<128, false, true>(mq, mk, mv, p, s) : launch_d<64, false, true>(mq, mk, mv, p, s);
   return d == 128 ? launch_d<128, false>(mq, mk, mv, p, s) : launch_d<64, false>(mq, mk, mv, p, s);
 }
 

@@ -61,13 +61,14 @@ def test_kv_len_masks(cuda_lib, d, causal):
 
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("Nq,Nk", [(64, 300), (128, 1), (3, 129), (100, 1000), (128, 640)])
-def test_short_query_block_splits_keys_between_slots(cuda_lib, Nq, Nk):
-    # At most 128 query rows without the mask (d = 128): both query-tile slots take the same rows
+def test_short_query_block_splits_keys_between_slots(cuda_lib, d, Nq, Nk):
+    # At most 128 query rows without the mask: both query-tile slots take the same rows
     # over alternate key tiles, each with its own running max, sum and O, merged per row at the
     # end.  Odd and even numbers of key tiles, a slot with no tile at all (one key tile), a batch
     # entry with no keys, a ragged key end, and large scores (each slot rescales on its own).
-    q, k, v = si.attn_inputs(2, 3, Nq, Nk, 128, torch.bfloat16, seed=5 * Nq + Nk)
+    q, k, v = si.attn_inputs(2, 3, Nq, Nk, d, torch.bfloat16, seed=5 * Nq + Nk + d)
     _check(cuda_lib, q, k, v)
     _check(cuda_lib, q, k, v, kv_len=[Nk // 2 + 1, 0])
     _check(cuda_lib, q, k, v, scale=1.0)
