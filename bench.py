@@ -2,15 +2,21 @@
 
 Prints ONE JSON line (rank 0).  The headline workload is the fused causal
 attention forward, bf16, B=1 H=32 N=8192 d=128 (one "step" = one forward
-over that batch); the row softmax + LSE on fp32 [4096, 32768] (the metric's
-second half), the non-causal B4 H16 N4096 d64 forward, the split-KV decode
-B32 H32 Nk32768 d128 (and the same over a grouped cache with 8 key/value
-heads) and a causal forward over 16 packed sequences of mixed length are
-measured in the same run and reported under "components", each against its
-own roofline.
+over that batch).  The other hot-path kernels (the row softmax + LSE on fp32
+[4096, 32768] -- the metric's second half --, the non-causal B4 H16 N4096 d64
+forward, split-KV decode, decode over a grouped cache, a causal forward over
+packed sequences, the backward passes) are measured in the same run and
+reported under "components", each against its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--components/--no-components] [--no-cpu-baseline]
+                  [--min-seconds S]
+  python bench.py --case NAME [--reps R] [--batch B]     (one case, for a profiler)
+
+Timing: W untimed warm-up steps, then the K-step loop is repeated until the
+timed region lasts at least --min-seconds (default 3 s), so that the clock
+record describes it; per-step figures come from every timed step.  Each
+launch is bracketed by CUDA events on the launching stream.
 
 --impl reference times the CPU oracle (the only reference this method has:
 the pages carry no implementation) on a bounded sample of the same workload.
@@ -40,6 +46,9 @@ METRIC = "attn fwd TFLOP/s (bf16, causal N=8192 d=128) & % tensor peak; softmax 
 WORKLOAD = "causal attention fwd bf16 B=1 H=32 Nq=Nk=8192 d=128 scale=1/sqrt(128)"
 B, H, N, D = 1, 32, 8192, 128
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# Dense bf16 tensor work one SM retires per clock: one 128 x 128 x 16 MMA (524,288 FLOPs) per
+# 64 cycles.  x SM count x SM clock = the hardware peak at the clock actually seen.
+BF16_FLOP_PER_SM_CLOCK = 8192
 
 
 # --------------------------------------------------------------------------
@@ -54,9 +63,24 @@ def dense_attn_flops(b, h, nq, nk, d):
     return 4.0 * b * h * nq * nk * d
 
 
+def causal_pairs(nq, nk):
+    """Visible (query, key) pairs of one head when query i sees keys j <= i + (nk - nq)."""
+    off = nk - nq
+    return sum(max(0, min(nk, i + off + 1)) for i in range(nq))
+
+
+def kvcache_causal_flops(b, h, nq, nk, d):
+    """4*d FLOPs per visible pair, the new queries being the last nq positions of nk keys."""
+    return 4.0 * b * h * d * causal_pairs(nq, nk)
+
+
 def causal_attn_bwd_flops(b, h, n, d):
     """10*d FLOPs per visible (query, key) pair: S = QK^T and dP = dO V^T recomputed, then dV, dK, dQ."""
     return 2.5 * causal_attn_flops(b, h, n, d)
+
+
+def dense_attn_bwd_flops(b, h, nq, nk, d):
+    return 2.5 * dense_attn_flops(b, h, nq, nk, d)
 
 
 def softmax_bytes(rows, cols):
@@ -112,33 +136,69 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 20 ms while running."""
+    """nvidia-smi clocks / throttle reasons, sampled every 20 ms while running.  Started before the
+    warm-up; wait_first() blocks until nvidia-smi has produced a sample, so the timed region that
+    follows is covered from its start."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.samples = []
+        self.unparsed = 0
+        self.error = None
         self.proc = None
         self.thread = None
+        self._first = threading.Event()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+        except OSError as e:
             self.proc = None
+            self.error = f"nvidia-smi not started: {e}"
+            self._first.set()
             return self
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
         return self
 
+    @staticmethod
+    def parse(line):
+        """(sm MHz, max SM MHz, power W, {reason: active}) of one csv line, or None."""
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            return None
+        try:
+            sm, smax = float(parts[1]), float(parts[2])
+        except ValueError:
+            return None
+        try:
+            pw = float(parts[3])
+        except ValueError:
+            pw = float("nan")
+        act = {n: v.lower().startswith("active") for n, v in zip(ClockSampler.REASONS, parts[5:9])}
+        return sm, smax, pw, act
+
     def _read(self):
         for line in self.proc.stdout:
-            self.samples.append((time.time(), line.strip()))
+            r = self.parse(line)
+            if r is None:
+                self.unparsed += 1
+                if self.unparsed == 1:
+                    self.error = f"unparsed nvidia-smi line: {line.strip()[:160]}"
+            else:
+                self.samples.append((time.time(), r))
+            self._first.set()
+        self._first.set()
+
+    def wait_first(self, timeout=10.0):
+        self._first.wait(timeout)
 
     def __exit__(self, *exc):
         if self.proc is not None:
@@ -147,30 +207,24 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+            if not self.samples and self.error is None:
+                err = (self.proc.stderr.read() or "").strip() if self.proc.stderr else ""
+                self.error = f"no samples; nvidia-smi said: {err[:200]}" if err else "no samples"
         if self.thread is not None:
             self.thread.join(timeout=5)
 
     def summary(self, t0, t1):
-        rows = []
-        for ts, line in self.samples:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
-            except ValueError:
-                continue
-        if not rows:
-            return None
-        inside = [r for r in rows if t0 <= r[0] <= t1] or sorted(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))[:3]
-        reasons = set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for r in inside:
-            for name, val in zip(names, r[3][1:]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
-                "reasons": sorted(reasons), "samples": len(inside)}
+        inside = [r for ts, r in self.samples if t0 <= ts <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "error": self.error or "no sample inside the timed region"}
+        reasons = sorted({n for r in inside for n, a in r[3].items() if a})
+        out = {"sm_mhz": statistics.median(r[0] for r in inside), "sm_max_mhz": max(r[1] for r in inside),
+               "reasons": reasons, "samples": len(inside),
+               "power_w_max": max((r[2] for r in inside if r[2] == r[2]), default=None)}
+        if self.unparsed:
+            out["unparsed_lines"] = self.unparsed
+        return out
 
 
 # --------------------------------------------------------------------------
@@ -202,19 +256,36 @@ def barrier(world: int):
         dist.barrier()
 
 
+def headline_config(world: int) -> dict:
+    """The workload description, identical in both arms."""
+    return {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": True,
+            "per_gpu_batch": "one (B=1, H=32) batch per rank",
+            "l2": "inputs larger than L2 (Q+K+V+O = 256 MiB > 129 MB); no flush in the timed loop",
+            "parallelism": f"replicas x{world} (independent batches, no collective)"}
+
+
+def repeats_for(floor_s: float, steps: int, step_ms: float) -> int:
+    """How many times the K-step loop runs so that the timed region lasts at least floor_s."""
+    if floor_s <= 0 or step_ms <= 0:
+        return 1
+    return max(1, math.ceil(floor_s * 1e3 / (steps * step_ms)))
+
+
 # --------------------------------------------------------------------------
 # GPU timing helpers
 # --------------------------------------------------------------------------
-def time_launches(fn, steps, warmup, flush=None):
-    """Run fn() warmup times, then `steps` times with CUDA events around each launch on the
-    current stream; returns per-launch milliseconds.  flush() (outside the events) evicts L2."""
+def time_launches(fn, steps, warmup, flush=None, min_seconds=0.0, max_launches=4000):
+    """Run fn() warmup times, then at least `steps` times and for at least min_seconds, with CUDA
+    events around each launch on the current stream; returns per-launch milliseconds.  flush()
+    (outside the events) evicts L2."""
     import torch
 
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     times = []
-    for _ in range(steps):
+    t0 = time.perf_counter()
+    while len(times) < steps or (time.perf_counter() - t0 < min_seconds and len(times) < max_launches):
         if flush is not None:
             flush()
         a = torch.cuda.Event(enable_timing=True)
@@ -227,8 +298,120 @@ def time_launches(fn, steps, warmup, flush=None):
     return times
 
 
-def components(oa, dev, peaks, peak_kind, steps):
-    """Each hot-path kernel other than the headline one, timed alone (L2 flushed between launches)."""
+# --------------------------------------------------------------------------
+# workloads: each builds its inputs on `dev` and returns a Case; the same table serves the
+# components of the bench line and `--case NAME` (one workload under a profiler)
+# --------------------------------------------------------------------------
+class Case:
+    def __init__(self, fn, work, unit, bound, workload, flush=True, launches=1, **extra):
+        self.fn, self.work, self.unit, self.bound, self.workload = fn, work, unit, bound, workload
+        self.flush, self.launches, self.extra = flush, launches, extra
+
+
+def _case_attn_causal(oa, si, torch, dev, batch):
+    q, k, v = si.attn_inputs(B, H, N, N, D, torch.bfloat16, seed=0, device=dev)
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    return Case(lambda: oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse), causal_attn_flops(B, H, N, D), "TFLOP/s",
+                "tensor", WORKLOAD)
+
+
+def _case_softmax(oa, si, torch, dev, batch):
+    x, *_ = si.softmax_input(4096, 32768, seed=0)
+    x = x.to(dev)
+    y, lse = torch.empty_like(x), torch.empty(4096, dtype=torch.float32, device=dev)
+    return Case(lambda: oa.softmax_rows(x, y=y, lse=lse), softmax_bytes(4096, 32768), "GB/s", "hbm",
+                "row softmax + LSE fp32 [4096, 32768], N(0,1)*4, 1% rows -inf, 10% -inf prefix")
+
+
+def _case_attn_noncausal(oa, si, torch, dev, batch):
+    q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
+    o, lse = torch.empty_like(q), torch.empty((4, 16, 4096), dtype=torch.float32, device=dev)
+    return Case(lambda: oa.attn_fwd(q, k, v, out=o, lse=lse), dense_attn_flops(4, 16, 4096, 4096, 64), "TFLOP/s",
+                "tensor", "non-causal attention fwd bf16 B=4 H=16 N=4096 d=64")
+
+
+def _case_decode(oa, si, torch, dev, batch):
+    b = batch or 32
+    q, k, v = si.attn_inputs(b, 32, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+    kv_len = si.decode_kv_len(b, 32768, seed=0)
+    kvd = kv_len.to(dev)
+    o, lse = torch.empty_like(q), torch.empty((b, 32, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(oa.splitkv_workspace_bytes(b, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+    return Case(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws),
+                decode_bytes(b, 32, 128, int(kv_len.sum())), "GB/s", "hbm",
+                f"split-KV decode bf16 B={b} H=32 Nq=1 Nk=32768 d=128, 64 chunks of 512, 5% of sequences "
+                f"truncated (inputs {b * 32 * 32768 * 128 * 4 / 1e9:.1f} GB)", flush=False, launches=2)
+
+
+def _case_decode_gqa(oa, si, torch, dev, batch):
+    b = batch or 32
+    q, k, v = si.attn_inputs_gqa(b, 32, 8, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
+    kv_len = si.decode_kv_len(b, 32768, seed=0)
+    kvd = kv_len.to(dev)
+    o, lse = torch.empty_like(q), torch.empty((b, 32, 1), dtype=torch.float32, device=dev)
+    ws = torch.empty(oa.splitkv_workspace_bytes(b, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
+    return Case(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws),
+                decode_bytes(b, 32, 128, int(kv_len.sum()), h_kv=8), "GB/s", "hbm",
+                f"decode bf16 over a grouped KV cache B={b} H=32 H_kv=8 Nq=1 Nk=32768 d=128, 5% of sequences "
+                "truncated, through oa_attn_splitkv_gqa: each group's 4 queries run as the rows of the "
+                "tensor-core forward (no key split; num_splits and the workspace are unused)")
+
+
+def _case_attn_varlen(oa, si, torch, dev, batch):
+    lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
+    q, k, v, cq, ck = si.varlen_inputs(lens, lens, 32, 8, 128, torch.bfloat16, seed=0, device=dev)
+    cq, ck = cq.to(dev), ck.to(dev)
+    o, lse = torch.empty_like(q), torch.empty((q.shape[0], 32), dtype=torch.float32, device=dev)
+    mx = max(lens)
+    return Case(lambda: oa.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse),
+                varlen_causal_flops(lens, 32, 128), "TFLOP/s", "tensor",
+                f"causal attention fwd bf16 over 16 packed sequences, lengths U[1024, 8192] (total {sum(lens)} "
+                "tokens), H=32 H_kv=8 d=128")
+
+
+def _bwd_case(oa, si, torch, dev, b, h, hkv, n, d, causal, workload):
+    q, k, v = si.attn_inputs_gqa(b, h, hkv, n, n, d, torch.bfloat16, seed=0, device=dev)
+    do = si.randn((b, h, n, d), 3, torch.bfloat16, dev)
+    o, lse = oa.attn_fwd(q, k, v, causal=causal)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(oa.attn_bwd_workspace_bytes(b, h, n, d), dtype=torch.uint8, device=dev)
+    fl = causal_attn_bwd_flops(b, h, n, d) if causal else dense_attn_bwd_flops(b, h, n, n, d)
+    return Case(lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws), fl,
+                "TFLOP/s", "tensor", workload, launches=3)
+
+
+def _case_bwd_causal(oa, si, torch, dev, batch):
+    return _bwd_case(oa, si, torch, dev, 1, 32, 32, 8192, 128, True,
+                     "causal attention bwd bf16 B=1 H=32 N=8192 d=128 (dQ, dK, dV from Q, K, V, O, LSE, dO)")
+
+
+def _case_bwd_causal_gqa(oa, si, torch, dev, batch):
+    return _bwd_case(oa, si, torch, dev, 1, 32, 8, 8192, 128, True,
+                     "causal attention bwd bf16 B=1 H=32 H_kv=8 N=8192 d=128")
+
+
+def _case_bwd_noncausal_d64(oa, si, torch, dev, batch):
+    return _bwd_case(oa, si, torch, dev, 4, 16, 16, 4096, 64, False,
+                     "non-causal attention bwd bf16 B=4 H=16 N=4096 d=64 (dQ, dK, dV from Q, K, V, O, LSE, dO)")
+
+
+CASES = {
+    "attn_causal": _case_attn_causal,
+    "softmax_rows": _case_softmax,
+    "attn_noncausal_d64": _case_attn_noncausal,
+    "attn_splitkv_decode": _case_decode,
+    "attn_decode_gqa": _case_decode_gqa,
+    "attn_varlen_causal_gqa": _case_attn_varlen,
+    "attn_bwd_causal": _case_bwd_causal,
+    "attn_bwd_causal_gqa": _case_bwd_causal_gqa,
+    "attn_bwd_noncausal_d64": _case_bwd_noncausal_d64,
+}
+COMPONENTS = [n for n in CASES if n != "attn_causal"]
+
+
+def components(oa, dev, peaks, peak_kind, steps, min_seconds):
+    """Each hot-path kernel other than the headline one, timed alone (L2 flushed between launches
+    unless its inputs are far larger than L2) for at least min_seconds."""
     import torch
 
     import synth_inputs as si
@@ -239,112 +422,45 @@ def components(oa, dev, peaks, peak_kind, steps):
     def flush():
         flush_buf.fill_(1.0)
 
-    # row softmax + LSE, fp32 [4096, 32768]
-    x, *_ = si.softmax_input(4096, 32768, seed=0)
-    x = x.to(dev)
-    y = torch.empty_like(x)
-    lse = torch.empty(4096, dtype=torch.float32, device=dev)
-    t = time_launches(lambda: oa.softmax_rows(x, y=y, lse=lse), steps, 3, flush)
-    ms = statistics.mean(t)
-    gbs = softmax_bytes(4096, 32768) / (ms * 1e-3) / 1e9
-    out["softmax_rows"] = {"workload": "row softmax + LSE fp32 [4096, 32768], N(0,1)*4, 1% rows -inf, 10% -inf prefix",
-                           "ms": ms, "value": gbs, "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
-                           "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
-                           "algorithmic_bytes": softmax_bytes(4096, 32768)}
-    del x, y, lse
-    # non-causal attention B4 H16 N4096 d64
-    q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((4, 16, 4096), dtype=torch.float32, device=dev)
-    t = time_launches(lambda: oa.attn_fwd(q, k, v, out=o, lse=lse), steps, 3, flush)
-    ms = statistics.mean(t)
-    tf = dense_attn_flops(4, 16, 4096, 4096, 64) / (ms * 1e-3) / 1e12
-    out["attn_noncausal_d64"] = {"workload": "non-causal attention fwd bf16 B=4 H=16 N=4096 d=64", "ms": ms,
-                                 "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
-                                 "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind}
-    del q, k, v, o, lse
-    # split-KV decode B32 H32 Nk32768 d128, 64 chunks of 512, 5% of sequences truncated
-    q, k, v = si.attn_inputs(32, 32, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
-    kv_len = si.decode_kv_len(32, 32768, seed=0)
-    kvd = kv_len.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((32, 32, 1), dtype=torch.float32, device=dev)
-    ws = torch.empty(oa.splitkv_workspace_bytes(32, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
-    t = time_launches(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws), steps, 3, None)
-    ms = statistics.mean(t)
-    nbytes = decode_bytes(32, 32, 128, int(kv_len.sum()))
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    out["attn_splitkv_decode"] = {"workload": "split-KV decode bf16 B=32 H=32 Nq=1 Nk=32768 d=128, 64 chunks of 512, "
-                                              "5% of sequences truncated (inputs 17 GB > L2)", "ms": ms, "value": gbs,
-                                  "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
-                                  "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
-                                  "algorithmic_bytes": nbytes, "launches_per_call": 2}
-    del q, k, v, o, lse, ws
-    # split-KV decode over a grouped KV cache: B32 H32 with 8 key/value heads, same lengths
-    q, k, v = si.attn_inputs_gqa(32, 32, 8, 1, 32768, 128, torch.bfloat16, seed=0, device=dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((32, 32, 1), dtype=torch.float32, device=dev)
-    ws = torch.empty(oa.splitkv_workspace_bytes(32, 32, 1, 128, 64), dtype=torch.uint8, device=dev)
-    t = time_launches(lambda: oa.attn_splitkv(q, k, v, 64, kv_len=kvd, out=o, lse=lse, workspace=ws), steps, 3,
-                      flush)
-    ms = statistics.mean(t)
-    nbytes = decode_bytes(32, 32, 128, int(kv_len.sum()), h_kv=8)
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    out["attn_splitkv_decode_gqa"] = {"workload": "decode bf16 B=32 H=32 H_kv=8 Nq=1 Nk=32768 d=128 through "
-                                                  "oa_attn_splitkv_gqa (each group's 4 queries as rows of the "
-                                                  "tensor-core forward), same truncations (KV 4.3 GB > L2)", "ms": ms,
-                                      "value": gbs, "unit": "GB/s", "bound": "hbm", "peak": peaks["hbm_gbs"],
-                                      "frac": gbs / peaks["hbm_gbs"], "peak_kind": peak_kind,
-                                      "algorithmic_bytes": nbytes, "launches_per_call": 2}
-    del q, k, v, o, lse, ws
-    # causal prefill over packed sequences of mixed length, grouped key/value heads
-    lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
-    q, k, v, cq, ck = si.varlen_inputs(lens, lens, 32, 8, 128, torch.bfloat16, seed=0, device=dev)
-    cq, ck = cq.to(dev), ck.to(dev)
-    o = torch.empty_like(q)
-    lse = torch.empty((q.shape[0], 32), dtype=torch.float32, device=dev)
-    mx = max(lens)
-    t = time_launches(lambda: oa.attn_fwd_varlen(q, k, v, cq, ck, mx, mx, causal=True, out=o, lse=lse), steps, 3,
-                      flush)
-    ms = statistics.mean(t)
-    tf = varlen_causal_flops(lens, 32, 128) / (ms * 1e-3) / 1e12
-    out["attn_varlen_causal_gqa"] = {"workload": f"causal attention fwd bf16 over 16 packed sequences, lengths U[1024, "
-                                                 f"8192] (total {sum(lens)} tokens), H=32 H_kv=8 d=128", "ms": ms,
-                                     "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
-                                     "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
-                                     "algorithmic_flops": varlen_causal_flops(lens, 32, 128)}
-    del q, k, v, o, lse
-    # attention backward, causal B1 H32 N8192 d128, O and LSE from the forward
-    q, k, v = si.attn_inputs(1, 32, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
-    do = si.randn((1, 32, 8192, 128), 3, torch.bfloat16, dev)
-    o, lse = oa.attn_fwd(q, k, v, causal=True)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ws = torch.empty(oa.attn_bwd_workspace_bytes(1, 32, 8192, 128), dtype=torch.uint8, device=dev)
-    t = time_launches(lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws), steps,
-                      3, flush)
-    ms = statistics.mean(t)
-    fl = causal_attn_bwd_flops(1, 32, 8192, 128)
-    tf = fl / (ms * 1e-3) / 1e12
-    out["attn_bwd_causal"] = {"workload": "causal attention bwd bf16 B=1 H=32 N=8192 d=128 (dQ, dK, dV from Q, K, V, "
-                                          "O, LSE, dO)", "ms": ms, "value": tf, "unit": "TFLOP/s", "bound": "tensor",
-                              "peak": peaks["bf16_tflops"], "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
-                              "algorithmic_flops": fl, "launches_per_call": 3}
-    del q, k, v, o, lse, dk, dv
-    # the same backward over grouped key/value heads (H_kv 8): dK, dV sum over each group's 4 query heads
-    q, k, v = si.attn_inputs_gqa(1, 32, 8, 8192, 8192, 128, torch.bfloat16, seed=0, device=dev)
-    o, lse = oa.attn_fwd(q, k, v, causal=True)
-    dk, dv = torch.empty_like(k), torch.empty_like(v)
-    t = time_launches(lambda: oa.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, workspace=ws), steps,
-                      3, flush)
-    ms = statistics.mean(t)
-    tf = fl / (ms * 1e-3) / 1e12
-    out["attn_bwd_causal_gqa"] = {"workload": "causal attention bwd bf16 B=1 H=32 H_kv=8 N=8192 d=128", "ms": ms,
-                                  "value": tf, "unit": "TFLOP/s", "bound": "tensor", "peak": peaks["bf16_tflops"],
-                                  "frac": tf / peaks["bf16_tflops"], "peak_kind": peak_kind,
-                                  "algorithmic_flops": fl, "launches_per_call": 3}
-    del q, k, v, do, o, lse, dq, dk, dv, ws, flush_buf
+    for name in COMPONENTS:
+        c = CASES[name](oa, si, torch, dev, None)
+        t = time_launches(c.fn, steps, 3, flush if c.flush else None, min_seconds)
+        ms = statistics.mean(t)
+        if c.unit == "GB/s":
+            val, peak = c.work / (ms * 1e-3) / 1e9, peaks["hbm_gbs"]
+            work = {"algorithmic_bytes": c.work}
+        else:
+            val, peak = c.work / (ms * 1e-3) / 1e12, peaks["bf16_tflops"]
+            work = {"algorithmic_flops": c.work}
+        out[name] = {"workload": c.workload, "ms": ms, "launches_timed": len(t), "value": val, "unit": c.unit,
+                     "bound": c.bound, "peak": peak, "frac": val / peak, "peak_kind": peak_kind,
+                     "launches_per_call": c.launches, "l2_flushed": c.flush, **work, **c.extra}
+        del c
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    oa.sync_status()
+    del flush_buf
     torch.cuda.empty_cache()
     return out
+
+
+def run_case(name, reps, batch):
+    """One workload on cuda:0: one launch, then `reps` timed launches (for a profiler's launch list)."""
+    import torch
+
+    import online_softmax_attention_tiled_gb300 as oa
+    import synth_inputs as si
+
+    if name not in CASES:
+        raise SystemExit(f"unknown case {name}; cases: {', '.join(CASES)}")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    c = CASES[name](oa, si, torch, dev, batch)
+    t = time_launches(c.fn, reps, 1)
+    oa.sync_status()
+    ms = statistics.mean(t)
+    val = c.work / (ms * 1e-3) / (1e9 if c.unit == "GB/s" else 1e12)
+    print(f"{name}: {ms:.4f} ms per call over {reps} calls, {val:.1f} {c.unit} ({c.workload})")
 
 
 # --------------------------------------------------------------------------
@@ -393,7 +509,15 @@ def main():
     ap.add_argument("--components", dest="components", action="store_true", default=True)
     ap.add_argument("--no-components", dest="components", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false", default=True)
+    ap.add_argument("--min-seconds", type=float, default=3.0,
+                    help="time floor of the headline's timed region (the K-step loop repeats until reached)")
+    ap.add_argument("--component-seconds", type=float, default=0.6, help="time floor of each component")
+    ap.add_argument("--case", default=None, help="run one workload only (see CASES), for a profiler")
+    ap.add_argument("--reps", type=int, default=2, help="--case: timed calls after one warm-up call")
+    ap.add_argument("--batch", type=int, default=None, help="--case: batch of the decode workloads (default 32)")
     args = ap.parse_args()
+    if args.case is not None:
+        return run_case(args.case, args.reps, args.batch)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     world, rank, local = dist_env()
@@ -417,6 +541,7 @@ def main():
         dist.init_process_group("nccl", device_id=dev)
     oa.load()
     peaks, peak_kind = load_peaks()
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
 
     q, k, v = si.attn_inputs(B, H, N, N, D, torch.bfloat16, seed=rank)
     q, k, v = q.to(dev), k.to(dev), v.to(dev)
@@ -427,15 +552,24 @@ def main():
     def step():
         oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    oa.sync_status()
-
-    # ---- timed region: K steps, one event pair per launch on the launching stream ----
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        # warm-up, timed once to size the repeats of the K-step loop
+        w0, w1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        step()
+        w0.record(stream)
+        for _ in range(args.warmup - 1):
+            step()
+        w1.record(stream)
+        torch.cuda.synchronize()
+        oa.sync_status()
+        warm_ms = w0.elapsed_time(w1) / max(1, args.warmup - 1)
+        repeats = int(max_over_ranks(float(repeats_for(args.min_seconds, args.steps, warm_ms)), world, dev))
+        clocks.wait_first()
+
+        # ---- timed region: the K-step loop, `repeats` times; one event pair per launch ----
+        n_timed = repeats * args.steps
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_timed)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         t_wall0 = time.time()
@@ -453,9 +587,18 @@ def main():
     per_launch = [a.elapsed_time(b) for a, b in ev]
     launch_ms = statistics.mean(per_launch)
     flops = causal_attn_flops(B, H, N, D)
-    value = world * args.steps * flops / (elapsed_ms * 1e-3) / 1e12
+    value = world * n_timed * flops / (elapsed_ms * 1e-3) / 1e12
     achieved = flops / (launch_ms * 1e-3) / 1e12
     clock_summary = clocks.summary(t_wall0, t_wall1)
+    sm_mhz = clock_summary.get("sm_mhz")
+    clock_norm = None
+    if sm_mhz:
+        hw_peak = sm_count * BF16_FLOP_PER_SM_CLOCK * sm_mhz * 1e6 / 1e12
+        clock_norm = {"sm_mhz_median": sm_mhz, "sm_count": sm_count,
+                      "tflops_per_sm_ghz": achieved / (sm_mhz / 1e3),
+                      "hw_peak_at_clock_tflops": hw_peak, "frac_of_hw_peak_at_clock": achieved / hw_peak,
+                      "basis": f"{BF16_FLOP_PER_SM_CLOCK} dense bf16 FLOP per SM per clock (one 128x128x16 MMA "
+                               "per 64 cycles) x SMs x median SM clock during the timed region"}
 
     # ---- end to end through the C ABI on host buffers: pinned Q/K/V in, pinned O/LSE out; the
     # library copies in, computes and copies out in pieces that overlap ----
@@ -493,7 +636,7 @@ def main():
     if args.components and rank == 0:
         del q, k, v, o, lse
         torch.cuda.empty_cache()
-        comps = components(oa, dev, peaks, peak_kind, max(5, min(args.steps, 20)))
+        comps = components(oa, dev, peaks, peak_kind, max(5, min(args.steps, 20)), args.component_seconds)
 
     cpu = None
     if args.cpu_baseline and rank == 0 and world == 1:
@@ -509,25 +652,26 @@ def main():
             "n_gpus": world,
             "steps": args.steps,
             "warmup": args.warmup,
-            "ms_per_step": elapsed_ms / args.steps,
+            "ms_per_step": elapsed_ms / n_timed,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic: seeded N(0,1) Q/K/V cast to bf16 (no dataset is named)",
-            "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": True,
-                       "per_gpu_batch": "one (B=1, H=32) batch per rank",
-                       "l2": "inputs larger than L2 (Q+K+V+O = 256 MiB > 129 MB); no flush in the timed loop",
-                       "parallelism": f"replicas x{world} (independent batches, no collective)"},
+            "config": headline_config(world),
+            "timing": {"repeats_of_k_steps": repeats, "timed_steps": n_timed, "timed_region_s": elapsed_ms / 1e3,
+                       "min_seconds": args.min_seconds,
+                       "rule": "the K-step loop repeats until the timed region reaches min_seconds; "
+                               "per-step figures come from all timed steps"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": achieved / peaks["bf16_tflops"], "traffic": profiled_traffic(),
                          "peak_kind": f"{peak_kind} bf16 dense burst", "launch_ms": launch_ms,
-                         "algorithmic_flops_per_launch": flops},
+                         "algorithmic_flops_per_launch": flops, "clock_normalised": clock_norm},
             "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12 * world, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                     "path": "oa_attn_fwd_host: pinned host Q/K/V in, O/LSE out; copies and kernels of 4 tapered "
                             "pieces overlapped", "matches_device_result": e2e_ok},
-            "gpu_launches": args.steps,
+            "gpu_launches": n_timed,
             "clocks": clock_summary,
             "cpu_baseline": cpu,
             "components": comps,
@@ -572,7 +716,7 @@ def main_reference(args, world, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "H": H, "Nq": N, "Nk": N, "d": D, "causal": True},
+        "config": headline_config(world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }))

@@ -338,11 +338,13 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
  * key/value heads than query heads): k and v are [B, H_kv, Nk, d] and query
  * head h reads head h / (H / H_kv); kv_len gives each sequence's cache
  * length.  Same workspace size and support matrix as oa_attn_splitkv.
- * With one query per row (Nq = 1), bf16 and d = 64 / 128, the H / H_kv
- * query heads of a group are consecutive rows of q, o and lse and are
- * computed together by the tensor-core forward kernel, every K/V row read
- * once for the whole group and no split taken (num_splits and the workspace
- * are then checked but not used); the result is the same attention.
+ * Grouped one-query decode takes no split: with Nq = 1, bf16 and d = 64 /
+ * 128 the H / H_kv query heads of a group are consecutive rows of q, o and
+ * lse and are computed together by the tensor-core forward kernel (one
+ * launch), every K/V row read once for the whole group.  On that path
+ * num_splits and the workspace are checked but NOT USED; the result is the
+ * same attention.  Other grouped calls (Nq > 1, fp32) split the keys into
+ * num_splits chunks and merge, as oa_attn_splitkv does.
  * Errors: those of oa_attn_splitkv, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */
@@ -363,8 +365,13 @@ oa_status oa_attn_splitkv_gqa(const void* q, const void* k, const void* v, void*
  *   Limit: num_splits * B*H*Nq * (d + 1) * 4 bytes <= 16 MiB; larger
  *          requests return OA_ERR_INVALID and launch nothing.
  *   Set-up: the first call on a device looks up the array's device address
- *          (cudaGetSymbolAddress) with that device current; make that first
- *          call before any stream capture.
+ *          (cudaGetSymbolAddress) with that device current.  Under CUDA's
+ *          default lazy module loading that lookup also loads the module
+ *          holding the array and commits its 16 MiB on that device, so the
+ *          first call is the only one that can fail for lack of device
+ *          memory (OA_ERR_CUDA) or wait on the driver: make one call with
+ *          valid arguments at start-up, before the latency-critical path
+ *          and before any stream capture.
  *   Sharing: every call uses the same array.  Calls whose work overlaps on
  *          the GPU (other streams, other host threads) race on it; the
  *          caller must serialise them.  Nothing in the array needs to start

@@ -132,6 +132,30 @@ def _require_cuda(*ts):
             raise OAError(OA_ERR_INVALID, "tensors must live on a CUDA device")
 
 
+def _same_device(device, *ts):
+    for t in ts:
+        if t is not None and t.device != device:
+            raise OAError(OA_ERR_INVALID, f"every tensor of a call must be on {device} (got one on {t.device})")
+
+
+def _check_out(t, shape, dtype, device, name):
+    """A caller-supplied output must be exactly what the kernel writes: contiguous, of `shape` and
+    `dtype`, on `device` (anything else would be written past its end or on another GPU)."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous() or t.device != device:
+        raise OAError(OA_ERR_INVALID, f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on "
+                      f"{device} (got {t.dtype} {tuple(t.shape)} on {t.device}, "
+                      f"{'' if t.is_contiguous() else 'non-'}contiguous)")
+
+
+def _check_workspace(ws, device):
+    if ws is None:
+        return
+    if ws.device != device or not ws.is_contiguous():
+        raise OAError(OA_ERR_INVALID, f"workspace must be a contiguous tensor on {device}")
+
+
 def version() -> int:
     return load().oa_version()
 
@@ -150,8 +174,11 @@ def softmax_rows(x: torch.Tensor, y: torch.Tensor | None = None, lse: torch.Tens
         y = torch.empty((rows, cols), dtype=torch.float32, device=x.device)
     if want_lse and lse is None:
         lse = torch.empty(rows, dtype=torch.float32, device=x.device)
-    if y is not None and (y.shape != x.shape or y.stride(1) != 1 or y.dtype != torch.float32):
-        raise OAError(OA_ERR_INVALID, "y must match x's shape with unit column stride")
+    if y is not None and (y.shape != x.shape or y.stride(1) != 1 or y.dtype != torch.float32 or y.device != x.device
+                          or (rows > 1 and y.stride(0) < cols)):
+        raise OAError(OA_ERR_INVALID, "y must be a float32 tensor of x's shape on x's device, unit column stride and "
+                      "row stride >= cols")
+    _check_out(lse, (rows,), torch.float32, x.device, "lse")
     with torch.cuda.device(x.device):
         _check(load().oa_softmax_rows(_ptr(x), rows, cols, x.stride(0), _ptr(y), y.stride(0) if y is not None else 0,
                                       _ptr(lse), _stream(x.device)))
@@ -171,6 +198,7 @@ def _attn_shapes(q, k, v, allow_groups=False):
                       + (" (need a divisor of H)" if allow_groups else " (need the same count)"))
     if not (q.dtype == k.dtype == v.dtype):
         raise OAError(OA_ERR_INVALID, "q, k, v must share a dtype")
+    _same_device(q.device, k, v)
     for t in (q, k, v):
         if not t.is_contiguous():
             raise OAError(OA_ERR_INVALID, "q, k, v must be contiguous")
@@ -194,6 +222,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, kv_len=N
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
+    _check_out(out, (B, H, Nq, d), q.dtype, q.device, "out")
+    _check_out(lse, (B, H, Nq), torch.float32, q.device, "lse")
     if out is None:
         out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
     if want_lse and lse is None:
@@ -269,6 +299,9 @@ def attn_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_
         raise OAError(OA_ERR_INVALID, "cu_seqlens_q and cu_seqlens_k must have the same length")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    _same_device(q.device, k, v)
+    _check_out(out, (Tq, H, d), q.dtype, q.device, "out")
+    _check_out(lse, (Tq, H), torch.float32, q.device, "lse")
     if out is None:
         out = torch.empty((Tq, H, d), dtype=q.dtype, device=q.device)
     if want_lse and lse is None:
@@ -290,6 +323,8 @@ def attn_fwd_f32_tiles(q, k, v, Br: int, Bc: int, causal: bool = False, scale: f
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
+    _check_out(out, (B, H, Nq, d), q.dtype, q.device, "out")
+    _check_out(lse, (B, H, Nq), torch.float32, q.device, "lse")
     if out is None:
         out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
     if lse is None:
@@ -321,6 +356,11 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
         raise OAError(OA_ERR_INVALID, "lse must be a contiguous float32 [B, H, Nq] tensor")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    _same_device(q.device, o, lse, dout)
+    _check_out(dq, (B, H, Nq, d), q.dtype, q.device, "dq")
+    _check_out(dk, (B, Hkv, Nk, d), q.dtype, q.device, "dk")
+    _check_out(dv, (B, Hkv, Nk, d), q.dtype, q.device, "dv")
+    _check_workspace(workspace, q.device)
     need = attn_bwd_workspace_bytes(B, H, Nq, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -362,6 +402,11 @@ def attn_bwd_varlen(q, k, v, o, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqle
         raise OAError(OA_ERR_INVALID, "cu_seqlens_q and cu_seqlens_k must have the same length")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    _same_device(q.device, k, v, o, lse, dout)
+    _check_out(dq, (Tq, H, d), q.dtype, q.device, "dq")
+    _check_out(dk, (Tk, Hkv, d), q.dtype, q.device, "dk")
+    _check_out(dv, (Tk, Hkv, d), q.dtype, q.device, "dv")
+    _check_workspace(workspace, q.device)
     need = attn_bwd_workspace_bytes(1, H, Tq, d)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -391,6 +436,9 @@ def attn_splitkv(q, k, v, num_splits: int, scale: float | None = None, kv_len=No
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
+    _check_out(out, (B, H, Nq, d), q.dtype, q.device, "out")
+    _check_out(lse, (B, H, Nq), torch.float32, q.device, "lse")
+    _check_workspace(workspace, q.device)
     need = splitkv_workspace_bytes(B, H, Nq, d, num_splits)
     if workspace is None:
         workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
@@ -415,6 +463,8 @@ def attn_splitkv_static(q, k, v, num_splits: int, scale: float | None = None, kv
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     kv = _kv_len_arg(kv_len, B, q.device)
+    _check_out(out, (B, H, Nq, d), q.dtype, q.device, "out")
+    _check_out(lse, (B, H, Nq), torch.float32, q.device, "lse")
     if out is None:
         out = torch.empty((B, H, Nq, d), dtype=q.dtype, device=q.device)
     if lse is None:
@@ -438,6 +488,13 @@ def lse_merge(part_o, part_lse, out_dtype=torch.float32, out=None, lse=None):
                 not part_o.is_contiguous():
             raise OAError(OA_ERR_INVALID, "part_o must be a contiguous float32 [S, R, d] tensor")
         d = part_o.shape[2]
+        _same_device(part_lse.device, part_o)
+    if out is not None:
+        if d == 0:
+            raise OAError(OA_ERR_INVALID, "out is only written when part_o is given")
+        _check_out(out, (R, d), out.dtype, part_lse.device, "out")
+        _dtype_code(out.dtype)
+    _check_out(lse, (R,), torch.float32, part_lse.device, "lse")
     if d > 0 and out is None:
         out = torch.empty((R, d), dtype=out_dtype, device=part_lse.device)
     if lse is None:

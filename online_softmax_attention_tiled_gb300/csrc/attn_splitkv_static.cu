@@ -8,10 +8,14 @@
 // latency-critical path where an allocation could block or fail.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds its 16 MiB until the process exits.  Host code cannot use
-// the array's name as a device address, so the address is looked up with
-// cudaGetSymbolAddress once per device (with that device current) on the
-// first call there, and then passed to the kernels.
+// library's module holding it keeps its 16 MiB until the process exits.
+// Host code cannot use the array's name as a device address, so the address
+// is looked up with cudaGetSymbolAddress once per device (with that device
+// current) on the first call there, and then passed to the kernels.  Under
+// CUDA's lazy module loading (the default) that first lookup is also what
+// loads the module onto the device and commits the 16 MiB, so the first
+// call on a device is the one that can fail for lack of device memory or
+// wait on the driver; callers should make it once at start-up.
 //
 // The kernels write every partial they later read (an empty chunk writes
 // o_c = 0, lse_c = -inf), so nothing in the array has to start at zero and
@@ -25,6 +29,9 @@
 
 namespace oa {
 oa_status api_fail(oa_status s, const char* msg);
+oa_status api_check_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
+                            int Hkv, int Nq, int Nk, int d, float scale, const int32_t* kv_len, int num_splits,
+                            const char* who);
 oa_status api_ok();
 bool api_dev_status(DevStatus* st);
 }  // namespace oa
@@ -66,22 +73,11 @@ extern "C" oa_status oa_attn_splitkv_static(const void* q, const void* k, const 
                                             oa_dtype dt, int B, int H, int Nq, int Nk, int d, float scale,
                                             const int32_t* kv_len, int num_splits, oa_stream_t stream) {
   using oa::api_fail;
-  if (!q || !k || !v || !o) return api_fail(OA_ERR_INVALID, "attn_splitkv_static: q, k, v and o must be non-NULL");
-  if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || d < 1)
-    return api_fail(OA_ERR_INVALID, "attn_splitkv_static: sizes must be >= 1");
-  if (!(scale > 0.f && scale < INFINITY))
-    return api_fail(OA_ERR_INVALID, "attn_splitkv_static: scale must be finite and > 0");
-  if (!is_aligned(q, 16) || !is_aligned(k, 16) || !is_aligned(v, 16) || !is_aligned(o, 16) || !is_aligned(lse, 4) ||
-      !is_aligned(kv_len, 4))
-    return api_fail(OA_ERR_INVALID, "attn_splitkv_static: q/k/v/o must be 16-byte aligned, lse and kv_len 4-byte");
-  if (dt != OA_BF16 && dt != OA_F32) return api_fail(OA_ERR_INVALID, "attn_splitkv_static: unknown dtype");
-  if (!oa::splitkv_supported(dt == OA_BF16, d))
-    return api_fail(OA_ERR_UNSUPPORTED, "attn_splitkv_static: unsupported (dtype, d)");
-  if (num_splits < 1 || num_splits > 1024)
-    return api_fail(OA_ERR_INVALID, "attn_splitkv_static: 1 <= num_splits <= 1024");
+  // the checks of oa_attn_splitkv (one key/value head per query head), then the scratch limit
+  const oa_status s =
+      oa::api_check_splitkv(q, k, v, o, lse, dt, B, H, H, Nq, Nk, d, scale, kv_len, num_splits, "attn_splitkv_static");
+  if (s != OA_OK) return s;
   const int64_t R = (int64_t)B * H * Nq;
-  if (R > ((int64_t)1 << 30) || R * num_splits > 2147483647)
-    return api_fail(OA_ERR_INVALID, "attn_splitkv_static: B*H*Nq*num_splits too large");
   const size_t need = (size_t)num_splits * (size_t)R * ((size_t)d + 1);
   if (need > kScratchFloats)
     return api_fail(OA_ERR_INVALID,

@@ -562,19 +562,30 @@ size_t oa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
   return (floats * sizeof(float) + 255) / 256 * 256;
 }
 
+// Every check of a split-KV call except its scratch memory (shared by oa_attn_splitkv,
+// oa_attn_splitkv_gqa and oa_attn_splitkv_static).
+static oa_status check_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
+                               int H, int Hkv, int Nq, int Nk, int d, float scale, const int32_t* kv_len,
+                               int num_splits, const char* who) {
+  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, 0, scale, who);
+  if (s != OA_OK) return s;
+  if ((s = check_heads(H, Hkv, who)) != OA_OK) return s;
+  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "%s: unknown dtype %d", who, (int)dt);
+  if (!oa::splitkv_supported(dt == OA_BF16, d))
+    return fail(OA_ERR_UNSUPPORTED, "%s: unsupported (dtype %d, d %d)", who, (int)dt, d);
+  if (num_splits < 1 || num_splits > 1024) return fail(OA_ERR_INVALID, "%s: 1 <= num_splits <= 1024", who);
+  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "%s: kv_len must be 4-byte aligned", who);
+  const int64_t R = (int64_t)B * H * Nq;
+  if (R * num_splits > kMaxGrid) return fail(OA_ERR_INVALID, "%s: rows * num_splits too large", who);
+  return OA_OK;
+}
+
 static oa_status attn_splitkv_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,
                                    int B, int H, int Hkv, int Nq, int Nk, int d, float scale, const int32_t* kv_len,
                                    int num_splits, void* workspace, size_t workspace_bytes, oa_stream_t stream) {
-  oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, 0, scale, "attn_splitkv");
+  oa_status s = check_splitkv(q, k, v, o, lse, dt, B, H, Hkv, Nq, Nk, d, scale, kv_len, num_splits, "attn_splitkv");
   if (s != OA_OK) return s;
-  if ((s = check_heads(H, Hkv, "attn_splitkv")) != OA_OK) return s;
-  if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "attn_splitkv: unknown dtype %d", (int)dt);
-  if (!oa::splitkv_supported(dt == OA_BF16, d))
-    return fail(OA_ERR_UNSUPPORTED, "attn_splitkv: unsupported (dtype %d, d %d)", (int)dt, d);
-  if (num_splits < 1 || num_splits > 1024) return fail(OA_ERR_INVALID, "attn_splitkv: 1 <= num_splits <= 1024");
-  if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_splitkv: kv_len must be 4-byte aligned");
   const int64_t R = (int64_t)B * H * Nq;
-  if (R * num_splits > kMaxGrid) return fail(OA_ERR_INVALID, "attn_splitkv: rows * num_splits too large");
   const size_t need = oa_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
     return fail(OA_ERR_INVALID, "attn_splitkv: workspace must be 16-byte aligned and >= %zu bytes", need);
@@ -659,6 +670,11 @@ oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream) {
 // last error / success for oa_last_error(), and fetch the status word.
 namespace oa {
 oa_status api_fail(oa_status s, const char* msg) { return fail(s, "%s", msg); }
+oa_status api_check_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B, int H,
+                            int Hkv, int Nq, int Nk, int d, float scale, const int32_t* kv_len, int num_splits,
+                            const char* who) {
+  return check_splitkv(q, k, v, o, lse, dt, B, H, Hkv, Nq, Nk, d, scale, kv_len, num_splits, who);
+}
 oa_status api_ok() { return ok(); }
 bool api_dev_status(DevStatus* st) { return dev_status(st); }
 }  // namespace oa

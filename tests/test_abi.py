@@ -199,3 +199,34 @@ def test_product_package_does_not_touch_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "oracle.c" not in text and "liboa_oracle" not in text, f
+
+
+def test_binding_rejects_mismatched_outputs_before_any_launch():
+    """The wrappers check caller-supplied outputs (shape, dtype, contiguity, device) before calling
+    the library: a wrong `out` would otherwise be written past its end or on another GPU."""
+    import torch
+
+    cpu = torch.device("cpu")
+    good = torch.empty((2, 3, 5, 8), dtype=torch.bfloat16)
+    oa._check_out(None, (2, 3, 5, 8), torch.bfloat16, cpu, "out")
+    oa._check_out(good, (2, 3, 5, 8), torch.bfloat16, cpu, "out")
+    bad = [
+        torch.empty((2, 3, 4, 8), dtype=torch.bfloat16),            # too small
+        torch.empty((2, 3, 5, 8), dtype=torch.float32),             # wrong dtype
+        torch.empty((2, 3, 8, 5), dtype=torch.bfloat16).transpose(2, 3),  # right shape, not contiguous
+    ]
+    for t in bad:
+        with pytest.raises(oa.OAError) as ei:
+            oa._check_out(t, (2, 3, 5, 8), torch.bfloat16, cpu, "out")
+        assert ei.value.status == oa.OA_ERR_INVALID
+    with pytest.raises(oa.OAError):
+        oa._check_out(good, (2, 3, 5, 8), torch.bfloat16, torch.device("cuda", 0), "out")
+    with pytest.raises(oa.OAError):
+        oa._same_device(torch.device("cuda", 0), good)
+    # every device wrapper that takes outputs checks them
+    import inspect
+
+    for name in ("attn_fwd", "attn_fwd_varlen", "attn_fwd_f32_tiles", "attn_splitkv", "attn_splitkv_static",
+                 "attn_bwd", "attn_bwd_varlen", "lse_merge", "softmax_rows"):
+        src = inspect.getsource(getattr(oa, name))
+        assert "_check_out(" in src, name

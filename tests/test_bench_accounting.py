@@ -45,3 +45,49 @@ def test_benchmarked_workloads():
     assert bench.decode_bytes(32, 32, 128, kv, h_kv=8) == pytest.approx(4060651520.0)
     lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
     assert bench.varlen_causal_flops(lens, 32, 128) == pytest.approx(5170632589312.0)
+
+
+@pytest.mark.parametrize("nq,nk", [(1, 1), (1, 9), (3, 7), (5, 5), (17, 40), (7, 3)])
+def test_kvcache_causal_counts_match_brute_force(nq, nk):
+    # the queries are the last nq positions of nk keys: query i sees keys j <= i + (nk - nq)
+    pairs = sum(1 for i, j in itertools.product(range(nq), range(nk)) if j <= i + nk - nq)
+    assert bench.causal_pairs(nq, nk) == pairs
+    assert bench.kvcache_causal_flops(2, 3, nq, nk, 8) == pytest.approx(4 * 8 * 2 * 3 * pairs)
+    if nq == nk:
+        assert bench.kvcache_causal_flops(2, 3, nq, nk, 8) == pytest.approx(bench.causal_attn_flops(2, 3, nq, 8))
+
+
+def test_dense_bwd_flops():
+    assert bench.dense_attn_bwd_flops(4, 16, 4096, 4096, 64) == pytest.approx(2.5 * 4 * 4 * 16 * 4096 * 4096 * 64)
+
+
+def test_time_floor_repeats():
+    # the K-step loop repeats until the timed region reaches the floor
+    assert bench.repeats_for(3.0, 20, 0.38) == 395  # ceil(3000 / 7.6)
+    assert bench.repeats_for(3.0, 400, 10.0) == 1
+    assert bench.repeats_for(0.0, 20, 0.38) == 1
+    r = bench.repeats_for(2.0, 20, 0.38)
+    assert r * 20 * 0.38 >= 2000.0 and (r - 1) * 20 * 0.38 < 2000.0
+
+
+def test_clock_line_parsing():
+    line = "0, 1965, 2070, 1012.55, 0x0000000000000004, Not Active, Not Active, Not Active, Active"
+    sm, smax, pw, act = bench.ClockSampler.parse(line)
+    assert (sm, smax, pw) == (1965.0, 2070.0, 1012.55)
+    assert act == {"hw_slowdown": False, "hw_thermal_slowdown": False, "sw_thermal_slowdown": False,
+                   "sw_power_cap": True}
+    assert bench.ClockSampler.parse("0, [N/A], 2070, 5, x, a, b, c, d") is None
+    assert bench.ClockSampler.parse("garbage") is None
+
+
+def test_both_arms_report_the_same_config():
+    import inspect
+    src = inspect.getsource(bench.main_reference) + inspect.getsource(bench.main)
+    assert src.count("headline_config(world)") == 2
+    cfg = bench.headline_config(1)
+    assert cfg["Nq"] == cfg["Nk"] == 8192 and cfg["causal"] is True and "parallelism" in cfg
+
+
+def test_case_table_covers_the_components():
+    assert set(bench.COMPONENTS) | {"attn_causal"} == set(bench.CASES)
+    assert "attn_bwd_noncausal_d64" in bench.COMPONENTS and "attn_decode_gqa" in bench.COMPONENTS
