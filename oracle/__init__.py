@@ -119,7 +119,9 @@ def attention(q, k, v, causal=False, scale=None, kv_len=None, rows=None, nthread
     """Materialised softmax(Q K^T * scale) V and per-row LSE, in fp64.
 
     q [B,H,Nq,d], k/v [B,Hkv,Nk,d] (same dtype code; Hkv divides H and query head h
-    reads key/value head h // (H // Hkv)).  kv_len: None or int array [B].
+    reads key/value head h // (H // Hkv)).  kv_len: None or int array [B] (keys j >= kv_len[b]
+    hidden).  causal: the queries are the last Nq positions of the Nk keys' sequence, so key j
+    is visible to query i iff j <= i + (Nk - Nq) (j <= i when Nq == Nk).
     rows: None for every row, else flattened row indices (b*H + h)*Nq + i; then the
     result has shape [len(rows), d] and [len(rows)].
     """
@@ -165,7 +167,7 @@ def attention_bwd(q, k, v, dout, causal=False, scale=None, nthreads=None):
 
     q, dout [B,H,Nq,d]; k, v [B,Hkv,Nk,d] (same dtype code; Hkv divides H and query head h reads
     key/value head h // (H // Hkv); the dk, dv of a key/value head sum over its query heads).
-    Causal: key j visible to query i iff j <= i.  P is recomputed from the scores (no stored
+    Causal: key j visible to query i iff j <= i + (Nk - Nq).  P is recomputed from the scores (no stored
     attention matrix), as the backward of the forward definition; see oracle.c for the formulas."""
     qa, code = _as_input(q)
     ka, kcode = _as_input(k)
@@ -222,7 +224,8 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, causal=False, scale=No
     """Attention over packed sequences, in fp64: q [Tq,H,d], k/v [Tk,Hkv,d] (token-major, same dtype
     code); sequence s is q tokens [cu_q[s], cu_q[s+1]) and k/v tokens [cu_k[s], cu_k[s+1]).  Each
     sequence is the attention() of its own tokens (the per-(b, h) definition above, one batch entry;
-    causal: key j visible to query i iff j <= i, positions counted within the sequence).  Only
+    causal: key j visible to query i iff j <= i + (lk - lq) for a sequence of lq queries and lk
+    keys, i.e. its queries are its last lq positions).  Only
     slicing and transposes happen here.  Returns (o [Tq,H,d], lse [Tq,H])."""
     qa, _ = _as_input(q)
     ka, _ = _as_input(k)

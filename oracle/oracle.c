@@ -23,8 +23,13 @@
  *   - a row whose elements are all -inf (fully masked) has output +0.0 and
  *     log-sum-exp -inf, never NaN ([OS-RM] s.7 "fully-masked rows";
  *     [OS-IL] Step 1, both-sides -inf special case);
- *   - causal visibility: key j is visible to query i iff j <= i
- *     ([OS-PT] "Why this matters for attention specifically": t2 = 0..t1);
+ *   - causal visibility: query t1 sees keys t2 = 0..t1 ([OS-PT] "Why this
+ *     matters for attention specifically"), positions counted along the
+ *     sequence.  With Nq queries and Nk keys the queries are the sequence's
+ *     last Nq positions (new tokens after a cache of Nk - Nq keys), so key j
+ *     is visible to query i iff j <= i + (Nk - Nq); for Nq == Nk that is
+ *     j <= i.  A query with no visible key (Nq > Nk, i < Nq - Nk) has output
+ *     +0.0 and log-sum-exp -inf;
  *   - the log-sum-exp is natural-log, over the scaled scores.
  *
  * Build: gcc -O2 -ffp-contract=off -fno-fast-math -shared -fPIC -pthread.
@@ -162,7 +167,8 @@ int oracle_softmax_rows(const void* x, int dtype, int64_t rows, int64_t cols, in
 /* Attention: materialise one full score row, safe softmax, weighted    */
 /* sum of value rows.                                                   */
 /* [OS-RM] s.5: A_i = sum_j softmax(Q K^T)_ij V_j;                      */
-/* [OS-PT]: s_t2 = (q_t1 . k_t2) / sqrt(hd), causal t2 <= t1;           */
+/* [OS-PT]: s_t2 = (q_t1 . k_t2) / sqrt(hd), causal t2 <= t1 (query i   */
+/* at position i + Nk - Nq of the sequence, see the conventions above); */
 /* [OS-IL] Step 2: S = q K^T * scale.                                   */
 /* Layout: q [B,H,Nq,d], k and v [B,Hkv,Nk,d], row-major contiguous;  */
 /* query head h reads key/value head h / (H / Hkv) (grouped heads;      */
@@ -194,9 +200,10 @@ static void attn_range(void* p, int64_t t0, int64_t t1, double* s) {
     }
     const int64_t h = bh % c->H, kvh = b * c->Hkv + h / (c->H / c->Hkv);
     const int64_t qbase = row * d, kvbase = kvh * c->Nk * d;
+    const int64_t last = i + (c->Nk - c->Nq); /* causal: last visible key */
     /* full score row, -inf where masked */
     for (int64_t j = 0; j < c->Nk; ++j) {
-      int visible = (j < kvl) && (!c->causal || j <= i);
+      int visible = (j < kvl) && (!c->causal || j <= last);
       if (!visible) {
         s[j] = -INFINITY;
         continue;
@@ -290,7 +297,7 @@ static void bwd_range(void* p, int64_t t0, int64_t t1, double* scratch) {
       double m = -INFINITY;
       for (int64_t j = 0; j < Nk; ++j) {
         double s = -INFINITY;
-        if (!c->causal || j <= i) {
+        if (!c->causal || j <= i + (Nk - Nq)) {
           double dot = 0.0;
           for (int64_t e = 0; e < d; ++e)
             dot += widen(c->q, c->dtype, qb + i * d + e) * widen(c->k, c->dtype, kb + j * d + e);
@@ -380,7 +387,7 @@ typedef struct {
 } bwds_ctx;
 
 static double bwds_score(const bwds_ctx* c, int64_t i, int64_t j) {
-  if (c->causal && j > i) return -INFINITY;
+  if (c->causal && j > i + (c->Nk - c->Nq)) return -INFINITY;
   double dot = 0.0;
   for (int64_t e = 0; e < c->d; ++e) dot += widen(c->q, c->dtype, i * c->d + e) * widen(c->k, c->dtype, j * c->d + e);
   return c->scale * dot;

@@ -213,16 +213,30 @@ def test_softmax_dtype_widening_is_exact():
 # Attention: SDPA in fp64, closed forms, invariants, brute force (FA-1 order)
 # ---------------------------------------------------------------------------
 
+def _lower_right_mask(Nq, Nk):
+    """torch's own lower-right causal mask (query i sees key j iff j <= i + Nk - Nq): an
+    independent statement of the bottom-right reading the oracle implements."""
+    import warnings
+
+    from torch.nn.attention.bias import causal_lower_right
+
+    with warnings.catch_warnings():
+        warnings.simplefilter("ignore")  # torch warns that Nq > Nk leaves rows without keys
+        return causal_lower_right(Nq, Nk)._materialize(torch.device("cpu"))
+
+
 def _sdpa_ref(q, k, v, causal, scale, kv_len=None):
-    """fp64 library reference with an explicit boolean mask, plus logsumexp of the scores."""
+    """fp64 library reference with an explicit boolean mask, plus logsumexp of the scores.  Rows with
+    no visible key (SDPA gives NaN there) are returned as O = 0, their logsumexp is -inf."""
     B, H, Nq, d = q.shape
     Nk = k.shape[2]
     vis = torch.ones(B, 1, Nq, Nk, dtype=torch.bool)
     if causal:
-        vis &= torch.ones(Nq, Nk, dtype=torch.bool).tril()
+        vis &= _lower_right_mask(Nq, Nk)
     if kv_len is not None:
         vis &= (torch.arange(Nk)[None, :] < torch.as_tensor(kv_len)[:, None]).view(B, 1, 1, Nk)
     o = F.scaled_dot_product_attention(q, k, v, attn_mask=vis, scale=scale)
+    o = torch.where(vis.any(-1, keepdim=True), o, torch.zeros_like(o))
     s = torch.einsum("bhid,bhjd->bhij", q, k) * scale
     s = s.masked_fill(~vis, NEG_INF)
     return o, torch.logsumexp(s, -1), vis
@@ -246,6 +260,55 @@ def test_attention_vs_sdpa_masked(causal):
     ro, rl, _ = _sdpa_ref(q, k, v, causal, 1 / math.sqrt(d), kv_len)
     np.testing.assert_allclose(o, ro.numpy(), rtol=0, atol=1e-12)
     np.testing.assert_allclose(lse, rl.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("Nq,Nk", [(1, 9), (3, 11), (7, 7), (5, 40), (12, 5), (4, 1)])
+def test_attention_kv_cache_causal_vs_lower_right_sdpa(Nq, Nk):
+    # Nq new queries against Nk keys (chunked prefill / multi-token decode): the queries are the last
+    # Nq positions, so query i sees keys j <= i + Nk - Nq -- torch's lower-right causal mask.  With
+    # Nq > Nk the first Nq - Nk queries see no key: O = +0.0 and LSE = -inf, no NaN.
+    B, H, d = 2, 3, 8
+    q, k, v = si.attn_inputs(B, H, Nq, Nk, d, torch.float64, seed=40 + Nq * 7 + Nk)
+    o, lse = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=True)
+    ro, rl, vis = _sdpa_ref(q, k, v, True, 1 / math.sqrt(d))
+    assert not np.isnan(o).any() and not np.isnan(lse).any()
+    np.testing.assert_allclose(o, ro.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(rl.numpy()))
+    fin = np.isfinite(rl.numpy())
+    np.testing.assert_allclose(lse[fin], rl.numpy()[fin], rtol=0, atol=1e-12)
+    empty = ~vis.any(-1).expand(B, H, Nq).numpy()
+    assert empty.sum() == B * H * max(0, Nq - Nk)
+    assert np.all(o[empty] == 0.0) and not np.any(np.signbit(o[empty]))
+
+
+def test_attention_kv_cache_causal_closed_forms():
+    # K == 0: every visible score is 0, so query i averages V_0 .. V_{i + Nk - Nq} and LSE = ln(i + Nk - Nq + 1)
+    Nq, Nk, d = 4, 10, 3
+    rng = np.random.default_rng(8)
+    q, v = rng.standard_normal((1, 1, Nq, d)), rng.standard_normal((1, 1, Nk, d))
+    o, lse = oracle.attention(q, np.zeros((1, 1, Nk, d)), v, causal=True)
+    for i in range(Nq):
+        last = i + Nk - Nq
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :last + 1].mean(0), rtol=1e-13, atol=1e-14)
+        assert lse[0, 0, i] == pytest.approx(math.log(last + 1), abs=1e-14)
+    # one new query sees the whole cache: causal is the same as non-causal
+    q1 = rng.standard_normal((2, 2, 1, d))
+    k1, v1 = rng.standard_normal((2, 2, 17, d)), rng.standard_normal((2, 2, 17, d))
+    oc, lc = oracle.attention(q1, k1, v1, causal=True)
+    on, ln_ = oracle.attention(q1, k1, v1, causal=False)
+    np.testing.assert_array_equal(oc, on)
+    np.testing.assert_array_equal(lc, ln_)
+
+
+def test_attention_chunked_prefill_equals_last_rows_of_full_causal():
+    # the last Nq rows of causal attention over a whole sequence of N tokens are the causal attention
+    # of those Nq queries against all N keys (the chunk after a cache of N - Nq keys)
+    N, Nq, d = 23, 6, 8
+    q, k, v = si.attn_inputs(2, 2, N, N, d, torch.float64, seed=44)
+    of, lf = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=True)
+    oc, lc = oracle.attention(q[:, :, N - Nq:].contiguous().numpy(), k.numpy(), v.numpy(), causal=True)
+    np.testing.assert_array_equal(oc, of[:, :, N - Nq:])
+    np.testing.assert_array_equal(lc, lf[:, :, N - Nq:])
 
 
 def test_attention_scale_and_noncausal_rectangular():
@@ -362,10 +425,12 @@ def _partials(q, k, v, chunk, kv_len=None):
 
 
 def _brute_attention_rows(q, k, v, causal, scale):
-    """softmax(q k^T scale) v for one head in plain fp64 numpy, -inf where masked (key j > query i)."""
+    """softmax(q k^T scale) v for one head in plain fp64 numpy, -inf where masked (causal: key j
+    hidden from query i when j > i + Nk - Nq, the queries being the sequence's last Nq positions)."""
     s = (q @ k.T) * scale
     if causal:
-        s = np.where(np.arange(k.shape[0])[None, :] > np.arange(q.shape[0])[:, None], -np.inf, s)
+        off = k.shape[0] - q.shape[0]
+        s = np.where(np.arange(k.shape[0])[None, :] > np.arange(q.shape[0])[:, None] + off, -np.inf, s)
     m = s.max(axis=1, keepdims=True) if s.shape[1] else np.full((s.shape[0], 1), -np.inf)
     o = np.zeros((q.shape[0], v.shape[1]))
     lse = np.full(q.shape[0], -np.inf)
@@ -419,7 +484,7 @@ def test_attention_varlen_equal_lengths_is_dense_batch():
 
 def test_attention_varlen_brute_force_mixed_lengths():
     # mixed lengths, a sequence without keys (O = 0, lse = -inf), one without queries, and causal
-    # with more keys than queries (key j visible to query i iff j <= i within the sequence)
+    # with more keys than queries (key j visible to query i iff j <= i + lk - lq within the sequence)
     rng = np.random.default_rng(7)
     H, Hkv, d = 4, 2, 8
     lq, lk = [5, 3, 0, 6], [7, 0, 2, 6]
@@ -447,9 +512,10 @@ def _autograd_bwd(q, k, v, dout, causal, scale):
     s = scale * tq @ tk.transpose(-1, -2)
     if causal:
         Nq, Nk = s.shape[-2:]
-        hide = torch.arange(Nk)[None, :] > torch.arange(Nq)[:, None]
-        s = s.masked_fill(hide, float("-inf"))
-    o = torch.softmax(s, dim=-1) @ tv
+        s = s.masked_fill(~_lower_right_mask(Nq, Nk), float("-inf"))
+    # a row without a visible key (Nq > Nk) has a constant zero output, so no gradient
+    p = torch.nan_to_num(torch.softmax(s, dim=-1), nan=0.0)
+    o = p @ tv
     o.backward(torch.tensor(dout, dtype=torch.float64))
     return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
 
@@ -494,7 +560,7 @@ def test_attention_bwd_grouped_heads_vs_fp64_autograd(causal):
 def test_attention_bwd_varlen_vs_fp64_autograd():
     # packed sequences of mixed lengths (one without keys, one without queries, causal with more keys than
     # queries): every token's gradient is that of its own sequence, computed here by torch autograd
-    lq, lk = [5, 0, 7, 3, 6], [5, 4, 7, 0, 9]
+    lq, lk = [5, 0, 7, 3, 6, 4], [5, 4, 7, 0, 9, 2]
     H, Hkv, d = 4, 2, 6
     rng = np.random.default_rng(77)
     Tq, Tk = sum(lq), sum(lk)
@@ -511,8 +577,8 @@ def test_attention_bwd_varlen_vs_fp64_autograd():
             tq, tk, tv = (torch.tensor(a.transpose(1, 0, 2), requires_grad=True) for a in (q[sl_q], k[sl_k], v[sl_k]))
             sc = 0.4 * tq @ tk.repeat_interleave(H // Hkv, 0).transpose(-1, -2)
             if causal:
-                sc = sc.masked_fill(torch.arange(lk[s])[None, :] > torch.arange(lq[s])[:, None], float("-inf"))
-            out = torch.softmax(sc, -1) @ tv.repeat_interleave(H // Hkv, 0)
+                sc = sc.masked_fill(~_lower_right_mask(lq[s], lk[s]), float("-inf"))
+            out = torch.nan_to_num(torch.softmax(sc, -1), nan=0.0) @ tv.repeat_interleave(H // Hkv, 0)
             out.backward(torch.tensor(do[sl_q].transpose(1, 0, 2)))
             rq[sl_q], rk[sl_k], rv[sl_k] = (t.grad.numpy().transpose(1, 0, 2) for t in (tq, tk, tv))
         for a, r in ((dq, rq), (dk, rk), (dv, rv)):
@@ -566,7 +632,7 @@ def test_attention_bwd_closed_forms():
     np.testing.assert_allclose(dv[:, :, 0], do.sum(axis=2), rtol=1e-12)
 
 
-@pytest.mark.parametrize("causal,Nq,Nk", [(False, 9, 13), (True, 11, 11), (False, 1, 1)])
+@pytest.mark.parametrize("causal,Nq,Nk", [(False, 9, 13), (True, 11, 11), (False, 1, 1), (True, 6, 14), (True, 9, 4)])
 def test_attention_bwd_sampled_vs_fp64_autograd(causal, Nq, Nk):
     # the row-sampled gradients against torch's fp64 autograd, at every row and at a shuffled subset
     rng = np.random.default_rng(100 + Nq)
