@@ -369,6 +369,17 @@ def _case_attn_varlen(oa, si, torch, dev, batch):
                 "tokens), H=32 H_kv=8 d=128")
 
 
+def _case_prefill_kv_cache(oa, si, torch, dev, batch):
+    b, h, hkv, nq, nk, d = batch or 8, 32, 8, 2048, 32768, 128
+    q, k, v = si.attn_inputs_gqa(b, h, hkv, nq, nk, d, torch.bfloat16, seed=0, device=dev)
+    o, lse = torch.empty_like(q), torch.empty((b, h, nq), dtype=torch.float32, device=dev)
+    return Case(lambda: oa.attn_fwd(q, k, v, causal=True, out=o, lse=lse), kvcache_causal_flops(b, h, nq, nk, d),
+                "TFLOP/s", "tensor",
+                f"chunked prefill: causal attention fwd bf16 of {nq} new queries against a {nk}-key cache (the "
+                f"queries are the last positions), B={b} H={h} H_kv={hkv} d={d}; FLOPs over visible pairs only "
+                f"(K/V {b * hkv * nk * d * 4 / 2**30:.1f} GiB > L2)", flush=False)
+
+
 def _bwd_case(oa, si, torch, dev, b, h, hkv, n, d, causal, workload):
     q, k, v = si.attn_inputs_gqa(b, h, hkv, n, n, d, torch.bfloat16, seed=0, device=dev)
     do = si.randn((b, h, n, d), 3, torch.bfloat16, dev)
@@ -402,6 +413,7 @@ CASES = {
     "attn_splitkv_decode": _case_decode,
     "attn_decode_gqa": _case_decode_gqa,
     "attn_varlen_causal_gqa": _case_attn_varlen,
+    "attn_prefill_kv_cache": _case_prefill_kv_cache,
     "attn_bwd_causal": _case_bwd_causal,
     "attn_bwd_causal_gqa": _case_bwd_causal_gqa,
     "attn_bwd_noncausal_d64": _case_bwd_noncausal_d64,

@@ -10,7 +10,10 @@
  *   - "Online Softmax" (research-hub concept page), "Key math": running
  *     (m, l, o) with rescale alpha = exp(m_old - m_new), exact result.
  *   - "Online softmax in attention -- why and how": scores
- *     (q . k) / sqrt(hd), causal mask t2 <= t1.
+ *     (q . k) / sqrt(hd), causal mask t2 <= t1 (positions along the
+ *     sequence; with Nq queries and Nk keys the queries are the sequence's
+ *     last Nq positions, so key j is visible to query i iff
+ *     j <= i + (Nk - Nq)).
  *   - "Online Softmax & FlashAttention -- AI infra interview lesson":
  *     Step 1 (m, l) merge with the both-sides -inf special case and
  *     LSE = m + log l; Step 2 normalised-output merge; Steps 3-5
@@ -99,7 +102,13 @@ oa_status oa_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld
  *   q      [B, H, Nq, d], k and v [B, H, Nk, d], o [B, H, Nq, d]: all of
  *          dtype dt, contiguous row-major, 16-byte aligned.
  *   lse    fp32 [B, H, Nq], or NULL.
- *   causal 0 or 1.  Key j is visible to query i iff j <= i; needs Nq == Nk.
+ *   causal 0 or 1.  The Nq queries are the last Nq positions of the Nk
+ *          keys' sequence (new tokens after a KV cache of Nk - Nq keys:
+ *          chunked prefill, multi-token decode), so key j is visible to
+ *          query i iff j <= i + (Nk - Nq); j <= i when Nq == Nk.  With
+ *          Nq > Nk the first Nq - Nk queries see no key (O = +0.0, LSE =
+ *          -inf).  kv_len masks keys on top of this; it does not move the
+ *          diagonal.
  *   scale  multiplies q . k before the softmax (callers normally pass
  *          1/sqrt(d)).  Must be finite and > 0.
  *   kv_len NULL, or a device int32 [B]: keys j >= kv_len[b] are masked
@@ -108,8 +117,8 @@ oa_status oa_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld
  * 64 or 128 (else OA_ERR_UNSUPPORTED).  fp32: SIMT kernel in fp32,
  * 1 <= d <= 256.
  * Errors: OA_ERR_INVALID for NULL q/k/v/o, sizes < 1 (B, H, Nq, Nk, d),
- * misalignment or a bad scale; OA_ERR_UNSUPPORTED for causal with
- * Nq != Nk or an unsupported (dtype, d).
+ * misalignment or a bad scale; OA_ERR_UNSUPPORTED for an unsupported
+ * (dtype, d).
  */
 oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt,
                       int B, int H, int Nq, int Nk, int d, int causal, float scale,
@@ -124,9 +133,10 @@ oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  * length and KV-cache calls) is read to ask for.
  *   q, o [B, H, Nq, d]; k, v [B, H_kv, Nk, d]; everything else as in
  *   oa_attn_fwd (dtype, alignment, lse, causal, scale, kv_len, support).
- * With one query per row (Nq = 1, not causal, bf16), the query heads of a
- * group are run as the rows of one [B, H_kv, H / H_kv, d] problem, so each
- * group's K/V is read once (the decode case).
+ * With one query per row (Nq = 1, bf16; causal changes nothing for one
+ * query, which sees every key), the query heads of a group are run as the
+ * rows of one [B, H_kv, H / H_kv, d] problem, so each group's K/V is read
+ * once (the decode case).
  * Errors: those of oa_attn_fwd, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */
@@ -150,7 +160,9 @@ oa_status oa_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
  *   max_seqlen_q, max_seqlen_k   the longest query / key sequence.  A
  *           query sequence longer than max_seqlen_q has its tail rows left
  *           unwritten and the status word records it (oa_sync_status).
- *   causal  0 or 1: key j of a sequence is visible to its query i iff j <= i.
+ *   causal  0 or 1: a sequence with lq queries and lk keys has its queries
+ *           at its last lq positions, so its key j is visible to its query
+ *           i iff j <= i + (lk - lq) (j <= i for equal lengths).
  *   d       64 or 128.
  * The caller keeps every buffer alive until the work has completed on
  * `stream`; nothing is allocated.
@@ -239,7 +251,8 @@ size_t oa_attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
  *           forward's outputs for the same q, k, v, causal and scale.
  *   lse     fp32 [B, H, Nq], non-NULL.  A row with lse = -inf (no visible
  *           key) gets dQ = 0 and contributes nothing to dK, dV.
- *   causal  0 or 1 (key j visible to query i iff j <= i; needs Nq == Nk).
+ *   causal  0 or 1 (key j visible to query i iff j <= i + (Nk - Nq), as in
+ *           oa_attn_fwd).
  *   scale   finite and > 0.
  *   d       64 or 128.
  *   workspace  device, >= oa_attn_bwd_workspace_bytes(B, H, Nq, d) bytes,
@@ -251,7 +264,7 @@ size_t oa_attn_bwd_workspace_bytes(int B, int H, int Nq, int d);
  * bits from run to run.
  * Errors: OA_ERR_INVALID (NULL pointers, sizes < 1, misalignment, a bad
  * scale, workspace too small); OA_ERR_UNSUPPORTED (dtype other than bf16,
- * d other than 64 / 128, causal with Nq != Nk).
+ * d other than 64 / 128).
  */
 oa_status oa_attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                       const float* lse, void* dq, void* dk, void* dv, oa_dtype dt, int B, int H,

@@ -13,8 +13,9 @@
 // kernel (attn_bwd_tc_kernel at d = 128, described here; attn_bwd_tc64_kernel at d = 64, the
 // same roles pipelined one step deeper, described at its definition), and a post-pass (dQ to
 // bf16).  Main kernel, key-tile outer: one CTA per (b, h, 128 keys); K_j and V_j stay in shared
-// memory while the query tiles i (causal: i >= j) stream through a 2-stage TMA ring with their
-// dO tiles.  Per query tile:
+// memory while the query tiles i that see any of its keys stream through a 2-stage TMA ring with
+// their dO tiles (causal: query i sees keys j <= i + Nk - Nq, the queries being the sequence's last
+// Nq positions; per sequence for packed sequences).  Per query tile:
 //   S^T  = K_j Q_i^T,   dP^T = V_j dO_i^T           (SS MMAs into TMEM, lanes = keys, N = 128)
 //   P^T  elementwise as soon as S^T is in, while dP^T computes (P^T as bf16 back into TMEM)
 //   dV_j += P^T dO_i                                 (TS MMA: A from TMEM), while the rows
@@ -152,7 +153,8 @@ __global__ void bwd_post_kernel(const float* __restrict__ dq_acc, __nv_bfloat16*
 // P^T for 64 queries q_first .. q_first + 63 of one key row: sr the fp32 S^T columns, nl the
 // negated LSE log2 e of those queries (four per float4).  pp keeps P^T in fp32 pairs for the dS^T
 // pass, pw the bf16 pairs that the dV MMA reads.  MASK applies the key and causal tests as an
-// exponent of -inf (no branch).
+// exponent of -inf (no branch); `key` is the key's index minus the causal offset, so the causal test
+// is key <= q.
 template <bool MASK>
 __device__ __forceinline__ void bwd_p(const uint32_t (&sr)[64], const float4* nl, uint64_t sl2x2, int key, int q_first,
                                       bool key_ok, bool causal, uint64_t (&pp)[32], uint32_t (&pw)[32]) {
@@ -202,8 +204,9 @@ __device__ __forceinline__ void bwd_ds(const uint32_t (&dr)[64], const float4* n
 struct BwdGeom {
   int j, k0;  // key tile and its first key
   int Nq, Nk, nqt, qrow0, krow0, qplane0, kplane;
+  int off;      // causal: query q sees key k iff k <= q + off (keys minus queries)
   int64_t lbase, lq, lt, dkbase, dks;
-  int i_begin;  // first visible query tile (causal: query tile i sees key tile j iff i >= j)
+  int i_begin;  // first query tile that sees a key of tile j (causal: the one holding query k0 - off)
   int n_it;     // steps: every visible query tile of every query head of the group, head by head
 };
 
@@ -254,7 +257,8 @@ __device__ __forceinline__ bool bwd_geometry(const BwdParams& p, BwdGeom& g) {
     g.dks = 1;
   }
   g.nqt = (g.Nq + BT - 1) / BT;
-  g.i_begin = p.causal ? g.j : 0;
+  g.off = g.Nk - g.Nq;
+  g.i_begin = (p.causal && g.k0 - g.off > 0) ? (g.k0 - g.off) / BT : 0;
   g.n_it = p.group * max(g.nqt - g.i_begin, 0);
   return true;
 }
@@ -572,7 +576,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int i = pos.i, q0 = i * BT;
       const uint32_t ph = (uint32_t)it & 1u;
       // every (key, query) pair of the step visible and inside the tensors
-      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || i > j);
+      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || k0 + BT - 1 <= q0 + g.off);
       if (!(ok = wait_all(bar_s(half), ph, B_S))) break;
       // -LSE log2 e and -D scale of query q0 + ld_q; a row past the end or with no visible key gets
       // -inf, so that exp2(s scale log2 e - inf) = 0 needs no test below
@@ -596,7 +600,7 @@ __global__ void __launch_bounds__(kBwdThreads)
         if (full)
           bwd_p<false>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, true, false, pp, pw);
         else
-          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
+          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key - g.off, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
         tmem_st32(sc, pw);
       }
       tmem_st_wait();
@@ -986,7 +990,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     for (int it = 0; ok && it < n_it; ++it) {
       const int i = pos.i, q0 = i * BT;
       const uint32_t ph = (uint32_t)it & 1u;
-      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || i > j);
+      const bool full = (k0 + BT <= Nk) && (q0 + BT <= Nq) && (!p.causal || k0 + BT - 1 <= q0 + g.off);
       if (!(ok = wait_all(bar_s, ph, B_S))) break;
       if (!(ok = wait_all(bar_ld(half), ph, B_LD))) break;
       tc_fence_after_sync();
@@ -1000,7 +1004,7 @@ __global__ void __launch_bounds__(kBwdThreads)
         if (full)
           bwd_p<false>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, true, false, pp, pw);
         else
-          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
+          bwd_p<true>(sr, nl4 + 16 * half, sl2x2, key - g.off, q0 + 64 * half, key_ok, p.causal != 0, pp, pw);
         tmem_st32(sc, pw);
       }
       tmem_st_wait();

@@ -9,8 +9,10 @@
 // with one normalisation o / l at the end and LSE = m + ln l.  Masked
 // scores are -inf; a row that has seen nothing keeps m = -inf and uses 0 as
 // its reference, so alpha and p are exactly 0 and no NaN forms.
-// Causal CTAs stop at their last visible key block (tiles above the
-// diagonal are skipped; the diagonal block is masked element-wise).
+// Causal: the Nq queries are the last Nq positions of the Nk keys' sequence,
+// so query i sees keys j <= i + (Nk - Nq) (j <= i when Nq == Nk).  Causal
+// CTAs stop at their last visible key block (blocks past the diagonal are
+// skipped; the blocks it crosses are masked element-wise).
 #include "oa_internal.h"
 
 namespace oa {
@@ -42,7 +44,8 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const float* __restr
   int kvl = Nk;
   if (kv_len != nullptr) kvl = min(max(kv_len[b], 0), Nk);
   const int br = min(Br, Nq - q0);
-  const int kv_end = causal ? min(kvl, q0 + br) : kvl;
+  const int off = Nk - Nq;  // causal: query i sees keys j <= i + off
+  const int kv_end = causal ? min(kvl, max(0, q0 + br + off)) : kvl;
 
   const float* qb = q + (bh * Nq + q0) * d;
   // query head h reads key/value head h / group
@@ -72,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const float* __restr
       const int r = i / bc, c = i % bc;
       const int col = j0 + c, row = q0 + r;
       float s = -INFINITY;
-      if (col < kvl && (!causal || col <= row)) {
+      if (col < kvl && (!causal || col <= row + off)) {
         float acc = 0.f;
         for (int e = 0; e < d; ++e) acc = fmaf(Qs[r * d + e], Ks[c * d + e], acc);
         s = acc * scale;

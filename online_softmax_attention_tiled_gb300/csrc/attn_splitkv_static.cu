@@ -65,8 +65,6 @@ float* scratch_address(cudaError_t* err) {
   return cache[dev];
 }
 
-bool is_aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
-
 }  // namespace
 
 extern "C" oa_status oa_attn_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,

@@ -152,7 +152,6 @@ static oa_status check_fwd(const void* q, const void* k, const void* v, void* o,
   oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, who);
   if (s != OA_OK) return s;
   if ((s = check_heads(H, Hkv, who)) != OA_OK) return s;
-  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "%s: causal needs Nq == Nk", who);
   if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "%s: kv_len must be 4-byte aligned", who);
   if (dt != OA_BF16 && dt != OA_F32) return fail(OA_ERR_INVALID, "%s: unknown dtype %d", who, (int)dt);
   if (dt == OA_BF16 && d != 64 && d != 128)
@@ -209,6 +208,8 @@ static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (s != OA_OK) return s;
   oa::DevStatus st;
   if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
+  // one query is the sequence's last position and sees every key: causal changes nothing
+  if (Nq == 1) causal = 0;
   if (grouped_single_query(dt, H, Hkv, Nq, d, causal))
     return launch_fwd(q, k, v, o, lse, dt, B, Hkv, Hkv, H / Hkv, Nk, d, 0, scale, kv_len, st, (cudaStream_t)stream,
                       who);
@@ -428,7 +429,6 @@ oa_status oa_attn_fwd_f32_tiles(const float* q, const float* k, const float* v, 
                                 int Bc, oa_stream_t stream) {
   oa_status s = check_attn(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, "attn_fwd_f32_tiles");
   if (s != OA_OK) return s;
-  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: causal needs Nq == Nk");
   if (!aligned(kv_len, 4)) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: kv_len must be 4-byte aligned");
   if (d > 256) return fail(OA_ERR_UNSUPPORTED, "attn_fwd_f32_tiles: d <= 256");
   if (Br < 1 || Br > 64 || Bc < 1 || Bc > 64) return fail(OA_ERR_INVALID, "attn_fwd_f32_tiles: 1 <= Br, Bc <= 64");
@@ -455,7 +455,6 @@ static oa_status attn_bwd_impl(const void* q, const void* k, const void* v, cons
   if (!o || !dout || !lse || !dk || !dv) return fail(OA_ERR_INVALID, "%s: o, dout, lse, dk and dv are required", who);
   if (!aligned(o, 16) || !aligned(dout, 16) || !aligned(dk, 16) || !aligned(dv, 16) || !aligned(lse, 4))
     return fail(OA_ERR_INVALID, "%s: o/dout/dk/dv must be 16-byte aligned, lse 4-byte", who);
-  if (causal && Nq != Nk) return fail(OA_ERR_UNSUPPORTED, "%s: causal needs Nq == Nk", who);
   if (dt != OA_BF16) return fail(OA_ERR_UNSUPPORTED, "%s: bf16 only", who);
   if (d != 64 && d != 128) return fail(OA_ERR_UNSUPPORTED, "%s: d = 64 or 128 (got %d)", who, d);
   if ((int64_t)B * Hkv * ((Nk + 127) / 128) > kMaxGrid) return fail(OA_ERR_INVALID, "%s: grid too large", who);

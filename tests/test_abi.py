@@ -88,7 +88,6 @@ def test_attn_fwd_validation(lib):
     assert call(causal=2) == oa.OA_ERR_INVALID
     assert call(q=FAKE_ODD) == oa.OA_ERR_INVALID
     assert call(dt=7) == oa.OA_ERR_INVALID
-    assert call(causal=1, Nk=9) == oa.OA_ERR_UNSUPPORTED
     assert call(d=96) == oa.OA_ERR_UNSUPPORTED  # bf16 tensor-core path: d in {64, 128}
     assert "d = 64 or 128" in _err(lib)
     assert call(dt=oa.OA_F32, d=300) == oa.OA_ERR_UNSUPPORTED
@@ -135,7 +134,6 @@ def test_attn_bwd_validation(lib):
                 dict(scale=-1.0), dict(causal=3), dict(dout=FAKE_ODD), dict(ws=NULL), dict(ws=FAKE_ODD),
                 dict(ws_bytes=need - 1)):
         assert call(**bad) == oa.OA_ERR_INVALID, bad
-    assert call(Nk=99) == oa.OA_ERR_UNSUPPORTED  # causal needs Nq == Nk
     assert call(dt=oa.OA_F32) == oa.OA_ERR_UNSUPPORTED
     assert call(d=96) == oa.OA_ERR_UNSUPPORTED
     assert "d = 64 or 128" in _err(lib)
@@ -164,7 +162,6 @@ def test_attn_fwd_host_validation(lib):
     for bad in (dict(q=NULL), dict(o=NULL), dict(q=FAKE_ODD), dict(Hkv=3), dict(causal=2), dict(chunks=-1),
                 dict(chunks=65), dict(ws=NULL), dict(ws=ctypes.c_void_p(0x100010)), dict(ws_bytes=need - 1)):
         assert call(**bad) == oa.OA_ERR_INVALID, bad
-    assert call(Nk=99) == oa.OA_ERR_UNSUPPORTED  # causal needs Nq == Nk
     assert call(d=96) == oa.OA_ERR_UNSUPPORTED
 
 

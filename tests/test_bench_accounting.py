@@ -91,3 +91,10 @@ def test_both_arms_report_the_same_config():
 def test_case_table_covers_the_components():
     assert set(bench.COMPONENTS) | {"attn_causal"} == set(bench.CASES)
     assert "attn_bwd_noncausal_d64" in bench.COMPONENTS and "attn_decode_gqa" in bench.COMPONENTS
+
+
+def test_chunked_prefill_work():
+    # 2048 queries at the end of 32768 keys: query i sees 30721 + i keys
+    pairs = sum(30721 + i for i in range(2048))
+    assert bench.causal_pairs(2048, 32768) == pairs == 65012736
+    assert bench.kvcache_causal_flops(8, 32, 2048, 32768, 128) == pytest.approx(4 * 128 * 8 * 32 * pairs)

@@ -51,8 +51,8 @@ def _bounds(q, k, v, do, causal, scale, q_rows, k_rows, block=512):
     for i0 in range(0, Nq, block):
         i1 = min(Nq, i0 + block)
         s = scale * (q[i0:i1] @ k.T)
-        if causal:
-            hide = torch.arange(Nk)[None, :] > torch.arange(i0, i1)[:, None]
+        if causal:  # the queries are the last Nq positions: query i sees keys j <= i + Nk - Nq
+            hide = torch.arange(Nk)[None, :] > torch.arange(i0, i1)[:, None] + (Nk - Nq)
             s = s.masked_fill(hide, float("-inf"))
         lse = torch.logsumexp(s, dim=1, keepdim=True)
         p = torch.where(torch.isfinite(lse), torch.exp(s - lse), torch.zeros_like(s))
@@ -100,6 +100,12 @@ CASES = [
     (1, 1, 1, 1, 128, True, None),
     (1, 1, 256, 256, 64, False, 0.5),
     (2, 2, 384, 384, 128, True, None),
+    # causal with more keys than queries (the queries at the end: chunked prefill against a cache)
+    # and with fewer (the first Nq - Nk queries see no key)
+    (1, 2, 200, 700, 64, True, None),
+    (1, 2, 130, 517, 128, True, None),
+    (1, 1, 300, 150, 64, True, None),
+    (1, 1, 257, 100, 128, True, None),
 ]
 
 
@@ -185,7 +191,7 @@ def test_attn_bwd_binding_rejects_bad_arguments():
     with pytest.raises(oa.OAError):
         oa.attn_bwd(q.float(), k.float(), v.float(), o.float(), lse, do.float())
     with pytest.raises(oa.OAError):
-        oa.attn_bwd(q, k[:, :, :63], v[:, :, :63], o, lse, do, causal=True)
+        oa.attn_bwd(q, k[:, :, :63], v, o, lse, do, causal=True)  # k and v of different lengths
 
 
 def test_attn_bwd_full_size_sampled_rows():
@@ -232,6 +238,7 @@ def test_attn_bwd_full_size_d64_sampled_rows():
     ([300, 129, 1, 257], [300, 129, 1, 257], 4, 2, 128, True),
     ([100, 0, 200, 64, 33], [150, 80, 0, 64, 200], 2, 2, 64, False),
     ([130, 70], [200, 70], 4, 1, 128, True),   # causal with more keys than queries
+    ([60, 300, 200], [500, 300, 90], 2, 1, 64, True),  # more keys, equal, fewer keys (bottom-right)
     ([700, 300, 1], [700, 300, 1], 4, 2, 64, True),  # d = 64, packed, several steps per CTA
 ])
 def test_attn_bwd_varlen_matches_oracle(lq, lk, H, Hkv, d, causal):
