@@ -110,8 +110,8 @@ struct TcParams {
   const int32_t* cu_q;
   const int32_t* cu_k;
   int Tq, Tk;
-  int H, Nq, Nk, causal, num_qblocks, BH;  // packed: Nq = longest query sequence, BH = sequences x H
-  int off;               // dense causal: query i sees keys j <= i + off (Nk - Nq)
+  int H, Nq, Nk, num_qblocks, BH;  // packed: Nq = longest query sequence, BH = sequences x H
+  int off;               // dense causal: query i sees keys j <= i + off (Nk - Nq); causality is the MODE
   int group;             // query heads per key/value head (H / H_kv)
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
   int l_rs;              // LSE row stride: 1 dense, H packed
@@ -124,6 +124,15 @@ enum WaitSite : unsigned {
   W_Q = 1, W_KFULL, W_KEMPTY, W_VFULL, W_VEMPTY, W_SFULL, W_PFULL, W_ODONE, W_DRAIN, W_SFREE, W_QEMPTY
 };
 
+// Masking mode, a template parameter of the kernel (each mode compiles to its own instance):
+//   kNonCausal  every key up to the sequence's length; items are numbered head-major, so the items
+//               of one key/value plane run together and share its K/V in L2
+//   kCausal     square causal (Nq == Nk, key offset 0), heaviest query blocks first
+//   kCausalOff  causal with a key offset (Nq != Nk, or packed sequences, each with its own)
+// A runtime offset in the mask measured 3 % slower on the square causal case, and a runtime
+// choice of the item order 1 % slower, hence three instances.
+enum Mode : int { kNonCausal = 0, kCausal = 1, kCausalOff = 2 };
+
 // One work item: 2 x 128 query rows of one (sequence, head).
 struct Item {
   int zq, zkv;      // tensor-map head plane of Q/O and of K/V
@@ -135,15 +144,18 @@ struct Item {
   int64_t ob, lb;   // offsets of the sequence's row 0 (this head) in O (elements) and in LSE
 };
 
-// Items are numbered heaviest first (for causal: the last query blocks); item idx covers
-// query block num_qblocks - 1 - idx / BH of (sequence, head) idx % BH.  Query head h reads
-// key/value head h / group.  SPLIT (at most 128 query rows): both query-tile slots hold
-// the same rows, slot 0 takes the even key tiles and slot 1 the odd ones.
-template <int D, bool PACKED, bool SPLIT = false>
+// Items are numbered heaviest first (causal, and packed sequences: the last query blocks);
+// item idx covers query block num_qblocks - 1 - idx / BH of (sequence, head) idx % BH.
+// Dense non-causal items weigh alike and are numbered head-major: query block idx % num_qblocks
+// of head plane idx / num_qblocks.  Query head h reads key/value head h / group.  SPLIT (at most
+// 128 query rows): both query-tile slots hold the same rows, slot 0 takes the even key tiles and
+// slot 1 the odd ones.
+template <int D, bool PACKED, bool SPLIT, int MODE>
 __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   Item it;
-  const int qb = p.num_qblocks - 1 - idx / p.BH;
-  const int sh = idx % p.BH;
+  constexpr bool kHeadMajor = !PACKED && MODE == kNonCausal;
+  const int qb = kHeadMajor ? idx % p.num_qblocks : p.num_qblocks - 1 - idx / p.BH;
+  const int sh = kHeadMajor ? idx / p.num_qblocks : idx % p.BH;
   const int sq = sh / p.H, h = sh % p.H, hk = h / p.group;
   const int Hkv = p.H / p.group;
   it.q0 = qb * 2 * BM;
@@ -168,7 +180,7 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   } else {
     it.nq = p.Nq;
     it.kvl = p.Nk;
-    it.off = p.off;  // from the shapes (Nk - Nq); kv_len only hides the tail
+    it.off = MODE == kCausalOff ? p.off : 0;  // from the shapes (Nk - Nq); kv_len only hides the tail
     if (p.kv_len != nullptr) it.kvl = min(max(p.kv_len[sq], 0), p.Nk);
     it.zq = sh;
     it.zkv = sq * Hkv + hk;
@@ -182,7 +194,7 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   // tile's last row (past nq its rows are computed and dropped, so the count for Nq == Nk is that of
   // a square diagonal); none when that key is negative.  Else every tile.
   auto tiles_to = [&](int r_last) {
-    return !p.causal ? nk_tiles : max(0, min(nk_tiles, (r_last + it.off + BN) / BN));
+    return MODE == kNonCausal ? nk_tiles : max(0, min(nk_tiles, (r_last + it.off + BN) / BN));
   };
   if constexpr (SPLIT) {
     const int nt = it.q0 < it.nq ? tiles_to(it.q0 + BM - 1) : 0;
@@ -215,10 +227,8 @@ __device__ __forceinline__ int item_of_round(int k, int total) {
 
 // No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
 // and the hint made ptxas spill more on this kernel.  PACKED: token-major packed sequences
-// (a separate instance, so the dense layout pays nothing for them).  OFF: causal with a key
-// offset (more or fewer keys than queries); the instance without it keeps the square diagonal's
-// mask, which measured 3 % faster than the general one at N = 8192.
-template <int D, bool PACKED, bool SPLIT, bool OFF>
+// (a separate instance, so the dense layout pays nothing for them).  MODE: see Mode.
+template <int D, bool PACKED, bool SPLIT, int MODE>
 __global__ void __launch_bounds__(Cfg<D>::THREADS)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
@@ -300,7 +310,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
       const int idx = item_of_round(k, total);
       if (idx < 0) continue;
-      const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
       if (it.n_all == 0) continue;
       // the previous item's S MMAs must have finished reading Q
       if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
         const int n = it.n_kv[i], sb = i ? st1 : st0, n_ld = 2 * n_loads_of<SPLIT>(it);
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
@@ -421,7 +431,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
         const int n = it.n_kv[i], sb = i ? st1 : st0;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
         ++nq;
@@ -521,7 +531,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
         ++nq;
@@ -589,11 +599,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       // (causal) r0 + off: the last key visible to the tile's first row; row + off: to this row's
       int n, kvl, r0, off;
       {
-        const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         n = it.n_kv[i];
         kvl = it.kvl;
         r0 = it.q0 + (SPLIT ? 0 : i * BM);
-        off = OFF ? it.off : 0;
+        off = MODE == kCausalOff ? it.off : 0;
       }
       const int row = r0 + tt;
       float m = -INFINITY;  // running max of the scaled scores, log2 units
@@ -612,11 +622,12 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         }
         float* s = reinterpret_cast<float*>(sr);
         const int col0 = (SPLIT ? 2 * j + i : j) * BN;  // SPLIT: this slot's j-th key tile is 2 j + i
-        if (col0 + BN > kvl || (p.causal && col0 + BN - 1 > r0 + off)) {
+        constexpr bool kCausalMask = MODE != kNonCausal;
+        if (col0 + BN > kvl || (kCausalMask && col0 + BN - 1 > r0 + off)) {
 #pragma unroll
           for (int c = 0; c < 128; ++c) {
             const int col = col0 + c;
-            if (col >= kvl || (p.causal && col > row + off)) s[c] = -INFINITY;
+            if (col >= kvl || (kCausalMask && col > row + off)) s[c] = -INFINITY;
           }
         }
         // row max of the raw scores (scale > 0 commutes with max)
@@ -728,7 +739,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         m = mm;
       }
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const Item it = item_at<D, PACKED, SPLIT>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
       const int64_t o_rs = PACKED ? p.o_rs : D;  // O row stride
       __nv_bfloat16* orow = p.o + it.ob + (int64_t)row * o_rs;
 #pragma unroll 1
@@ -798,7 +809,7 @@ constexpr int kMaxDevices = 64;
 // sequences) the items weigh alike, so the grid is the fewest CTAs that keep the number of rounds:
 // every CTA then works through the same number of items, and the memory-bound cases (grouped
 // decode) spread the same bytes over fewer, busier CTAs instead of a last round half empty.
-template <int D, bool PACKED, bool SPLIT, bool OFF>
+template <int D, bool PACKED, bool SPLIT, int MODE>
 cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const TcParams& p,
                      cudaStream_t s) {
   static bool attr_set[kMaxDevices] = {};
@@ -808,7 +819,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, PACKED, SPLIT, OFF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<D>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
@@ -817,12 +828,12 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
   }
   const long long total = (long long)p.num_qblocks * p.BH;
   long long g = total < sm_count[dev] ? total : sm_count[dev];
-  if (!PACKED && !p.causal) {
+  if (!PACKED && MODE == kNonCausal) {
     const long long rounds = (total + g - 1) / g;
     g = (total + rounds - 1) / rounds;
   }
   const unsigned grid = (unsigned)g;
-  attn_fwd_tc_kernel<D, PACKED, SPLIT, OFF><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -858,7 +869,6 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.H = a.H;
   p.Nq = a.Nq;
   p.Nk = a.Nk;
-  p.causal = a.causal;
   p.off = a.Nk - a.Nq;
   p.num_qblocks = (a.Nq + 2 * BM - 1) / (2 * BM);
   p.BH = a.B * a.H;
@@ -868,25 +878,35 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
-  // packed sequences may each have their own key offset; dense calls have one (Nk - Nq)
-  if (packed)
-    return d == 128 ? launch_d<128, true, false, true>(mq, mk, mv, p, s) : launch_d<64, true, false, true>(mq, mk, mv, p, s);
-  const bool off = a.causal && a.Nk != a.Nq;
+  // Instance by layout, query-tile use and masking mode (packed sequences may each have their own
+  // key offset; a dense call has one, Nk - Nq)
+  const int mode = !a.causal ? kNonCausal : (packed || a.Nk != a.Nq) ? kCausalOff : kCausal;
+  if (packed) {
+    if (mode == kNonCausal)
+      return d == 128 ? launch_d<128, true, false, kNonCausal>(mq, mk, mv, p, s)
+                      : launch_d<64, true, false, kNonCausal>(mq, mk, mv, p, s);
+    return d == 128 ? launch_d<128, true, false, kCausalOff>(mq, mk, mv, p, s)
+                    : launch_d<64, true, false, kCausalOff>(mq, mk, mv, p, s);
+  }
   // At most 128 query rows (decode, multi-token decode against a cache, and grouped decode whose
   // group's queries are the rows): an item fills only one query-tile slot, so both slots take the
-  // same rows over alternate key tiles and their results are merged (see item_at).
+  // same rows over alternate key tiles and their results are merged (see item_at).  A square
+  // causal call this small runs as the offset mode with offset 0.
   if (a.Nq <= BM) {
-    if (off)
-      return d == 128 ? launch_d<128, false, true, true>(mq, mk, mv, p, s)
-                      : launch_d<64, false, true, true>(mq, mk, mv, p, s);
-    return d == 128 ? launch_d<128, false, true, false>(mq, mk, mv, p, s)
-                    : launch_d<64, false, true, false>(mq, mk, mv, p, s);
+    if (mode == kNonCausal)
+      return d == 128 ? launch_d<128, false, true, kNonCausal>(mq, mk, mv, p, s)
+                      : launch_d<64, false, true, kNonCausal>(mq, mk, mv, p, s);
+    return d == 128 ? launch_d<128, false, true, kCausalOff>(mq, mk, mv, p, s)
+                    : launch_d<64, false, true, kCausalOff>(mq, mk, mv, p, s);
   }
-  if (off)
-    return d == 128 ? launch_d<128, false, false, true>(mq, mk, mv, p, s)
-                    : launch_d<64, false, false, true>(mq, mk, mv, p, s);
-  return d == 128 ? launch_d<128, false, false, false>(mq, mk, mv, p, s)
-                  : launch_d<64, false, false, false>(mq, mk, mv, p, s);
+  if (mode == kNonCausal)
+    return d == 128 ? launch_d<128, false, false, kNonCausal>(mq, mk, mv, p, s)
+                    : launch_d<64, false, false, kNonCausal>(mq, mk, mv, p, s);
+  if (mode == kCausal)
+    return d == 128 ? launch_d<128, false, false, kCausal>(mq, mk, mv, p, s)
+                    : launch_d<64, false, false, kCausal>(mq, mk, mv, p, s);
+  return d == 128 ? launch_d<128, false, false, kCausalOff>(mq, mk, mv, p, s)
+                  : launch_d<64, false, false, kCausalOff>(mq, mk, mv, p, s);
 }
 
 }  // namespace oa
