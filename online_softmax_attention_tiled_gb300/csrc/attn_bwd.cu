@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kBwdThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   BwdGeom g;
   if (!bwd_geometry<PACKED>(p, g)) return;
-  const int j = g.j, k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
+  const int k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
   const int64_t lbase = g.lbase, lq = g.lq, lt = g.lt;
   auto next_pos = [&](StepPos sp) { return sp.next(g); };
   const StepPos first_pos{0, g.i_begin};
@@ -741,7 +741,7 @@ __global__ void __launch_bounds__(kBwdThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   BwdGeom g;
   if (!bwd_geometry<PACKED>(p, g)) return;
-  const int j = g.j, k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
+  const int k0 = g.k0, Nq = g.Nq, Nk = g.Nk, qrow0 = g.qrow0, qplane0 = g.qplane0, n_it = g.n_it;
   const StepPos first_pos{0, g.i_begin};
 
   if (threadIdx.x == 0) {

@@ -59,7 +59,13 @@ namespace oa {
 namespace {
 
 constexpr int BM = 128;  // rows per query tile (= TMEM lanes)
-constexpr int BN = 128;  // keys per key/value tile
+// Keys per key/value tile at d = 128.  128: P_i is written over S_i, and each tile's softmax, PV and
+// next S follow one another.  64 would fit S tiles (64 columns each), O tiles (128 each) and separate
+// P columns (32 each) in the 512 TMEM columns and run the pipeline of d = 64 (S_i(j+1) computed
+// while the softmax of S_i(j) runs from registers); it measured 4 % slower at causal N = 8192: a
+// group's softmax of a 64-key tile costs about 80 % of a 128-key one (fixed per-tile latencies), and
+// the S MMAs at N = 64 take more MMA issue slots from the softmax warps that share their SMSPs.
+constexpr int kD128KeysPerTile = 128;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp0 = 9;  // MMA issuer of query tile 0; warp 10 issues for tile 1
 constexpr uint32_t kTmemCols = 512;
@@ -69,35 +75,42 @@ constexpr float kRescaleLog2 = 8.f;
 
 template <int D>
 struct Cfg {
+  static constexpr int BN = (D == 128) ? kD128KeysPerTile : 128;  // keys per key/value tile
   static constexpr int SLABS = D / 64;               // 128-byte swizzle atoms along d
-  static constexpr int SLAB_BYTES = BM * 128;        // 128 rows x 128 bytes
-  static constexpr int TILE_BYTES = SLABS * SLAB_BYTES;
+  static constexpr int Q_SLAB = BM * 128;            // 128 rows x 128 bytes
+  static constexpr int KV_SLAB = BN * 128;           // BN rows x 128 bytes
+  static constexpr int Q_TILE = SLABS * Q_SLAB;
+  static constexpr int KV_TILE = SLABS * KV_SLAB;
   // One ring of key/value tiles, filled in the order the MMAs consume them:
   // K_0, V_0, K_1, V_1, ... (load t = 2j for K_j, 2j + 1 for V_j, slot t % SLOTS).
-  static constexpr int SLOTS = (D == 128) ? 4 : 10;
-  // d = 64 leaves 128 TMEM columns free: P_i gets its own 64 columns, so S_i(j+1)
-  // can be computed while the softmax of S_i(j) runs (the group frees S_i as soon
-  // as it has read it).  At d = 128 P_i is written over S_i.
-  static constexpr bool SEP_P = (D == 64);
+  static constexpr int SLOTS = (KV_TILE <= 16384) ? 10 : 4;
+  // When S_0, S_1 (BN columns each), O_0, O_1 (D each) and P_0, P_1 (BN / 2 each, bf16 pairs)
+  // fit the 512 columns, P_i gets columns of its own, so S_i(j+1) can be computed while the
+  // softmax of S_i(j) runs (the group frees S_i as soon as it has read it).  Else P_i is
+  // written over S_i.
+  static constexpr bool SEP_P = (3 * BN + 2 * D <= 512);
   // With P_i separate each query tile's MMAs come from a warp of its own; with P_i over
   // S_i one warp issues both tiles' PV and S back to back, which keeps each tile's
   // critical loop (softmax -> PV_i -> S_i -> softmax) short.
   static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
   static constexpr int THREADS = 32 * (9 + MMA_WARPS);  // 8 softmax warps, producer, MMA warp(s)
   static constexpr int Q_OFF = 0;
-  static constexpr int RING_OFF = Q_OFF + 2 * TILE_BYTES;
-  static constexpr int BAR_OFF = RING_OFF + SLOTS * TILE_BYTES;
+  static constexpr int RING_OFF = Q_OFF + 2 * Q_TILE;
+  static constexpr int BAR_OFF = RING_OFF + SLOTS * KV_TILE;
   // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2], q_empty
   static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2 + 1;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
-  __host__ __device__ static constexpr uint32_t o_col(int i) { return 256u + (uint32_t)(i * D); }
-  // first TMEM column of P_i (bf16 pairs, 64 columns)
+  __host__ __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * BN); }
+  __host__ __device__ static constexpr uint32_t o_col(int i) { return (uint32_t)(2 * BN + i * D); }
+  // first TMEM column of P_i (bf16 pairs, BN / 2 columns)
   __host__ __device__ static constexpr uint32_t p_col(int i) {
-    return SEP_P ? 256u + 2u * (uint32_t)D + 64u * (uint32_t)i : (uint32_t)(i * BN);
+    return SEP_P ? (uint32_t)(2 * BN + 2 * D + i * (BN / 2)) : s_col(i);
   }
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BM, BN, false);  // Q K^T, both K-major
   static constexpr uint32_t IDESC_O = idesc_bf16_f32(BM, D, true);    // P V, V is MN-major
+  static_assert(BN == 64 || BN == 128, "key tile");
+  static_assert(SEP_P ? 3 * BN + 2 * D <= (int)kTmemCols : 2 * BN + 2 * D <= (int)kTmemCols, "TMEM columns");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
@@ -152,6 +165,7 @@ struct Item {
 // slot 1 the odd ones.
 template <int D, bool PACKED, bool SPLIT, int MODE>
 __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
+  constexpr int BN = Cfg<D>::BN;
   Item it;
   constexpr bool kHeadMajor = !PACKED && MODE == kNonCausal;
   const int qb = kHeadMajor ? idx % p.num_qblocks : p.num_qblocks - 1 - idx / p.BH;
@@ -244,7 +258,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   auto bar_full = [&](int t) { return bar0 + 8u * (1 + t % C::SLOTS); };             // ring load t landed
   auto bar_empty = [&](int t) { return bar0 + 8u * (1 + C::SLOTS + t % C::SLOTS); };  // slot of load t free
   auto ring_phase = [&](int t) { return (uint32_t)(t / C::SLOTS) & 1u; };
-  auto ring_addr = [&](int t) { return sbase + C::RING_OFF + (uint32_t)((t % C::SLOTS) * C::TILE_BYTES); };
+  auto ring_addr = [&](int t) { return sbase + C::RING_OFF + (uint32_t)((t % C::SLOTS) * C::KV_TILE); };
   auto bar_sfull = [&](int i) { return bar0 + 8u * (1 + 2 * C::SLOTS + i); };
   auto bar_pfull = [&](int i) { return bar0 + 8u * (3 + 2 * C::SLOTS + i); };
   auto bar_odone = [&](int i) { return bar0 + 8u * (5 + 2 * C::SLOTS + i); };
@@ -254,8 +268,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   static_assert(!SPLIT || !PACKED, "the split mode serves the dense layout");
   // SPLIT: Q tile 1's buffer (never loaded) holds group 1's (m, l) per row and two barriers:
   // xch (group 1's O_1, m, l ready; 4 warps) and xdone (group 0 has read them; 4 warps)
-  float2* xch_ml = reinterpret_cast<float2*>(smem + C::Q_OFF + C::TILE_BYTES);
-  const uint32_t bar_xch = sbase + C::Q_OFF + C::TILE_BYTES + BM * 8;
+  float2* xch_ml = reinterpret_cast<float2*>(smem + C::Q_OFF + C::Q_TILE);
+  const uint32_t bar_xch = sbase + C::Q_OFF + C::Q_TILE + BM * 8;
   const uint32_t bar_xdone = bar_xch + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
@@ -314,18 +328,18 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       if (it.n_all == 0) continue;
       // the previous item's S MMAs must have finished reading Q
       if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
-      mbar_arrive_expect_tx_elect(bar_q, (SPLIT ? 1 : 2) * C::TILE_BYTES);
+      mbar_arrive_expect_tx_elect(bar_q, (SPLIT ? 1 : 2) * C::Q_TILE);
       for (int i = 0; i < (SPLIT ? 1 : 2); ++i)
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(sbase + C::Q_OFF + i * C::TILE_BYTES + s * C::SLAB_BYTES, &tm_q, bar_q, s * 64,
+          tma_load_3d_elect(sbase + C::Q_OFF + i * C::Q_TILE + s * C::Q_SLAB, &tm_q, bar_q, s * 64,
                             it.yq + it.q0 + i * BM, it.zq);
       ++nq;
       for (int t = 0; t < 2 * n_loads_of<SPLIT>(it); ++t, ++tg) {
         if (!(ok = wait_all(bar_empty(tg), ring_phase(tg) ^ 1u, W_KEMPTY))) break;
-        mbar_arrive_expect_tx_elect(bar_full(tg), C::TILE_BYTES);
+        mbar_arrive_expect_tx_elect(bar_full(tg), C::KV_TILE);
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(ring_addr(tg) + s * C::SLAB_BYTES, map, bar_full(tg), s * 64, it.ykv + (t >> 1) * BN,
+          tma_load_3d_elect(ring_addr(tg) + s * C::KV_SLAB, map, bar_full(tg), s * 64, it.ykv + (t >> 1) * C::BN,
                             it.zkv);
       }
     }
@@ -339,16 +353,17 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     // operand stays warp-uniform.
     const uint64_t q_desc0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
     const uint64_t k_desc0 = smem_desc_sw128(sbase + C::RING_OFF, 16, 1024);            // K: K-major
-    const uint64_t v_desc0 = smem_desc_sw128(sbase + C::RING_OFF, C::SLAB_BYTES, 1024);  // V: MN-major
-    auto slot_off = [&](int t) { return (uint64_t)(((t % C::SLOTS) * C::TILE_BYTES) >> 4); };
+    const uint64_t v_desc0 = smem_desc_sw128(sbase + C::RING_OFF, C::KV_SLAB, 1024);  // V: MN-major
+    auto slot_off = [&](int t) { return (uint64_t)(((t % C::SLOTS) * C::KV_TILE) >> 4); };
     auto issue_s = [&](int i, int t) {  // S_i = Q_i K^T (SPLIT: Q_0 for both), K from ring load t
-      const uint32_t d_tmem = tmem_base + (uint32_t)(i * BN);
-      const uint64_t a = q_desc0 + (uint64_t)(((SPLIT ? 0 : i) * C::TILE_BYTES) >> 4);
+      const uint32_t d_tmem = tmem_base + C::s_col(i);
+      const uint64_t a = q_desc0 + (uint64_t)(((SPLIT ? 0 : i) * C::Q_TILE) >> 4);
       const uint64_t b = k_desc0 + slot_off(t);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint64_t off = (uint64_t)(((kk / 4) * C::SLAB_BYTES + (kk % 4) * 32) >> 4);
-        mma_ss_elect(d_tmem, a + off, b + off, C::IDESC_S, kk > 0 ? 1u : 0u);
+        const uint64_t a_off = (uint64_t)(((kk / 4) * C::Q_SLAB + (kk % 4) * 32) >> 4);
+        const uint64_t b_off = (uint64_t)(((kk / 4) * C::KV_SLAB + (kk % 4) * 32) >> 4);
+        mma_ss_elect(d_tmem, a + a_off, b + b_off, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
     };
     auto issue_pv = [&](int i, int t, bool accumulate) {  // O_i += P_i V, V from ring load t
@@ -356,7 +371,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
       const uint32_t a_tmem = tmem_base + C::p_col(i);
       const uint64_t b = v_desc0 + slot_off(t);
 #pragma unroll
-      for (int kk = 0; kk < BN / 16; ++kk)
+      for (int kk = 0; kk < C::BN / 16; ++kk)
         mma_ts_elect(d_tmem, a_tmem + kk * 8, b + (uint64_t)((kk * 2048) >> 4), C::IDESC_O,
                      (accumulate || kk > 0) ? 1u : 0u);
     };
@@ -584,7 +599,8 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
     const int i = warp >> 2;                 // query tile of this group
     const int tt = threadIdx.x & 127;        // row within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t s_addr = tmem_base + lane_base + (uint32_t)(i * BN);
+    constexpr int BN = C::BN;
+    const uint32_t s_addr = tmem_base + lane_base + C::s_col(i);
     const uint32_t o_addr = tmem_base + lane_base + C::o_col(i);
     const uint32_t p_addr = tmem_base + lane_base + C::p_col(i);
     const float sl2 = p.scale_log2;
@@ -613,8 +629,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         const uint32_t ph = (uint32_t)(sb + j) & 1u;
         if (!(ok = wait_all(bar_sfull(i), ph, W_SFULL))) break;
         tc_fence_after_sync();
-        uint32_t sr[128];
-        tmem_ld128(s_addr, sr);
+        uint32_t sr[BN];
+        if constexpr (BN == 128)
+          tmem_ld128(s_addr, sr);
+        else
+          tmem_ld32x2(s_addr, s_addr + 32, sr);
         if constexpr (C::SEP_P) {  // S_i may now be overwritten by S_i(j+1)
           tc_fence_before_sync();
           __syncwarp();
@@ -625,7 +644,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         constexpr bool kCausalMask = MODE != kNonCausal;
         if (col0 + BN > kvl || (kCausalMask && col0 + BN - 1 > r0 + off)) {
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
+          for (int c = 0; c < BN; ++c) {
             const int col = col0 + c;
             if (col >= kvl || (kCausalMask && col > row + off)) s[c] = -INFINITY;
           }
@@ -633,7 +652,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         // row max of the raw scores (scale > 0 commutes with max)
         float mx0 = fmaxf(s[0], s[1]), mx1 = fmaxf(s[2], s[3]), mx2 = fmaxf(s[4], s[5]), mx3 = fmaxf(s[6], s[7]);
 #pragma unroll
-        for (int c = 8; c < 128; c += 8) {
+        for (int c = 8; c < BN; c += 8) {
           mx0 = max3(mx0, s[c], s[c + 1]);
           mx1 = max3(mx1, s[c + 2], s[c + 3]);
           mx2 = max3(mx2, s[c + 4], s[c + 5]);
@@ -650,9 +669,11 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
         uint64_t acc0 = 0, acc1 = 0;  // packed partial row sums (bit pattern 0 == {+0.f, +0.f})
         // P = exp2(S * scale * log2 e - ref): pair c (columns 2c, 2c+1) is written as
-        // one bf16x2 word into sr[c], whose scores have already been consumed.
+        // one bf16x2 word into sr[c], whose scores have already been consumed.  The first half of
+        // P goes to TMEM as soon as it is complete.
+        constexpr int kHalfP = BN / 4;  // words in half of P
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < BN / 2; ++c) {
           float e0, e1;
           f2_unpack(f2_fma(f2_pack(s[2 * c], s[2 * c + 1]), sl2x2, nref2), e0, e1);
           const float p0 = ex2(e0), p1 = ex2(e1);
@@ -661,18 +682,26 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           else
             acc0 = f2_add(acc0, f2_pack(p0, p1));
           sr[c] = pack_bf16x2(p0, p1);
-          if (c == 31) {
+          if (c == kHalfP - 1) {
             if (C::SEP_P && j > 0) {
               // P_i(j) goes where PV_i(j-1) reads P_i(j-1): wait for that MMA (and O_i).
               // (At j = 0 the previous item's epilogue already waited for its last PV.)
               ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE);
               tc_fence_after_sync();
             }
-            if (ok) tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+            if (ok) {
+              if constexpr (kHalfP == 32)
+                tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
+              else
+                tmem_st16(p_addr, &sr[0]);
+            }
           }
         }
         if (!ok) break;
-        tmem_st32(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+        if constexpr (kHalfP == 32)
+          tmem_st32(p_addr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&sr[32]));
+        else
+          tmem_st16(p_addr + 16, &sr[16]);
         float a0, a1, a2, a3;
         f2_unpack(acc0, a0, a1);
         f2_unpack(acc1, a2, a3);
@@ -843,16 +872,17 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   const int d = a.d, Hkv = a.Hkv;
   const bool packed = a.cu_q != nullptr;
   const int64_t rb = 2 * (int64_t)d;  // bytes per row of one head
+  const int kv_rows = d == 128 ? Cfg<128>::BN : Cfg<64>::BN;  // key/value tile height (TMA box)
   CUtensorMap mq, mk, mv;
   bool maps_ok;
   if (packed)
-    maps_ok = make_tile_map(&mq, a.q, d, a.Tq, rb * a.H, a.H, rb) &&
-              make_tile_map(&mk, a.k, d, a.Tk, rb * Hkv, Hkv, rb) &&
-              make_tile_map(&mv, a.v, d, a.Tk, rb * Hkv, Hkv, rb);
+    maps_ok = make_tile_map(&mq, a.q, d, a.Tq, rb * a.H, a.H, rb, BM) &&
+              make_tile_map(&mk, a.k, d, a.Tk, rb * Hkv, Hkv, rb, kv_rows) &&
+              make_tile_map(&mv, a.v, d, a.Tk, rb * Hkv, Hkv, rb, kv_rows);
   else
-    maps_ok = make_tile_map(&mq, a.q, d, a.Nq, rb, a.B * a.H, rb * a.Nq) &&
-              make_tile_map(&mk, a.k, d, a.Nk, rb, a.B * Hkv, rb * a.Nk) &&
-              make_tile_map(&mv, a.v, d, a.Nk, rb, a.B * Hkv, rb * a.Nk);
+    maps_ok = make_tile_map(&mq, a.q, d, a.Nq, rb, a.B * a.H, rb * a.Nq, BM) &&
+              make_tile_map(&mk, a.k, d, a.Nk, rb, a.B * Hkv, rb * a.Nk, kv_rows) &&
+              make_tile_map(&mv, a.v, d, a.Nk, rb, a.B * Hkv, rb * a.Nk, kv_rows);
   if (!maps_ok) {
     if (why) *why = "cuTensorMapEncodeTiled failed or is unavailable";
     return cudaErrorInvalidValue;

@@ -28,11 +28,11 @@ cudaError_t launch_splitkv_partial(const void* q, const void* k, const void* v, 
                                    int num_splits, float* part_o, float* part_lse, cudaStream_t s);
 
 // bf16 rows of D elements viewed as a 3-D tensor for TMA (D innermost, then `rows` rows
-// `row_bytes` apart, then `planes` planes `plane_bytes` apart); box 64 x 128 x 1 with the
+// `row_bytes` apart, then `planes` planes `plane_bytes` apart); box 64 x box_rows x 1 with the
 // 128-byte swizzle; reads past the end return zero.  False if the encoder is unavailable or
 // rejects the layout.
 bool make_tile_map(CUtensorMap* map, const void* base, int D, int rows, int64_t row_bytes, int planes,
-                   int64_t plane_bytes);
+                   int64_t plane_bytes, int box_rows = 128);
 // fp32 [planes][rows][cols], box {32, box_rows, 1}, 128-byte swizzle (TMA reduce-add targets).
 bool make_f32_tile_map(CUtensorMap* map, const void* base, int cols, int rows, int64_t row_bytes, int planes,
                        int64_t plane_bytes, int box_rows);
