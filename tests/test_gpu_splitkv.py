@@ -87,3 +87,31 @@ def test_full_size_decode_b32_h32_nk32768(cuda_lib):
             assert_lse_close(lse[b, h], rl)
             assert_out_close(o[b, h], ro[0, 0], BF16_O_ATOL)
     assert not torch.isnan(o).any()
+
+
+@pytest.mark.parametrize("fill", [0x00, 0xFF, 0x01])
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2)])
+def test_workspace_contents_do_not_matter(cuda_lib, fill, H, Hkv):
+    # The workspace's contents on entry do not matter: every partial the merge reads is written by
+    # the same call (an empty chunk writes O_c = 0, lse_c = -inf), whatever the workspace held
+    # before (zeros, all ones, small values) and across repeated calls on the same workspace.
+    # Grouped heads with two queries per row take the group kernel.
+    oa = cuda_lib
+    B, Nq, Nk, d, splits = 3, 2, 2000, 128, 16
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.bfloat16, seed=fill + H)
+    kv_len = [2000, 700, 0]
+    kvd = torch.tensor(kv_len, dtype=torch.int32).cuda()
+    ws = torch.full((oa.splitkv_workspace_bytes(B, H, Nq, d, splits),), fill, dtype=torch.uint8, device="cuda")
+    g = H // Hkv
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k.repeat_interleave(g, dim=1)),
+                              bf16_bits(v.repeat_interleave(g, dim=1)), kv_len=kv_len)
+    out = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    for _ in range(3):
+        out.fill_(7.0)
+        lse.fill_(7.0)
+        oa.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), splits, kv_len=kvd, out=out, lse=lse, workspace=ws)
+        torch.cuda.synchronize()
+        oa.sync_status()
+        assert_lse_close(lse, rl)
+        assert_out_close(out, ro, BF16_O_ATOL, lse_ref=rl)
