@@ -323,6 +323,17 @@ def _case_softmax(oa, si, torch, dev, batch):
                 "row softmax + LSE fp32 [4096, 32768], N(0,1)*4, 1% rows -inf, 10% -inf prefix")
 
 
+def _case_softmax_wide(oa, si, torch, dev, batch):
+    rows, cols = 256, 262144
+    x, *_ = si.softmax_input(rows, cols, seed=0)
+    x = x.to(dev)
+    y, lse = torch.empty_like(x), torch.empty(rows, dtype=torch.float32, device=dev)
+    return Case(lambda: oa.softmax_rows(x, y=y, lse=lse), softmax_bytes(rows, cols), "GB/s", "hbm",
+                f"row softmax + LSE fp32 [{rows}, {cols}] (rows wider than a cluster's registers: 16 CTAs of a "
+                "cluster per row, each reading its 64 KB slice twice, the second time from L2), N(0,1)*4, 1% rows "
+                "-inf, 10% -inf prefix")
+
+
 def _case_attn_noncausal(oa, si, torch, dev, batch):
     q, k, v = si.attn_inputs(4, 16, 4096, 4096, 64, torch.bfloat16, seed=0, device=dev)
     o, lse = torch.empty_like(q), torch.empty((4, 16, 4096), dtype=torch.float32, device=dev)
@@ -409,6 +420,7 @@ def _case_bwd_noncausal_d64(oa, si, torch, dev, batch):
 CASES = {
     "attn_causal": _case_attn_causal,
     "softmax_rows": _case_softmax,
+    "softmax_rows_wide": _case_softmax_wide,
     "attn_noncausal_d64": _case_attn_noncausal,
     "attn_splitkv_decode": _case_decode,
     "attn_decode_gqa": _case_decode_gqa,

@@ -10,8 +10,16 @@
 //      associative and commutative, so any tree works);
 //   3. y = exp(x - m) / l is written from the registers.
 // Loads and stores are 128-bit and coalesced when the rows are 16-byte
-// aligned.  Rows wider than the cluster's register capacity stream their
-// slice twice (statistics pass, then output pass).
+// aligned.  Up to 65,536 columns a row is held on chip: 8192 columns per
+// CTA (256 threads x 32 fp32 in registers), up to 8 CTAs of a cluster per
+// row.  Wider rows give each CTA a slice of two such pieces (16,384
+// columns), up to 16 CTAs of a cluster per row where the device schedules
+// that non-portable size, and the CTA reads its slice twice (statistics
+// pass, then output pass): the second read of a 64 KB slice, issued right
+// after the first, comes back from L2, so X still crosses HBM once.  This
+// measured faster than holding 16,384 columns a CTA in registers (two CTAs
+// per SM: 3.4 against 4.9 TB/s at 256 x 262,144) and than one-read clusters
+// of 16 x 8192 (4.5 against 5.3 TB/s at 512 x 131,072).
 // A row whose elements are all -inf has l = 0: it writes y = +0.0 and
 // lse = -inf without forming -inf - -inf anywhere.
 #include <cooperative_groups.h>
@@ -253,11 +261,44 @@ cudaError_t launch_cfg(const float* x, int64_t rows, int64_t cols, int64_t ld_x,
   return cudaLaunchKernelEx(&cfg, softmax_rows_kernel<E, VEC>, x, cols, ld_x, y, ld_y, lse, cluster, slice);
 }
 
+constexpr int kMaxDevices = 64;
+
+// Largest cluster the 32-element instance may use on the current device: 16 when the device
+// schedules a non-portable cluster of that size for it, else the portable 8.
+template <bool VEC>
+int wide_cluster_limit(cudaStream_t s) {
+  static int limit[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 8;
+  if (limit[dev] == 0) {
+    int lim = 8;
+    if (cudaFuncSetAttribute(softmax_rows_kernel<32, VEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(16, 1, 1);
+      cfg.blockDim = dim3(kMaxThreads, 1, 1);
+      cfg.stream = s;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 16;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, softmax_rows_kernel<32, VEC>, &cfg) == cudaSuccess && n > 0) lim = 16;
+    }
+    (void)cudaGetLastError();  // a refused query leaves no error behind
+    limit[dev] = lim;
+  }
+  return limit[dev];
+}
+
 template <bool VEC>
 cudaError_t launch_vec(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
                        float* lse, cudaStream_t s) {
-  // Register capacity of one CTA: 256 threads x 32 fp32.  Up to 8 CTAs
-  // (a portable cluster) share a row; beyond that each CTA streams.
+  // Register capacity of one CTA: 256 threads x 32 fp32.  Up to 8 CTAs (a portable cluster) hold a
+  // row on chip; wider rows take slices of two pieces, up to 16 CTAs a row (see the file comment).
   constexpr int64_t kCtaCap = (int64_t)kMaxThreads * 32;
   if (cols <= 1024) {
     const int threads = (int)(((cols + 3) / 4 + 31) / 32 * 32);
@@ -266,7 +307,13 @@ cudaError_t launch_vec(const float* x, int64_t rows, int64_t cols, int64_t ld_x,
   if (cols <= 2048) return launch_cfg<8, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
   if (cols <= 4096) return launch_cfg<16, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
   int cluster = (int)((cols + kCtaCap - 1) / kCtaCap);
-  if (cluster > 8) cluster = 8;
+  if (cluster > 8) {
+    cluster = (int)((cols + 2 * kCtaCap - 1) / (2 * kCtaCap));
+    if (cluster > 8) {
+      const int lim = wide_cluster_limit<VEC>(s);
+      if (cluster > lim) cluster = lim;
+    }
+  }
   const int64_t slice = ((cols + cluster - 1) / cluster + 3) / 4 * 4;
   return launch_cfg<32, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, s);
 }

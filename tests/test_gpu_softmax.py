@@ -38,10 +38,21 @@ def test_worked_examples(cuda_lib):
 
 
 @pytest.mark.parametrize("cols", [1, 3, 37, 128, 1000, 1023, 1025, 2048, 4097, 8192, 8193, 20000, 32768, 40960,
-                                  40964, 65536, 70001])
+                                  40964, 65536, 70001, 98304, 131072, 131073, 200003, 262144, 262148, 400000])
 def test_ragged_widths_with_masks(cuda_lib, cols):
     rows = 24
     x, full, pre, _ = si.softmax_input(rows, cols, seed=cols, frac_full=0.1, frac_prefix=0.3)
+    y, lse = _run(cuda_lib, x)
+    ry, rl = oracle.softmax_rows(x.numpy())
+    assert_softmax_close(y, ry)
+    assert_lse_close(lse, rl)
+
+
+@pytest.mark.parametrize("cols", [70001, 150001, 262145])
+def test_wide_unaligned_rows(cuda_lib, cols):
+    # odd widths: rows are not 16-byte aligned, so the scalar form of the wide instance runs (one read
+    # up to 16 x 16384 columns, streaming beyond)
+    x, *_ = si.softmax_input(6, cols, seed=cols + 1, frac_full=0.2, frac_prefix=0.4)
     y, lse = _run(cuda_lib, x)
     ry, rl = oracle.softmax_rows(x.numpy())
     assert_softmax_close(y, ry)
