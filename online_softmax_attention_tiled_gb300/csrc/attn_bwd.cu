@@ -681,6 +681,11 @@ __global__ void __launch_bounds__(kBwdThreads)
 // this step's dK and dQ MMAs:
 //   MMA warp:   dV_n, S_{n+1}, dK_n, dQ_n (once dQ_{n-1} has been read out), dP_{n+1}
 //   row warps:  P pass n, dQ_{n-1} read-out and staging, dS pass n, (LSE, D) of step n + 1
+// The last 64 TMEM columns hold K and V (bf16 pairs, copied in by the row warps once per CTA), so the
+// S^T = K Q^T and dP^T = V dO^T MMAs take their A operand from TMEM: the two 16 KB tiles are not
+// re-read from shared memory every step, whose bandwidth the tensor core's operand reads and the row
+// warps' accesses otherwise share.  The (LSE, D) entries of a step are double-buffered, so the row
+// warps write the next step's entries as soon as their own dS pass is done.
 // Everything else (roles, passes, masks, the dQ reduce-adds, the dK / dV epilogue) is as in
 // attn_bwd_tc_kernel.
 // ---------------------------------------------------------------------------------------------
@@ -694,14 +699,17 @@ struct Bwd64Cfg {
   static constexpr int DO_OFF = Q_OFF + NST * TILE_BYTES;
   static constexpr int ST_OFF = DO_OFF + NST * TILE_BYTES;  // dS of a step: two 64-query slabs
   static constexpr int DQB_OFF = ST_OFF + 2 * TILE_BYTES;   // dQ staging: warp w's 32 x 32 fp32 block at w * 4 KB
-  static constexpr int LD_OFF = DQB_OFF + kBwdRowWarps * 4096;  // -LSE log2 e, then -D scale, of the step's queries
-  static constexpr int BAR_OFF = LD_OFF + BT * 8;
+  // two buffers (step parity) of the step's 128 (-LSE log2 e) then 128 (-D scale)
+  static constexpr int LD_OFF = DQB_OFF + kBwdRowWarps * 4096;
+  static constexpr int LD_BYTES = BT * 8;
+  static constexpr int BAR_OFF = LD_OFF + 2 * LD_BYTES;
   // kv_full, qdo_full[3], qdo_empty[3], s_full, dp_full, p_ready[2], ds_ready[2], dq_full, dq_read,
   // dq_staged, dqb_empty, ld_ready[2], done
-  static constexpr int NUM_BARS = 20;
+  static constexpr int NUM_BARS = 21;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
-  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384;
+  static constexpr uint32_t S_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 320, DQ_COL = 384, K_COL = 448,
+                            V_COL = 480;
   static constexpr uint32_t IDESC_S = idesc_bf16_f32(BT, BT, false);
   static constexpr uint32_t IDESC_KV = idesc_bf16_f32(BT, D, true);
   static constexpr uint32_t IDESC_Q = idesc_bf16_f32(BT, D, true, true);
@@ -735,6 +743,7 @@ __global__ void __launch_bounds__(kBwdThreads)
   const uint32_t bar_dqb_empty = bar0 + 8u * 16;                    // staged blocks read by their adds
   auto bar_ld = [&](int h) { return bar0 + 8u * (17 + h); };        // half h's (LSE, D) entries written
   const uint32_t bar_done = bar0 + 8u * 19;                         // every MMA of the CTA complete
+  const uint32_t bar_kvt = bar0 + 8u * 20;                          // K, V copied into TMEM (8 warps)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::MISC_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
@@ -762,6 +771,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     mbar_init(bar_dq_staged, kBwdRowWarps);
     mbar_init(bar_dqb_empty, 1);
     mbar_init(bar_done, 1);
+    mbar_init(bar_kvt, kBwdRowWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -812,8 +822,6 @@ __global__ void __launch_bounds__(kBwdThreads)
     mbar_wait(bar_kv, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
   } else if (warp == kBwdMma) {
     // =================== MMA issue (whole warp, one elected lane) ===================
-    const uint64_t k_kmaj = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);                 // A of S^T
-    const uint64_t v_kmaj = smem_desc_sw128(sbase + C::V_OFF, 16, 1024);                 // A of dP^T
     const uint64_t k_nmaj = smem_desc_sw128(sbase + C::K_OFF, C::TILE_BYTES, 1024);      // B of dQ
     const uint64_t st_mmaj = smem_desc_sw128(sbase + C::ST_OFF, C::TILE_BYTES, 1024);    // A of dQ
     auto kmaj = [&](int s0, int st, int kk) {  // K-major tile of stage st, K step kk (16 of the 64 dims)
@@ -824,21 +832,22 @@ __global__ void __launch_bounds__(kBwdThreads)
     auto pcol = [](int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); };  // P^T / dS^T column
     // S^T (into S_COL, whose P^T the dV MMAs issued before have read) and dP^T (into DP_COL, whose
     // dS^T the dK MMAs issued before have read) of the step in stage st
+    // A from TMEM: K (V) row k of the tile in lane k, dims 16 kk .. 16 kk + 15 in columns 8 kk .. + 7
     auto issue_s = [&](int st) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_elect(tmem_base + C::S_COL, k_kmaj + (uint64_t)((kk * 32) >> 4), kmaj(C::Q_OFF, st, kk), C::IDESC_S,
+        mma_ts_elect(tmem_base + C::S_COL, tmem_base + C::K_COL + 8 * kk, kmaj(C::Q_OFF, st, kk), C::IDESC_S,
                      kk > 0 ? 1u : 0u);
       mma_commit_elect(bar_s);
     };
     auto issue_dp = [&](int st) {
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss_elect(tmem_base + C::DP_COL, v_kmaj + (uint64_t)((kk * 32) >> 4), kmaj(C::DO_OFF, st, kk),
-                     C::IDESC_S, kk > 0 ? 1u : 0u);
+        mma_ts_elect(tmem_base + C::DP_COL, tmem_base + C::V_COL + 8 * kk, kmaj(C::DO_OFF, st, kk), C::IDESC_S,
+                     kk > 0 ? 1u : 0u);
       mma_commit_elect(bar_dp);
     };
-    bool ok = wait_all(bar_kv, 0, B_KV);
+    bool ok = wait_all(bar_kv, 0, B_KV) && wait_all(bar_kvt, 0, B_KV);
     if (ok && n_it > 0 && (ok = wait_all(bar_qdo(0), 0, B_QDO))) {
       tc_fence_after_sync();
       issue_s(0);
@@ -927,12 +936,31 @@ __global__ void __launch_bounds__(kBwdThreads)
     const int key = k0 + tt;
     const bool key_ok = key < Nk;
     uint8_t* st_row = smem + C::ST_OFF + half * C::TILE_BYTES + tt * 128;  // key row in slab `half`
-    const float4* nl4 = reinterpret_cast<const float4*>(smem + C::LD_OFF);
-    const float4* nd4 = reinterpret_cast<const float4*>(smem + C::LD_OFF + BT * 4);
+    // entries of the step with parity b: -LSE log2 e of its 128 queries, then -D scale
+    auto nl4_of = [&](int b) { return reinterpret_cast<const float4*>(smem + C::LD_OFF + b * C::LD_BYTES); };
+    auto nd4_of = [&](int b) { return reinterpret_cast<const float4*>(smem + C::LD_OFF + b * C::LD_BYTES + BT * 4); };
     // threads 0-63 of each half own the (LSE, D) entries of that half's queries
     const int ld_q = 64 * half + tt;
-    float* nl_mine = reinterpret_cast<float*>(smem + C::LD_OFF) + ld_q;
-    float* nd_mine = reinterpret_cast<float*>(smem + C::LD_OFF + BT * 4) + ld_q;
+    // This warp's key rows of K (warps 0-3) or V (warps 4-7) into their TMEM columns, once: the
+    // 128-byte row of the swizzled tile (16-byte chunk c of row r at chunk c ^ (r % 8)), as the bf16
+    // pairs of the S^T / dP^T MMAs' A operand.
+    {
+      bool kv_ok = wait_all(bar_kv, 0, B_KV);
+      if (kv_ok) {
+        const uint8_t* trow = smem + (half ? C::V_OFF : C::K_OFF) + tt * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(trow + ((c ^ (tt & 7)) * 16));
+          w[4 * c] = u.x, w[4 * c + 1] = u.y, w[4 * c + 2] = u.z, w[4 * c + 3] = u.w;
+        }
+        tmem_st32(tl + (half ? C::V_COL : C::K_COL), w);
+        tmem_st_wait();
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_kvt);
+    }
     const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t sl2 = f2_pack(p.scale, p.scale);
     auto load_ld = [&](int step, StepPos sp, float& l, float& dd) {
@@ -947,10 +975,10 @@ __global__ void __launch_bounds__(kBwdThreads)
     };
     // -LSE log2 e and -D scale of a step's queries; a row past the end or with no visible key gets -inf,
     // so that exp2(s scale log2 e - inf) = 0 needs no test
-    auto write_ld = [&](float l, float dd) {
+    auto write_ld = [&](int b, float l, float dd) {
       if (tt < 64) {
-        *nl_mine = l == -INFINITY ? -INFINITY : -l * kLog2e;
-        *nd_mine = -dd * p.scale;
+        reinterpret_cast<float*>(smem + C::LD_OFF + b * C::LD_BYTES)[ld_q] = l == -INFINITY ? -INFINITY : -l * kLog2e;
+        reinterpret_cast<float*>(smem + C::LD_OFF + b * C::LD_BYTES + BT * 4)[ld_q] = -dd * p.scale;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ld(half));
@@ -977,12 +1005,14 @@ __global__ void __launch_bounds__(kBwdThreads)
       if (lane == 0) mbar_arrive(bar_dq_staged);
       return true;
     };
-    // the entries of step it are written during step it - 1, after every warp of the half is past
-    // its dS pass (the last reader of the previous entries); their loads a step before that
+    // the entries of step it go to buffer it % 2 during step it - 1, once this warp is past its dS
+    // pass: every warp of the half has then read the entries of step it - 2 (it waited for all of them
+    // to write the entries of step it - 1, which each does after its own dS pass of step it - 2);
+    // their loads a step before that
     StepPos lpos = first_pos;
     float next_l, next_d;
     load_ld(0, lpos, next_l, next_d);
-    write_ld(next_l, next_d);
+    write_ld(0, next_l, next_d);
     lpos = lpos.next(g);
     load_ld(1, lpos, next_l, next_d);
     bool ok = true;
@@ -997,6 +1027,8 @@ __global__ void __launch_bounds__(kBwdThreads)
       // P^T of this warp's 64 queries over the first 32 of its S^T columns (read by it alone)
       const uint32_t sc = tl + C::S_COL + 64 * half;
       const uint32_t dc = tl + C::DP_COL + 64 * half;
+      const float4* nl4 = nl4_of(it & 1);
+      const float4* nd4 = nd4_of(it & 1);
       uint64_t pp[32];
       {
         uint32_t sr[64], pw[32];
@@ -1031,8 +1063,7 @@ __global__ void __launch_bounds__(kBwdThreads)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds(half));
       pos = pos.next(g);
-      if (!(ok = wait_all(bar_ds(half), ph, B_DS))) break;
-      write_ld(next_l, next_d);
+      write_ld((it + 1) & 1, next_l, next_d);
       lpos = lpos.next(g);
       load_ld(it + 2, lpos, next_l, next_d);
     }
