@@ -14,9 +14,10 @@
 // CTA (256 threads x 32 fp32 in registers), up to 8 CTAs of a cluster per
 // row.  Wider rows give each CTA a slice of two such pieces (16,384
 // columns), up to 16 CTAs of a cluster per row where the device schedules
-// that non-portable size, and the CTA reads its slice twice (statistics
-// pass, then output pass): the second read of a 64 KB slice, issued right
-// after the first, comes back from L2, so X still crosses HBM once.  This
+// that non-portable size, and the CTA reads its slice in a statistics pass,
+// then writes the output of the piece still in its registers and reads the
+// others again: the second read of a 64 KB slice, issued right after the
+// first, comes back from L2, so X still crosses HBM once.  This
 // measured faster than holding 16,384 columns a CTA in registers (two CTAs
 // per SM: 3.4 against 4.9 TB/s at 256 x 262,144) and than one-read clusters
 // of 16 x 8192 (4.5 against 5.3 TB/s at 512 x 131,072).
@@ -159,9 +160,9 @@ __device__ __forceinline__ void store_piece(float* __restrict__ yr, int64_t base
 // CTAs per SM the register budget is cut for: five 256-thread CTAs (48 registers) hide each
 // other's load and reduction phases better than four (64 registers: 0.194 -> 0.187 ms at
 // 4096 x 32768; three at 80 registers were 0.8 % slower than four); the scalar 32-element
-// instance keeps four, at 48 registers it would spill.
+// instance runs three (at four, 64 registers, its streaming branch spills).
 template <int E, bool VEC>
-constexpr int kSoftmaxMinBlocks = (E == 32 && !VEC) ? 4 : 5;
+constexpr int kSoftmaxMinBlocks = (E == 32 && !VEC) ? 3 : 5;
 
 // grid.x = rows * cluster; the `cluster` CTAs of a row split its columns into
 // slices of `slice` columns (a multiple of 4).
@@ -231,7 +232,11 @@ __global__ void __launch_bounds__(kMaxThreads, kSoftmaxMinBlocks<E, VEC>)
     if (resident) {
       store_piece<E, VEC>(yr, c0, c1, v, ref, inv_l);
     } else {
-      for (int64_t b = c0; b < c1; b += piece) {
+      // the statistics pass ended on the slice's last piece, still in registers: it goes out
+      // first, without a second read; the earlier pieces are read again (from L2)
+      const int64_t last = c0 + (c1 - c0 - 1) / piece * piece;
+      store_piece<E, VEC>(yr, last, c1, v, ref, inv_l);
+      for (int64_t b = c0; b < last; b += piece) {
         load_piece<E, VEC, false>(xr, b, c1, v);
         store_piece<E, VEC>(yr, b, c1, v, ref, inv_l);
       }
