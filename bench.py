@@ -88,10 +88,10 @@ def softmax_bytes(rows, cols):
     return 4.0 * rows * cols * 2 + 4.0 * rows
 
 
-def decode_bytes(b, h, d, kv_len_sum, esize=2, h_kv=None):
-    """q, the visible K and V rows (h_kv heads; default h), O and LSE."""
+def decode_bytes(b, h, d, kv_len_sum, esize=2, h_kv=None, nq=1):
+    """q, the visible K and V rows (h_kv heads; default h), O and LSE, for nq new tokens per sequence."""
     h_kv = h if h_kv is None else h_kv
-    return esize * (2.0 * h_kv * d * kv_len_sum + b * h * d * 2) + 4.0 * b * h
+    return esize * (2.0 * h_kv * d * kv_len_sum + b * h * nq * d * 2) + 4.0 * b * h * nq
 
 
 def varlen_causal_flops(lengths, h, d):
@@ -368,6 +368,19 @@ def _case_decode_gqa(oa, si, torch, dev, batch):
                 "tensor-core forward (no key split; num_splits and the workspace are unused)")
 
 
+def _case_decode_gqa_4tok(oa, si, torch, dev, batch):
+    b, nq = batch or 32, 4
+    q, k, v = si.attn_inputs_gqa(b, 32, 8, nq, 32768, 128, torch.bfloat16, seed=0, device=dev)
+    kv_len = si.decode_kv_len(b, 32768, seed=0)
+    kvd = kv_len.to(dev)
+    o, lse = torch.empty_like(q), torch.empty((b, 32, nq), dtype=torch.float32, device=dev)
+    return Case(lambda: oa.attn_fwd(q, k, v, causal=True, kv_len=kvd, out=o, lse=lse),
+                decode_bytes(b, 32, 128, int(kv_len.sum()), h_kv=8, nq=nq), "GB/s", "hbm",
+                f"multi-token decode bf16: {nq} new tokens per sequence (causal, at the end of the cache) against a "
+                f"grouped KV cache B={b} H=32 H_kv=8 Nk=32768 d=128, 5% of sequences truncated; each group's 4 heads "
+                f"x {nq} tokens run as 16 rows of one plane of the tensor-core forward")
+
+
 def _case_attn_varlen(oa, si, torch, dev, batch):
     lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
     q, k, v, cq, ck = si.varlen_inputs(lens, lens, 32, 8, 128, torch.bfloat16, seed=0, device=dev)
@@ -424,6 +437,7 @@ CASES = {
     "attn_noncausal_d64": _case_attn_noncausal,
     "attn_splitkv_decode": _case_decode,
     "attn_decode_gqa": _case_decode_gqa,
+    "attn_decode_gqa_4tok": _case_decode_gqa_4tok,
     "attn_varlen_causal_gqa": _case_attn_varlen,
     "attn_prefill_kv_cache": _case_prefill_kv_cache,
     "attn_bwd_causal": _case_bwd_causal,

@@ -133,10 +133,12 @@ oa_status oa_attn_fwd(const void* q, const void* k, const void* v, void* o, floa
  * length and KV-cache calls) is read to ask for.
  *   q, o [B, H, Nq, d]; k, v [B, H_kv, Nk, d]; everything else as in
  *   oa_attn_fwd (dtype, alignment, lse, causal, scale, kv_len, support).
- * With one query per row (Nq = 1, bf16; causal changes nothing for one
- * query, which sees every key), the query heads of a group are run as the
- * rows of one [B, H_kv, H / H_kv, d] problem, so each group's K/V is read
- * once (the decode case).
+ * Decode (bf16, d = 64 / 128, (H / H_kv) * Nq <= 128: one or a few new
+ * tokens per sequence): the query heads of a group hold (H / H_kv) * Nq
+ * consecutive rows of q, o and lse, which run as the rows of one
+ * [B, H_kv, (H / H_kv) * Nq, d] problem, so each group's K/V is read once;
+ * causal positions are taken per query token (a row's index modulo Nq).
+ * One query with causal set sees every key and runs as non-causal.
  * Errors: those of oa_attn_fwd, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */
@@ -351,13 +353,14 @@ oa_status oa_attn_splitkv(const void* q, const void* k, const void* v, void* o, 
  * key/value heads than query heads): k and v are [B, H_kv, Nk, d] and query
  * head h reads head h / (H / H_kv); kv_len gives each sequence's cache
  * length.  Same workspace size and support matrix as oa_attn_splitkv.
- * Grouped one-query decode takes no split: with Nq = 1, bf16 and d = 64 /
- * 128 the H / H_kv query heads of a group are consecutive rows of q, o and
- * lse and are computed together by the tensor-core forward kernel (one
- * launch), every K/V row read once for the whole group.  On that path
- * num_splits and the workspace are checked but NOT USED; the result is the
- * same attention.  Other grouped calls (Nq > 1, fp32) split the keys into
- * num_splits chunks and merge, as oa_attn_splitkv does.
+ * Grouped decode takes no split: with bf16, d = 64 / 128 and
+ * (H / H_kv) * Nq <= 128, the group's query heads x queries are
+ * consecutive rows of q, o and lse and are computed together by the
+ * tensor-core forward kernel (one launch), every K/V row read once for the
+ * whole group.  On that path num_splits and the workspace are checked but
+ * NOT USED; the result is the same attention.  Other grouped calls (more
+ * rows per group, fp32) split the keys into num_splits chunks and merge, as
+ * oa_attn_splitkv does.
  * Errors: those of oa_attn_splitkv, plus OA_ERR_INVALID when H_kv < 1 or
  * H_kv does not divide H.
  */

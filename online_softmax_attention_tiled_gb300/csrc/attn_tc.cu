@@ -125,6 +125,7 @@ struct TcParams {
   int Tq, Tk;
   int H, Nq, Nk, num_qblocks, BH;  // packed: Nq = longest query sequence, BH = sequences x H
   int off;               // dense causal: query i sees keys j <= i + off (Nk - Nq); causality is the MODE
+  int qmod;              // > 0: a row's causal position is its index modulo qmod (grouped decode rows)
   int group;             // query heads per key/value head (H / H_kv)
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
   int l_rs;              // LSE row stride: 1 dense, H packed
@@ -622,6 +623,10 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         off = MODE == kCausalOff ? it.off : 0;
       }
       const int row = r0 + tt;
+      // causal position of the row: its index, or its index modulo qmod when a plane's rows are the
+      // queries of several heads -- at most 128 rows, so the split-slot instance (the smallest
+      // position, 0, is row r0's: the tile-level test stays valid)
+      const int rpos = (SPLIT && MODE == kCausalOff && p.qmod > 0) ? row % p.qmod : row;
       float m = -INFINITY;  // running max of the scaled scores, log2 units
       float l = 0.f;
 
@@ -646,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
 #pragma unroll
           for (int c = 0; c < BN; ++c) {
             const int col = col0 + c;
-            if (col >= kvl || (kCausalMask && col > row + off)) s[c] = -INFINITY;
+            if (col >= kvl || (kCausalMask && col > rpos + off)) s[c] = -INFINITY;
           }
         }
         // row max of the raw scores (scale > 0 commutes with max)
@@ -899,7 +904,8 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.H = a.H;
   p.Nq = a.Nq;
   p.Nk = a.Nk;
-  p.off = a.Nk - a.Nq;
+  p.off = a.Nk - (a.qmod > 0 ? a.qmod : a.Nq);
+  p.qmod = a.qmod;
   p.num_qblocks = (a.Nq + 2 * BM - 1) / (2 * BM);
   p.BH = a.B * a.H;
   p.group = a.H / Hkv;
@@ -910,7 +916,7 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
   // Instance by layout, query-tile use and masking mode (packed sequences may each have their own
   // key offset; a dense call has one, Nk - Nq)
-  const int mode = !a.causal ? kNonCausal : (packed || a.Nk != a.Nq) ? kCausalOff : kCausal;
+  const int mode = !a.causal ? kNonCausal : (packed || a.qmod > 0 || a.Nk != a.Nq) ? kCausalOff : kCausal;
   if (packed) {
     if (mode == kNonCausal)
       return d == 128 ? launch_d<128, true, false, kNonCausal>(mq, mk, mv, p, s)

@@ -163,9 +163,11 @@ static oa_status check_fwd(const void* q, const void* k, const void* v, void* o,
 }
 
 // The dense forward on `stream`, arguments already checked.
+// qmod > 0: each plane's rows are the queries of several query heads, qmod per head (grouped decode),
+// and a row's causal position is its index modulo qmod.
 static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
                             int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
-                            const oa::DevStatus& st, cudaStream_t stream, const char* who) {
+                            const oa::DevStatus& st, cudaStream_t stream, const char* who, int qmod = 0) {
   if (dt == OA_BF16) {
     oa::TcArgs a{};
     a.q = q;
@@ -182,6 +184,7 @@ static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o
     a.causal = causal;
     a.scale = scale;
     a.kv_len = kv_len;
+    a.qmod = qmod;
     const char* why = nullptr;
     cudaError_t e = oa::launch_attn_tc(a, st, stream, &why);
     if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_fwd launch");
@@ -193,12 +196,13 @@ static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o
   return e == cudaSuccess ? ok() : cuda_fail(e, "attn_fwd launch");
 }
 
-// One query per head with grouped key/value heads (decode): the g = H / H_kv query heads of a group
-// are g consecutive rows of q, o and lse, so the batch is also a [B, H_kv, g, d] forward in which
-// each plane's K/V rows are streamed once for all g queries by the tensor-core kernel (0.70 ms
-// instead of 0.97 ms split-KV for B32 H32 H_kv8 Nk32768 d128; 0.35 instead of 1.17 at H_kv 4).
-static bool grouped_single_query(oa_dtype dt, int H, int Hkv, int Nq, int d, int causal) {
-  return dt == OA_BF16 && Nq == 1 && Hkv < H && (d == 64 || d == 128) && !causal;
+// Decode with grouped key/value heads (one or a few new tokens per sequence): the g = H / H_kv query
+// heads of a group hold g * Nq consecutive rows of q, o and lse, so the batch is also a
+// [B, H_kv, g Nq, d] forward in which each plane's K/V rows are streamed once for all the group's
+// queries by the tensor-core kernel (0.70 ms instead of 0.97 ms split-KV for B32 H32 H_kv8 Nq1
+// Nk32768 d128; 0.35 instead of 1.17 at H_kv 4).  Causal: a row's position is its index modulo Nq.
+static bool grouped_queries(oa_dtype dt, int H, int Hkv, int Nq, int d) {
+  return dt == OA_BF16 && Hkv < H && (d == 64 || d == 128) && (int64_t)(H / Hkv) * Nq <= 128;
 }
 
 static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
@@ -210,9 +214,9 @@ static oa_status attn_fwd_impl(const void* q, const void* k, const void* v, void
   if (!dev_status(&st)) return fail(OA_ERR_CUDA, "%s: no current CUDA device", who);
   // one query is the sequence's last position and sees every key: causal changes nothing
   if (Nq == 1) causal = 0;
-  if (grouped_single_query(dt, H, Hkv, Nq, d, causal))
-    return launch_fwd(q, k, v, o, lse, dt, B, Hkv, Hkv, H / Hkv, Nk, d, 0, scale, kv_len, st, (cudaStream_t)stream,
-                      who);
+  if (grouped_queries(dt, H, Hkv, Nq, d))
+    return launch_fwd(q, k, v, o, lse, dt, B, Hkv, Hkv, H / Hkv * Nq, Nk, d, causal, scale, kv_len, st,
+                      (cudaStream_t)stream, who, causal ? Nq : 0);
   return launch_fwd(q, k, v, o, lse, dt, B, H, Hkv, Nq, Nk, d, causal, scale, kv_len, st, (cudaStream_t)stream, who);
 }
 
@@ -588,11 +592,11 @@ static oa_status attn_splitkv_impl(const void* q, const void* k, const void* v, 
   const size_t need = oa_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16))
     return fail(OA_ERR_INVALID, "attn_splitkv: workspace must be 16-byte aligned and >= %zu bytes", need);
-  if (grouped_single_query(dt, H, Hkv, Nq, d, 0)) {  // the whole group per plane, no split needed
+  if (grouped_queries(dt, H, Hkv, Nq, d)) {  // the whole group per plane, no split needed
     oa::DevStatus st;
     if (!dev_status(&st)) return fail(OA_ERR_CUDA, "attn_splitkv: no current CUDA device");
-    return launch_fwd(q, k, v, o, lse, dt, B, Hkv, Hkv, H / Hkv, Nk, d, 0, scale, kv_len, st, (cudaStream_t)stream,
-                      "attn_splitkv");
+    return launch_fwd(q, k, v, o, lse, dt, B, Hkv, Hkv, H / Hkv * Nq, Nk, d, 0, scale, kv_len, st,
+                      (cudaStream_t)stream, "attn_splitkv");
   }
   float* part_o = static_cast<float*>(workspace);
   float* part_lse = part_o + (size_t)num_splits * R * d;

@@ -52,6 +52,9 @@ struct TcArgs {
   const int32_t* kv_len;
   const int32_t *cu_q, *cu_k;
   int Tq, Tk;
+  // > 0: the rows of a plane are the queries of several query heads, qmod each (grouped decode); a
+  // row's causal position is its index modulo qmod, and Nk - qmod is the causal key offset
+  int qmod;
 };
 // `why` gets a static message when the host-side set-up (tensor maps) fails.
 cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s, const char** why);

@@ -98,3 +98,11 @@ def test_chunked_prefill_work():
     pairs = sum(30721 + i for i in range(2048))
     assert bench.causal_pairs(2048, 32768) == pairs == 65012736
     assert bench.kvcache_causal_flops(8, 32, 2048, 32768, 128) == pytest.approx(4 * 128 * 8 * 32 * pairs)
+
+
+def test_multi_token_decode_bytes():
+    b, h, d, kv, nq = 2, 4, 8, [5, 3], 3
+    # bf16 q and o (b h nq d each), K and V of the visible keys over one key/value head, fp32 LSE per row
+    want = 2 * (b * h * nq * d) * 2 + 2 * (2 * 1 * d * sum(kv)) + 4 * b * h * nq
+    assert bench.decode_bytes(b, h, d, sum(kv), h_kv=1, nq=nq) == want
+    assert bench.decode_bytes(b, h, d, sum(kv), h_kv=1) == bench.decode_bytes(b, h, d, sum(kv), h_kv=1, nq=1)

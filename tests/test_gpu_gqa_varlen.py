@@ -73,8 +73,8 @@ def test_gqa_splitkv_decode(cuda_lib, dtype, d):
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("nq", [1, 2])
 def test_gqa_decode_groups(cuda_lib, H, Hkv, d, nq):
-    # one query per head runs each group as the rows of one plane (forward kernel); two queries per head
-    # take the split-KV group kernel; both entry points, every group size, against the oracle
+    # one or two queries per head run each group's (head, query) pairs as the rows of one plane (forward
+    # kernel); both entry points, every group size, against the oracle
     B, Nk = 3, 700
     q, k, v = si.attn_inputs_gqa(B, H, Hkv, nq, Nk, d, torch.bfloat16, seed=70 + H // Hkv + d + nq)
     kv_len = [700, 129, 0]
@@ -88,6 +88,24 @@ def test_gqa_decode_groups(cuda_lib, H, Hkv, d, nq):
     _sync(cuda_lib)
     assert_lse_close(lse2, rl)
     assert_out_close(o2, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("H,Hkv,nq", [(16, 2, 20), (8, 2, 40), (16, 4, 33)])
+def test_gqa_splitkv_group_kernel(cuda_lib, H, Hkv, nq):
+    # more than 128 (head, query) rows per group: split-KV takes its group kernel (each K/V row read once
+    # and scored against every query of the group, chunks merged by LSE)
+    B, Nk, d = 2, 1500, 128
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, nq, Nk, d, torch.bfloat16, seed=80 + nq)
+    kv_len = [1500, 611]
+    kvd = torch.tensor(kv_len, dtype=torch.int32).cuda()
+    g = H // Hkv
+    assert g * nq > 128
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k.repeat_interleave(g, dim=1)),
+                              bf16_bits(v.repeat_interleave(g, dim=1)), kv_len=kv_len)
+    o, lse = cuda_lib.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), 12, kv_len=kvd)
+    _sync(cuda_lib)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
 
 
 def _varlen_check(oa, lq, lk, H, Hkv, d, causal, seed, max_q=None, max_k=None):

@@ -125,3 +125,41 @@ def test_full_size_chunked_prefill_grouped(cuda_lib):
                                   bf16_bits(v[b:b + 1, hk:hk + 1]), causal=True, rows=rows)
         assert_lse_close(lse[b, h][torch.from_numpy(rows).cuda()], rl)
         assert_out_close(o[b, h][torch.from_numpy(rows).cuda()], ro, BF16_O_ATOL)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("Nq", [2, 4, 8])
+@pytest.mark.parametrize("causal", [False, True])
+def test_grouped_multi_token_decode(cuda_lib, d, Nq, causal):
+    # a few new tokens per sequence against a grouped KV cache: the group's query heads x new tokens run
+    # as the rows of one plane (each K/V row read once per group); causal: a row's position is its token
+    B, H, Hkv, Nk = 3, 16, 4, 3000
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.bfloat16, seed=600 + d + Nq)
+    kv_len = [3000, 777, 0]
+    kvd = torch.tensor(kv_len, dtype=torch.int32).cuda()
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, kv_len=kvd)
+    _sync(cuda_lib)
+    g = H // Hkv
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k.repeat_interleave(g, dim=1)),
+                              bf16_bits(v.repeat_interleave(g, dim=1)), causal=causal, kv_len=kv_len)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+    if not causal:  # the split-KV entry point takes the same grouped path
+        o2, lse2 = cuda_lib.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), 8, kv_len=kvd)
+        _sync(cuda_lib)
+        assert_lse_close(lse2, rl)
+        assert_out_close(o2, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("H,Hkv,Nq", [(32, 2, 8), (32, 2, 9), (8, 1, 17)])
+def test_grouped_decode_rows_at_and_past_128(cuda_lib, H, Hkv, Nq):
+    # g * Nq = 128 rows fill a plane exactly; 144 rows take the one-item-per-query-head path
+    B, Nk, d = 2, 700, 128
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.bfloat16, seed=700 + Nq)
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    _sync(cuda_lib)
+    g = H // Hkv
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k.repeat_interleave(g, dim=1)),
+                              bf16_bits(v.repeat_interleave(g, dim=1)), causal=True)
+    assert_lse_close(lse, rl)
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
