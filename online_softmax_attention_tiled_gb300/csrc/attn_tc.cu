@@ -21,28 +21,32 @@
 // and barrier phases run on across items, so the next item's Q, K and V are loaded and
 // its first score tiles computed while the current item finishes.
 //
-// GB300 mapping (320 threads at d=128, 352 at d=64):
+// GB300 mapping (352 threads; 320 at d = 128 with two query tiles):
 //   warps 0-3   softmax for query tile 0 (rows q0 .. q0+127): thread t owns
 //               row t, i.e. TMEM lane t, so row max / sum are thread-local
 //   warps 4-7   softmax for query tile 1 (rows q0+128 .. q0+255)
 //   warp 8      TMA producer: Q per item, then K and V tiles into one 4-slot
 //               (d=128) / 10-slot (d=64) shared-memory ring in load order
 //               K0,V0,K1,V1,... (128-byte swizzle), mbarrier complete_tx
-//   warp 9(,10) MMA issue (whole warp, one elected lane): S_i = Q_i K^T
-//               (SMEM x SMEM -> TMEM) and O_i += P_i V (P from TMEM, V from
-//               SMEM -> TMEM); warp 9 owns the TMEM allocation
+//   warps 9, 10 MMA issue for query tile 0 / 1 (whole warp, one elected lane):
+//               S_i = Q_i K^T (SMEM x SMEM -> TMEM) and O_i += P_i V (P from
+//               TMEM, V from SMEM -> TMEM); warp 9 owns the TMEM allocation.
+//               One warp issues an N <= 128 MMA in about 70 (A from shared
+//               memory) to 90 (A from TMEM) cycles, about as long as the
+//               tensor core takes for an N = 128 one and twice as long as for
+//               N = 64, so each tile has its own issuer -- except at d = 128
+//               with two query tiles, where warp 9 alone issues both tiles'
+//               MMAs (see Cfg::mma_warps)
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d).
 //   d = 128: P_i (bf16, two per column) is written over the first 64 columns
-//   of S_i, so S_i(j+1) can only follow the PV MMA that reads P_i(j).  One
-//   warp issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1): each tile's own MMAs
-//   run back to back, and each softmax group works while the tensor core
-//   runs the other group's.
+//   of S_i, so S_i(j+1) can only follow the PV MMA that reads P_i(j): tile
+//   i's warp issues PV_i(j), S_i(j+1), and each softmax group works while the
+//   tensor core runs the other group's MMAs.
 //   d = 64: P_i gets its own columns [384 + 64 i, +64), so the group frees
 //   S_i as soon as it has read it and S_i(j+1) is computed during the
-//   softmax of S_i(j).  Warp 9 issues tile 0's MMAs and warp 10 tile 1's, in
-//   the order S_i(j+1), PV_i(j); before writing P_i(j) a group waits for
-//   PV_i(j-1).
+//   softmax of S_i(j): the order is S_i(j+1), PV_i(j); before writing P_i(j)
+//   a group waits for PV_i(j-1).
 //   SPLIT instances (dense, at most 128 query rows: decode, multi-token decode):
 //   an item would fill only query tile 0, so both tiles hold the same rows
 //   and take alternate key tiles (tile 0 the even, tile 1 the odd ones) with
@@ -72,6 +76,9 @@ constexpr uint32_t kTmemCols = 512;
 // A row's running max is only moved (and O, l rescaled) when a tile raises it
 // by more than this many log2 units, i.e. a factor 2^8.
 constexpr float kRescaleLog2 = 8.f;
+// P over S: pairs of P computed after the first half of P is stored and before that half is handed
+// to the MMA warp (causal N = 8192, d = 128: 0 or 8 pairs 1540 TFLOP/s, 16 pairs 1544-1549)
+constexpr int kPHandoffLag = 16;
 
 template <int D>
 struct Cfg {
@@ -89,16 +96,24 @@ struct Cfg {
   // softmax of S_i(j) runs (the group frees S_i as soon as it has read it).  Else P_i is
   // written over S_i.
   static constexpr bool SEP_P = (3 * BN + 2 * D <= 512);
-  // With P_i separate each query tile's MMAs come from a warp of its own; with P_i over
-  // S_i one warp issues both tiles' PV and S back to back, which keeps each tile's
-  // critical loop (softmax -> PV_i -> S_i -> softmax) short.
-  static constexpr int MMA_WARPS = SEP_P ? 2 : 1;
-  static constexpr int THREADS = 32 * (9 + MMA_WARPS);  // 8 softmax warps, producer, MMA warp(s)
+  // MMA issuing warps: one per query tile, except with P_i over S_i in the two-tile (non-SPLIT)
+  // instances, where one warp issues both tiles' MMAs: a tile's PV_i(j), S_i(j+1) then run back to
+  // back instead of interleaved with the other tile's, which keeps each tile's critical loop
+  // (softmax -> PV_i -> S_i -> softmax) short (measured 12 % faster than two issuers at causal
+  // N = 8192, d = 128).
+  template <bool SPLIT>
+  static constexpr int mma_warps() { return (!SEP_P && !SPLIT) ? 1 : 2; }
+  template <bool SPLIT>
+  static constexpr int threads() { return 32 * (9 + mma_warps<SPLIT>()); }  // 8 softmax warps, producer
   static constexpr int Q_OFF = 0;
   static constexpr int RING_OFF = Q_OFF + 2 * Q_TILE;
   static constexpr int BAR_OFF = RING_OFF + SLOTS * KV_TILE;
-  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2], q_empty
-  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2 + 1;
+  // With P_i over S_i the group hands P_i over in two halves: the PV MMAs of the first half of the
+  // keys are issued while the group still computes the second half.
+  static constexpr bool HALF_P = !SEP_P;
+  // q_full, full[SLOTS], empty[SLOTS], s_full[2], p_full[2], o_done[2], drain, s_free[2], q_empty,
+  // p_half[2]
+  static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2 + 1 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
   __host__ __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * BN); }
@@ -244,7 +259,7 @@ __device__ __forceinline__ int item_of_round(int k, int total) {
 // and the hint made ptxas spill more on this kernel.  PACKED: token-major packed sequences
 // (a separate instance, so the dense layout pays nothing for them).  MODE: see Mode.
 template <int D, bool PACKED, bool SPLIT, int MODE>
-__global__ void __launch_bounds__(Cfg<D>::THREADS)
+__global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
   using C = Cfg<D>;
@@ -266,6 +281,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
   const uint32_t bar_drain = bar0 + 8u * (7 + 2 * C::SLOTS);
   auto bar_sfree = [&](int i) { return bar0 + 8u * (8 + 2 * C::SLOTS + i); };  // S_i read by its group
   const uint32_t bar_qempty = bar0 + 8u * (10 + 2 * C::SLOTS);               // Q read by the last S MMAs
+  auto bar_phalf = [&](int i) { return bar0 + 8u * (11 + 2 * C::SLOTS + i); };  // first half of P_i written
   static_assert(!SPLIT || !PACKED, "the split mode serves the dense layout");
   // SPLIT: Q tile 1's buffer (never loaded) holds group 1's (m, l) per row and two barriers:
   // xch (group 1's O_1, m, l ready; 4 warps) and xdone (group 0 has read them; 4 warps)
@@ -277,22 +293,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.num_qblocks * p.BH;
+  constexpr int kIssuers = C::template mma_warps<SPLIT>();
+  constexpr bool kOneIssuer = kIssuers == 1;
 
   // ---- set-up: barriers, TMEM (once; the CTA then works through its items) ----
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
     for (int t = 0; t < C::SLOTS; ++t) {
       mbar_init(bar_full(t), 1);
-      mbar_init(bar_empty(t), C::MMA_WARPS);  // released by every MMA warp
+      mbar_init(bar_empty(t), kIssuers);  // released by every MMA warp
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar_sfull(i), 1);
       mbar_init(bar_pfull(i), 4);  // one arrival per softmax warp
       mbar_init(bar_odone(i), 1);
       mbar_init(bar_sfree(i), 4);  // one arrival per softmax warp
+      mbar_init(bar_phalf(i), 4);  // one arrival per softmax warp
     }
-    mbar_init(bar_drain, C::MMA_WARPS);
-    mbar_init(bar_qempty, C::MMA_WARPS);
+    mbar_init(bar_drain, kIssuers);
+    mbar_init(bar_qempty, kIssuers);
     if constexpr (SPLIT) {
       mbar_init(bar_xch, 4);
       mbar_init(bar_xdone, 4);
@@ -367,182 +386,36 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         mma_ss_elect(d_tmem, a + a_off, b + b_off, C::IDESC_S, kk > 0 ? 1u : 0u);
       }
     };
-    auto issue_pv = [&](int i, int t, bool accumulate) {  // O_i += P_i V, V from ring load t
+    // O_i += P_i V over keys [16 kk0, 16 kk1) of the tile, V from ring load t
+    auto issue_pv = [&](int i, int t, bool accumulate, int kk0, int kk1) {
       const uint32_t d_tmem = tmem_base + C::o_col(i);
       const uint32_t a_tmem = tmem_base + C::p_col(i);
       const uint64_t b = v_desc0 + slot_off(t);
 #pragma unroll
       for (int kk = 0; kk < C::BN / 16; ++kk)
-        mma_ts_elect(d_tmem, a_tmem + kk * 8, b + (uint64_t)((kk * 2048) >> 4), C::IDESC_O,
-                     (accumulate || kk > 0) ? 1u : 0u);
+        if (kk >= kk0 && kk < kk1)
+          mma_ts_elect(d_tmem, a_tmem + kk * 8, b + (uint64_t)((kk * 2048) >> 4), C::IDESC_O,
+                       (accumulate || kk > 0) ? 1u : 0u);
+    };
+    // PV_i over the whole tile once P_i is written (with HALF_P: the first half of the keys as
+    // soon as the group has written their half of P_i)
+    auto wait_issue_pv = [&](int i, int t, uint32_t ph, bool accumulate) {
+      constexpr int kSteps = C::BN / 16;
+      if constexpr (C::HALF_P) {
+        if (!wait_all(bar_phalf(i), ph, W_PFULL)) return false;
+        tc_fence_after_sync();
+        issue_pv(i, t, accumulate, 0, kSteps / 2);
+      }
+      if (!wait_all(bar_pfull(i), ph, W_PFULL)) return false;
+      tc_fence_after_sync();
+      issue_pv(i, t, accumulate, C::HALF_P ? kSteps / 2 : 0, kSteps);
+      return true;
     };
     // Running counters across items: tg = first ring load of the item, nq = Q loads so far,
     // st_i = score tiles of query tile i so far (the phase of s_full / p_full / o_done / s_free).
     int tg = 0, nq = 0, st0 = 0, st1 = 0;
     bool ok = true;
-    if constexpr (C::SEP_P && SPLIT) {
-      // ---- one warp per slot, the slots on alternate key tiles: slot i's m-th key tile is key
-      // tile 2 m + i (K in load tg + 4 m + 2 i, V in the load after it).  The other slot's loads
-      // are released by a plain arrival once they have landed, in load order as this warp moves
-      // past them, so neither warp holds ring slots the other needs.
-      const int i = warp - kMmaWarp0;
-      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-        const int idx = item_of_round(k, total);
-        if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
-        if (it.n_all == 0) continue;
-        const int n = it.n_kv[i], sb = i ? st1 : st0, n_ld = 2 * n_loads_of<SPLIT>(it);
-        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
-        ++nq;
-        int rel = 0;  // loads tg + rel onwards not yet passed
-        auto release_to = [&](int t_end) {  // plain arrivals for the other slot's loads before t_end
-          for (; rel < t_end; ++rel) {
-            if (((rel >> 1) & 1) == i) continue;  // this slot's own load: released by a commit
-            if (!wait_all(bar_full(tg + rel), ring_phase(tg + rel), W_DRAIN)) return false;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty(tg + rel));
-          }
-          return true;
-        };
-        auto k_ld = [&](int m) { return 4 * m + 2 * i; };  // load of slot i's m-th K (V follows)
-        if (n > 0) {
-          if (!(ok = release_to(k_ld(0)))) break;
-          if (!(ok = wait_all(bar_full(tg + k_ld(0)), ring_phase(tg + k_ld(0)), W_KFULL))) break;
-          tc_fence_after_sync();
-          issue_s(i, tg + k_ld(0));
-          mma_commit_elect(bar_sfull(i));
-          mma_commit_elect(bar_empty(tg + k_ld(0)));
-          if (n == 1) mma_commit_elect(bar_qempty);
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_qempty);  // Q(this item) has landed: the arrival is in phase
-        }
-        for (int m = 0; ok && m < n; ++m) {
-          const int tv = tg + k_ld(m) + 1, tk = tg + k_ld(m + 1);
-          const uint32_t ph = (uint32_t)(sb + m) & 1u;
-          if (m + 1 < n) {  // S_i of the next tile as soon as the softmax group has read S_i
-            if (!(ok = release_to(k_ld(m + 1)))) break;
-            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-            if (!(ok = wait_all(bar_sfree(i), ph, W_SFREE))) break;
-            tc_fence_after_sync();
-            issue_s(i, tk);
-            mma_commit_elect(bar_sfull(i));
-            mma_commit_elect(bar_empty(tk));
-            if (m + 2 == n) mma_commit_elect(bar_qempty);
-          }
-          if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-          if (!(ok = wait_all(bar_pfull(i), ph, W_PFULL))) break;
-          tc_fence_after_sync();
-          issue_pv(i, tv, m > 0);
-          mma_commit_elect(bar_odone(i));
-          mma_commit_elect(bar_empty(tv));
-        }
-        if (ok) ok = release_to(n_ld);
-        tg += n_ld;
-        if (i) st1 += n; else st0 += n;
-      }
-    } else if constexpr (C::SEP_P) {
-      // ---- one warp per query tile: warp 9 for tile 0, warp 10 for tile 1 ----
-      const int i = warp - kMmaWarp0;
-      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-        const int idx = item_of_round(k, total);
-        if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
-        if (it.n_all == 0) continue;
-        const int n = it.n_kv[i], sb = i ? st1 : st0;
-        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
-        ++nq;
-        // Loads tg + 2j (K_j) and tg + 2j + 1 (V_j) for j < n are this tile's; it releases
-        // each with a commit after the MMAs that read it.
-        if (n > 0) {
-          if (!(ok = wait_all(bar_full(tg), ring_phase(tg), W_KFULL))) break;
-          tc_fence_after_sync();
-          issue_s(i, tg);
-          mma_commit_elect(bar_sfull(i));
-          mma_commit_elect(bar_empty(tg));
-          if (n == 1) mma_commit_elect(bar_qempty);
-        } else {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_qempty);  // Q(this item) has landed: the arrival is in phase
-        }
-        for (int j = 0; ok && j < n; ++j) {
-          const int tv = tg + 2 * j + 1, tk = tg + 2 * j + 2;  // loads holding V_j and K_{j+1}
-          const uint32_t ph = (uint32_t)(sb + j) & 1u;
-          if (j + 1 < n) {  // S_i(j+1) as soon as the softmax group has read S_i(j)
-            if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-            if (!(ok = wait_all(bar_sfree(i), ph, W_SFREE))) break;
-            tc_fence_after_sync();
-            issue_s(i, tk);
-            mma_commit_elect(bar_sfull(i));
-            mma_commit_elect(bar_empty(tk));
-            if (j + 2 == n) mma_commit_elect(bar_qempty);
-          }
-          if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-          if (!(ok = wait_all(bar_pfull(i), ph, W_PFULL))) break;
-          tc_fence_after_sync();
-          issue_pv(i, tv, j > 0);
-          mma_commit_elect(bar_odone(i));
-          mma_commit_elect(bar_empty(tv));
-        }
-        // Loads this tile does not use (the other tile's last key tile, or every load for an
-        // empty tile) are released by a plain arrival once they have landed, which keeps each
-        // arrival in its slot's current phase.
-        for (int t = tg + 2 * n; ok && t < tg + 2 * it.n_all; ++t) {
-          if (!(ok = wait_all(bar_full(t), ring_phase(t), W_DRAIN))) break;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_empty(t));
-        }
-        tg += 2 * it.n_all;
-        if (i) st1 += n; else st0 += n;
-      }
-    } else if constexpr (SPLIT) {
-      // ---- one warp, the two slots on alternate key tiles: slot i's m-th key tile is key tile
-      // 2 m + i (K in load tg + 4 m + 2 i, V in the load after it); per m: PV_0, S_0 of its next
-      // tile, PV_1, S_1 of its next tile.  Every load is read by exactly one MMA, released by a
-      // commit after it.
-      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-        const int idx = item_of_round(k, total);
-        if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
-        if (it.n_all == 0) continue;
-        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
-        ++nq;
-        int s_left = it.n_kv[0] + it.n_kv[1];  // S MMAs of the item still to issue
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (it.n_kv[i] == 0) continue;
-          const int tk = tg + 2 * i;
-          if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-          tc_fence_after_sync();
-          issue_s(i, tk);
-          mma_commit_elect(bar_sfull(i));
-          mma_commit_elect(bar_empty(tk));
-          if (--s_left == 0) mma_commit_elect(bar_qempty);
-        }
-        for (int m = 0; ok && m < it.n_all; ++m) {
-          for (int i = 0; i < 2 && ok; ++i) {
-            if (m >= it.n_kv[i]) continue;
-            const int tv = tg + 4 * m + 2 * i + 1, tk = tg + 4 * (m + 1) + 2 * i;
-            if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
-            if (!(ok = wait_all(bar_pfull(i), (uint32_t)((i ? st1 : st0) + m) & 1u, W_PFULL))) break;
-            tc_fence_after_sync();
-            issue_pv(i, tv, m > 0);
-            mma_commit_elect(bar_odone(i));
-            mma_commit_elect(bar_empty(tv));
-            if (m + 1 < it.n_kv[i]) {  // P_i lives in S_i's columns: S_i of the next tile after PV_i
-              if (!(ok = wait_all(bar_full(tk), ring_phase(tk), W_KFULL))) break;
-              tc_fence_after_sync();
-              issue_s(i, tk);
-              mma_commit_elect(bar_sfull(i));
-              mma_commit_elect(bar_empty(tk));
-              if (--s_left == 0) mma_commit_elect(bar_qempty);
-            }
-          }
-        }
-        tg += 2 * n_loads_of<SPLIT>(it);
-        st0 += it.n_kv[0];
-        st1 += it.n_kv[1];
-      }
-    } else {
+    if constexpr (kOneIssuer) {
       // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
       for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
         const int idx = item_of_round(k, total);
@@ -566,9 +439,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
           if (!(ok = wait_all(bar_full(tv), ring_phase(tv), W_VFULL))) break;
           for (int i = 0; i < 2 && ok; ++i) {
             if (j >= it.n_kv[i]) continue;
-            if (!(ok = wait_all(bar_pfull(i), (uint32_t)((i ? st1 : st0) + j) & 1u, W_PFULL))) break;
-            tc_fence_after_sync();
-            issue_pv(i, tv, j > 0);
+            if (!(ok = wait_issue_pv(i, tv, (uint32_t)((i ? st1 : st0) + j) & 1u, j > 0))) break;
             mma_commit_elect(bar_odone(i));
             if (j + 1 < it.n_kv[i]) {  // P_i lives in S_i's columns: S_i(j+1) after PV_i(j)
               if (!k_next_ready) {
@@ -588,6 +459,78 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         tg += 2 * n_loads_of<SPLIT>(it);
         st0 += it.n_kv[0];
         st1 += it.n_kv[1];
+      }
+    } else {
+      // Each query tile's MMAs come from a warp of its own (warp 9: tile 0, warp 10: tile 1).  Per
+      // tile the order follows where P_i lives: with P_i separate, S_i(j+1) as soon as the group
+      // has read S_i(j), then PV_i(j); with P_i over S_i, PV_i(j) then S_i(j+1) (MMAs of one
+      // thread run in issue order).
+      const int i = warp - kMmaWarp0;
+      auto s_next = [&](int tk, uint32_t ph, bool last_s) {  // S_i of the tile after the current one
+        if (!wait_all(bar_full(tk), ring_phase(tk), W_KFULL)) return false;
+        if (C::SEP_P && !wait_all(bar_sfree(i), ph, W_SFREE)) return false;
+        tc_fence_after_sync();
+        issue_s(i, tk);
+        mma_commit_elect(bar_sfull(i));
+        mma_commit_elect(bar_empty(tk));
+        if (last_s) mma_commit_elect(bar_qempty);
+        return true;
+      };
+      auto pv = [&](int tv, uint32_t ph, bool accumulate) {
+        if (!wait_all(bar_full(tv), ring_phase(tv), W_VFULL)) return false;
+        if (!wait_issue_pv(i, tv, ph, accumulate)) return false;
+        mma_commit_elect(bar_odone(i));
+        mma_commit_elect(bar_empty(tv));
+        return true;
+      };
+      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
+        const int idx = item_of_round(k, total);
+        if (idx < 0) continue;
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+        if (it.n_all == 0) continue;
+        const int n = it.n_kv[i], sb = i ? st1 : st0, n_ld = 2 * n_loads_of<SPLIT>(it);
+        if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
+        ++nq;
+        // Ring loads of the item: K_j in load 2j, V_j in 2j + 1.  SPLIT: slot i's m-th key tile is
+        // key tile 2m + i.  The loads a tile does not read (SPLIT: the other slot's; else the other
+        // tile's last key tiles) are released by a plain arrival once they have landed, in load
+        // order as this warp moves past them: neither warp holds ring slots the other needs, and
+        // every arrival falls in its slot's current phase.
+        int rel = 0;  // loads tg + rel onwards not yet passed
+        auto release_to = [&](int t_end) {
+          for (; rel < t_end; ++rel) {
+            const bool mine = SPLIT ? (((rel >> 1) & 1) == i) : (rel < 2 * n);
+            if (mine) continue;  // read by this tile's MMAs: released by a commit
+            if (!wait_all(bar_full(tg + rel), ring_phase(tg + rel), W_DRAIN)) return false;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty(tg + rel));
+          }
+          return true;
+        };
+        auto k_ld = [&](int m) { return SPLIT ? 4 * m + 2 * i : 2 * m; };  // load of the tile's m-th K
+        if (n > 0) {
+          if (!(ok = release_to(k_ld(0)))) break;
+          if (!(ok = wait_all(bar_full(tg + k_ld(0)), ring_phase(tg + k_ld(0)), W_KFULL))) break;
+          tc_fence_after_sync();
+          issue_s(i, tg + k_ld(0));
+          mma_commit_elect(bar_sfull(i));
+          mma_commit_elect(bar_empty(tg + k_ld(0)));
+          if (n == 1) mma_commit_elect(bar_qempty);
+        } else {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_qempty);  // Q(this item) has landed: the arrival is in phase
+        }
+        for (int m = 0; ok && m < n; ++m) {
+          const int tv = tg + k_ld(m) + 1, tk = tg + k_ld(m + 1);
+          const uint32_t ph = (uint32_t)(sb + m) & 1u;
+          const bool more = m + 1 < n;
+          if (C::SEP_P && more && !(ok = release_to(k_ld(m + 1)) && s_next(tk, ph, m + 2 == n))) break;
+          if (!(ok = pv(tv, ph, m > 0))) break;
+          if (!C::SEP_P && more && !(ok = release_to(k_ld(m + 1)) && s_next(tk, ph, m + 2 == n))) break;
+        }
+        if (ok) ok = release_to(n_ld);
+        tg += n_ld;
+        if (i) st1 += n; else st0 += n;
       }
     }
     {
@@ -673,9 +616,32 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         const float ref = (m == -INFINITY) ? 0.f : m;
         const uint64_t sl2x2 = f2_pack(sl2, sl2), nref2 = f2_pack(-ref, -ref);
         uint64_t acc0 = 0, acc1 = 0;  // packed partial row sums (bit pattern 0 == {+0.f, +0.f})
+        // O_i *= alpha where the reference moved.  O_i holds PV_i(j-1) by then: with P_i separate
+        // the group has waited for it before writing P_i; with P_i over S_i, S_i(j) was issued after
+        // PV_i(j-1) by the same thread, so that MMA finished before S_i(j) did.
+        // (HALF_P: decided before the exponentials, as O_i is rescaled before the first half of P_i
+        // is handed over; else at the end)
+        const bool rescale = C::HALF_P && j > 0 && __any_sync(0xffffffffu, grow);
+        auto rescale_o = [&]() {
+          const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+          for (int c = 0; c < D; c += 32) {
+            uint32_t orr[32];
+            tmem_ld32(o_addr + c, orr);
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float o0, o1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al2), o0, o1);
+              orr[e] = __float_as_uint(o0);
+              orr[e + 1] = __float_as_uint(o1);
+            }
+            tmem_st32(o_addr + c, orr);
+          }
+        };
         // P = exp2(S * scale * log2 e - ref): pair c (columns 2c, 2c+1) is written as
         // one bf16x2 word into sr[c], whose scores have already been consumed.  The first half of
-        // P goes to TMEM as soon as it is complete.
+        // P goes to TMEM as soon as it is complete (HALF_P: O_i rescaled first, and the half handed
+        // to the MMA warp at once).
         constexpr int kHalfP = BN / 4;  // words in half of P
 #pragma unroll
         for (int c = 0; c < BN / 2; ++c) {
@@ -694,12 +660,25 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
               ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE);
               tc_fence_after_sync();
             }
+            if (C::HALF_P && rescale) {
+              ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE);  // complete already (see rescale_o)
+              tc_fence_after_sync();
+              if (ok) rescale_o();
+            }
             if (ok) {
               if constexpr (kHalfP == 32)
                 tmem_st32(p_addr, *reinterpret_cast<const uint32_t(*)[32]>(&sr[0]));
               else
                 tmem_st16(p_addr, &sr[0]);
             }
+          }
+          // the half is handed over a few pairs later, when its stores have (nearly) landed:
+          // waiting for them at once would stall the exponentials behind the store latency
+          if (C::HALF_P && c == kHalfP - 1 + kPHandoffLag && ok) {
+            tmem_st_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_phalf(i));
           }
         }
         if (!ok) break;
@@ -711,27 +690,7 @@ __global__ void __launch_bounds__(Cfg<D>::THREADS)
         f2_unpack(acc0, a0, a1);
         f2_unpack(acc1, a2, a3);
         l = alpha * l + ((a0 + a1) + (a2 + a3));
-        if (j > 0 && __any_sync(0xffffffffu, grow)) {
-          // O_i must hold PV_i(j-1) before it is rescaled (already waited for when P_i is separate)
-          if (!C::SEP_P) {
-            if (!(ok = wait_all(bar_odone(i), ph ^ 1u, W_ODONE))) break;
-            tc_fence_after_sync();
-          }
-          const uint64_t al2 = f2_pack(alpha, alpha);
-#pragma unroll 1
-          for (int c = 0; c < D; c += 32) {
-            uint32_t orr[32];
-            tmem_ld32(o_addr + c, orr);
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float o0, o1;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(orr[e]), __uint_as_float(orr[e + 1])), al2), o0, o1);
-              orr[e] = __float_as_uint(o0);
-              orr[e + 1] = __float_as_uint(o1);
-            }
-            tmem_st32(o_addr + c, orr);
-          }
-        }
+        if (!C::HALF_P && j > 0 && __any_sync(0xffffffffu, grow)) rescale_o();
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
@@ -867,7 +826,7 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     g = (total + rounds - 1) / rounds;
   }
   const unsigned grid = (unsigned)g;
-  attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::THREADS, Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::template threads<SPLIT>(), Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
