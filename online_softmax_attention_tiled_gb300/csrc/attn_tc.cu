@@ -40,9 +40,12 @@
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d).
 //   d = 128: P_i (bf16, two per column) is written over the first 64 columns
-//   of S_i, so S_i(j+1) can only follow the PV MMA that reads P_i(j): tile
-//   i's warp issues PV_i(j), S_i(j+1), and each softmax group works while the
-//   tensor core runs the other group's MMAs.
+//   of S_i, so S_i(j+1) can only follow the PV MMA that reads P_i(j).  Warp 9
+//   issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) (the split-slot instances: each
+//   slot's warp its own), and each softmax group works while the tensor core
+//   runs the other group's MMAs.  PV_i(j) goes in two halves: keys 0-63 once
+//   the group has handed over the first half of P_i (p_half), keys 64-127 once
+//   all of P_i is written (p_full).
 //   d = 64: P_i gets its own columns [384 + 64 i, +64), so the group frees
 //   S_i as soon as it has read it and S_i(j+1) is computed during the
 //   softmax of S_i(j): the order is S_i(j+1), PV_i(j); before writing P_i(j)
