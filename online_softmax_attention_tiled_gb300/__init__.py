@@ -21,7 +21,10 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "liboa.so")
+# OA_DEBUG=1 in the environment loads the debug build (bounds and alignment checks in the kernels,
+# recorded in the status word that sync_status reads) instead of the release library.
+DEBUG = os.environ.get("OA_DEBUG", "") == "1"
+LIB_PATH = os.path.join(_PKG, "liboa_debug.so" if DEBUG else "liboa.so")
 
 OA_OK, OA_ERR_INVALID, OA_ERR_UNSUPPORTED, OA_ERR_CUDA, OA_ERR_TIMEOUT = 0, 1, 2, 3, 4
 OA_F32, OA_BF16 = 0, 1
@@ -61,7 +64,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                 raise RuntimeError(f"CUDA library not built: {LIB_PATH}")
             from ._build import build
 
-            build()
+            build(debug=DEBUG)
         lib = ctypes.CDLL(LIB_PATH)
         vp, i64, i32, f32, u64, sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                                       ctypes.c_uint64, ctypes.c_size_t)

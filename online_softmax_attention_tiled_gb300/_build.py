@@ -1,7 +1,10 @@
 """Builds liboa.so (the CUDA library behind include/oa.h) in-tree for sm_103a.
 
 Each .cu file is compiled to an object in parallel, then linked into one
-shared object next to this file.  No cmake; nvcc only.
+shared object next to this file.  No cmake; nvcc only.  ``build(debug=True)``
+builds liboa_debug.so instead: the same sources with -DOA_DEBUG, whose kernels
+check the bounds and alignment of their computed global accesses and record a
+failed check in the status word (see oa_common.cuh).
 """
 from __future__ import annotations
 
@@ -17,6 +20,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_PATH = os.path.join(PKG, "liboa.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "liboa_debug.so")
 
 SOURCES = ["oa_api.cu", "tma_map.cu", "softmax_rows.cu", "lse_merge.cu", "attn_f32.cu", "attn_splitkv.cu", "attn_tc.cu",
            "attn_bwd.cu", "attn_splitkv_static.cu"]
@@ -39,10 +43,10 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-    cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose_ptxas else []) + \
-        ["-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, debug: bool = False) -> str:
+    obj = os.path.join(BUILD_DIR, ("debug_" if debug else "") + os.path.splitext(src)[0] + ".o")
+    cmd = [nvcc()] + ARCH + NVCC_FLAGS + (["-DOA_DEBUG"] if debug else []) + \
+        (["-Xptxas", "-v"] if verbose_ptxas else []) + ["-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc failed for {src}:\n{r.stdout}\n{r.stderr}")
@@ -51,21 +55,23 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link liboa.so if any input is newer than it.  Returns its path."""
-    if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _inputs_mtime():
-        return LIB_PATH
+def build(force: bool = False, verbose_ptxas: bool = False, debug: bool = False) -> str:
+    """Compile and link liboa.so (debug: liboa_debug.so) if any input is newer than it.  Returns its
+    path."""
+    path = DEBUG_LIB_PATH if debug else LIB_PATH
+    if not force and os.path.exists(path) and os.path.getmtime(path) >= _inputs_mtime():
+        return path
     os.makedirs(BUILD_DIR, exist_ok=True)
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, debug), SOURCES))
+    tmp = path + f".tmp{os.getpid()}"
     cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, debug="--debug" in sys.argv))

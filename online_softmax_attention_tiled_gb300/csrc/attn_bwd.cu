@@ -108,6 +108,7 @@ struct BwdParams {
   const int32_t *cu_q, *cu_k;       // packed: sequence offsets [num_seqs + 1] (NULL: dense)
   int total_q, total_k;             // packed: tokens in the Q / K tensors
   float scale, scale_log2;
+  int64_t lse_elems, dk_elems;  // extents of lse / dsum and of dk / dv (the debug build's checks)
   DevStatus st;
 };
 
@@ -303,7 +304,8 @@ __device__ __forceinline__ void bwd_store_dkdv(const BwdParams& p, const BwdGeom
       k32[e] = pack_bf16x2(__uint_as_float(rk[2 * e]), __uint_as_float(rk[2 * e + 1]));
       v32[e] = pack_bf16x2(__uint_as_float(rv[2 * e]), __uint_as_float(rv[2 * e + 1]));
     }
-    if (key_ok) {
+    if (key_ok && OA_DCHECK(p.st, (g.dkbase + (int64_t)key * g.dks) * D + c + 32 <= p.dk_elems,
+                            (K_ATTN_BWD << 8) | kSiteDebugBase)) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         reinterpret_cast<uint4*>(dkrow + c)[e] = wk[e];
@@ -563,8 +565,10 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int q = sp.i * BT + ld_q;
       if (tt < 64 && step < n_it && q < Nq) {
         const int64_t row = lbase + (int64_t)q * lq + (int64_t)sp.t * lt;
-        l = p.lse[row];
-        dd = p.dsum[row];
+        if (OA_DCHECK(p.st, row < p.lse_elems, (K_ATTN_BWD << 8) | (kSiteDebugBase + 1))) {
+          l = p.lse[row];
+          dd = p.dsum[row];
+        }
       }
     };
     // issued one step ahead: the loads' latency hides behind the step's dV / dK / dQ MMAs
@@ -969,8 +973,10 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int q = sp.i * BT + ld_q;
       if (tt < 64 && step < n_it && q < Nq) {
         const int64_t row = g.lbase + (int64_t)q * g.lq + (int64_t)sp.t * g.lt;
-        l = p.lse[row];
-        dd = p.dsum[row];
+        if (OA_DCHECK(p.st, row < p.lse_elems, (K_ATTN_BWD << 8) | (kSiteDebugBase + 1))) {
+          l = p.lse[row];
+          dd = p.dsum[row];
+        }
       }
     };
     // -LSE log2 e and -D scale of a step's queries; a row past the end or with no visible key gets -inf,
@@ -1166,6 +1172,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus&
   p.total_k = a.Nk;
   p.scale = a.scale;
   p.scale_log2 = a.scale * kLog2e;
+  p.lse_elems = rows;
+  p.dk_elems = (int64_t)(packed ? 1 : a.B) * a.Hkv * a.Nk * d;
   p.st = st;
   if (p.nkt < 1) p.nkt = 1;
   if (packed)

@@ -146,6 +146,7 @@ struct TcParams {
   int qmod;              // > 0: a row's causal position is its index modulo qmod (grouped decode rows)
   int group;             // query heads per key/value head (H / H_kv)
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
+  int64_t o_elems, lse_elems;  // extents of o and lse (the debug build's store checks)
   int l_rs;              // LSE row stride: 1 dense, H packed
   int o_v8;  // o is 32-byte aligned: rows are written with 32-byte stores
   float scale_log2;
@@ -738,6 +739,8 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
       const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
       const int64_t o_rs = PACKED ? p.o_rs : D;  // O row stride
       __nv_bfloat16* orow = p.o + it.ob + (int64_t)row * o_rs;
+      const bool row_in = row < it.nq && OA_DCHECK(p.st, it.ob + (int64_t)row * o_rs + D <= p.o_elems,
+                                                   (K_ATTN_TC << 8) | kSiteDebugBase);
 #pragma unroll 1
       for (int c = 0; c < D; c += 32) {
         uint32_t orr[32];
@@ -763,7 +766,7 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
           w[e] = pack_bf16x2(__uint_as_float(orr[2 * e]) * inv_l, __uint_as_float(orr[2 * e + 1]) * inv_l);
         // Each thread writes its own row: a warp's store touches 32 rows, so whole 32-byte
         // sectors per thread (half as many requests as 16-byte stores) matter here.
-        if (row < it.nq) {
+        if (row_in) {
           if (p.o_v8) {
             st_global_v8(orow + c, w);
             st_global_v8(orow + c + 16, w + 8);
@@ -776,7 +779,8 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
           }
         }
       }
-      if (p.lse != nullptr && row < it.nq)
+      if (p.lse != nullptr && row < it.nq &&
+          OA_DCHECK(p.st, it.lb + (int64_t)row * (PACKED ? p.l_rs : 1) < p.lse_elems, (K_ATTN_TC << 8) | (kSiteDebugBase + 1)))
         p.lse[it.lb + (int64_t)row * (PACKED ? p.l_rs : 1)] = (l > 0.f) ? (m + log2f(l)) * kLn2 : -INFINITY;
       // O_i has been read out: the next item's PV_i(0) (issued after this group's next P)
       // may overwrite it
@@ -872,6 +876,8 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.BH = a.B * a.H;
   p.group = a.H / Hkv;
   p.o_rs = packed ? (int64_t)a.H * d : d;
+  p.o_elems = packed ? (int64_t)a.Tq * a.H * d : (int64_t)a.B * a.H * a.Nq * d;
+  p.lse_elems = packed ? (int64_t)a.Tq * a.H : (int64_t)a.B * a.H * a.Nq;
   p.l_rs = packed ? a.H : 1;
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;

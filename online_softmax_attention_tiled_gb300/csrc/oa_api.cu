@@ -654,6 +654,9 @@ oa_status oa_sync_status(oa_stream_t stream) {
   if (word == oa::kSiteBwdBadSeqlen)
     return fail(OA_ERR_INVALID, "a packed key sequence is longer than the declared max_seqlen_k; "
                                 "its keys past that length got no dK, dV");
+  if ((word & 0xF0u) == oa::kSiteDebugBase)
+    return fail(OA_ERR_INVALID, "debug build: bounds or alignment check %u of kernel %u failed (the access was skipped)",
+                word & 0x0Fu, word >> 8);
   return fail(OA_ERR_TIMEOUT, "device wait expired: kernel %u, wait site %u", word >> 8, word & 0xFFu);
 }
 

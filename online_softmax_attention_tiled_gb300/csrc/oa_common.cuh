@@ -48,6 +48,22 @@ __device__ __forceinline__ void record_failure(const DevStatus& st, unsigned sit
   atomicCAS(st.word, 0u, site);
 }
 
+// Debug builds (-DOA_DEBUG: liboa_debug.so, loaded instead of liboa.so when the environment
+// variable OA_DEBUG is 1): bounds and alignment checks at the kernels' computed global accesses.
+// A failed check records its site -- (kernel id << 8) | 0xD0 + n -- in the status word like an
+// expired wait, and the access is skipped; kernels never trap.  In release builds a check is the
+// constant true and its condition is not evaluated.
+constexpr unsigned kSiteDebugBase = 0xD0u;
+#ifdef OA_DEBUG
+__device__ __forceinline__ bool oa_dcheck(const DevStatus& st, bool ok, unsigned site) {
+  if (!ok) record_failure(st, site);
+  return ok;
+}
+#define OA_DCHECK(st, cond, site) ::oa::oa_dcheck((st), (cond), (site))
+#else
+#define OA_DCHECK(st, cond, site) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

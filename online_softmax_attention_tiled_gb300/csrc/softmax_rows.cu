@@ -169,8 +169,8 @@ constexpr int kSoftmaxMinBlocks = (E == 32 && !VEC) ? 3 : 5;
 // statistics in parallel (the instance for clusters of more than 4 CTAs).
 template <int E, bool VEC, bool PAR = false>
 __global__ void __launch_bounds__(kMaxThreads, kSoftmaxMinBlocks<E, VEC>)
-    softmax_rows_kernel(const float* __restrict__ x, int64_t cols, int64_t ld_x, float* __restrict__ y, int64_t ld_y,
-                        float* __restrict__ lse, int cluster, int64_t slice) {
+    softmax_rows_kernel(const float* __restrict__ x, int64_t rows, int64_t cols, int64_t ld_x, float* __restrict__ y,
+                        int64_t ld_y, float* __restrict__ lse, int cluster, int64_t slice, DevStatus status) {
   __shared__ ML warp_ml[kMaxThreads / 32];
   __shared__ ML cta_ml;  // this CTA's merged statistics (read by peers)
   __shared__ ML row_ml;  // statistics of the whole row
@@ -180,7 +180,14 @@ __global__ void __launch_bounds__(kMaxThreads, kSoftmaxMinBlocks<E, VEC>)
   const int64_t row = blockIdx.x / cluster;
   const float* xr = x + row * ld_x;
   const int64_t c0 = (int64_t)rank * slice;
-  const int64_t c1 = (c0 + slice < cols) ? c0 + slice : cols;
+  // (debug build) a row past the tensor or a vector path on unaligned memory leaves the slice
+  // empty -- no loads or stores -- while the CTA still takes part in the cluster's barriers
+  const bool in_ok =
+      OA_DCHECK(status, row < rows, (K_SOFTMAX << 8) | kSiteDebugBase) &&
+      (!VEC || OA_DCHECK(status, (reinterpret_cast<uintptr_t>(xr + c0) & 15) == 0 &&
+                                 (y == nullptr || (reinterpret_cast<uintptr_t>(y + row * ld_y + c0) & 15) == 0),
+                         (K_SOFTMAX << 8) | (kSiteDebugBase + 1)));
+  const int64_t c1 = !in_ok ? c0 : (c0 + slice < cols) ? c0 + slice : cols;
   const int64_t piece = (int64_t)T * E;
   const bool resident = (c1 - c0) <= piece;
 
@@ -259,7 +266,7 @@ __global__ void __launch_bounds__(kMaxThreads, kSoftmaxMinBlocks<E, VEC>)
 
 template <int E, bool VEC, bool PAR = false>
 cudaError_t launch_cfg(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
-                       float* lse, int threads, int cluster, int64_t slice, cudaStream_t s) {
+                       float* lse, int threads, int cluster, int64_t slice, const DevStatus& st, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(rows * cluster), 1, 1);
   cfg.blockDim = dim3(threads, 1, 1);
@@ -274,7 +281,8 @@ cudaError_t launch_cfg(const float* x, int64_t rows, int64_t cols, int64_t ld_x,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, softmax_rows_kernel<E, VEC, PAR>, x, cols, ld_x, y, ld_y, lse, cluster, slice);
+  return cudaLaunchKernelEx(&cfg, softmax_rows_kernel<E, VEC, PAR>, x, rows, cols, ld_x, y, ld_y, lse, cluster, slice,
+                            st);
 }
 
 constexpr int kMaxDevices = 64;
@@ -312,16 +320,16 @@ int wide_cluster_limit(cudaStream_t s) {
 
 template <bool VEC>
 cudaError_t launch_vec(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y, int64_t ld_y,
-                       float* lse, cudaStream_t s) {
+                       float* lse, const DevStatus& st, cudaStream_t s) {
   // Register capacity of one CTA: 256 threads x 32 fp32.  Up to 8 CTAs (a portable cluster) hold a
   // row on chip; wider rows take slices of two pieces, up to 16 CTAs a row (see the file comment).
   constexpr int64_t kCtaCap = (int64_t)kMaxThreads * 32;
   if (cols <= 1024) {
     const int threads = (int)(((cols + 3) / 4 + 31) / 32 * 32);
-    return launch_cfg<4, VEC>(x, rows, cols, ld_x, y, ld_y, lse, threads, 1, (cols + 3) / 4 * 4, s);
+    return launch_cfg<4, VEC>(x, rows, cols, ld_x, y, ld_y, lse, threads, 1, (cols + 3) / 4 * 4, st, s);
   }
-  if (cols <= 2048) return launch_cfg<8, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
-  if (cols <= 4096) return launch_cfg<16, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, s);
+  if (cols <= 2048) return launch_cfg<8, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, st, s);
+  if (cols <= 4096) return launch_cfg<16, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, 1, cols, st, s);
   int cluster = (int)((cols + kCtaCap - 1) / kCtaCap);
   if (cluster > 8) {
     cluster = (int)((cols + 2 * kCtaCap - 1) / (2 * kCtaCap));
@@ -331,18 +339,18 @@ cudaError_t launch_vec(const float* x, int64_t rows, int64_t cols, int64_t ld_x,
     }
   }
   const int64_t slice = ((cols + cluster - 1) / cluster + 3) / 4 * 4;
-  if (cluster > 4) return launch_cfg<32, VEC, true>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, s);
-  return launch_cfg<32, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, s);
+  if (cluster > 4) return launch_cfg<32, VEC, true>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, st, s);
+  return launch_cfg<32, VEC>(x, rows, cols, ld_x, y, ld_y, lse, kMaxThreads, cluster, slice, st, s);
 }
 
 }  // namespace
 
 cudaError_t launch_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld_x, float* y,
-                                int64_t ld_y, float* lse, const DevStatus& /*st*/, cudaStream_t s) {
+                                int64_t ld_y, float* lse, const DevStatus& st, cudaStream_t s) {
   const bool vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (ld_x % 4 == 0) &&
                    (y == nullptr || ((reinterpret_cast<uintptr_t>(y) % 16 == 0) && (ld_y % 4 == 0)));
-  return vec ? launch_vec<true>(x, rows, cols, ld_x, y, ld_y, lse, s)
-             : launch_vec<false>(x, rows, cols, ld_x, y, ld_y, lse, s);
+  return vec ? launch_vec<true>(x, rows, cols, ld_x, y, ld_y, lse, st, s)
+             : launch_vec<false>(x, rows, cols, ld_x, y, ld_y, lse, st, s);
 }
 
 }  // namespace oa
