@@ -826,12 +826,19 @@ __global__ void __launch_bounds__(kBwdThreads)
     mbar_wait(bar_kv, 0, p.st, nullptr, (K_ATTN_BWD << 8) | B_DONE);
   } else if (warp == kBwdMma) {
     // =================== MMA issue (whole warp, one elected lane) ===================
+    // Descriptors are built once; a stage or K step only adds to the start-address field (shared
+    // memory addresses >> 4 stay below 2^14, so the field never carries into the next one).
     const uint64_t k_nmaj = smem_desc_sw128(sbase + C::K_OFF, C::TILE_BYTES, 1024);      // B of dQ
     const uint64_t st_mmaj = smem_desc_sw128(sbase + C::ST_OFF, C::TILE_BYTES, 1024);    // A of dQ
+    const uint64_t q_kmaj0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
+    const uint64_t do_kmaj0 = smem_desc_sw128(sbase + C::DO_OFF, 16, 1024);
+    const uint64_t q_nmaj0 = smem_desc_sw128(sbase + C::Q_OFF, C::TILE_BYTES, 1024);
+    const uint64_t do_nmaj0 = smem_desc_sw128(sbase + C::DO_OFF, C::TILE_BYTES, 1024);
+    auto stage_off = [](int st) { return (uint64_t)((st * C::TILE_BYTES) >> 4); };
     auto kmaj = [&](int s0, int st, int kk) {  // K-major tile of stage st, K step kk (16 of the 64 dims)
-      return smem_desc_sw128(sbase + s0 + st * C::TILE_BYTES, 16, 1024) + (uint64_t)((kk * 32) >> 4);
+      return (s0 == C::Q_OFF ? q_kmaj0 : do_kmaj0) + stage_off(st) + (uint64_t)((kk * 32) >> 4);
     };
-    auto nmaj = [&](int s0, int st) { return smem_desc_sw128(sbase + s0 + st * C::TILE_BYTES, C::TILE_BYTES, 1024); };
+    auto nmaj = [&](int s0, int st) { return (s0 == C::Q_OFF ? q_nmaj0 : do_nmaj0) + stage_off(st); };
     auto rows16_off = [](int kk) { return (uint64_t)((kk * 16 * 128) >> 4); };  // 16 rows of 128 bytes
     auto pcol = [](int kk) { return (uint32_t)(kk * 8 + (kk >= 4 ? 32 : 0)); };  // P^T / dS^T column
     // S^T (into S_COL, whose P^T the dV MMAs issued before have read) and dP^T (into DP_COL, whose
