@@ -112,15 +112,23 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_digest():
-    """Digest of the attention kernel's code (its // comments and blank lines left out, so that an
-    edit of the comments alone keeps a profile taken on the same code current)."""
+def code_digest(texts):
+    """Digest of source texts with their // comments, trailing blanks and blank lines left out, so that
+    an edit of the comments alone keeps a profile taken on the same code current."""
     h = hashlib.sha256()
-    for f in ("attn_tc.cu", "oa_common.cuh"):
-        with open(os.path.join(ROOT, "online_softmax_attention_tiled_gb300", "csrc", f), encoding="utf-8") as fh:
-            code = re.sub(r"//[^\n]*", "", fh.read())
+    for text in texts:
+        code = re.sub(r"//[^\n]*", "", text)
         h.update("\n".join(ln.rstrip() for ln in code.splitlines() if ln.strip()).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_digest():
+    """code_digest of the attention kernel's sources."""
+    texts = []
+    for f in ("attn_tc.cu", "oa_common.cuh"):
+        with open(os.path.join(ROOT, "online_softmax_attention_tiled_gb300", "csrc", f), encoding="utf-8") as fh:
+            texts.append(fh.read())
+    return code_digest(texts)
 
 
 def profiled_traffic():

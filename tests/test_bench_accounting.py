@@ -106,3 +106,31 @@ def test_multi_token_decode_bytes():
     want = 2 * (b * h * nq * d) * 2 + 2 * (2 * 1 * d * sum(kv)) + 4 * b * h * nq
     assert bench.decode_bytes(b, h, d, sum(kv), h_kv=1, nq=nq) == want
     assert bench.decode_bytes(b, h, d, sum(kv), h_kv=1) == bench.decode_bytes(b, h, d, sum(kv), h_kv=1, nq=1)
+
+
+def test_code_digest_ignores_comments_but_not_code():
+    src = "int a = 1;  // the first\n\n// a note\nint b = a + 2;\n"
+    same = "int a = 1;   // reworded\n// another note\n\n\nint b = a + 2;\n"
+    changed = "int a = 1;\nint b = a + 3;\n"
+    assert bench.code_digest([src]) == bench.code_digest([same])
+    assert bench.code_digest([src]) != bench.code_digest([changed])
+    # the files' order and boundaries count
+    assert bench.code_digest(["int a = 1;", "int b;"]) != bench.code_digest(["int b;", "int a = 1;"])
+
+
+def test_profiled_traffic_needs_the_current_digest(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    csrc = tmp_path / "online_softmax_attention_tiled_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "attn_tc.cu").write_text("int k = 1;  // kernel\n")
+    (csrc / "oa_common.cuh").write_text("int c = 2;\n")
+    dig = bench.kernel_source_digest()
+    f = prof / "attn_fwd_tc_causal_b1h32n8192d128.md"
+    f.write_text(f"kernel_source_digest: {dig}\ndram_bytes_per_launch: 1234\n")
+    assert bench.profiled_traffic() == 1234.0
+    (csrc / "attn_tc.cu").write_text("int k = 1;  // kernel, comment reworded\n")
+    assert bench.profiled_traffic() == 1234.0
+    (csrc / "attn_tc.cu").write_text("int k = 2;\n")
+    assert bench.profiled_traffic() is None
