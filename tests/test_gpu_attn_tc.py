@@ -118,6 +118,26 @@ def test_scale_and_large_scores(cuda_lib):
     _check(cuda_lib, q, k, v, causal=True, scale=8.0, lse_atol=lse_atol)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_running_max_grows_every_key_tile(cuda_lib, d, causal):
+    # Scores that climb ~40 log2 units per 128-key tile for even query rows and fall for odd ones:
+    # every key tile raises the running max of half the lanes of every warp past the lazy-rescale
+    # threshold (O and l rescaled before the next PV), and leaves the other half's untouched.
+    B, H, N = 1, 2, 512
+    sign = torch.ones(N, dtype=torch.float32)
+    sign[1::2] = -1.0
+    q = sign.view(1, 1, N, 1).expand(B, H, N, d).contiguous()
+    ramp = 0.02 * torch.arange(N, dtype=torch.float32).view(1, 1, N, 1)
+    k = ramp + 0.05 * si.randn((B, H, N, d), 31, torch.float32)
+    v = si.randn((B, H, N, d), 32, torch.float32)
+    q, k, v = q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+    qf, kf = q.float().numpy(), k.float().numpy()
+    abs_dot = np.einsum("bhqd,bhkd->bhqk", np.abs(qf), np.abs(kf)).max()
+    lse_atol = 1e-4 + 4 * math.sqrt(d) * 2.0 ** -24 * abs_dot / math.sqrt(d)
+    _check(cuda_lib, q, k, v, causal=causal, lse_atol=lse_atol)
+
+
 def test_causal_row0_closed_form(cuda_lib):
     q, k, v = si.attn_inputs(1, 4, 256, 256, 128, torch.bfloat16, seed=13)
     o, lse = _run(cuda_lib, q, k, v, causal=True)
