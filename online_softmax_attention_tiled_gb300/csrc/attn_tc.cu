@@ -32,11 +32,11 @@
 //               S_i = Q_i K^T (SMEM x SMEM -> TMEM) and O_i += P_i V (P from
 //               TMEM, V from SMEM -> TMEM); warp 9 owns the TMEM allocation.
 //               One warp issues an N <= 128 MMA in about 70 (A from shared
-//               memory) to 90 (A from TMEM) cycles, about as long as the
-//               tensor core takes for an N = 128 one and twice as long as for
-//               N = 64, so each tile has its own issuer -- except at d = 128
-//               with two query tiles, where warp 9 alone issues both tiles'
-//               MMAs (see Cfg::mma_warps)
+//               memory) to 90 (A from TMEM) cycles, a little longer than the
+//               64 the tensor core takes for an N = 128 one and two to three
+//               times the 32 of an N = 64 one, so each tile has its own issuer
+//               -- except at d = 128 with two query tiles, where warp 9 alone
+//               issues both tiles' MMAs (see Cfg::mma_warps)
 // TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
 // O_0 [256, 256+d), O_1 [256+d, 256+2d).
 //   d = 128: P_i (bf16, two per column) is written over the first 64 columns
