@@ -871,11 +871,11 @@ __global__ void __launch_bounds__(kBwdThreads)
       const int st1 = st + 1 == NST ? 0 : st + 1;           // stage of step it + 1
       const uint32_t par1 = st1 == 0 ? par ^ 1u : par;
       const bool more = it + 1 < n_it;
-      // dV += P^T dO_it, half by half as the rows write P^T
+      // dV += P^T dO_it once both halves of P^T are written
+      if (!(ok = wait_all(bar_p(0), ph, B_DS) && wait_all(bar_p(1), ph, B_DS))) break;
+      tc_fence_after_sync();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!(ok = wait_all(bar_p(h), ph, B_DS))) break;
-        tc_fence_after_sync();
 #pragma unroll
         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
           mma_ts_elect(tmem_base + C::DV_COL, tmem_base + C::S_COL + pcol(kk), nmaj(C::DO_OFF, st) + rows16_off(kk),
@@ -888,11 +888,11 @@ __global__ void __launch_bounds__(kBwdThreads)
         tc_fence_after_sync();
         issue_s(st1);
       }
-      // dK += dS^T Q_it
+      // dK += dS^T Q_it once both halves of dS^T are written
+      if (!(ok = wait_all(bar_ds(0), ph, B_DS) && wait_all(bar_ds(1), ph, B_DS))) break;
+      tc_fence_after_sync();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!(ok = wait_all(bar_ds(h), ph, B_DS))) break;
-        tc_fence_after_sync();
 #pragma unroll
         for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
           mma_ts_elect(tmem_base + C::DK_COL, tmem_base + C::DP_COL + pcol(kk), nmaj(C::Q_OFF, st) + rows16_off(kk),
