@@ -437,6 +437,18 @@ void oa_set_wait_limit_ns(uint64_t ns);
  */
 oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream);
 
+/*
+ * Self-test of the debug build's checks: launches one warp whose single
+ * store of 1 to the device int `flag` is guarded by a check that fails.  In
+ * the debug build (the library compiled with -DOA_DEBUG, liboa_debug.so) the
+ * check records its site in the status word and skips the store, so *flag is
+ * left as it was and oa_sync_status() returns OA_ERR_INVALID; in the release
+ * build checks are compiled out, the store happens and oa_sync_status()
+ * returns OA_OK.  flag: device pointer to one int, 4-byte aligned.  Errors:
+ * OA_ERR_INVALID for a NULL or misaligned flag.
+ */
+oa_status oa_selftest_debug_check(int* flag, oa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

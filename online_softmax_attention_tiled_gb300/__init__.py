@@ -9,7 +9,7 @@ PyTorch fallback -- if the library is missing or cannot load, calls raise.
 Entry points (same names as the C ABI, without the ``oa_`` prefix):
   softmax_rows, attn_fwd, attn_fwd_f32_tiles, attn_splitkv,
   splitkv_workspace_bytes, attn_splitkv_static, lse_merge, sync_status, set_wait_limit_ns,
-  selftest_wait_timeout.
+  selftest_wait_timeout, selftest_debug_check.
 """
 from __future__ import annotations
 
@@ -34,7 +34,7 @@ EXPORTS = (
     "oa_attn_fwd_varlen", "oa_attn_fwd_f32_tiles", "oa_splitkv_workspace_bytes", "oa_attn_splitkv",
     "oa_attn_splitkv_gqa", "oa_attn_splitkv_static", "oa_lse_merge", "oa_attn_bwd_workspace_bytes", "oa_attn_bwd",
     "oa_attn_fwd_host_workspace_bytes", "oa_attn_fwd_host", "oa_attn_bwd_gqa", "oa_attn_bwd_varlen",
-    "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout",
+    "oa_sync_status", "oa_set_wait_limit_ns", "oa_selftest_wait_timeout", "oa_selftest_debug_check",
 )
 
 
@@ -98,6 +98,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
             "oa_sync_status": ([vp], i32),
             "oa_set_wait_limit_ns": ([u64], None),
             "oa_selftest_wait_timeout": ([u64, vp], i32),
+            "oa_selftest_debug_check": ([vp, vp], i32),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -525,3 +526,15 @@ def selftest_wait_timeout(limit_ns: int = 1_000_000, device=None):
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         _check(load().oa_selftest_wait_timeout(int(limit_ns), _stream(dev)))
+
+
+def selftest_debug_check(device=None) -> int:
+    """Launch one store guarded by a failing debug check (see oa.h); returns the flag it guards (0 when
+    the debug build skipped the store, 1 in the release build).  The caller reads the check's report
+    with sync_status()."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    flag = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(load().oa_selftest_debug_check(flag.data_ptr(), _stream(dev)))
+        torch.cuda.current_stream(dev).synchronize()
+    return int(flag.item())

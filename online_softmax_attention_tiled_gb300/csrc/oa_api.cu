@@ -81,9 +81,19 @@ __global__ void selftest_wait_kernel(oa::DevStatus st) {
   __syncthreads();
 }
 
+// A debug check whose condition is false: the debug build records the failure and skips the
+// store it guards; the release build compiles the check to true and performs the store.
+__global__ void selftest_check_kernel(oa::DevStatus st, int* out) {
+  if (threadIdx.x == 0 && OA_DCHECK(st, out == nullptr, (oa::K_SELFTEST << 8) | oa::kSiteDebugBase)) *out = 1;
+}
+
 }  // namespace
 
 namespace oa {
+cudaError_t launch_selftest_check(const DevStatus& st, int* out, cudaStream_t s) {
+  selftest_check_kernel<<<1, 32, 0, s>>>(st, out);
+  return cudaGetLastError();
+}
 cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s) {
   selftest_wait_kernel<<<1, 32, 0, s>>>(st);
   return cudaGetLastError();
@@ -658,6 +668,15 @@ oa_status oa_sync_status(oa_stream_t stream) {
     return fail(OA_ERR_INVALID, "debug build: bounds or alignment check %u of kernel %u failed (the access was skipped)",
                 word & 0x0Fu, word >> 8);
   return fail(OA_ERR_TIMEOUT, "device wait expired: kernel %u, wait site %u", word >> 8, word & 0xFFu);
+}
+
+oa_status oa_selftest_debug_check(int* flag, oa_stream_t stream) {
+  if (flag == nullptr) return fail(OA_ERR_INVALID, "selftest_debug_check: flag is NULL");
+  if (!aligned(flag, 4)) return fail(OA_ERR_INVALID, "selftest_debug_check: flag must be 4-byte aligned");
+  oa::DevStatus st;
+  if (!dev_status(&st)) return fail(OA_ERR_CUDA, "selftest_debug_check: no current CUDA device");
+  cudaError_t e = oa::launch_selftest_check(st, flag, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "selftest_debug_check launch");
 }
 
 oa_status oa_selftest_wait_timeout(uint64_t limit_ns, oa_stream_t stream) {

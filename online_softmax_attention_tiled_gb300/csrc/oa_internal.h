@@ -79,5 +79,6 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, float* workspace, const DevStatus&
                             const char** why);
 
 cudaError_t launch_selftest_wait(const DevStatus& st, cudaStream_t s);
+cudaError_t launch_selftest_check(const DevStatus& st, int* out, cudaStream_t s);
 
 }  // namespace oa

@@ -4,7 +4,9 @@ library (gpu).  Small and odd shapes run through every checked kernel -- the row
 clusters with the serial and the parallel merge, the unaligned scalar path), the tensor-core
 forward (both head sizes, square and offset causal, grouped heads, packed sequences) and both
 backward kernels -- in two subprocesses, one per build: no check fires (sync_status is OK) and
-every output is bit-identical, so the checks change nothing but the reporting.
+every output is bit-identical, so the checks change nothing but the reporting.  A check that fails
+on purpose (oa_selftest_debug_check) is reported as OA_ERR_INVALID, its store skipped, by the debug
+build alone.
 """
 import os
 import subprocess
@@ -50,6 +52,15 @@ for d in (64, 128):
     out["bwd d%d" % d] = oa.attn_bwd(q, k, v, o, lse, do, causal=True)
 oa.sync_status()  # raises if a check fired
 torch.save({key: tuple(t.cpu() for t in val) for key, val in out.items()}, sys.argv[1])
+# a check that fails on purpose: reported (and its store skipped) only by the debug build
+flag = oa.selftest_debug_check()
+try:
+    oa.sync_status()
+    reported = False
+except oa.OAError as e:
+    reported = e.status == oa.OA_ERR_INVALID
+print("check", flag, int(reported))
+oa.sync_status()  # the word was cleared: later calls start clean
 print("ok", len(out))
 '''
 
@@ -63,6 +74,8 @@ def _run(tmp_path, debug: bool):
     r = subprocess.run([sys.executable, str(script), str(dest), ROOT, "1" if debug else "0"], env=env, cwd=ROOT,
                        capture_output=True, text=True, timeout=1200)
     assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-4000:]
+    check = [ln for ln in r.stdout.splitlines() if ln.startswith("check ")]
+    assert check == (["check 0 1"] if debug else ["check 1 0"]), r.stdout[-2000:]
     return torch.load(dest)
 
 
