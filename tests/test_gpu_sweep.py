@@ -1,0 +1,106 @@
+"""Seeded random sweep of the bf16 forward, the backward and the row softmax against the fp64 oracle (gpu).
+
+The hand-picked cases of the other files pin each feature; here fixed pseudo-random draws combine
+them -- batch, query and key/value heads (grouping), query and key lengths (ragged against the
+128-row and 128-key tiles, more queries than keys, single rows), head size, causality, per-sequence
+key lengths including empty ones, softmax widths across the one-CTA, cluster and streaming paths --
+so that combinations nobody wrote down get checked too.  Every draw is a deterministic function of
+its case number.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth_inputs as si
+from parity import BF16_O_ATOL, assert_lse_close, assert_out_close, assert_softmax_close, bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd_case(n):
+    r = np.random.default_rng(1000 + n)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.choice([1, 2, 3]))
+    g = int(r.choice([1, 2, 4]))
+    B = int(r.integers(1, 4))
+    Nq = int(r.choice([1, 2, 7, 64, 127, 128, 129, 200, 256, 257, 383, 511]))
+    Nk = int(r.choice([1, 5, 100, 128, 129, 300, 513, 700])) if r.random() < 0.6 else Nq
+    causal = bool(r.random() < 0.6)
+    kv_len = None
+    if r.random() < 0.4:
+        kv_len = [int(x) for x in r.integers(0, Nk + 1, size=B)]
+    return B, hkv * g, hkv, Nq, Nk, d, causal, kv_len
+
+
+@pytest.mark.parametrize("n", range(64))
+def test_forward_sweep(cuda_lib, n):
+    B, H, Hkv, Nq, Nk, d, causal, kv_len = _fwd_case(n)
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.bfloat16, seed=2000 + n)
+    kvd = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int32).cuda()
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=causal, kv_len=kvd)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=causal, kv_len=kv_len)
+    assert_lse_close(lse, rl, what=f"lse case {n}")
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("n", range(16))
+def test_backward_sweep(cuda_lib, n):
+    # held to the per-element bound of the backward tests (first-order error of the bf16 roundings of
+    # P, dS and the outputs; summed over a group's query heads for dK, dV)
+    from test_gpu_attn_bwd import _assert_within, _bounds
+
+    r = np.random.default_rng(3000 + n)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.choice([1, 2]))
+    g = int(r.choice([1, 2]))
+    H = hkv * g
+    Nq = int(r.choice([64, 129, 200, 300]))
+    Nk = int(r.choice([64, 129, 250, 400])) if r.random() < 0.5 else Nq
+    causal = bool(r.random() < 0.6)
+    sc = 1.0 / math.sqrt(d)
+    q, k, v = si.attn_inputs_gqa(1, H, hkv, Nq, Nk, d, torch.bfloat16, seed=4000 + n)
+    do = si.randn((1, H, Nq, d), 5000 + n, torch.bfloat16)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = cuda_lib.attn_fwd(qc, kc, vc, causal=causal)
+    dq, dk, dv = cuda_lib.attn_bwd(qc, kc, vc, o, lse, doc, causal=causal)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    rq, rk, rv = oracle.attention_bwd(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(do), causal=causal,
+                                      scale=sc)
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    for hk in range(hkv):
+        tk_sum, tv_sum = 0.0, 0.0
+        for t in range(g):
+            h = hk * g + t
+            f64 = [x.to(torch.float64) for x in (q[0, h], k[0, hk], v[0, hk], do[0, h])]
+            tq, tk, tv = _bounds(*f64, causal, sc, np.arange(Nq), np.arange(Nk))
+            _assert_within(dq[0, h], rq[0, h], tq, f"dQ[{h}] case {n}")
+            tk_sum, tv_sum = tk_sum + tk, tv_sum + tv
+        _assert_within(dk[0, hk], rk[0, hk], tk_sum, f"dK[{hk}] case {n}")
+        _assert_within(dv[0, hk], rv[0, hk], tv_sum, f"dV[{hk}] case {n}")
+
+
+@pytest.mark.parametrize("n", range(24))
+def test_softmax_sweep(cuda_lib, n):
+    r = np.random.default_rng(6000 + n)
+    cols = int(r.choice([1, 3, 31, 257, 1023, 2049, 4097, 9000, 33000, 65537, 70000, 140000]))
+    rows = int(r.integers(1, 9))
+    x = si.softmax_input(rows, cols, seed=7000 + n)[0]
+    unaligned = bool(r.random() < 0.3)
+    if unaligned:  # a column slice: rows start off the 16-byte grid (the scalar path)
+        big = torch.empty(rows, cols + 3)
+        big[:, 1:cols + 1] = x
+        xd = big.cuda()[:, 1:cols + 1]
+    else:
+        xd = x.cuda()
+    y, lse = cuda_lib.softmax_rows(xd)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ry, rl = oracle.softmax_rows(x.numpy())
+    assert_softmax_close(y, ry, what=f"y case {n} ({rows}x{cols}{' unaligned' if unaligned else ''})")
+    assert_lse_close(lse, rl, what=f"lse case {n}")
