@@ -4,8 +4,10 @@ The hand-picked cases of the other files pin each feature; here fixed pseudo-ran
 them -- batch, query and key/value heads (grouping), query and key lengths (ragged against the
 128-row and 128-key tiles, more queries than keys, single rows), head size, causality, per-sequence
 key lengths including empty ones, softmax widths across the one-CTA, cluster and streaming paths --
-so that combinations nobody wrote down get checked too.  Every draw is a deterministic function of
-its case number.
+so that combinations nobody wrote down get checked too; likewise packed sequences (lengths from 0,
+queries and keys of different lengths), split-KV decode over grouped caches with per-sequence
+lengths, and the fp32 forward with random tiles.  Every draw is a deterministic function of its
+case number.
 """
 import math
 
@@ -104,3 +106,69 @@ def test_softmax_sweep(cuda_lib, n):
     ry, rl = oracle.softmax_rows(x.numpy())
     assert_softmax_close(y, ry, what=f"y case {n} ({rows}x{cols}{' unaligned' if unaligned else ''})")
     assert_lse_close(lse, rl, what=f"lse case {n}")
+
+
+@pytest.mark.parametrize("n", range(16))
+def test_packed_forward_sweep(cuda_lib, n):
+    r = np.random.default_rng(8000 + n)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.choice([1, 2]))
+    H = hkv * int(r.choice([1, 2, 4]))
+    S = int(r.integers(1, 7))
+    lq = [int(x) for x in r.choice([0, 1, 3, 64, 127, 128, 129, 300, 513], size=S)]
+    same = r.random() < 0.5
+    lk = list(lq) if same else [int(x) for x in r.choice([0, 1, 5, 100, 129, 256, 400, 700], size=S)]
+    if sum(lq) == 0:
+        lq[0] = 1
+    if sum(lk) == 0:
+        lk[-1] = 1
+    causal = bool(r.random() < 0.6)
+    q, k, v, cq, ck = si.varlen_inputs(lq, lk, H, hkv, d, torch.bfloat16, seed=9000 + n)
+    o, lse = cuda_lib.attn_fwd_varlen(q.cuda(), k.cuda(), v.cuda(), cq.cuda(), ck.cuda(), max(max(lq), 1),
+                                      max(max(lk), 1), causal=causal)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ro, rl = oracle.attention_varlen(bf16_bits(q), bf16_bits(k), bf16_bits(v), cq.numpy(), ck.numpy(), causal=causal)
+    assert_lse_close(lse, rl, what=f"lse case {n} (lq {lq}, lk {lk}, H{H}/{hkv}, d{d}, causal {causal})")
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("n", range(12))
+def test_splitkv_sweep(cuda_lib, n):
+    r = np.random.default_rng(10000 + n)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.choice([1, 2, 4]))
+    H = hkv * int(r.choice([1, 2, 4]))
+    B = int(r.integers(1, 5))
+    Nq = int(r.choice([1, 1, 2, 5]))
+    Nk = int(r.choice([1, 37, 512, 1000, 3000]))
+    splits = int(r.choice([1, 2, 7, 16, 64]))
+    kv_len = [int(x) for x in r.integers(0, Nk + 1, size=B)] if r.random() < 0.5 else None
+    q, k, v = si.attn_inputs_gqa(B, H, hkv, Nq, Nk, d, torch.bfloat16, seed=11000 + n)
+    kvd = None if kv_len is None else torch.tensor(kv_len, dtype=torch.int32).cuda()
+    o, lse = cuda_lib.attn_splitkv(q.cuda(), k.cuda(), v.cuda(), splits, kv_len=kvd)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), kv_len=kv_len)
+    what = f"case {n} (B{B} H{H}/{hkv} {Nq}x{Nk} d{d} splits {splits} kv_len {kv_len})"
+    assert_lse_close(lse, rl, what=f"lse {what}")
+    assert_out_close(o, ro, BF16_O_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("n", range(8))
+def test_fp32_forward_sweep(cuda_lib, n):
+    from parity import F32_ATTN_ATOL
+
+    r = np.random.default_rng(12000 + n)
+    d = int(r.choice([4, 16, 32, 64]))
+    Nq = int(r.choice([1, 6, 37, 100]))
+    Nk = int(r.choice([1, 3, 37, 129])) if r.random() < 0.5 else Nq
+    causal = bool(r.random() < 0.5)
+    Br, Bc = int(r.integers(1, 65)), int(r.integers(1, 65))
+    q, k, v = si.attn_inputs(2, 2, Nq, Nk, d, torch.float32, seed=13000 + n)
+    o, lse = cuda_lib.attn_fwd_f32_tiles(q.cuda(), k.cuda(), v.cuda(), Br, Bc, causal=causal)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=causal)
+    assert_lse_close(lse, rl, what=f"lse case {n} ({Nq}x{Nk} d{d} Br{Br} Bc{Bc} causal {causal})")
+    assert_out_close(o, ro, F32_ATTN_ATOL, lse_ref=rl)
