@@ -172,3 +172,49 @@ def test_fp32_forward_sweep(cuda_lib, n):
     ro, rl = oracle.attention(q.numpy(), k.numpy(), v.numpy(), causal=causal)
     assert_lse_close(lse, rl, what=f"lse case {n} ({Nq}x{Nk} d{d} Br{Br} Bc{Bc} causal {causal})")
     assert_out_close(o, ro, F32_ATTN_ATOL, lse_ref=rl)
+
+
+@pytest.mark.parametrize("n", range(10))
+def test_packed_backward_sweep(cuda_lib, n):
+    from test_gpu_attn_bwd import _assert_within, _bounds
+
+    r = np.random.default_rng(14000 + n)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.choice([1, 2]))
+    g = int(r.choice([1, 2]))
+    H = hkv * g
+    S = int(r.integers(1, 5))
+    lq = [int(x) for x in r.choice([0, 1, 64, 129, 200, 300], size=S)]
+    lk = list(lq) if r.random() < 0.5 else [int(x) for x in r.choice([0, 1, 100, 129, 250], size=S)]
+    if sum(lq) == 0:
+        lq[0] = 1
+    if sum(lk) == 0:
+        lk[-1] = 1
+    causal = bool(r.random() < 0.6)
+    sc = 1.0 / math.sqrt(d)
+    q, k, v, cq, ck = si.varlen_inputs(lq, lk, H, hkv, d, torch.bfloat16, seed=15000 + n)
+    do = si.randn(tuple(q.shape), 16000 + n, torch.bfloat16)
+    qd, kd, vd, dod, cqd, ckd = (t.cuda() for t in (q, k, v, do, cq, ck))
+    mq, mk = max(max(lq), 1), max(max(lk), 1)
+    o, lse = cuda_lib.attn_fwd_varlen(qd, kd, vd, cqd, ckd, mq, mk, causal=causal, scale=sc)
+    dq, dk, dv = cuda_lib.attn_bwd_varlen(qd, kd, vd, o, lse, dod, cqd, ckd, mq, mk, causal=causal, scale=sc)
+    torch.cuda.synchronize()
+    cuda_lib.sync_status()
+    dq, dk, dv = dq.cpu(), dk.cpu(), dv.cpu()
+    rq, rk, rv = oracle.attention_bwd_varlen(bf16_bits(q), bf16_bits(k), bf16_bits(v), bf16_bits(do), cq.numpy(),
+                                             ck.numpy(), causal=causal, scale=sc)
+    for s in range(S):
+        sq, sk = slice(int(cq[s]), int(cq[s + 1])), slice(int(ck[s]), int(ck[s + 1]))
+        if lq[s] == 0 or lk[s] == 0:  # no query or no key: the gradients there are exactly zero
+            assert torch.all(dq[sq] == 0) and torch.all(dk[sk] == 0) and torch.all(dv[sk] == 0), f"case {n} seq {s}"
+            continue
+        for hk in range(hkv):
+            tk_sum, tv_sum = 0.0, 0.0
+            for t in range(g):
+                h = hk * g + t
+                f64 = [x.to(torch.float64) for x in (q[sq, h], k[sk, hk], v[sk, hk], do[sq, h])]
+                tq, tk, tv = _bounds(*f64, causal, sc, np.arange(lq[s]), np.arange(lk[s]))
+                _assert_within(dq[sq, h], rq[sq, h], tq, f"dQ case {n} seq {s} head {h}")
+                tk_sum, tv_sum = tk_sum + tk, tv_sum + tv
+            _assert_within(dk[sk, hk], rk[sk, hk], tk_sum, f"dK case {n} seq {s} head {hk}")
+            _assert_within(dv[sk, hk], rv[sk, hk], tv_sum, f"dV case {n} seq {s} head {hk}")
