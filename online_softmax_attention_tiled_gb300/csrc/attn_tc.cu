@@ -17,8 +17,11 @@
 //
 // Persistent: one CTA per SM, each working through items (2 x 128 query rows of one
 // (b, h)) numbered heaviest first and dealt out in rounds of one per CTA, alternating
-// direction between rounds.  Barriers, TMEM and descriptors are set up once; ring loads
-// and barrier phases run on across items, so the next item's Q, K and V are loaded and
+// direction between rounds.  Causal launches whose K/V exceeds L2 sweep bands of heads in
+// phases (each phase dealt this way, odd phases in mirrored CTA order), and odd rounds read
+// the key tiles top down, so K/V is read from DRAM about once.  Q and O, read and written
+// once, carry an evict-first L2 policy.  Barriers, TMEM and descriptors are set up once; ring
+// loads and barrier phases run on across items, so the next item's Q, K and V are loaded and
 // its first score tiles computed while the current item finishes.
 //
 // GB300 mapping (352 threads; 320 at d = 128 with two query tiles):
@@ -61,6 +64,9 @@
 // the CTA abort flag, every role falls through to the teardown, in-flight
 // TMA loads and MMAs are drained (bounded), and TMEM is always freed.
 #include "oa_internal.h"
+
+#include <algorithm>
+#include <vector>
 
 namespace oa {
 namespace {
@@ -145,6 +151,13 @@ struct TcParams {
   int off;               // dense causal: query i sees keys j <= i + off (Nk - Nq); causality is the MODE
   int qmod;              // > 0: a row's causal position is its index modulo qmod (grouped decode rows)
   int group;             // query heads per key/value head (H / H_kv)
+  // Heaviest-first items are dealt in n_groups phases, each over the heads of a band of
+  // key/value planes (group_items items, group_rounds rounds of the grid); 1 phase otherwise
+  int n_groups, group_items, group_rounds;
+  // The key-tile order of a causal item follows the round it has in the dealing of the whole call
+  // (dir_hs heads a phase, dir_G CTAs), in which this launch's head plane 0 is plane dir_sh0
+  int dir_hs, dir_G, dir_sh0;
+  int call_bh, call_sh0;  // the whole call's planes and this launch's first (host side, see TcArgs)
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
   int64_t o_elems, lse_elems;  // extents of o and lse (the debug build's store checks)
   int l_rs;              // LSE row stride: 1 dense, H packed
@@ -174,11 +187,19 @@ struct Item {
   int nq, kvl;      // query rows and keys of the sequence
   int off;          // causal: query i sees keys j <= i + off (keys minus queries of the sequence)
   int n_kv[2], n_all;
+  int nrev;         // key tiles read in descending order: load L < nrev holds key tile nrev - 1 - L
   int64_t ob, lb;   // offsets of the sequence's row 0 (this head) in O (elements) and in LSE
 };
 
-// Items are numbered heaviest first (causal, and packed sequences: the last query blocks);
-// item idx covers query block num_qblocks - 1 - idx / BH of (sequence, head) idx % BH.
+// Dense causal launches deal their items in phases over bands of heads (see item_of); the
+// others in one.
+template <bool PACKED, bool SPLIT, int MODE>
+constexpr bool phased() { return !PACKED && !SPLIT && MODE != kNonCausal; }
+
+// Items are numbered heaviest first (causal, and packed sequences: the last query blocks) within
+// each phase: item idx = f * group_items + r of phase f covers query block num_qblocks - 1 - r / hs
+// of (sequence, head) f * hs + r % hs, hs = BH / n_groups heads per phase (all of them with one
+// phase).
 // Dense non-causal items weigh alike and are numbered head-major: query block idx % num_qblocks
 // of head plane idx / num_qblocks.  Query head h reads key/value head h / group.  SPLIT (at most
 // 128 query rows): both query-tile slots hold the same rows, slot 0 takes the even key tiles and
@@ -188,8 +209,11 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   constexpr int BN = Cfg<D>::BN;
   Item it;
   constexpr bool kHeadMajor = !PACKED && MODE == kNonCausal;
-  const int qb = kHeadMajor ? idx % p.num_qblocks : p.num_qblocks - 1 - idx / p.BH;
-  const int sh = kHeadMajor ? idx / p.num_qblocks : idx % p.BH;
+  constexpr bool kPhased = phased<PACKED, SPLIT, MODE>();
+  const int phase = kPhased ? idx / p.group_items : 0;
+  const int r = idx - phase * p.group_items, hs = kPhased ? p.BH / p.n_groups : p.BH;
+  const int qb = kHeadMajor ? idx % p.num_qblocks : p.num_qblocks - 1 - r / hs;
+  const int sh = kHeadMajor ? idx / p.num_qblocks : phase * hs + r % hs;
   const int sq = sh / p.H, h = sh % p.H, hk = h / p.group;
   const int Hkv = p.H / p.group;
   it.q0 = qb * 2 * BM;
@@ -242,21 +266,45 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
     }
   }
   it.n_all = max(it.n_kv[0], it.n_kv[1]);
+  // Causal items of odd rounds read the key tiles that both query tiles share from the top down
+  // (the longer tile's extra tiles still come last, so both tiles start at the item's first load
+  // and the shorter one stops early).  Every round starts a new item on every CTA; read from the
+  // bottom, a round would begin on the key tiles the previous round read first, which L2 has
+  // evicted by then when the phase's K/V does not fit, and re-read them from DRAM.  Starting
+  // from the top it begins on the tiles the previous round read last.  The online softmax does
+  // not depend on the order of the key tiles.
+  it.nrev = 0;
+  if constexpr (!SPLIT && MODE != kNonCausal) {
+    // an odd round of its phase (in this launch's own dealing when it is the whole call)
+    if (((((p.num_qblocks - 1 - qb) * p.dir_hs + (p.dir_sh0 + sh) % p.dir_hs)) / p.dir_G) & 1) {
+      const int a = it.n_kv[0], b = it.n_kv[1];
+      it.nrev = (a > 0 && b > 0) ? min(a, b) : it.n_all;
+    }
+  }
   return it;
 }
+
+// The key tile held by the item's L-th K/V load.
+__device__ __forceinline__ int key_tile(int L, int nrev) { return L < nrev ? nrev - 1 - L : L; }
 
 // Key tiles an item loads (K_0, V_0, K_1, V_1, ...): each once, shared by both slots, or (SPLIT)
 // split between them.
 template <bool SPLIT>
 __device__ __forceinline__ int n_loads_of(const Item& it) { return SPLIT ? it.n_kv[0] + it.n_kv[1] : it.n_all; }
 
-// The k-th item of this CTA: round k of the persistent grid takes items [k G, k G + G), in
-// CTA order on even rounds and in reverse on odd ones, so the heavy and light ends of the
-// list pair up across rounds.  Negative past the end of the list.
-__device__ __forceinline__ int item_of_round(int k, int total) {
-  const int G = (int)gridDim.x, c = (int)blockIdx.x;
-  const int idx = k * G + ((k & 1) ? (G - 1 - c) : c);
-  return idx < total ? idx : -1;
+// The k-th item of this CTA.  Phase f = k / group_rounds runs after phase f - 1 on every CTA;
+// round k' = k % group_rounds of a phase takes its items [k' G, k' G + G), in CTA order on even
+// rounds and in reverse on odd ones, so the heavy and light ends of the phase's list pair up
+// across rounds; odd phases deal in mirrored CTA order, so that the last, partial rounds of two
+// consecutive phases fall on CTAs at opposite ends of the grid.  Negative past the end of a
+// phase.  (One phase: item k G + c or k G + G - 1 - c of the whole list.)
+template <bool PHASED>
+__device__ __forceinline__ int item_of(int k, const TcParams& p) {
+  const int G = (int)gridDim.x;
+  const int f = PHASED ? k / p.group_rounds : 0, kr = k - f * p.group_rounds;
+  const int c = (f & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
+  const int r = kr * G + ((kr & 1) ? (G - 1 - c) : c);
+  return r < p.group_items ? f * p.group_items + r : -1;
 }
 
 // No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
@@ -296,7 +344,7 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int total = p.num_qblocks * p.BH;
+  const int rounds = p.n_groups * p.group_rounds;  // items per CTA, at most
   constexpr int kIssuers = C::template mma_warps<SPLIT>();
   constexpr bool kOneIssuer = kIssuers == 1;
 
@@ -345,8 +393,11 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     // Ring loads are numbered across items (tg), so slots and phases run on.
     int tg = 0, nq = 0;
     bool ok = true;
-    for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-      const int idx = item_of_round(k, total);
+    // Q is read once: its lines are the first to leave L2, before the K/V tiles that later items
+    // read again
+    const uint64_t read_once = l2_policy_evict_first();
+    for (int k = 0; ok && k < rounds; ++k) {
+      const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
       if (idx < 0) continue;
       const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
       if (it.n_all == 0) continue;
@@ -355,16 +406,16 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
       mbar_arrive_expect_tx_elect(bar_q, (SPLIT ? 1 : 2) * C::Q_TILE);
       for (int i = 0; i < (SPLIT ? 1 : 2); ++i)
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(sbase + C::Q_OFF + i * C::Q_TILE + s * C::Q_SLAB, &tm_q, bar_q, s * 64,
-                            it.yq + it.q0 + i * BM, it.zq);
+          tma_load_3d_elect_hint(sbase + C::Q_OFF + i * C::Q_TILE + s * C::Q_SLAB, &tm_q, bar_q, s * 64,
+                                 it.yq + it.q0 + i * BM, it.zq, read_once);
       ++nq;
       for (int t = 0; t < 2 * n_loads_of<SPLIT>(it); ++t, ++tg) {
         if (!(ok = wait_all(bar_empty(tg), ring_phase(tg) ^ 1u, W_KEMPTY))) break;
         mbar_arrive_expect_tx_elect(bar_full(tg), C::KV_TILE);
         const CUtensorMap* map = (t & 1) ? &tm_v : &tm_k;
         for (int s = 0; s < C::SLABS; ++s)
-          tma_load_3d_elect(ring_addr(tg) + s * C::KV_SLAB, map, bar_full(tg), s * 64, it.ykv + (t >> 1) * C::BN,
-                            it.zkv);
+          tma_load_3d_elect(ring_addr(tg) + s * C::KV_SLAB, map, bar_full(tg), s * 64,
+                            it.ykv + (SPLIT ? (t >> 1) : key_tile(t >> 1, it.nrev)) * C::BN, it.zkv);
       }
     }
     // drain: every load issued must have landed before the CTA can exit
@@ -421,8 +472,8 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     bool ok = true;
     if constexpr (kOneIssuer) {
       // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
-      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-        const int idx = item_of_round(k, total);
+      for (int k = 0; ok && k < rounds; ++k) {
+        const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
         if (idx < 0) continue;
         const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
@@ -487,8 +538,8 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
         mma_commit_elect(bar_empty(tv));
         return true;
       };
-      for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-        const int idx = item_of_round(k, total);
+      for (int k = 0; ok && k < rounds; ++k) {
+        const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
         if (idx < 0) continue;
         const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         if (it.n_all == 0) continue;
@@ -552,19 +603,21 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     const uint32_t o_addr = tmem_base + lane_base + C::o_col(i);
     const uint32_t p_addr = tmem_base + lane_base + C::p_col(i);
     const float sl2 = p.scale_log2;
+    const uint64_t write_once = l2_policy_evict_first();
     int sb = 0;  // score tiles of this group in earlier items (barrier phases run on)
     int nx = 0;  // SPLIT: items handed over so far (the phase of xch / xdone)
     bool ok = true;
-    for (int k = 0; ok && k * (int)gridDim.x < total; ++k) {
-      const int idx = item_of_round(k, total);
+    for (int k = 0; ok && k < rounds; ++k) {
+      const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
       if (idx < 0) continue;
       // only what the score loop needs stays live through it; the epilogue looks the item up
       // again for its output offsets
       // (causal) r0 + off: the last key visible to the tile's first row; row + off: to this row's
-      int n, kvl, r0, off;
+      int n, kvl, r0, off, nrev;
       {
         const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
         n = it.n_kv[i];
+        nrev = it.nrev;
         kvl = it.kvl;
         r0 = it.q0 + (SPLIT ? 0 : i * BM);
         off = MODE == kCausalOff ? it.off : 0;
@@ -592,7 +645,7 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
           if (lane == 0) mbar_arrive(bar_sfree(i));
         }
         float* s = reinterpret_cast<float*>(sr);
-        const int col0 = (SPLIT ? 2 * j + i : j) * BN;  // SPLIT: this slot's j-th key tile is 2 j + i
+        const int col0 = (SPLIT ? 2 * j + i : key_tile(j, nrev)) * BN;  // SPLIT: this slot's j-th key tile is 2 j + i
         constexpr bool kCausalMask = MODE != kNonCausal;
         if (col0 + BN > kvl || (kCausalMask && col0 + BN - 1 > r0 + off)) {
 #pragma unroll
@@ -767,9 +820,9 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
         // Each thread writes its own row: a warp's store touches 32 rows, so whole 32-byte
         // sectors per thread (half as many requests as 16-byte stores) matter here.
         if (row_in) {
-          if (p.o_v8) {
-            st_global_v8(orow + c, w);
-            st_global_v8(orow + c + 16, w + 8);
+          if (p.o_v8) {  // O is written once: first out of L2 (see the Q loads)
+            st_global_v8_hint(orow + c, w, write_once);
+            st_global_v8_hint(orow + c + 16, w + 8, write_once);
           } else {
             uint4* dst = reinterpret_cast<uint4*>(orow + c);
             dst[0] = pk[0];
@@ -804,6 +857,61 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
 
 constexpr int kMaxDevices = 64;
 
+// Phases of the heaviest-first dealing (see item_of) for a dense causal launch on G CTAs.  When
+// the K/V of the launch does not fit in L2, the heads are split into bands of whole key/value
+// planes swept one after the other, so that the items running at the same time read the K/V of
+// one band only; the count is the largest of 2, 4 and 8 whose dealing leaves the busiest CTA at
+// most 0.5 % busier than one phase does (weights: the key tiles an item loads plus two for its
+// Q load and epilogue; kv_len, unknown here, is taken as Nk).  The choice is kept per shape.
+template <int D, int MODE>
+int causal_phases(const TcParams& p, int G) {
+  constexpr int BN = Cfg<D>::BN;
+  constexpr long long kL2Bytes = 48ll << 20;  // K/V that stays in L2 through a phase
+  const int planes = p.BH / p.group;
+  const long long kv_bytes = (long long)planes * p.Nk * D * 2 * 2;
+  const long long total = (long long)p.num_qblocks * p.BH;
+  if (kv_bytes <= kL2Bytes || total > (1 << 16) || G < 1) return 1;
+  struct Entry { int nqb, bh, group, nq, nk, off, G, phases; };
+  thread_local Entry cache[4] = {};
+  thread_local int next = 0;
+  const int off = MODE == kCausalOff ? p.off : 0;
+  for (const Entry& c : cache)
+    if (c.phases > 0 && c.nqb == p.num_qblocks && c.bh == p.BH && c.group == p.group && c.nq == p.Nq &&
+        c.nk == p.Nk && c.off == off && c.G == G)
+      return c.phases;
+  // weight of an item of query block qb (both query tiles share its key tiles)
+  std::vector<long long> w(p.num_qblocks);
+  const int nk_tiles = (p.Nk + BN - 1) / BN;
+  for (int qb = 0; qb < p.num_qblocks; ++qb) {
+    int n = 0;
+    for (int i = 0; i < 2; ++i) {
+      const int r0 = qb * 2 * BM + i * BM;
+      if (r0 < p.Nq) n = std::max(n, std::max(0, std::min(nk_tiles, (r0 + BM - 1 + off + BN) / BN)));
+    }
+    w[qb] = n + 2;
+  }
+  std::vector<long long> load(G);
+  auto busiest = [&](int ng) {
+    const int hs = p.BH / ng, gi = hs * p.num_qblocks, gr = (gi + G - 1) / G;
+    std::fill(load.begin(), load.end(), 0ll);
+    for (int f = 0; f < ng; ++f)
+      for (int kr = 0; kr < gr; ++kr)
+        for (int b = 0; b < G; ++b) {
+          const int c = (f & 1) ? G - 1 - b : b;
+          const int r = kr * G + ((kr & 1) ? (G - 1 - c) : c);
+          if (r < gi) load[b] += w[p.num_qblocks - 1 - r / hs];
+        }
+    return *std::max_element(load.begin(), load.end());
+  };
+  const long long one = busiest(1);
+  int best = 1;
+  for (int ng = 2; ng <= 8; ng *= 2)
+    if (planes % ng == 0 && (double)busiest(ng) <= 1.005 * (double)one) best = ng;
+  cache[next] = Entry{p.num_qblocks, p.BH, p.group, p.Nq, p.Nk, off, G, best};
+  next = (next + 1) % 4;
+  return best;
+}
+
 // Persistent grid: one CTA per SM (the kernel holds an SM's TMEM and most of its shared
 // memory), never more CTAs than work items.  Without the causal mask (and without packed
 // sequences) the items weigh alike, so the grid is the fewest CTAs that keep the number of rounds:
@@ -832,8 +940,24 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     const long long rounds = (total + g - 1) / g;
     g = (total + rounds - 1) / rounds;
   }
+  TcParams q = p;
+  q.n_groups = phased<PACKED, SPLIT, MODE>() ? causal_phases<D, MODE>(p, (int)g) : 1;
+  q.group_items = (int)(total / q.n_groups);
+  q.group_rounds = (int)((q.group_items + g - 1) / g);
+  q.dir_hs = q.BH / q.n_groups;
+  q.dir_G = (int)g;
+  q.dir_sh0 = 0;
+  if (phased<PACKED, SPLIT, MODE>() && p.call_bh > p.BH) {  // a piece of a call of call_bh planes
+    TcParams whole = p;
+    whole.BH = p.call_bh;
+    const long long total_w = (long long)p.num_qblocks * whole.BH;
+    const long long g_w = total_w < sm_count[dev] ? total_w : sm_count[dev];
+    q.dir_hs = whole.BH / causal_phases<D, MODE>(whole, (int)g_w);
+    q.dir_G = (int)g_w;
+    q.dir_sh0 = p.call_sh0;
+  }
   const unsigned grid = (unsigned)g;
-  attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::template threads<SPLIT>(), Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, p);
+  attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::template threads<SPLIT>(), Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, q);
   return cudaGetLastError();
 }
 
@@ -881,6 +1005,8 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.l_rs = packed ? a.H : 1;
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;
+  p.call_bh = (!packed && a.order_bh > p.BH) ? a.order_bh : p.BH;
+  p.call_sh0 = (!packed && a.order_bh > p.BH) ? a.order_sh0 : 0;
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows
   // Instance by layout, query-tile use and masking mode (packed sequences may each have their own
   // key offset; a dense call has one, Nk - Nq)

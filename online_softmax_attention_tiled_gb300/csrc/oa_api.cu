@@ -175,9 +175,11 @@ static oa_status check_fwd(const void* q, const void* k, const void* v, void* o,
 // The dense forward on `stream`, arguments already checked.
 // qmod > 0: each plane's rows are the queries of several query heads, qmod per head (grouped decode),
 // and a row's causal position is its index modulo qmod.
+// order_bh / order_sh0: a piece of a call of order_bh planes, from plane order_sh0 (see TcArgs).
 static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, oa_dtype dt, int B,
                             int H, int Hkv, int Nq, int Nk, int d, int causal, float scale, const int32_t* kv_len,
-                            const oa::DevStatus& st, cudaStream_t stream, const char* who, int qmod = 0) {
+                            const oa::DevStatus& st, cudaStream_t stream, const char* who, int qmod = 0,
+                            int order_bh = 0, int order_sh0 = 0) {
   if (dt == OA_BF16) {
     oa::TcArgs a{};
     a.q = q;
@@ -195,6 +197,8 @@ static oa_status launch_fwd(const void* q, const void* k, const void* v, void* o
     a.scale = scale;
     a.kv_len = kv_len;
     a.qmod = qmod;
+    a.order_bh = order_bh;
+    a.order_sh0 = order_sh0;
     const char* why = nullptr;
     cudaError_t e = oa::launch_attn_tc(a, st, stream, &why);
     if (e != cudaSuccess) return why ? fail(OA_ERR_CUDA, "%s: %s", who, why) : cuda_fail(e, "attn_fwd launch");
@@ -373,7 +377,7 @@ oa_status oa_attn_fwd_host(const void* q_host, const void* k_host, const void* v
     if ((e = cudaStreamWaitEvent(p->comp, p->landed[c], 0)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host wait");
     s = launch_fwd(qd + u0 * g * qplane, kd + u0 * kvplane, vd + u0 * kvplane, od + u0 * g * qplane,
                    lsed ? lsed + u0 * g * Nq : nullptr, dt, 1, (int)(nu * g), (int)nu, Nq, Nk, d, causal, scale,
-                   nullptr, st, p->comp, who);
+                   nullptr, st, p->comp, who, 0, B * H, (int)(u0 * g));
     if (s != OA_OK) return s;
     if ((e = cudaEventRecord(p->done[c], p->comp)) != cudaSuccess) return cuda_fail(e, "attn_fwd_host record");
     // out: O and LSE of the chunk

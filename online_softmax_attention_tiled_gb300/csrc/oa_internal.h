@@ -55,6 +55,10 @@ struct TcArgs {
   // > 0: the rows of a plane are the queries of several query heads, qmod each (grouped decode); a
   // row's causal position is its index modulo qmod, and Nk - qmod is the causal key offset
   int qmod;
+  // Dense: this launch computes planes [order_sh0, order_sh0 + B H) of a call of order_bh planes
+  // cut into pieces (0: the launch is the whole call); the order of each item's key tiles is that
+  // of the whole call, so the pieces give its results bit for bit
+  int order_bh, order_sh0;
 };
 // `why` gets a static message when the host-side set-up (tensor maps) fails.
 cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s, const char** why);

@@ -25,6 +25,10 @@ def _pinned(*ts):
     (1, 3, 3, 129, 128, True, 64),   # more pieces requested than planes
     (1, 2, 1, 200, 128, True, 1),    # one piece: no overlap, same result
     (3, 4, 4, 64, 64, False, 5),
+    # several rounds of the persistent grid (odd rounds read key tiles top down) and, with 64 MiB of
+    # K/V, two phases over bands of heads: each piece must follow the whole call's order
+    (1, 16, 16, 4096, 128, True, 3),
+    (1, 32, 16, 8192, 128, True, 3),
 ])
 def test_host_forward_equals_device_forward(B, H, Hkv, N, d, causal, chunks):
     q, k, v = si.attn_inputs_gqa(B, H, Hkv, N, N, d, torch.bfloat16, seed=11 + N)
