@@ -116,6 +116,10 @@ oa_status oa_softmax_rows(const float* x, int64_t rows, int64_t cols, int64_t ld
  * bf16: tcgen05 tensor-core kernel, fp32 accumulation, bf16 O; d must be
  * 64 or 128 (else OA_ERR_UNSUPPORTED).  fp32: SIMT kernel in fp32,
  * 1 <= d <= 256.
+ * Results are deterministic for a given shape and device.  A causal row's
+ * key tiles are summed in an order that follows how the launch deals its
+ * work to the SMs, so devices with different SM counts may differ in the
+ * last bits (within the stated tolerances).
  * Errors: OA_ERR_INVALID for NULL q/k/v/o, sizes < 1 (B, H, Nq, Nk, d),
  * misalignment or a bad scale; OA_ERR_UNSUPPORTED for an unsupported
  * (dtype, d).
@@ -194,8 +198,9 @@ size_t oa_attn_fwd_host_workspace_bytes(oa_dtype dt, int B, int H, int H_kv, int
  * in; the copy in of piece c + 1, the kernel of piece c and the copy out of
  * piece c - 1 run at the same time on three streams the library keeps for
  * each device (created on the first call on that device; make that call
- * before any stream capture).  Every piece's result equals that of
- * oa_attn_fwd_gqa on the whole batch.
+ * before any stream capture).  The result equals that of oa_attn_fwd_gqa
+ * on the whole batch bit for bit (each piece sums its key tiles in the
+ * whole call's order).
  *   q_host, k_host, v_host, o_host, lse_host: host memory in the layouts of
  *          oa_attn_fwd_gqa (lse_host may be NULL), 16-byte aligned.  For the
  *          copies to overlap they must be page-locked (cudaHostAlloc,
