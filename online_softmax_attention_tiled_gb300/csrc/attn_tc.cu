@@ -157,7 +157,9 @@ struct TcParams {
   // The key-tile order of a causal item follows the round it has in the dealing of the whole call
   // (dir_hs heads a phase, dir_G CTAs), in which this launch's head plane 0 is plane dir_sh0
   int dir_hs, dir_G, dir_sh0;
+  int dir_alt;  // 0: every item reads its key tiles bottom up (a call dealt plane by plane)
   int call_bh, call_sh0;  // the whole call's planes and this launch's first (host side, see TcArgs)
+  int plane_major;        // kCausalOff, dense, one phase: items numbered plane by plane (see item_at)
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
   int64_t o_elems, lse_elems;  // extents of o and lse (the debug build's store checks)
   int l_rs;              // LSE row stride: 1 dense, H packed
@@ -212,8 +214,13 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   constexpr bool kPhased = phased<PACKED, SPLIT, MODE>();
   const int phase = kPhased ? idx / p.group_items : 0;
   const int r = idx - phase * p.group_items, hs = kPhased ? p.BH / p.n_groups : p.BH;
-  const int qb = kHeadMajor ? idx % p.num_qblocks : p.num_qblocks - 1 - r / hs;
-  const int sh = kHeadMajor ? idx / p.num_qblocks : phase * hs + r % hs;
+  // a causal launch with a key offset whose items weigh nearly alike (a chunk of queries after a
+  // long cache) numbers them plane by plane, heaviest first within a plane: the items running at
+  // the same time then share few K/V planes
+  const bool by_plane = MODE == kCausalOff && kPhased && p.plane_major;
+  const int qb = kHeadMajor ? idx % p.num_qblocks
+                            : p.num_qblocks - 1 - (by_plane ? r % p.num_qblocks : r / hs);
+  const int sh = kHeadMajor ? idx / p.num_qblocks : by_plane ? r / p.num_qblocks : phase * hs + r % hs;
   const int sq = sh / p.H, h = sh % p.H, hk = h / p.group;
   const int Hkv = p.H / p.group;
   it.q0 = qb * 2 * BM;
@@ -276,7 +283,7 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   it.nrev = 0;
   if constexpr (!SPLIT && MODE != kNonCausal) {
     // an odd round of its phase (in this launch's own dealing when it is the whole call)
-    if (((((p.num_qblocks - 1 - qb) * p.dir_hs + (p.dir_sh0 + sh) % p.dir_hs)) / p.dir_G) & 1) {
+    if (p.dir_alt && ((((p.num_qblocks - 1 - qb) * p.dir_hs + (p.dir_sh0 + sh) % p.dir_hs)) / p.dir_G) & 1) {
       const int a = it.n_kv[0], b = it.n_kv[1];
       it.nrev = (a > 0 && b > 0) ? min(a, b) : it.n_all;
     }
@@ -857,28 +864,36 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
 
 constexpr int kMaxDevices = 64;
 
-// Phases of the heaviest-first dealing (see item_of) for a dense causal launch on G CTAs.  When
-// the K/V of the launch does not fit in L2, the heads are split into bands of whole key/value
-// planes swept one after the other, so that the items running at the same time read the K/V of
-// one band only; the count is the largest of 2, 4 and 8 whose dealing leaves the busiest CTA at
-// most 0.5 % busier than one phase does (weights: the key tiles an item loads plus two for its
-// Q load and epilogue; kv_len, unknown here, is taken as Nk).  The choice is kept per shape.
+// Dealing of a dense causal launch on G CTAs (see item_of).  When the K/V of the launch does not
+// fit in L2, either (key offset, items of nearly equal weight) the items are numbered plane by
+// plane, or the heads are split into bands of whole key/value planes swept one after the other
+// in phases; either way the items running at the same time read the K/V of few planes.  The phase
+// count is the largest of 2, 4 and 8 whose dealing leaves the busiest CTA at most 0.5 % busier
+// than one phase does, and the plane-by-plane numbering is taken when the lightest item weighs
+// at least 0.9 of the heaviest and its dealing leaves the busiest CTA at most 0.2 % busier
+// (chunked prefill B8 H32 H_kv 8, 2048 queries after 30720 cached keys: +0.8 %; at B2, 0.4 %
+// busier in the simulation, it measured 0.8 % slower) (weights: the key tiles an item loads plus
+// two for its Q load and epilogue; kv_len, unknown here, is taken as Nk).  The choice is kept per
+// shape.
+struct Dealing {
+  int phases, plane_major;
+};
 template <int D, int MODE>
-int causal_phases(const TcParams& p, int G) {
+Dealing causal_dealing(const TcParams& p, int G) {
   constexpr int BN = Cfg<D>::BN;
   constexpr long long kL2Bytes = 48ll << 20;  // K/V that stays in L2 through a phase
   const int planes = p.BH / p.group;
   const long long kv_bytes = (long long)planes * p.Nk * D * 2 * 2;
   const long long total = (long long)p.num_qblocks * p.BH;
-  if (kv_bytes <= kL2Bytes || total > (1 << 16) || G < 1) return 1;
-  struct Entry { int nqb, bh, group, nq, nk, off, G, phases; };
+  if (kv_bytes <= kL2Bytes || total > (1 << 16) || G < 1) return Dealing{1, 0};
+  struct Entry { int nqb, bh, group, nq, nk, off, G; Dealing d; };
   thread_local Entry cache[4] = {};
   thread_local int next = 0;
   const int off = MODE == kCausalOff ? p.off : 0;
   for (const Entry& c : cache)
-    if (c.phases > 0 && c.nqb == p.num_qblocks && c.bh == p.BH && c.group == p.group && c.nq == p.Nq &&
+    if (c.d.phases > 0 && c.nqb == p.num_qblocks && c.bh == p.BH && c.group == p.group && c.nq == p.Nq &&
         c.nk == p.Nk && c.off == off && c.G == G)
-      return c.phases;
+      return c.d;
   // weight of an item of query block qb (both query tiles share its key tiles)
   std::vector<long long> w(p.num_qblocks);
   const int nk_tiles = (p.Nk + BN - 1) / BN;
@@ -891,7 +906,7 @@ int causal_phases(const TcParams& p, int G) {
     w[qb] = n + 2;
   }
   std::vector<long long> load(G);
-  auto busiest = [&](int ng) {
+  auto busiest = [&](int ng, bool by_plane) {
     const int hs = p.BH / ng, gi = hs * p.num_qblocks, gr = (gi + G - 1) / G;
     std::fill(load.begin(), load.end(), 0ll);
     for (int f = 0; f < ng; ++f)
@@ -899,14 +914,19 @@ int causal_phases(const TcParams& p, int G) {
         for (int b = 0; b < G; ++b) {
           const int c = (f & 1) ? G - 1 - b : b;
           const int r = kr * G + ((kr & 1) ? (G - 1 - c) : c);
-          if (r < gi) load[b] += w[p.num_qblocks - 1 - r / hs];
+          if (r < gi) load[b] += w[p.num_qblocks - 1 - (by_plane ? r % p.num_qblocks : r / hs)];
         }
     return *std::max_element(load.begin(), load.end());
   };
-  const long long one = busiest(1);
-  int best = 1;
-  for (int ng = 2; ng <= 8; ng *= 2)
-    if (planes % ng == 0 && (double)busiest(ng) <= 1.005 * (double)one) best = ng;
+  const long long one = busiest(1, false);
+  Dealing best{1, 0};
+  const long long w_min = *std::min_element(w.begin(), w.end()), w_max = *std::max_element(w.begin(), w.end());
+  if (MODE == kCausalOff && 10 * w_min >= 9 * w_max && (double)busiest(1, true) <= 1.002 * (double)one) {
+    best.plane_major = 1;
+  } else {
+    for (int ng = 2; ng <= 8; ng *= 2)
+      if (planes % ng == 0 && (double)busiest(ng, false) <= 1.005 * (double)one) best.phases = ng;
+  }
   cache[next] = Entry{p.num_qblocks, p.BH, p.group, p.Nq, p.Nk, off, G, best};
   next = (next + 1) % 4;
   return best;
@@ -941,20 +961,25 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     g = (total + rounds - 1) / rounds;
   }
   TcParams q = p;
-  q.n_groups = phased<PACKED, SPLIT, MODE>() ? causal_phases<D, MODE>(p, (int)g) : 1;
+  const Dealing deal = phased<PACKED, SPLIT, MODE>() ? causal_dealing<D, MODE>(p, (int)g) : Dealing{1, 0};
+  q.n_groups = deal.phases;
+  q.plane_major = deal.plane_major;
   q.group_items = (int)(total / q.n_groups);
   q.group_rounds = (int)((q.group_items + g - 1) / g);
   q.dir_hs = q.BH / q.n_groups;
   q.dir_G = (int)g;
   q.dir_sh0 = 0;
+  q.dir_alt = !deal.plane_major;  // a plane's items read its K/V together, in step
   if (phased<PACKED, SPLIT, MODE>() && p.call_bh > p.BH) {  // a piece of a call of call_bh planes
     TcParams whole = p;
     whole.BH = p.call_bh;
     const long long total_w = (long long)p.num_qblocks * whole.BH;
     const long long g_w = total_w < sm_count[dev] ? total_w : sm_count[dev];
-    q.dir_hs = whole.BH / causal_phases<D, MODE>(whole, (int)g_w);
+    const Dealing dw = causal_dealing<D, MODE>(whole, (int)g_w);
+    q.dir_hs = whole.BH / dw.phases;
     q.dir_G = (int)g_w;
     q.dir_sh0 = p.call_sh0;
+    q.dir_alt = !dw.plane_major;
   }
   const unsigned grid = (unsigned)g;
   attn_fwd_tc_kernel<D, PACKED, SPLIT, MODE><<<grid, Cfg<D>::template threads<SPLIT>(), Cfg<D>::SMEM_BYTES, s>>>(mq, mk, mv, q);

@@ -4,7 +4,8 @@ library (gpu).  Small and odd shapes run through every checked kernel -- the row
 clusters with the serial and the parallel merge, the unaligned scalar path), the tensor-core
 forward (both head sizes, square and offset causal, grouped heads, packed sequences) and both
 backward kernels -- in two subprocesses, one per build: no check fires (sync_status is OK) and
-every output is bit-identical, so the checks change nothing but the reporting.  A check that fails
+every output is bit-identical (but the backward's dQ, summed by fp32 reduce-adds in arrival order,
+which may differ by a rounding), so the checks change nothing but the reporting.  A check that fails
 on purpose (oa_selftest_debug_check) is reported as OA_ERR_INVALID, its store skipped, by the debug
 build alone.
 """
@@ -90,6 +91,11 @@ def test_debug_build_matches_release_and_no_check_fires(tmp_path):
     assert rel.keys() == dbg.keys()
     for key in rel:
         assert len(rel[key]) == len(dbg[key]), key
-        for a, b in zip(rel[key], dbg[key]):
+        for i, (a, b) in enumerate(zip(rel[key], dbg[key])):
             assert a.dtype == b.dtype and a.shape == b.shape, key
-            assert torch.equal(_bits(a), _bits(b)), key
+            if key.startswith("bwd") and i == 0:
+                # dQ: the same fp32 terms added in arrival order, then rounded to bf16 -- equal up to
+                # one bf16 rounding of the sum
+                assert torch.allclose(a.float(), b.float(), rtol=2.0 ** -7, atol=1e-6), key
+            else:
+                assert torch.equal(_bits(a), _bits(b)), key
