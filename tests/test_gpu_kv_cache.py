@@ -109,6 +109,25 @@ def test_fp32_queries_at_the_end(cuda_lib, Nq, Nk):
         assert_out_close(o, ro, F32_ATTN_ATOL, lse_ref=rl)
 
 
+@pytest.mark.parametrize("Nq", [8192, 4096])
+def test_launch_dealt_in_phases_with_kv_len_and_grouped_heads(cuda_lib, Nq):
+    # 64 MiB of K/V (B2 H_kv8 Nk8192 d128) exceeds what a phase of the dealing keeps in L2, so the
+    # launch runs over bands of heads, with odd rounds reading key tiles top down; the second
+    # sequence's cache ends at 5000 keys.  Square (Nq = Nk) and offset (Nq < Nk) causal; sampled rows.
+    B, H, Hkv, Nk, d = 2, 16, 8, 8192, 128
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, d, torch.bfloat16, seed=500 + Nq)
+    kv_len = [Nk, 5000]
+    o, lse = cuda_lib.attn_fwd(q.cuda(), k.cuda(), v.cuda(), causal=True,
+                               kv_len=torch.tensor(kv_len, dtype=torch.int32).cuda())
+    _sync(cuda_lib)
+    rows_i = si.sample_rows(Nq, 48, seed=Nq + 1).numpy()
+    flat = np.concatenate([(bh * Nq) + rows_i for bh in range(B * H)])
+    ro, rl = oracle.attention(bf16_bits(q), bf16_bits(k), bf16_bits(v), causal=True, kv_len=kv_len, rows=flat)
+    assert_lse_close(lse.reshape(-1)[torch.from_numpy(flat).cuda()], rl)
+    assert_out_close(o.reshape(-1, d)[torch.from_numpy(flat).cuda()], ro, BF16_O_ATOL, lse_ref=rl)
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
 @pytest.mark.slow
 def test_full_size_chunked_prefill_grouped(cuda_lib):
     """The benchmarked chunked prefill: B8 H32 H_kv8, 2048 new queries against a 32768-key cache, d128,
