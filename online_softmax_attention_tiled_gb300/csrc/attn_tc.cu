@@ -18,8 +18,9 @@
 // Persistent: one CTA per SM, each working through items (2 x 128 query rows of one
 // (b, h)) numbered heaviest first and dealt out in rounds of one per CTA, alternating
 // direction between rounds.  Causal launches whose K/V exceeds L2 sweep bands of heads in
-// phases (each phase dealt this way, odd phases in mirrored CTA order), and odd rounds read
-// the key tiles top down, so K/V is read from DRAM about once.  Q and O, read and written
+// phases (each phase dealt this way, odd phases in mirrored CTA order; the host picks the count
+// for the dense layout, the kernel from the sequence lengths for packed sequences), and odd
+// rounds read the key tiles top down, so K/V is read from DRAM about once.  Q and O, read and written
 // once, carry an evict-first L2 policy.  Barriers, TMEM and descriptors are set up once; ring
 // loads and barrier phases run on across items, so the next item's Q, K and V are loaded and
 // its first score tiles computed while the current item finishes.
@@ -124,7 +125,8 @@ struct Cfg {
   // p_half[2]
   static constexpr int NUM_BARS = 1 + 2 * SLOTS + 6 + 1 + 2 + 1 + 2;
   static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = MISC_OFF + 16 + 1024;  // + slack to align the base to 1024
+  // MISC: TMEM address (4 bytes), abort flag (4), at 16 a PackedDeal (12)
+  static constexpr int SMEM_BYTES = MISC_OFF + 32 + 1024;  // + slack to align the base to 1024
   __host__ __device__ static constexpr uint32_t s_col(int i) { return (uint32_t)(i * BN); }
   __host__ __device__ static constexpr uint32_t o_col(int i) { return (uint32_t)(2 * BN + i * D); }
   // first TMEM column of P_i (bf16 pairs, BN / 2 columns)
@@ -160,6 +162,7 @@ struct TcParams {
   int dir_alt;  // 0: every item reads its key tiles bottom up (a call dealt plane by plane)
   int call_bh, call_sh0;  // the whole call's planes and this launch's first (host side, see TcArgs)
   int plane_major;        // kCausalOff, dense, one phase: items numbered plane by plane (see item_at)
+  int decide_phases;      // packed causal: the kernel picks the phase count from the sequence lengths
   int64_t o_rs;          // O row stride (elements): d dense, H d packed
   int64_t o_elems, lse_elems;  // extents of o and lse (the debug build's store checks)
   int l_rs;              // LSE row stride: 1 dense, H packed
@@ -193,10 +196,16 @@ struct Item {
   int64_t ob, lb;   // offsets of the sequence's row 0 (this head) in O (elements) and in LSE
 };
 
-// Dense causal launches deal their items in phases over bands of heads (see item_of); the
-// others in one.
+// Causal launches deal their items in phases over bands of heads (see item_of); the others in
+// one.  Dense: the host picks the phase count; packed: the kernel does, from the sequence lengths
+// (PackedDeal).
 template <bool PACKED, bool SPLIT, int MODE>
-constexpr bool phased() { return !PACKED && !SPLIT && MODE != kNonCausal; }
+constexpr bool phased() { return !SPLIT && MODE != kNonCausal; }
+
+// The dealing of a packed causal launch, decided by every CTA at its start (see the kernel).
+struct PackedDeal {
+  int phases, items, rounds;  // phase count, items per phase, rounds of the grid per phase
+};
 
 // Items are numbered heaviest first (causal, and packed sequences: the last query blocks) within
 // each phase: item idx = f * group_items + r of phase f covers query block num_qblocks - 1 - r / hs
@@ -207,13 +216,15 @@ constexpr bool phased() { return !PACKED && !SPLIT && MODE != kNonCausal; }
 // 128 query rows): both query-tile slots hold the same rows, slot 0 takes the even key tiles and
 // slot 1 the odd ones.
 template <int D, bool PACKED, bool SPLIT, int MODE>
-__device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
+__device__ __forceinline__ Item item_at(const TcParams& p, int idx, const PackedDeal* pd) {
   constexpr int BN = Cfg<D>::BN;
   Item it;
   constexpr bool kHeadMajor = !PACKED && MODE == kNonCausal;
   constexpr bool kPhased = phased<PACKED, SPLIT, MODE>();
-  const int phase = kPhased ? idx / p.group_items : 0;
-  const int r = idx - phase * p.group_items, hs = kPhased ? p.BH / p.n_groups : p.BH;
+  const int n_groups = (PACKED && kPhased) ? pd->phases : p.n_groups;
+  const int group_items = (PACKED && kPhased) ? pd->items : p.group_items;
+  const int phase = kPhased ? idx / group_items : 0;
+  const int r = idx - phase * group_items, hs = kPhased ? p.BH / n_groups : p.BH;
   // a causal launch with a key offset whose items weigh nearly alike (a chunk of queries after a
   // long cache) numbers them plane by plane, heaviest first within a plane: the items running at
   // the same time then share few K/V planes
@@ -283,7 +294,10 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx) {
   it.nrev = 0;
   if constexpr (!SPLIT && MODE != kNonCausal) {
     // an odd round of its phase (in this launch's own dealing when it is the whole call)
-    if (p.dir_alt && ((((p.num_qblocks - 1 - qb) * p.dir_hs + (p.dir_sh0 + sh) % p.dir_hs)) / p.dir_G) & 1) {
+    // (packed: the launch is the whole call, so its own dealing)
+    const int dir_hs = PACKED ? hs : p.dir_hs, dir_G = PACKED ? (int)gridDim.x : p.dir_G;
+    const int dir_sh0 = PACKED ? 0 : p.dir_sh0;
+    if ((PACKED || p.dir_alt) && ((((p.num_qblocks - 1 - qb) * dir_hs + (dir_sh0 + sh) % dir_hs)) / dir_G) & 1) {
       const int a = it.n_kv[0], b = it.n_kv[1];
       it.nrev = (a > 0 && b > 0) ? min(a, b) : it.n_all;
     }
@@ -306,12 +320,35 @@ __device__ __forceinline__ int n_loads_of(const Item& it) { return SPLIT ? it.n_
 // consecutive phases fall on CTAs at opposite ends of the grid.  Negative past the end of a
 // phase.  (One phase: item k G + c or k G + G - 1 - c of the whole list.)
 template <bool PHASED>
-__device__ __forceinline__ int item_of(int k, const TcParams& p) {
+__device__ __forceinline__ int item_of(int k, int group_items, int group_rounds) {
   const int G = (int)gridDim.x;
-  const int f = PHASED ? k / p.group_rounds : 0, kr = k - f * p.group_rounds;
+  const int f = PHASED ? k / group_rounds : 0, kr = k - f * group_rounds;
   const int c = (f & 1) ? G - 1 - (int)blockIdx.x : (int)blockIdx.x;
   const int r = kr * G + ((kr & 1) ? (G - 1 - c) : c);
-  return r < p.group_items ? f * p.group_items + r : -1;
+  return r < group_items ? f * group_items + r : -1;
+}
+
+// Key tiles an item of query block qb of a packed sequence with nq_raw queries and kvl keys
+// loads (n_all of item_at; nq_raw above the declared maximum Nq is cut to it there).
+template <int D>
+__device__ __forceinline__ int packed_item_tiles(int nq_raw, int kvl, int qb, int Nq) {
+  constexpr int BN = Cfg<D>::BN;
+  const int off = kvl - nq_raw, nq = min(nq_raw, Nq), nk_tiles = (kvl + BN - 1) / BN;
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r0 = qb * 2 * BM + i * BM;
+    if (r0 < nq) n = max(n, max(0, min(nk_tiles, (r0 + BM - 1 + off + BN) / BN)));
+  }
+  return n;
+}
+
+// x / y for 0 <= x < 2^22 and 1 <= y, by a float reciprocal and one correction each way.
+__device__ __forceinline__ int small_div(int x, int y, float inv_y) {
+  int q = __float2int_rz(__int2float_rn(x) * inv_y);
+  if (q * y > x) --q;
+  if ((q + 1) * y <= x) ++q;
+  return q;
 }
 
 // No minimum-blocks hint: one CTA per SM follows from the shared memory and TMEM it takes,
@@ -351,7 +388,8 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::MISC_OFF + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int rounds = p.n_groups * p.group_rounds;  // items per CTA, at most
+  constexpr bool kPhased = phased<PACKED, SPLIT, MODE>();
+  PackedDeal* pdeal = reinterpret_cast<PackedDeal*>(smem + C::MISC_OFF + 16);
   constexpr int kIssuers = C::template mma_warps<SPLIT>();
   constexpr bool kOneIssuer = kIssuers == 1;
 
@@ -391,6 +429,99 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  if constexpr (PACKED && kPhased) {
+    // ---- the dealing of a packed causal launch, decided alike by every CTA ----
+    // When the K/V does not fit in L2 (decide_phases), every CTA simulates the dealing with 1, 4
+    // and 16 phases over bands of (sequence, head) planes -- weights: the key tiles an item loads
+    // plus two -- and takes the largest count that leaves the busiest CTA at most 0.5 % busier
+    // than one phase does (over random batches the phases balanced 1-2 % better on average, and
+    // read K/V from DRAM 3-4x less).  The weight table and loads live in the K/V ring, which no
+    // TMA load has touched yet.  Any count dividing the planes is a valid dealing; the choice only
+    // affects speed.
+    constexpr int kTable = 16384;  // (sequence, query block) weights at most
+    constexpr int kCands[3] = {1, 4, 16};
+    const int G = (int)gridDim.x, NQB = p.num_qblocks, BH = p.BH, S = p.BH / p.H;
+    // scratch in the ring: lengths (2 S ints), weights (S NQB ints), loads (3 G long longs)
+    const long long w_off = (8ll * S + 15) / 16 * 16, l_off = (w_off + 4ll * S * NQB + 15) / 16 * 16;
+    const bool decide = p.decide_phases != 0 && (long long)S * NQB <= kTable &&
+                        (long long)BH * NQB <= (1ll << 22) && l_off + 24ll * G <= (long long)C::SLOTS * C::KV_TILE;
+    if (decide) {
+      int* lens = reinterpret_cast<int*>(smem + C::RING_OFF);  // queries, keys of each sequence
+      int* W = reinterpret_cast<int*>(smem + C::RING_OFF + w_off);
+      long long* load = reinterpret_cast<long long*>(smem + C::RING_OFF + l_off);
+      for (int sq = threadIdx.x; sq < S; sq += blockDim.x) {
+        // lengths clamped as item_at clamps them
+        const int q_beg = min(max(p.cu_q[sq], 0), p.Tq), q_end = min(max(p.cu_q[sq + 1], q_beg), p.Tq);
+        const int k_beg = min(max(p.cu_k[sq], 0), p.Tk), k_end = min(max(p.cu_k[sq + 1], k_beg), p.Tk);
+        lens[2 * sq] = q_end - q_beg;
+        lens[2 * sq + 1] = k_end - k_beg;
+      }
+      __syncthreads();
+      for (int e = threadIdx.x; e < S * NQB; e += blockDim.x) {
+        const int sq = e / NQB, qb = e - sq * NQB;
+        const int n = packed_item_tiles<D>(lens[2 * sq], lens[2 * sq + 1], qb, p.Nq);
+        W[e] = n > 0 ? n + 2 : 0;
+      }
+      __syncthreads();
+      const float inv_h = 1.f / (float)p.H;
+      for (int task = threadIdx.x; task < 3 * G; task += blockDim.x) {
+        const int ci = task / G, b = task - ci * G, ng = kCands[ci];
+        long long sum = -1;  // -1: the count does not divide the planes, or a phase is under 2 rounds
+        if (BH % ng == 0 && (BH / ng) % p.group == 0 && (ng == 1 || (long long)(BH / ng) * NQB >= 2ll * G)) {
+          const int hs = BH / ng, gi = hs * NQB, gr = (gi + G - 1) / G;
+          const float inv_hs = 1.f / (float)hs;
+          sum = 0;
+          for (int f = 0; f < ng; ++f) {
+            const int c = (f & 1) ? G - 1 - b : b;
+#pragma unroll 4
+            for (int kr = 0; kr < gr; ++kr) {
+              const int r = kr * G + ((kr & 1) ? (G - 1 - c) : c);
+              if (r >= gi) continue;
+              const int lvl = small_div(r, hs, inv_hs), sh = f * hs + (r - lvl * hs);
+              sum += W[small_div(sh, p.H, inv_h) * NQB + (NQB - 1 - lvl)];
+            }
+          }
+        }
+        load[ci * G + b] = sum;
+      }
+      __syncthreads();
+      if (warp == 0) {  // the busiest CTA of each count (-1: the count is not allowed)
+        long long mx[3];
+#pragma unroll
+        for (int ci = 0; ci < 3; ++ci) {
+          long long m = 0;
+          for (int b = lane; b < G; b += 32) m = (load[ci * G + b] < 0 || m < 0) ? -1 : max(m, load[ci * G + b]);
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            const long long x = __shfl_xor_sync(0xffffffffu, m, o);
+            m = (x < 0 || m < 0) ? -1 : max(m, x);
+          }
+          mx[ci] = m;
+        }
+        if (lane == 0) {
+          int best = 1;
+#pragma unroll
+          for (int ci = 1; ci < 3; ++ci)
+            if (mx[ci] >= 0 && mx[ci] * 1000 <= mx[0] * 1005) best = kCands[ci];
+          pdeal->phases = best;
+          pdeal->items = (BH / best) * NQB;
+          pdeal->rounds = (pdeal->items + G - 1) / G;
+        }
+      }
+      fence_proxy_async_smem();  // the table's stores come before the TMA loads into the ring
+    } else if (threadIdx.x == 0) {
+      pdeal->phases = 1;
+      pdeal->items = p.group_items;
+      pdeal->rounds = p.group_rounds;
+    }
+    __syncthreads();
+  }
+  // items of this CTA, at most, and the k-th of them
+  const int rounds = (PACKED && kPhased) ? pdeal->phases * pdeal->rounds : p.n_groups * p.group_rounds;
+  auto next_item = [&](int k) {
+    return (PACKED && kPhased) ? item_of<kPhased>(k, pdeal->items, pdeal->rounds)
+                               : item_of<kPhased>(k, p.group_items, p.group_rounds);
+  };
   auto wait_all = [&](uint32_t bar, uint32_t parity, unsigned site) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, p.st, abort_flag, (K_ATTN_TC << 8) | site));
   };
@@ -404,9 +535,9 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     // read again
     const uint64_t read_once = l2_policy_evict_first();
     for (int k = 0; ok && k < rounds; ++k) {
-      const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
+      const int idx = next_item(k);
       if (idx < 0) continue;
-      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx, pdeal);
       if (it.n_all == 0) continue;
       // the previous item's S MMAs must have finished reading Q
       if (nq > 0 && !(ok = wait_all(bar_qempty, (uint32_t)(nq - 1) & 1u, W_QEMPTY))) break;
@@ -480,9 +611,9 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     if constexpr (kOneIssuer) {
       // ---- one warp for both tiles: per key tile j, PV_0(j), S_0(j+1), PV_1(j), S_1(j+1) ----
       for (int k = 0; ok && k < rounds; ++k) {
-        const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
+        const int idx = next_item(k);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx, pdeal);
         if (it.n_all == 0) continue;
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
         ++nq;
@@ -546,9 +677,9 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
         return true;
       };
       for (int k = 0; ok && k < rounds; ++k) {
-        const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
+        const int idx = next_item(k);
         if (idx < 0) continue;
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx, pdeal);
         if (it.n_all == 0) continue;
         const int n = it.n_kv[i], sb = i ? st1 : st0, n_ld = 2 * n_loads_of<SPLIT>(it);
         if (!(ok = wait_all(bar_q, (uint32_t)nq & 1u, W_Q))) break;
@@ -615,14 +746,14 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     int nx = 0;  // SPLIT: items handed over so far (the phase of xch / xdone)
     bool ok = true;
     for (int k = 0; ok && k < rounds; ++k) {
-      const int idx = item_of<phased<PACKED, SPLIT, MODE>()>(k, p);
+      const int idx = next_item(k);
       if (idx < 0) continue;
       // only what the score loop needs stays live through it; the epilogue looks the item up
       // again for its output offsets
       // (causal) r0 + off: the last key visible to the tile's first row; row + off: to this row's
       int n, kvl, r0, off, nrev;
       {
-        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+        const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx, pdeal);
         n = it.n_kv[i];
         nrev = it.nrev;
         kvl = it.kvl;
@@ -796,7 +927,7 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
         m = mm;
       }
       const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx);
+      const Item it = item_at<D, PACKED, SPLIT, MODE>(p, idx, pdeal);
       const int64_t o_rs = PACKED ? p.o_rs : D;  // O row stride
       __nv_bfloat16* orow = p.o + it.ob + (int64_t)row * o_rs;
       const bool row_in = row < it.nq && OA_DCHECK(p.st, it.ob + (int64_t)row * o_rs + D <= p.o_elems,
@@ -961,7 +1092,9 @@ cudaError_t launch_d(const CUtensorMap& mq, const CUtensorMap& mk, const CUtenso
     g = (total + rounds - 1) / rounds;
   }
   TcParams q = p;
-  const Dealing deal = phased<PACKED, SPLIT, MODE>() ? causal_dealing<D, MODE>(p, (int)g) : Dealing{1, 0};
+  // (packed: one phase here; the kernel may choose more, see PackedDeal)
+  const Dealing deal = (phased<PACKED, SPLIT, MODE>() && !PACKED) ? causal_dealing<D, MODE>(p, (int)g)
+                                                                   : Dealing{1, 0};
   q.n_groups = deal.phases;
   q.plane_major = deal.plane_major;
   q.group_items = (int)(total / q.n_groups);
@@ -1030,6 +1163,8 @@ cudaError_t launch_attn_tc(const TcArgs& a, const DevStatus& st, cudaStream_t s,
   p.l_rs = packed ? a.H : 1;
   p.scale_log2 = a.scale * kLog2e;
   p.st = st;
+  // packed causal with more K/V than L2 keeps: the kernel decides its phases (see PackedDeal)
+  p.decide_phases = (packed && a.causal && (long long)a.Tk * Hkv * d * 4 > (48ll << 20)) ? 1 : 0;
   p.call_bh = (!packed && a.order_bh > p.BH) ? a.order_bh : p.BH;
   p.call_sh0 = (!packed && a.order_bh > p.BH) ? a.order_sh0 : 0;
   if ((long long)p.num_qblocks * p.BH == 0) return cudaSuccess;  // no query rows

@@ -198,3 +198,42 @@ def test_full_size_varlen_causal_grouped(cuda_lib):
             assert_lse_close(lse[a + rows, h], rl)
             assert_out_close(o[a + rows, h], ro, BF16_O_ATOL)
     assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+
+
+@pytest.mark.parametrize("lens", [
+    [4096] * 16,                                          # equal lengths
+    [8192] + [512] * 15,                                  # one long sequence among short ones
+    "bench",                                              # the benchmarked U[1024, 8192] lengths
+])
+def test_packed_causal_dealt_in_phases_covers_every_row(cuda_lib, lens):
+    """Packed causal launches whose K/V exceeds L2 pick their phase count in the kernel from the
+    sequence lengths; whatever it picks, every row of every sequence and head must come out.  Each
+    sequence is also run alone through the dense path (another instance and dealing) and every row
+    compared; a few rows per sequence against the oracle."""
+    if lens == "bench":
+        lens = si.varlen_lengths(16, 8192, seed=0, min_len=1024)
+    H, Hkv, d = 32, 8, 128
+    q, k, v, cq, ck = si.varlen_inputs(lens, lens, H, Hkv, d, torch.bfloat16, seed=len(lens) + max(lens))
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    o, lse = cuda_lib.attn_fwd_varlen(qd, kd, vd, cq.cuda(), ck.cuda(), max(lens), max(lens), causal=True)
+    _sync(cuda_lib)
+    assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+    for s_, L in enumerate(lens):
+        a = int(cq[s_])
+        qs = qd[a:a + L].permute(1, 0, 2).unsqueeze(0).contiguous()
+        ks = kd[a:a + L].permute(1, 0, 2).unsqueeze(0).contiguous()
+        vs = vd[a:a + L].permute(1, 0, 2).unsqueeze(0).contiguous()
+        od, ld = cuda_lib.attn_fwd(qs, ks, vs, causal=True)
+        _sync(cuda_lib)
+        # the same rows through another dealing: equal up to the order of the key tiles
+        assert torch.allclose(lse[a:a + L].t().float(), ld[0].float(), atol=1e-3, rtol=0), s_
+        assert (o[a:a + L].permute(1, 0, 2).float() - od[0].float()).abs().max().item() <= BF16_O_ATOL, s_
+        if s_ % 5 == 0:
+            rows = si.sample_rows(L, 16, seed=s_)
+            h = s_ % H
+            hk = h // (H // Hkv)
+            ro, rl = oracle.attention(bf16_bits(q[a:a + L, h].reshape(1, 1, L, d)),
+                                      bf16_bits(k[a:a + L, hk].reshape(1, 1, L, d)),
+                                      bf16_bits(v[a:a + L, hk].reshape(1, 1, L, d)), causal=True, rows=rows.numpy())
+            assert_lse_close(lse[a + rows, h].cpu(), rl)
+            assert_out_close(o[a + rows, h].cpu(), ro, BF16_O_ATOL)
