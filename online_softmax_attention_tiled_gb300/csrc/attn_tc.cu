@@ -293,8 +293,9 @@ __device__ __forceinline__ Item item_at(const TcParams& p, int idx, const Packed
   // not depend on the order of the key tiles.
   it.nrev = 0;
   if constexpr (!SPLIT && MODE != kNonCausal) {
-    // an odd round of its phase (in this launch's own dealing when it is the whole call)
-    // (packed: the launch is the whole call, so its own dealing)
+    // an odd round of the item's phase in the dealing of the whole call: this launch's own,
+    // unless it is a piece of a dense call cut into pieces (dir_*); a packed launch is always a
+    // whole call
     const int dir_hs = PACKED ? hs : p.dir_hs, dir_G = PACKED ? (int)gridDim.x : p.dir_G;
     const int dir_sh0 = PACKED ? 0 : p.dir_sh0;
     if ((PACKED || p.dir_alt) && ((((p.num_qblocks - 1 - qb) * dir_hs + (dir_sh0 + sh) % dir_hs)) / dir_G) & 1) {
