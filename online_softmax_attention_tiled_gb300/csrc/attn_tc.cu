@@ -435,8 +435,10 @@ __global__ void __launch_bounds__(Cfg<D>::template threads<SPLIT>())
     // When the K/V does not fit in L2 (decide_phases), every CTA simulates the dealing with 1, 4
     // and 16 phases over bands of (sequence, head) planes -- weights: the key tiles an item loads
     // plus two -- and takes the largest count that leaves the busiest CTA at most 0.5 % busier
-    // than one phase does (over random batches the phases balanced 1-2 % better on average, and
-    // read K/V from DRAM 3-4x less).  The weight table and loads live in the K/V ring, which no
+    // than one phase does (simulated over random batches, the phases balanced 1-2 % better on
+    // average and read K/V from DRAM 3-4x less; 16 packed sequences of 1894-8091 tokens, H32
+    // H_kv 8: 1.6 % faster over 3 s under the power cap, from a higher clock with 2.8x less DRAM
+    // traffic, at 3 % more SM cycles).  The weight table and loads live in the K/V ring, which no
     // TMA load has touched yet.  Any count dividing the planes is a valid dealing; the choice only
     // affects speed.
     constexpr int kTable = 16384;  // (sequence, query block) weights at most
