@@ -41,6 +41,23 @@ def test_host_forward_equals_device_forward(B, H, Hkv, N, d, causal, chunks):
     assert torch.equal(lse, rl.cpu())
 
 
+@pytest.mark.parametrize("B,H,Hkv,Nq,Nk,chunks", [
+    (1, 32, 8, 1024, 16384, 3),   # 64 MiB of K/V, items of near-equal weight: dealt plane by plane
+    (1, 16, 16, 2048, 8192, 4),   # 64 MiB of K/V, items of unequal weight: dealt in phases
+])
+def test_host_forward_with_a_key_offset_equals_device_forward(B, H, Hkv, Nq, Nk, chunks):
+    # new queries after a cache, cut into pieces: each piece must sum its key tiles in the order
+    # of the whole call (bottom up throughout when the call is dealt plane by plane)
+    q, k, v = si.attn_inputs_gqa(B, H, Hkv, Nq, Nk, 128, torch.bfloat16, seed=Nq + Nk)
+    qh, kh, vh = _pinned(q, k, v)
+    o, lse = oa.attn_fwd_host(qh, kh, vh, causal=True, chunks=chunks)
+    torch.cuda.synchronize()
+    ro, rl = oa.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, ro.cpu())
+    assert torch.equal(lse, rl.cpu())
+
+
 def test_host_forward_matches_oracle_and_skips_lse():
     q, k, v = si.attn_inputs(1, 2, 300, 300, 128, torch.bfloat16, seed=4)
     o, lse = oa.attn_fwd_host(*_pinned(q, k, v), causal=True, chunks=2)
