@@ -171,7 +171,11 @@ oa_status oa_attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, 
  *           i iff j <= i + (lk - lq) (j <= i for equal lengths).
  *   d       64 or 128.
  * The caller keeps every buffer alive until the work has completed on
- * `stream`; nothing is allocated.
+ * `stream`; nothing is allocated.  As for oa_attn_fwd, results are
+ * deterministic for given inputs and device; a causal row's key tiles are
+ * summed in an order that follows the launch's dealing, which the kernel
+ * chooses from the sequence lengths, so the last bits may differ between
+ * devices with different SM counts.
  * Errors: OA_ERR_INVALID (NULL pointers, sizes, alignment, H_kv not
  * dividing H, bad scale); OA_ERR_UNSUPPORTED (dtype other than bf16, d).
  */
